@@ -1,0 +1,434 @@
+"""Benchmark of the FP8 delayed-scaling linear layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+for every layer of the workload, the fused casts (+amax, +transposed copies,
++bias gradient), the forward, dgrad and wgrad FP8 GEMMs, and one delayed
+scale update of all slots.  Inputs are resident in HBM before timing; the L2
+is flushed (a 512 MB write) between timed steps, outside the step events.
+
+Prints one JSON line (rank 0).  `value` is TFLOP/s of algorithmic GEMM work
+(2*M*N*K per GEMM) over the step time; `roofline` is the dominant kernel (the
+GEMM) against the dense FP8 peak derived from the measured bf16 peak.
+`--impl reference` times the CPU oracle (the reference arm of this build) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def llama_layers():
+    return [(name, k, n) for name, k, n in wl.LLAMA_PROJ]
+
+
+WORKLOADS = {
+    "llama_proj": dict(desc="Llama-7B-shaped projections fwd+dgrad+wgrad, HYBRID delayed scaling, history 1024: "
+                            "8192 tokens; QKV 4096->12288, out 4096->4096, up 4096->11008, down 11008->4096",
+                       tokens=8192, layers=llama_layers(), hist=1024, fmt="hybrid", x_dtype=torch.bfloat16,
+                       training=True),
+    "linear_hybrid": dict(desc="te.Linear 2048 tokens 768->3072 fwd+bwd, HYBRID, history 16",
+                          tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="hybrid",
+                          x_dtype=torch.float32, training=True),
+    "linear_fwd": dict(desc="te.Linear 2048 tokens 768->3072 forward, E4M3, history 16",
+                       tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="e4m3", x_dtype=torch.float32,
+                       training=False),
+}
+
+
+def step_flops(cfg):
+    M = cfg["tokens"]
+    per = sum(2 * M * n * k for _, k, n in cfg["layers"])
+    return per * (3 if cfg["training"] else 1)
+
+
+def cast_bytes(cfg):
+    """Algorithmic HBM bytes of all casts in one step (read once, write each output once)."""
+    M = cfg["tokens"]
+    esz_x = 2 if cfg["x_dtype"] == torch.bfloat16 else 4
+    tot = 0
+    for _, k, n in cfg["layers"]:
+        t = 2 if cfg["training"] else 1
+        tot += M * k * esz_x + M * k * t          # X -> qX (+ qX^T)
+        tot += n * k * esz_x + n * k * t          # W -> qW (+ qW^T)
+        if cfg["training"]:
+            tot += M * n * 2 + 2 * M * n + 4 * n  # dY bf16 -> qdY + qdY^T + dbias
+    return tot
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+class Model:
+    def __init__(self, cfg, dev, seed):
+        import fp8_delayed_scaling_gb300 as fd
+        from fp8_delayed_scaling_gb300.linear import Fp8Linear, make_state
+        self.fd = fd
+        self.cfg = cfg
+        fmt = fd.FORMAT_HYBRID if cfg["fmt"] == "hybrid" else fd.FORMAT_E4M3
+        self.recipe = fd.Recipe(margin=0, interval=1, fp8_format=fmt, amax_history_len=cfg["hist"])
+        self.state = make_state(self.recipe, len(cfg["layers"]), device=dev)
+        M = cfg["tokens"]
+        self.layers, self.x, self.dy = [], [], []
+        for i, (name, k, n) in enumerate(cfg["layers"]):
+            w = wl.normal((n, k), 0.02, wl.generator(seed, "W/" + name), cfg["x_dtype"]).to(dev)
+            b = torch.zeros(n, dtype=cfg["x_dtype"], device=dev)
+            self.layers.append(Fp8Linear(self.state, i, w, b, M, training=cfg["training"]))
+            if cfg["x_dtype"] == torch.bfloat16:
+                x = wl.student_t3((M, k), 0.5, wl.generator(seed, "X/" + name))
+            else:
+                x = wl.normal((M, k), 1.0, wl.generator(seed, "X/" + name))
+            self.x.append(x.to(dev))
+            if cfg["training"]:
+                self.dy.append(wl.normal((M, n), 1e-3, wl.generator(seed, "dY/" + name), torch.bfloat16).to(dev))
+        self.step_no = 0
+        for lin, x in zip(self.layers, self.x):
+            lin.seed_forward(x)
+        for lin, dy in zip(self.layers, self.dy):
+            lin.seed_backward(dy)
+
+    def launches_per_step(self):
+        per = 3 if not self.cfg["training"] else 3 + 1 + 1 + 2  # casts X, W, gemm; cast dY (+reduce), 2 gemms
+        return per * len(self.layers) + 1
+
+    def step(self, timers=None):
+        for lin, x in zip(self.layers, self.x):
+            lin.forward(x)
+        for lin, dy in zip(self.layers, self.dy):
+            lin.backward(dy)
+        self.state.update(self.step_no)
+        self.step_no += 1
+
+
+def run_ours(args, cfg, dev, rank, world):
+    seed = 2
+    model = Model(cfg, dev, seed)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        model.step()
+    torch.cuda.synchronize()
+
+    # per-kernel timing pass (events around each launch class) to find the dominant kernel
+    kt = profile_kernels(model, flush, stream)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    evs = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        model.step()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = t.item()
+
+    e2e = run_e2e(args, model, dev, stream, world)
+    return model, ms, kt, clk, e2e
+
+
+def profile_kernels(model, flush, stream, reps=5):
+    """Average device time per launch class (cast / gemm / update) over `reps` steps."""
+    fd = model.fd
+    import fp8_delayed_scaling_gb300.linear as L
+    times = {"gemm": [], "cast": [], "update": []}
+    flops_per_gemm_step = step_flops(model.cfg)
+    orig_gemm, orig_cast, orig_update = L.fp8_gemm, L.fp8_cast_amax_transpose, model.state.update
+
+    def timed(kind, fn):
+        def w(*a, **k):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(*a, **k)
+            e1.record(stream)
+            times[kind].append((e0, e1))
+        return w
+
+    L.fp8_gemm = timed("gemm", orig_gemm)
+    L.fp8_cast_amax_transpose = timed("cast", orig_cast)
+    model.state.update = timed("update", orig_update)
+    try:
+        for _ in range(reps):
+            flush.fill_(1)
+            model.step()
+        torch.cuda.synchronize()
+    finally:
+        L.fp8_gemm, L.fp8_cast_amax_transpose = orig_gemm, orig_cast
+        model.state.update = orig_update
+    out = {}
+    for k, v in times.items():
+        tot = sum(a.elapsed_time(b) for a, b in v)
+        out[k] = {"ms_per_step": tot / reps, "launches_per_step": len(v) // reps,
+                  "avg_launch_ms": tot / max(1, len(v))}
+    out["gemm"]["flops_per_step"] = flops_per_gemm_step
+    out["cast"]["bytes_per_step"] = cast_bytes(model.cfg)
+    return out
+
+
+def run_e2e(args, model, dev, stream, world):
+    """Same step through the C ABI with HOST inputs and outputs: per step, H2D of every
+    layer's X and dY from pinned memory, the step, D2H of every layer's dW and db."""
+    hx = [x.cpu().pin_memory() for x in model.x]
+    hdy = [d.cpu().pin_memory() for d in model.dy]
+    outs = []
+    for lin in model.layers:
+        if model.cfg["training"]:
+            outs.append((lin.dw, torch.empty_like(lin.dw, device="cpu").pin_memory()))
+            if lin.db is not None:
+                outs.append((lin.db, torch.empty_like(lin.db, device="cpu").pin_memory()))
+        else:
+            outs.append((lin.y, torch.empty_like(lin.y, device="cpu").pin_memory()))
+    h2d = sum(t.numel() * t.element_size() for t in hx + hdy)
+    d2h = sum(h.numel() * h.element_size() for _, h in outs)
+    steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for d, h in zip(model.x, hx):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(model.dy, hdy):
+            d.copy_(h, non_blocking=True)
+        model.step()
+        for d, h in outs:
+            h.copy_(d, non_blocking=True)
+        torch.cuda.synchronize()
+    sec = (time.perf_counter() - t0) / steps
+    if world > 1:
+        t = torch.tensor([sec], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        sec = t.item()
+    return sec, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# oracle (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+def run_oracle_sample(cfg, seed, budget_s=15.0):
+    """Time the oracle on a bounded sample of one step; returns (TFLOP/s-equivalent, cores, sample text).
+
+    Sample: for every layer, the casts of a 64-row slab of X, W and dY, and the
+    GEMM reference on 8 output rows of each of the three GEMMs; time is scaled
+    to a whole step by algorithmic work (elements for casts, FLOPs for GEMMs)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    M = cfg["tokens"]
+    rows = 64
+    gemm_rows = 8
+    t_cast = 0.0
+    cast_elems_done = 0
+    cast_elems_total = 0
+    t_gemm = 0.0
+    flops_done = 0
+    t_begin = time.perf_counter()
+    for name, k, n in cfg["layers"]:
+        if time.perf_counter() - t_begin > budget_s:
+            break
+        gx = wl.generator(seed, "X/" + name)
+        x = (wl.student_t3((rows, k), 0.5, gx) if cfg["x_dtype"] == torch.bfloat16
+             else wl.normal((rows, k), 1.0, gx))
+        w = wl.normal((rows, k), 0.02, wl.generator(seed, "W/" + name), cfg["x_dtype"])
+        dy = wl.normal((rows, n), 1e-3, wl.generator(seed, "dY/" + name), torch.bfloat16)
+        arrs = [wl.host_array(x), wl.host_array(w)] + ([wl.bf16_bits(dy)] if cfg["training"] else [])
+        t0 = time.perf_counter()
+        for a in arrs:
+            am = oracle.amax(a)
+            oracle.quantize(0, a, float(448.0 / max(float(am), 1e-30)))
+        t_cast += time.perf_counter() - t0
+        cast_elems_done += sum(a.size for a in arrs)
+        cast_elems_total += M * k + n * k + (M * n if cfg["training"] else 0)
+        # GEMM: full K reduction for gemm_rows output rows of [rows x n] against a random [n x k] B
+        rng = np.random.default_rng(0)
+        A = rng.integers(0, 0x7E, (gemm_rows, k), dtype=np.uint8)
+        B = rng.integers(0, 0x7E, (n, k), dtype=np.uint8)
+        ms, ns = np.meshgrid(np.arange(gemm_rows), np.arange(n), indexing="ij")
+        t0 = time.perf_counter()
+        oracle.gemm_elems(A, 0, B, 0, 1.0, 1.0, None, ms.ravel(), ns.ravel())
+        t_gemm += time.perf_counter() - t0
+        flops_done += 2 * gemm_rows * n * k
+    total_flops = step_flops(cfg)
+    # seconds for a whole step = cast part scaled by elements + GEMM part scaled by FLOPs
+    layers_frac = cast_elems_done / max(1, cast_elems_total)
+    step_s = t_cast / max(layers_frac, 1e-12) + t_gemm * total_flops / max(1, flops_done)
+    sample = ("oracle on %d host threads: casts+amax of %d-row slabs of X/W/dY and the fp64 GEMM reference of %d "
+              "output rows per layer GEMM (%.1f MFLOP), scaled to one step by elements and FLOPs"
+              % (cores, rows, gemm_rows, flops_done / 1e6))
+    return total_flops / step_s / 1e12, cores, sample, step_s
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama_proj", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = WORKLOADS[args.workload]
+    peaks, peak_src = load_peaks()
+    config = {"workload": args.workload, "desc": cfg["desc"], "tokens": cfg["tokens"],
+              "l2": "flushed between timed steps (512 MB write)", "parallelism": "replicas" if world > 1 else "single"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        val, cores, sample, step_s = run_oracle_sample(cfg, 2)
+        line = {"impl": "reference", "metric": "FP8 linear fwd+bwd TFLOP/s (oracle, CPU)", "value": val,
+                "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    model, ms, kt, clk, (e2e_s, h2d, d2h) = run_ours(args, cfg, dev, rank, world)
+    flops = step_flops(cfg)
+    value = flops * world / (ms * 1e-3) / 1e12
+    g = kt["gemm"]
+    gemm_ms = g["ms_per_step"]
+    achieved = g["flops_per_step"] / (gemm_ms * 1e-3) / 1e12
+    burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP8_PER_BF16
+    c = kt["cast"]
+    cast_gbs = c["bytes_per_step"] / (c["ms_per_step"] * 1e-3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    line = {
+        "metric": "FP8 linear fwd+bwd TFLOP/s & cast/amax GB/s, % of GB300 FP8/HBM peak",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8(e4m3/e5m2)->fp32acc->bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": config,
+        "roofline": {"bound": "tensor", "kernel": "fp8_gemm", "achieved": round(achieved, 1),
+                     "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
+                     "traffic": None,
+                     "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},
+        "cast": {"achieved_gbs": round(cast_gbs, 1), "peak_gbs": hbm, "frac": round(cast_gbs / hbm, 4),
+                 "ms_per_step": round(c["ms_per_step"], 4), "launches_per_step": c["launches_per_step"]},
+        "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                    for k, v in kt.items()},
+        "gpu_launches": model.launches_per_step() * args.steps,
+        "e2e": {"value": round(flops * world / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    if clk:
+        line["clocks"] = clk
+    if rank == 0 and world == 1:
+        val, cores, sample, _ = run_oracle_sample(cfg, 2)
+        line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,92 @@
+// abi.cu — library state of the C ABI: error messages, device checks, version.
+#include <stdarg.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace fp8dl {
+
+static thread_local char g_last_error[512] = "";
+
+static bool debug_enabled() {
+    static int flag = -1;
+    if (flag < 0) {
+        const char *e = getenv("FP8DL_DEBUG");
+        flag = (e && e[0] && e[0] != '0') ? 1 : 0;
+    }
+    return flag == 1;
+}
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    if (debug_enabled()) fprintf(stderr, "[fp8dl] %s\n", g_last_error);
+}
+
+fp8dl_status fail(fp8dl_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    if (debug_enabled()) fprintf(stderr, "[fp8dl] error %d: %s\n", (int)st, g_last_error);
+    return st;
+}
+
+fp8dl_status check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    if (debug_enabled()) fprintf(stderr, "[fp8dl] launched %s\n", what);
+    return FP8DL_OK;
+}
+
+// Per-device cache: 0 = unknown, 1 = supported, -1 = unsupported.
+static int g_dev_state[64];
+static int g_dev_sms[64];
+
+static int probe_device(int dev) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (dev >= 0 && dev < 64) g_dev_sms[dev] = sms;
+    return (major == 10 && minor == 3) ? 1 : -1;
+}
+
+fp8dl_status current_device(int *dev, int *num_sms) {
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (d < 0 || d >= 64) return fail(FP8DL_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", d);
+    if (g_dev_state[d] == 0) g_dev_state[d] = probe_device(d);
+    if (g_dev_state[d] != 1)
+        return fail(FP8DL_ERR_UNSUPPORTED_DEVICE, "device %d is not an sm_103 (GB300) GPU", d);
+    if (dev) *dev = d;
+    if (num_sms) *num_sms = g_dev_sms[d];
+    return FP8DL_OK;
+}
+
+}  // namespace fp8dl
+
+extern "C" {
+
+const char *fp8dl_last_error(void) { return fp8dl::g_last_error; }
+
+int32_t fp8dl_version(void) { return 100; }
+
+int32_t fp8dl_device_supported(int32_t device) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (device < 0 || device >= n || device >= 64) return 0;
+    return fp8dl::probe_device(device) == 1 ? 1 : 0;
+}
+
+}  // extern "C"

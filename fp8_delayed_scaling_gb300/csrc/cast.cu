@@ -1,0 +1,238 @@
+// cast.cu — fused FP8 cast + amax + transposed copy (+ bias gradient).
+//
+// "FP8 低精度训练：Transformer Engine 简析", §三.3 "FP8框架TE计算流程": before
+// fp8_gemm the input and weight are cast to FP8 with the scale stored in
+// fp8_meta and the cast writes the tensor's amax into the amax history; §三.1:
+// delayed scaling knows the scale before the cast, so cast and amax happen in
+// one pass over the high-precision tensor (no extra HBM round trip, unlike
+// just-in-time scaling).  The transposed copy feeds the backward GEMMs, which
+// need the other operand orientation (every GEMM here is K-contiguous).
+//
+// Design (HBM-bound; one read of x, one write per requested output):
+//   tile = 128 rows x 128 cols, 256 threads, persistent grid-stride loop.
+//   phase 1: thread (rb, cb) loads rows 4rb..4rb+3, cols 16cb..16cb+15 with
+//            16-byte loads, converts with cvt.rn.satfinite, stores 16-byte
+//            row-major codes, and stages them in shared memory (16-byte chunks
+//            XOR-swizzled by row so both phases are bank-conflict free).
+//   phase 2: thread (w, 16-row half) gathers 16 rows x 4 cols, transposes 4x4
+//            byte blocks with prmt, and stores 16 bytes per transposed row
+//            (two neighbouring threads fill one 32-byte sector).
+//   amax: |x| max per thread -> warp shuffle -> one atomicMax per CTA.
+//   dbias: per-tile column sums (fp32, fixed order) to a workspace row per
+//          128-row tile, then a second kernel sums the tile rows in order.
+#include "common.cuh"
+
+namespace fp8dl {
+
+constexpr int CT_ROWS = 128, CT_COLS = 128, CT_THREADS = 256;
+
+template <int XKIND>  // 0 = fp32, 1 = bf16
+struct RowSeg16;      // 16 consecutive elements of one row
+
+template <>
+struct RowSeg16<FP8DL_BF16> {
+    uint4 v[2];
+    __device__ __forceinline__ void load(const void *p) {
+        const uint4 *q = reinterpret_cast<const uint4 *>(p);
+        v[0] = ldg_stream(q);
+        v[1] = ldg_stream(q + 1);
+    }
+    __device__ __forceinline__ float get(int j) const {
+        const uint32_t w = reinterpret_cast<const uint32_t *>(v)[j >> 1];
+        return (j & 1) ? bf16_hi(w) : bf16_lo(w);
+    }
+};
+
+template <>
+struct RowSeg16<FP8DL_F32> {
+    uint4 v[4];
+    __device__ __forceinline__ void load(const void *p) {
+        const uint4 *q = reinterpret_cast<const uint4 *>(p);
+#pragma unroll
+        for (int i = 0; i < 4; i++) v[i] = ldg_stream(q + i);
+    }
+    __device__ __forceinline__ float get(int j) const {
+        return __uint_as_float(reinterpret_cast<const uint32_t *>(v)[j]);
+    }
+};
+
+// Byte offset of 16-byte chunk `chunk` of staged row `r` (rows are 128 bytes).
+__device__ __forceinline__ int stage_off(int r, int chunk) { return r * CT_COLS + ((chunk ^ ((r >> 2) & 7)) << 4); }
+
+template <int XKIND, int FMT>
+__global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict__ x, int64_t rows, int64_t cols,
+                                                          const float *__restrict__ scale_p,
+                                                          uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
+                                                          float *__restrict__ amax_p, float *__restrict__ ws) {
+    constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
+    __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
+    __shared__ float red[32][CT_COLS + 1];
+
+    const int t = threadIdx.x;
+    const int cb = t & 7, rb = t >> 3;                               // phase 1
+    const int lane = t & 31, wi = t >> 5;                            // phase 2
+    const int p2_h = lane & 1, p2_w = (wi & 1) * 16 + (lane >> 1), p2_rg = wi >> 1;
+    const float scale = out || out_t ? __ldg(scale_p) : 1.0f;
+    const int64_t tiles_c = (cols + CT_COLS - 1) / CT_COLS;
+    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * tiles_c;
+    float amax = 0.0f;
+
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t r0 = (tile / tiles_c) * CT_ROWS, c0 = (tile % tiles_c) * CT_COLS;
+        const bool p1_ok = (r0 + 4 * rb < rows) && (c0 + 16 * cb < cols);
+        float csum[16];
+#pragma unroll
+        for (int j = 0; j < 16; j++) csum[j] = 0.0f;
+        if (p1_ok) {
+            RowSeg16<XKIND> seg[4];
+            const char *base = static_cast<const char *>(x) + ((r0 + 4 * rb) * cols + c0 + 16 * cb) * ESZ;
+#pragma unroll
+            for (int i = 0; i < 4; i++) seg[i].load(base + i * cols * ESZ);
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    float v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; j++) {
+                        const float xv = seg[i].get(4 * q + j);
+                        amax = fmaxf(amax, fabsf(xv));
+                        csum[4 * q + j] += xv;
+                        v[j] = __fmul_rn(xv, scale);
+                    }
+                    w[q] = pack4<FMT>(v[0], v[1], v[2], v[3]);
+                }
+                const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
+                const int r = 4 * rb + i;
+                if (out) *reinterpret_cast<uint4 *>(out + (r0 + r) * cols + c0 + 16 * cb) = codes;
+                if (out_t) *reinterpret_cast<uint4 *>(stage + stage_off(r, cb)) = codes;
+            }
+        }
+        if (ws) {
+#pragma unroll
+            for (int j = 0; j < 16; j++) red[rb][16 * cb + j] = csum[j];
+        }
+        if (out_t || ws) __syncthreads();
+        if (out_t) {
+            const int rl = 32 * p2_rg + 16 * p2_h;  // first of this thread's 16 rows within the tile
+            if (r0 + rl < rows && c0 + 4 * p2_w < cols) {
+                uint32_t col[4][4];  // col[j][g]: rows rl+4g..rl+4g+3 of column 4*p2_w+j
+#pragma unroll
+                for (int g = 0; g < 4; g++) {
+                    uint32_t W[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++) {
+                        const int r = rl + 4 * g + k;
+                        W[k] = *reinterpret_cast<const uint32_t *>(stage + stage_off(r, p2_w >> 2) + 4 * (p2_w & 3));
+                    }
+                    const uint32_t t0 = __byte_perm(W[0], W[1], 0x5140), t1 = __byte_perm(W[2], W[3], 0x5140);
+                    const uint32_t t2 = __byte_perm(W[0], W[1], 0x7362), t3 = __byte_perm(W[2], W[3], 0x7362);
+                    col[0][g] = __byte_perm(t0, t1, 0x5410);
+                    col[1][g] = __byte_perm(t0, t1, 0x7632);
+                    col[2][g] = __byte_perm(t2, t3, 0x5410);
+                    col[3][g] = __byte_perm(t2, t3, 0x7632);
+                }
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    *reinterpret_cast<uint4 *>(out_t + (c0 + 4 * p2_w + j) * rows + r0 + rl) =
+                        make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+            }
+        }
+        if (ws) {
+            const int64_t tr = r0 / CT_ROWS;
+            if (t < CT_COLS && c0 + t < cols) {
+                float s = 0.0f;
+                for (int k = 0; k < 32; k++) s += red[k][t];
+                ws[tr * cols + c0 + t] = s;
+            }
+        }
+        if (out_t || ws) __syncthreads();
+    }
+    if (amax_p) {
+        __shared__ float wmax[CT_THREADS / 32];
+        const float m = warp_max(amax);
+        if (lane == 0) wmax[wi] = m;
+        __syncthreads();
+        if (t == 0) {
+            float mm = wmax[0];
+            for (int k = 1; k < CT_THREADS / 32; k++) mm = fmaxf(mm, wmax[k]);
+            atomic_max_nonneg(amax_p, mm);
+        }
+    }
+}
+
+// dbias[c] = sum over row tiles (in order) of ws[tile][c].
+__global__ void colsum_reduce_kernel(const float *__restrict__ ws, int64_t n_tiles, int64_t cols,
+                                     float *__restrict__ dbias) {
+    const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float s = 0.0f;
+    for (int64_t k = 0; k < n_tiles; k++) s += ws[k * cols + c];
+    dbias[c] = s;
+}
+
+template <int XKIND, int FMT>
+static void launch_cast(dim3 grid, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
+                        uint8_t *out, uint8_t *out_t, float *amax, float *ws) {
+    cast_kernel<XKIND, FMT><<<grid, CT_THREADS, 0, st>>>(x, rows, cols, scale, out, out_t, amax, ws);
+}
+
+}  // namespace fp8dl
+
+using namespace fp8dl;
+
+extern "C" {
+
+size_t fp8_cast_workspace_size(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)((rows + CT_ROWS - 1) / CT_ROWS) * (size_t)cols * sizeof(float);
+}
+
+fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t out_dtype,
+                                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *dbias,
+                                     void *workspace, size_t workspace_bytes, fp8dl_stream_t stream) {
+    FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
+    FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
+    FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "out_dtype must be E4M3 or E5M2");
+    FP8DL_CHECK_ARG(!(out || out_t) || scale != nullptr, "scale is NULL but an FP8 output was requested");
+    FP8DL_CHECK_ARG(out || out_t || amax || dbias, "nothing to compute: all outputs are NULL");
+    if (!dim_ok(rows, 16) || !dim_ok(cols, 16))
+        return fail(FP8DL_ERR_SHAPE, "rows (%lld) and cols (%lld) must be positive multiples of 16",
+                    (long long)rows, (long long)cols);
+    if (!aligned16(x) || !aligned16(out) || !aligned16(out_t) || !aligned16(dbias))
+        return fail(FP8DL_ERR_ALIGN, "x, out, out_t and dbias must be 16-byte aligned");
+    if (dbias) {
+        if (!workspace || workspace_bytes < fp8_cast_workspace_size(rows, cols))
+            return fail(FP8DL_ERR_WORKSPACE, "dbias needs a workspace of %zu bytes (got %zu)",
+                        fp8_cast_workspace_size(rows, cols), workspace ? workspace_bytes : (size_t)0);
+        if (!aligned16(workspace)) return fail(FP8DL_ERR_ALIGN, "workspace must be 16-byte aligned");
+    }
+    int sms = 0;
+    FP8DL_TRY(current_device(nullptr, &sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    const int64_t max_ctas = (int64_t)sms * 8;
+    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
+    float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
+    if (x_dtype == FP8DL_BF16) {
+        if (out_dtype == FP8DL_E4M3)
+            launch_cast<FP8DL_BF16, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+        else
+            launch_cast<FP8DL_BF16, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+    } else {
+        if (out_dtype == FP8DL_E4M3)
+            launch_cast<FP8DL_F32, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+        else
+            launch_cast<FP8DL_F32, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+    }
+    FP8DL_TRY(check_launch("fp8_cast_amax_transpose"));
+    if (dbias) {
+        const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
+        colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws, n_tiles, cols, dbias);
+        FP8DL_TRY(check_launch("fp8_cast_amax_transpose(dbias reduce)"));
+    }
+    return FP8DL_OK;
+}
+
+}  // extern "C"

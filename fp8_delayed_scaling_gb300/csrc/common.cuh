@@ -1,0 +1,89 @@
+// common.cuh — shared host/device helpers of the fp8dl library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "fp8dl.h"
+
+namespace fp8dl {
+
+// ---------------------------------------------------------------------------
+// Host-side error reporting: a thread-local message and a status code.
+// ---------------------------------------------------------------------------
+void set_error(const char *fmt, ...);
+fp8dl_status fail(fp8dl_status st, const char *fmt, ...);
+fp8dl_status check_launch(const char *what);
+
+// Validates the current device (sm_103) once per device and caches the SM count.
+fp8dl_status current_device(int *dev, int *num_sms);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool dim_ok(int64_t d, int64_t mult) { return d > 0 && d % mult == 0 && d <= (int64_t(1) << 31); }
+
+#define FP8DL_CHECK_ARG(cond, ...)                                                                \
+    do {                                                                                          \
+        if (!(cond)) return ::fp8dl::fail(FP8DL_ERR_INVALID_ARG, __VA_ARGS__);                    \
+    } while (0)
+
+#define FP8DL_TRY(expr)                                                                           \
+    do {                                                                                          \
+        fp8dl_status _s = (expr);                                                                 \
+        if (_s != FP8DL_OK) return _s;                                                            \
+    } while (0)
+
+// ---------------------------------------------------------------------------
+// Device-side FP8 conversion through the hardware cvt (round to nearest even,
+// saturating to the largest finite value; NaN stays NaN).
+// cvt.rn.satfinite.{e4m3x2,e5m2x2}.f32 d, a, b packs a into the high byte.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four fp32 values -> four codes packed little-endian (v0 in byte 0).
+template <int FMT>
+__device__ __forceinline__ uint32_t pack4(float v0, float v1, float v2, float v3) {
+    uint32_t lo, hi;
+    if (FMT == FP8DL_E4M3) {
+        lo = cvt_e4m3x2(v1, v0);
+        hi = cvt_e4m3x2(v3, v2);
+    } else {
+        lo = cvt_e5m2x2(v1, v0);
+        hi = cvt_e5m2x2(v3, v2);
+    }
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Non-negative floats order like their bit patterns: atomicMax on the bits.
+__device__ __forceinline__ void atomic_max_nonneg(float *addr, float v) {
+    atomicMax(reinterpret_cast<unsigned int *>(addr), __float_as_uint(v));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Streaming 16-byte global load that bypasses L1 allocation.
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+}  // namespace fp8dl

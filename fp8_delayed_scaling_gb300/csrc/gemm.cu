@@ -1,0 +1,352 @@
+// gemm.cu — FP8 GEMM on the tcgen05 tensor cores with a dequantising epilogue.
+//
+// "FP8 低精度训练：Transformer Engine 简析", §三.3: fp8_gemm multiplies the FP8
+// casts, reading the scales kept in fp8_meta; §三.4: FP8 math runs only on the
+// tensor cores, two FP8 matrices in and a high-precision (FP16/FP32) result out,
+// and every GEMM dimension is a multiple of 16.  The page's kernel unit
+// (wmma::mma_sync, 16x16) is the Hopper-era interface; on sm_103a the same
+// contraction is a tcgen05.mma of kind::f8f6f4 (M=128, N=256, K=32 per
+// instruction) with the accumulator in tensor memory.
+//
+//   D[m,n] = round( acc[m,n] * fl32(a_scale_inv * b_scale_inv) + bias[n] ),
+//   acc = sum_k A[m,k] * B[n,k] (fp32 accumulate), A [M x K], B [N x K].
+//
+// Kernel structure (persistent, one CTA per SM, 192 threads):
+//   warp 0      TMA producer: 128x128-byte A and 256x128-byte B tiles into a
+//               STAGES-deep ring of 128-byte-swizzled shared-memory stages.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//               issues 4 MMAs per stage from one thread; tcgen05.commit frees
+//               the stage and, after the last k-block, hands the accumulator
+//               to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, scale, bias,
+//               round, store.  Two accumulators let the epilogue of one tile
+//               overlap the main loop of the next.
+// Tile order: groups of up to 16 row-tiles sweep all column-tiles, so the
+// tiles in flight share A and B panels in L2.
+// Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
+// copies and MMAs, frees TMEM and exits, reporting through *status.
+#include <cuda_bf16.h>
+
+#include "tc.cuh"
+
+namespace fp8dl {
+
+namespace g1 {
+constexpr int BM = 128, BN = 256, BK = 128;  // BK in bytes = FP8 elements
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int GROUP_M = 16;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* barriers */ + 1024 /* alignment slack */;
+}  // namespace g1
+
+struct GemmArgs {
+    int64_t M, N, K;
+    uint32_t idesc;
+    const float *a_scale_inv, *b_scale_inv;
+    const void *bias;
+    int bias_dtype;  // -1 none, else fp8dl_hp_dtype
+    void *D;
+    int d_dtype;
+    int32_t *status;
+};
+
+__device__ __forceinline__ void tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t &tm,
+                                            int64_t &tn) {
+    const int64_t per_group = (int64_t)g1::GROUP_M * tiles_n;
+    const int64_t g = tile / per_group;
+    const int64_t first_m = g * g1::GROUP_M;
+    const int64_t gsize = min((int64_t)g1::GROUP_M, tiles_m - first_m);
+    const int64_t local = tile - g * per_group;
+    tm = first_m + local % gsize;
+    tn = local / gsize;
+}
+
+__device__ __forceinline__ float load_bias(const void *bias, int dtype, int64_t n) {
+    if (dtype == FP8DL_BF16) return __bfloat162float(static_cast<const __nv_bfloat16 *>(bias)[n]);
+    return static_cast<const float *>(bias)[n];
+}
+
+__global__ void __launch_bounds__(g1::THREADS, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                    const GemmArgs args) {
+    using namespace g1;
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms.
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    uint8_t *bar_area = smem + STAGES * STAGE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(bar_area);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tiles_m = (args.M + BM - 1) / BM, tiles_n = (args.N + BN - 1) / BN;
+    const int64_t tiles = tiles_m * tiles_n;
+    const int num_kb = (int)((args.K + BK - 1) / BK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 4);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_map(&tmap_a);
+        tma_prefetch_map(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                int64_t tm, tn;
+                tile_coords(tile, tiles_m, tiles_n, tm, tn);
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_expect_tx(fb, STAGE_BYTES);
+                    uint8_t *sa = smem + s * STAGE_BYTES;
+                    tma_load_2d(smem_u32(sa), &tmap_a, fb, kb * BK, (int32_t)(tm * BM));
+                    tma_load_2d(smem_u32(sa + A_BYTES), &tmap_b, fb, kb * BK, (int32_t)(tn * BN));
+                    issued++;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok) {  // let every issued copy land before the CTA can exit
+                for (int64_t i = issued - 1; i >= 0 && i >= issued - STAGES; i--)
+                    mbar_drain(smem_u32(&full[i % STAGES]), (uint32_t)((i / STAGES) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true, any = false;
+            uint32_t last_bar = 0, last_par = 0;
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1, abort_flag, args.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; kk++) {
+                        umma_f8f6f4(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), args.idesc,
+                                    (kb | kk) != 0);
+                    }
+                    umma_commit(smem_u32(&empty[s]));
+                    any = true;
+                    last_bar = smem_u32(&empty[s]);
+                    last_par = ph;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&tfull[acc]));
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            if (!ok && any) mbar_drain(last_bar, last_par);  // MMAs in flight finish before TMEM is freed
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const float s = __fmul_rn(__ldg(args.a_scale_inv), __ldg(args.b_scale_inv));
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+            int64_t tm, tn;
+            tile_coords(tile, tiles_m, tiles_n, tm, tn);
+            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
+            tc_fence_after();
+            const int64_t row = tm * BM + 32 * q + lane;
+            const bool row_ok = row < args.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c++) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * BN + c * 32) + ((uint32_t)(32 * q) << 16), r);
+                tmem_ld_wait();
+                const int64_t n0 = tn * BN + c * 32;
+                if (row_ok && n0 < args.N) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * s;
+                    if (args.bias_dtype >= 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; j++)
+                            if (n0 + j < args.N) v[j] += load_bias(args.bias, args.bias_dtype, n0 + j);
+                    }
+                    if (args.d_dtype == FP8DL_BF16) {
+                        __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.D) + row * args.N + n0;
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
+                            if (n0 + 8 * g < args.N) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int p = 0; p < 4; p++) {
+                                    __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * g + 2 * p], v[8 * g + 2 * p + 1]);
+                                    w[p] = *reinterpret_cast<uint32_t *>(&h);
+                                }
+                                *reinterpret_cast<uint4 *>(drow + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    } else {
+                        float *drow = static_cast<float *>(args.D) + row * args.N + n0;
+#pragma unroll
+                        for (int g = 0; g < 8; g++)
+                            if (n0 + 4 * g < args.N)
+                                *reinterpret_cast<float4 *>(drow + 4 * g) =
+                                    make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+fp8dl_status encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                               uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                               CUtensorMapSwizzle swizzle) {
+    if (!g_encode_tiled) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return fail(FP8DL_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FP8DL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return FP8DL_OK;
+}
+
+static fp8dl_status check_gemm_common(int64_t M, int64_t N, int64_t K, int64_t mult, const void *A, const void *B,
+                                      const void *bias, int32_t bias_dtype, const void *D, int32_t d_dtype) {
+    FP8DL_CHECK_ARG(A && B && D, "A, B and D must be non-NULL");
+    FP8DL_CHECK_ARG(d_dtype == FP8DL_BF16 || d_dtype == FP8DL_F32, "d_dtype must be FP8DL_BF16 or FP8DL_F32");
+    FP8DL_CHECK_ARG(!bias || bias_dtype == FP8DL_BF16 || bias_dtype == FP8DL_F32,
+                    "bias_dtype must be FP8DL_BF16 or FP8DL_F32");
+    if (!dim_ok(M, mult) || !dim_ok(N, mult) || !dim_ok(K, mult))
+        return fail(FP8DL_ERR_SHAPE, "M, N, K (%lld, %lld, %lld) must be positive multiples of %lld", (long long)M,
+                    (long long)N, (long long)K, (long long)mult);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !aligned16(bias))
+        return fail(FP8DL_ERR_ALIGN, "A, B, bias and D must be 16-byte aligned");
+    return FP8DL_OK;
+}
+
+}  // namespace fp8dl
+
+using namespace fp8dl;
+
+extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
+                                 int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
+                                 const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype, int32_t *dev_status,
+                                 fp8dl_stream_t stream) {
+    FP8DL_TRY(check_gemm_common(M, N, K, 16, A, B, bias, bias_dtype, D, d_dtype));
+    FP8DL_CHECK_ARG((a_dtype == FP8DL_E4M3 || a_dtype == FP8DL_E5M2) && (b_dtype == FP8DL_E4M3 || b_dtype == FP8DL_E5M2),
+                    "a_dtype and b_dtype must be E4M3 or E5M2");
+    FP8DL_CHECK_ARG(a_scale_inv && b_scale_inv, "a_scale_inv and b_scale_inv must be non-NULL");
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
+
+    CUtensorMap ta, tb;
+    FP8DL_TRY(encode_tmap_2d_u8(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, g1::BK, g1::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B));
+    FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g1::BK, g1::BN,
+                                CU_TENSOR_MAP_SWIZZLE_128B));
+    GemmArgs args;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    // Instruction descriptor, kind::f8f6f4: D fp32 (bit 4), A type bits 7-9, B type bits 10-12
+    // (0 = E4M3, 1 = E5M2), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
+    args.idesc = (1u << 4) | ((uint32_t)a_dtype << 7) | ((uint32_t)b_dtype << 10) | ((uint32_t)(g1::BN >> 3) << 17) |
+                 ((uint32_t)(g1::BM >> 4) << 24);
+    args.a_scale_inv = a_scale_inv;
+    args.b_scale_inv = b_scale_inv;
+    args.bias = bias;
+    args.bias_dtype = bias ? bias_dtype : -1;
+    args.D = D;
+    args.d_dtype = d_dtype;
+    args.status = dev_status;
+
+    static bool attr_set[64] = {};
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             g1::SMEM_BYTES);
+        if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        attr_set[dev] = true;
+    }
+    const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
+    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+    fp8_gemm_kernel<<<grid, g1::THREADS, g1::SMEM_BYTES, (cudaStream_t)stream>>>(ta, tb, args);
+    return check_launch("fp8_gemm");
+}

@@ -1,0 +1,108 @@
+"""te.Linear under a DelayedScaling recipe, sequenced over the C ABI.
+
+"FP8 低精度训练：Transformer Engine 简析", §三.3 "FP8框架TE计算流程": inside
+the FP8 autocast a TE module casts its input and weight to FP8 with the scales
+stored in fp8_meta, records their amaxes, and calls fp8_gemm; the backward
+casts grad_output (E5M2 in HYBRID, §三.1) and runs the gradient GEMMs; at
+autocast exit the recorded amaxes update the history and the scales used by
+the next step.
+
+Slots of one layer in the shared ScalingState: base+0 input (E4M3),
+base+1 weight (E4M3), base+2 grad_output (E5M2 in HYBRID, else E4M3).
+
+Per step, for D = X W^T + b with X [M x K], W [N x K]:
+  forward   cast X -> qX (+ qX^T for wgrad), cast W -> qW (+ qW^T for dgrad)
+            Y[M,N]  = fp8_gemm(qX, qW)            * sx_inv * sw_inv + b
+  backward  cast dY -> qdY, qdY^T (+ db = column sums of dY)
+            dX[M,K] = fp8_gemm(qdY, qW^T)        * sdy_inv * sw_inv
+            dW[N,K] = fp8_gemm(qdY^T, qX^T)      * sdy_inv * sx_inv
+  update    fp8_update_scale over all slots (one launch)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (BF16, E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose,
+               fp8_cast_workspace_size, fp8_gemm, fp8_seed_amax_history)
+
+SLOTS_PER_LAYER = 3
+IN, WEIGHT, GRAD = 0, 1, 2
+
+
+def layer_slot_dtypes(recipe: Recipe):
+    return [E4M3, E4M3, E5M2 if recipe.fp8_format == FORMAT_HYBRID else E4M3]
+
+
+def make_state(recipe: Recipe, n_layers: int, device="cuda") -> ScalingState:
+    return ScalingState(recipe, layer_slot_dtypes(recipe) * n_layers, device=device)
+
+
+class Fp8Linear:
+    """One linear layer's FP8 buffers and step sequencing (no autograd)."""
+
+    def __init__(self, state: ScalingState, layer_index: int, weight: torch.Tensor, bias: torch.Tensor | None,
+                 tokens: int, out_dtype=torch.bfloat16, training: bool = True):
+        self.state = state
+        self.base = layer_index * SLOTS_PER_LAYER
+        self.recipe = state.recipe
+        self.w = weight
+        self.b = bias
+        self.N, self.K = weight.shape
+        self.M = tokens
+        dev = weight.device
+        u8 = dict(dtype=torch.uint8, device=dev)
+        M, N, K = self.M, self.N, self.K
+        self.training = training
+        self.qx = torch.empty((M, K), **u8)
+        self.qw = torch.empty((N, K), **u8)
+        self.y = torch.empty((M, N), dtype=out_dtype, device=dev)
+        if training:
+            self.qxT = torch.empty((K, M), **u8)
+            self.qwT = torch.empty((K, N), **u8)
+            self.qdy = torch.empty((M, N), **u8)
+            self.qdyT = torch.empty((N, M), **u8)
+            self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+            self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+            self.db = torch.empty((N,), dtype=torch.float32, device=dev) if bias is not None else None
+            self.ws = torch.empty(fp8_cast_workspace_size(M, N), dtype=torch.uint8, device=dev)
+        self.bwd_dtype = E5M2 if self.recipe.fp8_format == FORMAT_HYBRID else E4M3
+
+    def slot(self, k: int) -> int:
+        return self.base + k
+
+    def _state_at(self, k: int) -> int:
+        return self.state.buf.data_ptr() + self.slot(k) * self.state.stride
+
+    def seed_forward(self, x: torch.Tensor, stream=None) -> None:
+        """First step: amax-only passes over input and weight, then seed their histories."""
+        st = self.state
+        fp8_cast_amax_transpose(x, E4M3, None, amax=st.amax(self.slot(IN)), stream=stream)
+        fp8_cast_amax_transpose(self.w, E4M3, None, amax=st.amax(self.slot(WEIGHT)), stream=stream)
+        fp8_seed_amax_history(self.recipe, 2, self._state_at(IN), stream=stream)
+
+    def seed_backward(self, dy: torch.Tensor, stream=None) -> None:
+        st = self.state
+        fp8_cast_amax_transpose(dy, self.bwd_dtype, None, amax=st.amax(self.slot(GRAD)), stream=stream)
+        fp8_seed_amax_history(self.recipe, 1, self._state_at(GRAD), stream=stream)
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        st = self.state
+        tr = self.training
+        fp8_cast_amax_transpose(x, E4M3, st.scale(self.slot(IN)), out=self.qx, out_t=self.qxT if tr else None,
+                                amax=st.amax(self.slot(IN)), stream=stream)
+        fp8_cast_amax_transpose(self.w, E4M3, st.scale(self.slot(WEIGHT)), out=self.qw,
+                                out_t=self.qwT if tr else None, amax=st.amax(self.slot(WEIGHT)), stream=stream)
+        fp8_gemm(self.qx, E4M3, self.qw, E4M3, st.scale_inv(self.slot(IN)), st.scale_inv(self.slot(WEIGHT)),
+                 self.y, bias=self.b, stream=stream)
+        return self.y
+
+    def backward(self, dy: torch.Tensor, stream=None):
+        st = self.state
+        g = self.slot(GRAD)
+        fp8_cast_amax_transpose(dy, self.bwd_dtype, st.scale(g), out=self.qdy, out_t=self.qdyT, amax=st.amax(g),
+                                dbias=self.db, workspace=self.ws if self.db is not None else None, stream=stream)
+        fp8_gemm(self.qdy, self.bwd_dtype, self.qwT, E4M3, st.scale_inv(g), st.scale_inv(self.slot(WEIGHT)),
+                 self.dx, stream=stream)
+        fp8_gemm(self.qdyT, self.bwd_dtype, self.qxT, E4M3, st.scale_inv(g), st.scale_inv(self.slot(IN)),
+                 self.dw, stream=stream)
+        return self.dx, self.dw, self.db

@@ -1,0 +1,210 @@
+/*
+ * fp8dl.h — C ABI of the GB300 (sm_103a) FP8 delayed-scaling linear layer.
+ *
+ * The method (per-tensor FP8 training with delayed scaling, as run by
+ * Transformer Engine's te.Linear under a DelayedScaling recipe) is described
+ * in "FP8 低精度训练：Transformer Engine 简析" (m.haoling.cc), §三 "FP8技术分析":
+ *   - §三.1 "宏观实现框架": one scale per tensor, symmetric linear quantisation;
+ *     delayed scaling takes the max of an amax history window and sets
+ *     scale = (FP8_MAX / amax) / 2^margin; recipe parameters margin, interval,
+ *     fp8_format (forward E4M3, backward E5M2 in HYBRID), amax_history_len.
+ *   - §三.3 "FP8框架TE计算流程": inputs and weights are cast to FP8 with the
+ *     stored scale, the cast writes its amax into the history, fp8_gemm
+ *     computes; at autocast exit the amaxes update history and scale.
+ *   - §三.4 "Tensor Core如何进行FP8训练": the GEMM returns a high-precision
+ *     result; every dimension is a multiple of 16.
+ * MXFP8 (block-scaled FP8) is named by the Transformer Engine README
+ * ("亮点": MXFP8 on Blackwell); the pages do not define it.  This library reads
+ * it as E4M3 data with one E8M0 (power-of-two) scale per 32 consecutive
+ * elements along the reduction axis.
+ *
+ * Conventions shared by every call
+ *   Memory      All pointers are DEVICE pointers owned by the caller, unless a
+ *               parameter says "host".  The library allocates no device memory;
+ *               where a call needs scratch space the caller passes it in
+ *               (see fp8_cast_workspace_size).
+ *   Layout      Matrices are row-major and densely packed.  FP8 data are one
+ *               byte per element (E4M3 or E5M2 codes).  bf16 is IEEE bfloat16.
+ *   GEMMs       Every GEMM is "TN": D[M,N] = A[M,K] * B[N,K]^T, both operands
+ *               row-major with K contiguous.  The linear layer uses it three
+ *               times: forward Y = X W^T (A = X, B = W), dgrad dX = dY W
+ *               (A = dY, B = W^T, the transposed copy of W's cast), wgrad
+ *               dW = dY^T X (A = dY^T, B = X^T, the transposed copies).
+ *   Shapes      Every dimension must be a positive multiple of 16 (32 for the
+ *               MXFP8 calls); otherwise FP8DL_ERR_SHAPE.  Pointers must be
+ *               16-byte aligned (FP8DL_ERR_ALIGN).
+ *   Streams     Every call is asynchronous on `stream` (NULL = the legacy
+ *               default stream) and never synchronises with the host.
+ *               Scales are read from device memory, so a training step never
+ *               waits for the host.
+ *   Errors      Argument checks run on the host before any launch and return a
+ *               status; nothing throws across the ABI and no kernel traps.
+ *               fp8dl_last_error() returns the calling thread's last message.
+ *               GEMM pipelines bound every wait; if a wait runs out the kernel
+ *               stops, writes FP8DL_ERR_TIMEOUT into *dev_status (when given)
+ *               and returns, leaving D undefined.
+ *   Device      The library is built for sm_103a only (GB300).  Calls on any
+ *               other device return FP8DL_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef FP8DL_H
+#define FP8DL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t. */
+typedef struct CUstream_st *fp8dl_stream_t;
+
+typedef enum {
+    FP8DL_OK = 0,
+    FP8DL_ERR_INVALID_ARG = 1,        /* null pointer, unknown enum, bad recipe   */
+    FP8DL_ERR_SHAPE = 2,              /* dimension not a positive multiple of 16  */
+    FP8DL_ERR_ALIGN = 3,              /* pointer not 16-byte aligned              */
+    FP8DL_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103             */
+    FP8DL_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed        */
+    FP8DL_ERR_TIMEOUT = 6,            /* written to *dev_status by a kernel only  */
+    FP8DL_ERR_WORKSPACE = 7           /* workspace missing or too small           */
+} fp8dl_status;
+
+/* FP8 element formats.  E4M3: bias 7, max 448, no infinity, S.1111.111 = NaN.
+ * E5M2: bias 15, max 57344, S.11111.00 = infinity, other S.11111.xx = NaN. */
+typedef enum { FP8DL_E4M3 = 0, FP8DL_E5M2 = 1 } fp8dl_fp8_dtype;
+
+/* High-precision element types. */
+typedef enum { FP8DL_F32 = 0, FP8DL_BF16 = 1 } fp8dl_hp_dtype;
+
+/* Recipe format: E4M3 everywhere, or HYBRID (E4M3 forward, E5M2 gradients). */
+typedef enum { FP8DL_FORMAT_E4M3 = 0, FP8DL_FORMAT_HYBRID = 1 } fp8dl_format;
+
+/* Delayed-scaling recipe (§三.1 "宏观实现框架" lists margin, interval,
+ * fp8_format and amax_history_len; "max" is the window algorithm of the
+ * Transformer Engine tutorial's HYBRID recipe).  Host struct. */
+typedef struct {
+    int32_t margin;            /* scale = (FP8_MAX/amax) / 2^margin, 0 <= margin <= 126 */
+    int32_t interval;          /* recompute the scale when step % interval == 0, >= 1   */
+    int32_t fp8_format;        /* fp8dl_format; informs which slots use E5M2            */
+    int32_t amax_history_len;  /* L >= 1, window length of the amax history            */
+    int32_t amax_compute_algo; /* 0 = max over the window (the only algorithm)         */
+} fp8dl_recipe;
+
+/* ----------------------------------------------------------------------------
+ * Scaling state.  One "slot" per scaled tensor (e.g. input, weight and
+ * grad_output of each GEMM).  The state of n slots is one caller-allocated
+ * device block of fp8dl_scaling_state_bytes(L, n) bytes; slot i starts at
+ * byte i * fp8dl_slot_stride(L) and holds
+ *     float   scale       offset 0   multiplier used by the next casts
+ *     float   scale_inv   offset 4   1/scale, read by the GEMM epilogue
+ *     float   amax        offset 8   amax recorded since the last update;
+ *                                    casts max their |x| into it atomically
+ *     int32   hist_pos    offset 12  next write position in the history ring
+ *     int32   fp8_dtype   offset 16  fp8dl_fp8_dtype of the slot (FP8_MAX)
+ *     int32   reserved[3]
+ *     float   hist[L]     offset 32  amax history ring
+ * The block is plain data: saving and restoring it (with the caller's step
+ * counter) resumes training bit-identically.
+ * ------------------------------------------------------------------------- */
+size_t fp8dl_slot_stride(int32_t amax_history_len);
+size_t fp8dl_scaling_state_bytes(int32_t amax_history_len, int32_t n_slots);
+
+/* Initialise n_slots slots: scale = scale_inv = 1, amax = 0, hist = 0,
+ * hist_pos = 0, fp8_dtype = slot_fp8_dtype[i] (HOST array of n_slots). */
+fp8dl_status fp8_scaling_state_init(const fp8dl_recipe *recipe, int32_t n_slots,
+                                    const int32_t *slot_fp8_dtype, void *state,
+                                    fp8dl_stream_t stream);
+
+/* Delayed scale update of every slot (§三.1 "宏观实现框架", §三.3: at autocast
+ * exit the recorded amaxes update the history and the scale).  Per slot:
+ *   hist[hist_pos] = amax; hist_pos = (hist_pos + 1) % L; amax = 0;
+ *   if (step % interval == 0):
+ *       a = max(hist[0..L))
+ *       if a > 0 and finite: s = fl32(FP8_MAX / a) / 2^margin
+ *           if s > 0 and finite: scale = s, scale_inv = fl32(1 / s)
+ *   (otherwise scale and scale_inv keep their values).
+ * `step` is the caller's step counter.  One launch for all slots. */
+fp8dl_status fp8_update_scale(const fp8dl_recipe *recipe, int32_t n_slots, void *state,
+                              int64_t step, fp8dl_stream_t stream);
+
+/* First step: fill every history entry with the slot's recorded amax (from
+ * an amax-only cast pass), clear amax, set hist_pos = 0 and derive the scale
+ * as above, so the first real cast already uses a data-derived scale. */
+fp8dl_status fp8_seed_amax_history(const fp8dl_recipe *recipe, int32_t n_slots, void *state,
+                                   fp8dl_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Fused cast + amax (+ transpose) (+ bias gradient) (§三.1 / §三.3: the cast
+ * to FP8 uses the stored scale and records the tensor's amax).
+ *   x        [rows x cols], x_dtype (FP8DL_F32 or FP8DL_BF16)
+ *   scale    device float (a slot's scale)
+ *   out      [rows x cols] FP8 codes, out[i,j] = enc(fl32(x[i,j] * scale)), or NULL
+ *   out_t    [cols x rows] FP8 codes, out_t[j,i] = out[i,j], or NULL
+ *   amax     device float, atomically max-ed with max |x| (pre-scale), or NULL
+ *   dbias    [cols] fp32 column sums of x (the bias gradient when x is
+ *            grad_output), or NULL; overwritten, not accumulated
+ *   workspace/workspace_bytes  scratch of fp8_cast_workspace_size(rows, cols)
+ *            bytes, needed only when dbias != NULL
+ * Encoding: round to nearest even, saturating to +-FP8_MAX (including
+ * infinities); NaN gives a NaN code.  With out, out_t and dbias all NULL the
+ * call is an amax-only pass. */
+size_t fp8_cast_workspace_size(int64_t rows, int64_t cols);
+
+fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
+                                     int32_t out_dtype, const float *scale, uint8_t *out,
+                                     uint8_t *out_t, float *amax, float *dbias, void *workspace,
+                                     size_t workspace_bytes, fp8dl_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * FP8 GEMM with dequantising epilogue (§三.3 fp8_gemm; §三.4 high-precision
+ * output, dims multiple of 16):
+ *   D[m,n] = round_d( acc[m,n] * fl32(a_scale_inv * b_scale_inv) + bias[n] )
+ *   acc[m,n] = sum_k A[m,k] * B[n,k] on the tcgen05 tensor cores, fp32 accumulate.
+ *   A [M x K] codes of a_dtype, B [N x K] codes of b_dtype (E4M3/E5M2 mixed ok)
+ *   a_scale_inv, b_scale_inv   device floats (the operands' slots' scale_inv)
+ *   bias       [N] of bias_dtype, or NULL
+ *   D          [M x N] of d_dtype (FP8DL_BF16 or FP8DL_F32)
+ *   dev_status device int or NULL; set to FP8DL_ERR_TIMEOUT if a pipeline wait
+ *              runs out (never reset to 0 by the library). */
+fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype,
+                      int64_t M, int64_t N, int64_t K, const float *a_scale_inv,
+                      const float *b_scale_inv, const void *bias, int32_t bias_dtype, void *D,
+                      int32_t d_dtype, int32_t *dev_status, fp8dl_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * MXFP8 quantisation (block-scaled FP8, named by the Transformer Engine
+ * README).  x [rows x cols] (bf16 or fp32).  Blocks are 32 consecutive
+ * elements; per block: e = the smallest integer with amax_b * 2^-e <= 448,
+ * clamped to [-127, 127] (amax_b = 0 gives e = 0); scale byte = e + 127 (E8M0);
+ * data = enc_e4m3(fl32(x * 2^-e)).
+ *   row_q [rows x cols], row_s [rows x cols/32]: blocks along each row, or NULL
+ *   col_q [cols x rows], col_s [cols x rows/32]: blocks along each column,
+ *         stored transposed (row j of col_q is column j of x), or NULL
+ * rows and cols must be multiples of 32. */
+fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
+                            uint8_t *row_q, uint8_t *row_s, uint8_t *col_q, uint8_t *col_s,
+                            fp8dl_stream_t stream);
+
+/* MXFP8 GEMM: D[m,n] = round_d( sum_b 2^(ea[m,b]+eb[n,b]) * sum_{k in b} A[m,k]*B[n,k]
+ *                               + bias[n] )
+ * A [M x K] E4M3, A_s [M x K/32] E8M0; B [N x K] E4M3, B_s [N x K/32] E8M0
+ * (layouts as produced by mxfp8_quantize).  M, N, K multiples of 32.
+ * bias, D, dev_status as for fp8_gemm. */
+fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, const uint8_t *B_s,
+                        int64_t M, int64_t N, int64_t K, const void *bias, int32_t bias_dtype,
+                        void *D, int32_t d_dtype, int32_t *dev_status, fp8dl_stream_t stream);
+
+/* ----------------------------------------------------------------------------
+ * Library state. */
+/* 1 if `device` is an sm_103 GPU this library can run on, else 0. */
+int32_t fp8dl_device_supported(int32_t device);
+/* Last error message of the calling thread ("" if none). */
+const char *fp8dl_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t fp8dl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8DL_H */

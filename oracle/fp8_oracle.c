@@ -72,6 +72,17 @@ static uint8_t orc_max_code(int fmt) { return fmt == ORC_E4M3 ? 0x7E : 0x7B; }
 
 double orc_fp8_max(int fmt) { return orc_fp8_decode(fmt, orc_max_code(fmt)); }
 
+/* Decoded value of every code, filled once when the library is loaded. */
+static double orc_table[2][256];
+
+__attribute__((constructor)) static void orc_fill_tables(void)
+{
+    int f, c;
+    for (f = 0; f < 2; f++)
+        for (c = 0; c < 256; c++)
+            orc_table[f][c] = orc_fp8_decode(f, (uint8_t)c);
+}
+
 /*
  * Encode one fp32 value.  Reading (the pages give only the ranges):
  * round to the nearest representable value, ties to the code with an even
@@ -86,6 +97,7 @@ double orc_fp8_max(int fmt) { return orc_fp8_decode(fmt, orc_max_code(fmt)); }
  */
 uint8_t orc_fp8_encode(int fmt, float v)
 {
+    const double *tab = orc_table[fmt == ORC_E4M3 ? 0 : 1];
     const uint8_t sign = signbit(v) ? 0x80 : 0x00;
     const uint8_t top = orc_max_code(fmt);
     double a = fabs((double)v);
@@ -93,18 +105,18 @@ uint8_t orc_fp8_encode(int fmt, float v)
     double dlo, dhi;
     if (isnan(v))
         return (uint8_t)(sign | 0x7F);
-    if (a >= orc_fp8_decode(fmt, top))
+    if (a >= tab[top])
         return (uint8_t)(sign | top);
-    /* binary search: decode(lo) <= a < decode(hi) */
+    /* binary search: tab[lo] <= a < tab[hi] */
     while (hi - lo > 1) {
         mid = (uint8_t)((lo + hi) / 2);
-        if (orc_fp8_decode(fmt, mid) <= a)
+        if (tab[mid] <= a)
             lo = mid;
         else
             hi = mid;
     }
-    dlo = a - orc_fp8_decode(fmt, lo);
-    dhi = orc_fp8_decode(fmt, hi) - a;
+    dlo = a - tab[lo];
+    dhi = tab[hi] - a;
     if (dlo < dhi)
         return (uint8_t)(sign | lo);
     if (dhi < dlo)

@@ -1,0 +1,152 @@
+"""GPU parity of the scale update and the fused cast + amax + transpose
+(+ bias gradient) against the oracle: bit-exact codes, amax and scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import gpu, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _fd():
+    import fp8_delayed_scaling_gb300 as fd
+    return fd
+
+
+def _run_cast(x, fmt, scale_val, transpose=True, dbias=False):
+    fd = _fd()
+    dev = x.device
+    rows, cols = x.shape
+    scale = torch.tensor([scale_val], dtype=torch.float32, device=dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    out = torch.full((rows, cols), 0xAA, dtype=torch.uint8, device=dev)
+    out_t = torch.full((cols, rows), 0xAA, dtype=torch.uint8, device=dev) if transpose else None
+    db = torch.full((cols,), float("nan"), dtype=torch.float32, device=dev) if dbias else None
+    ws = torch.empty(fd.fp8_cast_workspace_size(rows, cols), dtype=torch.uint8, device=dev) if dbias else None
+    fd.fp8_cast_amax_transpose(x, fmt, scale, out=out, out_t=out_t, amax=amax, dbias=db, workspace=ws)
+    torch.cuda.synchronize()
+    return out, out_t, amax, db
+
+
+SHAPES = [(16, 16), (48, 80), (128, 128), (144, 272), (256, 48), (2048, 768), (400, 1040)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("kind,fmt", [(torch.float32, 0), (torch.bfloat16, 0), (torch.bfloat16, 1),
+                                      (torch.float32, 1)])
+def test_cast_parity(shape, kind, fmt):
+    dev = gpu()
+    g = wl.generator(31, "cast/%s/%s/%d" % (shape, kind, fmt))
+    x = wl.normal(shape, 1.0 if fmt == 0 else 1e-3, g, kind)
+    if fmt == 1:
+        x = wl.with_outliers(x, 0.001, 1000.0, g)
+    xs = host(x)
+    a = oracle.amax(xs)
+    scale = np.float32(oracle.fp8_max(fmt)) / a / np.float32(2.0)  # some non-trivial fp32 scale
+    out, out_t, amax, db = _run_cast(x.to(dev), fmt, float(scale), dbias=True)
+    q = oracle.quantize(fmt, xs, float(scale))
+    assert np.array_equal(out.cpu().numpy(), q)
+    assert np.array_equal(out_t.cpu().numpy(), q.T)
+    assert amax.item() == a
+    s, sabs = oracle.colsum(xs)
+    rows = shape[0]
+    bound = rows * 2.0 ** -24 * sabs + 1e-30
+    assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= bound)
+
+
+def test_cast_special_values():
+    """NaN, infinities, overflow, fp32 subnormals and signed zeros through the hardware cvt."""
+    dev = gpu()
+    vals = np.array([0.0, -0.0, 1e-45, -1e-45, 1e-40, 2.0 ** -10, -2.0 ** -10, 447.9, 448.0, 464.0, 480.0, 1e30,
+                     np.inf, -np.inf, np.nan, 57343.0, 57344.0, 61439.0, 61440.0, 1e38, 3.0e-5, 1.5e-5, -7.7e-6],
+                    np.float32)
+    x = np.resize(vals, 32 * 32).astype(np.float32).reshape(32, 32)
+    for fmt in (0, 1):
+        out, out_t, amax, _ = _run_cast(torch.from_numpy(x).to(dev), fmt, 1.0)
+        q = oracle.quantize(fmt, x, 1.0)
+        got = out.cpu().numpy()
+        tab = oracle.decode_table(fmt)
+        nan = np.isnan(x)
+        assert np.all(np.isnan(tab[got[nan]]))
+        assert np.array_equal(got[~nan], q[~nan]), (fmt, x[~nan][got[~nan] != q[~nan]])
+        assert amax.item() == oracle.amax(x)  # inf
+
+
+def _sweep_chunk(fmt, start, count, dev):
+    fd = _fd()
+    bits = torch.arange(start, start + count, dtype=torch.int64, device=dev).to(torch.int32)
+    x = bits.view(torch.float32).reshape(count // 16384, 16384)
+    scale = torch.ones(1, dtype=torch.float32, device=dev)
+    out = torch.empty_like(x, dtype=torch.uint8)
+    fd.fp8_cast_amax_transpose(x, fmt, scale, out=out)
+    return out.reshape(-1).cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_encoder_all_fp32_inputs(fmt):
+    """Every one of the 2^32 fp32 bit patterns, scale 1: GPU codes == oracle codes
+    (NaN inputs: any NaN code)."""
+    dev = gpu()
+    chunk = 1 << 27
+    tab = oracle.decode_table(fmt)
+    for start in range(0, 1 << 32, chunk):
+        got = _sweep_chunk(fmt, start, chunk, dev)
+        v = np.arange(start, start + chunk, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        want = oracle.encode(fmt, v)
+        nan = np.isnan(v)
+        if nan.any():
+            assert np.all(np.isnan(tab[got[nan]]))
+            got, want = got[~nan], want[~nan]
+        bad = np.nonzero(got != want)[0]
+        assert bad.size == 0, (hex(start), bad[:5], got[bad[:5]], want[bad[:5]])
+
+
+def test_amax_only_pass_and_accumulation():
+    fd = _fd()
+    dev = gpu()
+    g = wl.generator(5, "amax-only")
+    x1 = wl.normal((512, 256), 2.0, g, torch.bfloat16)
+    x2 = wl.normal((512, 256), 0.5, g, torch.bfloat16)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    fd.fp8_cast_amax_transpose(x2.to(dev), 0, None, amax=amax)
+    fd.fp8_cast_amax_transpose(x1.to(dev), 0, None, amax=amax)
+    torch.cuda.synchronize()
+    assert amax.item() == max(oracle.amax(host(x1)), oracle.amax(host(x2)))
+
+
+def test_update_scale_parity_random_sequences():
+    """fp8_update_scale vs the oracle over 40 steps: scale, scale_inv, history and
+    position bit-exact, for several recipes and HYBRID slot formats."""
+    fd = _fd()
+    dev = gpu()
+    rng = np.random.default_rng(17)
+    for L, margin, interval in [(16, 0, 1), (4, 2, 3), (1024, 0, 1), (1, 5, 2), (7, 0, 4)]:
+        recipe = fd.Recipe(margin=margin, interval=interval, fp8_format=fd.FORMAT_HYBRID, amax_history_len=L)
+        fmts = [0, 0, 1, 0, 0, 1]
+        st = fd.ScalingState(recipe, fmts, device=dev)
+        ost = oracle.ScalingState(fmts, hist_len=L, margin=margin, interval=interval)
+        view = st.buf.view(torch.float32).view(len(fmts), st.stride // 4)
+        for step in range(40):
+            a = (rng.uniform(0, 3, len(fmts)) * 10.0 ** rng.integers(-6, 4, len(fmts))).astype(np.float32)
+            if step % 11 == 5:
+                a[1] = 0.0
+            if step % 13 == 7:
+                a[4] = np.inf
+            view[:, 2] = torch.from_numpy(a).to(dev)
+            for i in range(len(fmts)):
+                ost.record_amax(i, a[i])
+            if step == 0:
+                st.seed()
+                ost.seed()
+            else:
+                st.update(step)
+                ost.update(step)
+            got = st.read()
+            assert np.array_equal(got["scale"], ost.scale), (L, step)
+            assert np.array_equal(got["scale_inv"], ost.scale_inv), (L, step)
+            assert np.array_equal(got["hist"], ost.hist), (L, step)
+            assert np.array_equal(got["pos"], ost.pos), (L, step)
+            assert np.all(got["amax"] == 0)

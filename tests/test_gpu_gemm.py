@@ -1,0 +1,99 @@
+"""GPU parity of the tcgen05 FP8 GEMM against the oracle (error bound per element)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import check_gemm, gpu, sample_elems
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes(rng, fmt, shape):
+    tab = oracle.decode_table(fmt)
+    ok = np.array([c for c in range(256) if np.isfinite(tab[c])], np.uint8)
+    # mostly moderate magnitudes, some extremes
+    idx = rng.integers(0, ok.size, shape)
+    return ok[idx]
+
+
+def _gemm(A, afmt, B, bfmt, sa, sb, bias, d_dtype, dev):
+    import fp8_delayed_scaling_gb300 as fd
+    M, K = A.shape
+    N = B.shape[0]
+    At = torch.from_numpy(A).to(dev)
+    Bt = torch.from_numpy(B).to(dev)
+    sat = torch.tensor([sa], dtype=torch.float32, device=dev)
+    sbt = torch.tensor([sb], dtype=torch.float32, device=dev)
+    D = torch.full((M, N), float("nan"), dtype=d_dtype, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    fd.fp8_gemm(At, afmt, Bt, bfmt, sat, sbt, D, bias=bias, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return D
+
+
+SHAPES = [(128, 256, 128), (16, 16, 16), (48, 80, 32), (144, 272, 400), (256, 512, 384), (384, 768, 1040),
+          (2048, 3072, 768), (1000 // 16 * 16, 2000 // 16 * 16, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("afmt,bfmt", [(0, 0), (1, 0), (0, 1)])
+def test_gemm_full_parity(M, N, K, afmt, bfmt):
+    dev = gpu()
+    rng = np.random.default_rng(M * 7 + N * 3 + K + 10 * afmt + bfmt)
+    A = _codes(rng, afmt, (M, K))
+    B = _codes(rng, bfmt, (N, K))
+    sa, sb = np.float32(rng.uniform(0.001, 2)), np.float32(rng.uniform(0.001, 2))
+    D = _gemm(A, afmt, B, bfmt, sa, sb, None, torch.bfloat16, dev)
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    ms, ns = ms.ravel(), ns.ravel()
+    if ms.size > 400000:
+        sel = rng.choice(ms.size, 400000, replace=False)
+        ms, ns = ms[sel], ns[sel]
+    ref, absr = oracle.gemm_elems(A, afmt, B, bfmt, sa, sb, None, ms, ns)
+    check_gemm(D, ref, absr, ms, ns)
+
+
+@pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("d_dtype", [torch.bfloat16, torch.float32])
+def test_gemm_bias_and_output_types(bias_dtype, d_dtype):
+    dev = gpu()
+    rng = np.random.default_rng(3)
+    M, N, K = 272, 528, 256
+    A = _codes(rng, 0, (M, K))
+    B = _codes(rng, 0, (N, K))
+    g = wl.generator(9, "bias")
+    bias = wl.normal((N,), 3.0, g, bias_dtype)
+    D = _gemm(A, 0, B, 0, 0.01, 0.02, bias.to(dev), d_dtype, dev)
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    bh = bias.detach().cpu()
+    bh = bh.view(torch.int16).numpy().view(np.uint16) if bias_dtype == torch.bfloat16 else bh.numpy()
+    ref, absr = oracle.gemm_elems(A, 0, B, 0, 0.01, 0.02, bh, ms.ravel(), ns.ravel())
+    check_gemm(D, ref, absr, ms.ravel(), ns.ravel())
+
+
+def test_gemm_identity_is_exact():
+    """A * I^T with I = identity in E4M3 (code 0x38 = 1.0) returns A exactly."""
+    dev = gpu()
+    rng = np.random.default_rng(5)
+    M, K = 256, 512
+    A = _codes(rng, 0, (M, K))
+    I = np.zeros((K, K), np.uint8)
+    I[np.arange(K), np.arange(K)] = 0x38
+    D = _gemm(A, 0, I, 0, 1.0, 1.0, None, torch.float32, dev)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), oracle.decode_table(0)[A])
+
+
+def test_gemm_large_sampled():
+    """A full-size projection shape (8192 x 12288 x 4096), sampled output elements."""
+    dev = gpu()
+    rng = np.random.default_rng(8)
+    M, N, K = 8192, 12288, 4096
+    A = _codes(rng, 1, (M, K))
+    B = _codes(rng, 0, (N, K))
+    D = _gemm(A, 1, B, 0, 1e-3, 3e-2, None, torch.bfloat16, dev)
+    ms, ns = sample_elems(M, N, rng)
+    ref, absr = oracle.gemm_elems(A, 1, B, 0, 1e-3, 3e-2, None, ms, ns)
+    check_gemm(D, ref, absr, ms, ns)
