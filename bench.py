@@ -356,6 +356,69 @@ def run_oracle_sample(cfg, seed, budget_s=15.0):
 
 
 # ---------------------------------------------------------------------------
+# single-kernel mode (for per-kernel timing and small ncu captures)
+# ---------------------------------------------------------------------------
+def run_only(args, dev):
+    """Time one kernel alone at one shape: `--only gemm --shape M,N,K` (E4M3 x E4M3 -> bf16),
+    `--only cast --shape R,C` (bf16 -> E4M3 + transposed copy + amax),
+    `--only mxq --shape R,C` (bf16 -> row- and column-wise MXFP8),
+    `--only mxgemm --shape M,N,K`.  Inputs are seeded; L2 is flushed between launches."""
+    import fp8_delayed_scaling_gb300 as fd
+    shape = [int(v) for v in args.shape.split(",")]
+    g = torch.Generator(device="cpu").manual_seed(1)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    if args.only in ("gemm", "mxgemm"):
+        M, N, K = shape
+        A = torch.randint(0, 0x70, (M, K), dtype=torch.uint8, generator=g).to(dev)
+        B = torch.randint(0, 0x70, (N, K), dtype=torch.uint8, generator=g).to(dev)
+        D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        one = torch.ones(1, dtype=torch.float32, device=dev)
+        if args.only == "gemm":
+            fn = lambda: fd.fp8_gemm(A, fd.E4M3, B, fd.E4M3, one, one, D)  # noqa: E731
+        else:
+            As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, generator=g).to(dev)
+            Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, generator=g).to(dev)
+            fn = lambda: fd.mxfp8_gemm(A, As, B, Bs, D)  # noqa: E731
+        work, unit = 2.0 * M * N * K, "TFLOP/s"
+    else:
+        R, C = shape
+        x = wl.normal((R, C), 1.0, g, torch.bfloat16).to(dev)
+        if args.only == "cast":
+            q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+            qt = torch.empty((C, R), dtype=torch.uint8, device=dev)
+            sc = torch.ones(1, dtype=torch.float32, device=dev)
+            am = torch.zeros(1, dtype=torch.float32, device=dev)
+            fn = lambda: fd.fp8_cast_amax_transpose(x, fd.E4M3, sc, out=q, out_t=qt, amax=am)  # noqa: E731
+            work = R * C * (2 + 1 + 1)
+        else:
+            rq = torch.empty((R, C), dtype=torch.uint8, device=dev)
+            rs = torch.empty((R, C // 32), dtype=torch.uint8, device=dev)
+            cq = torch.empty((C, R), dtype=torch.uint8, device=dev)
+            cs = torch.empty((C, R // 32), dtype=torch.uint8, device=dev)
+            fn = lambda: fd.mxfp8_quantize(x, rq, rs, cq, cs)  # noqa: E731
+            work = R * C * (2 + 1 + 1) + 2 * R * C // 32
+        unit = "GB/s"
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    avg = sum(ms) / len(ms)
+    rate = work / (avg * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    print(json.dumps({"only": args.only, "shape": shape, "avg_ms": round(avg, 5), "min_ms": round(min(ms), 5),
+                      "rate": round(rate, 1), "unit": unit, "launches": args.warmup + args.steps}))
+
+
+# ---------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -363,6 +426,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama_proj", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--only", default=None, choices=["gemm", "cast", "mxq", "mxgemm"])
+    ap.add_argument("--shape", default="8192,12288,4096")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -391,6 +456,10 @@ def main():
         torch.distributed.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.only:
+        if rank == 0:
+            run_only(args, dev)
+        return
     model, ms, kt, clk, (e2e_s, h2d, d2h) = run_ours(args, cfg, dev, rank, world)
     flops = step_flops(cfg)
     value = flops * world / (ms * 1e-3) / 1e12
