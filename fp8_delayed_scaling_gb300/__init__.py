@@ -48,6 +48,7 @@ _SIGS = {
     "fp8_seed_amax_history": (_i32, [ctypes.POINTER(fp8dl_recipe), _i32, _vp, _vp]),
     "fp8_cast_workspace_size": (_sz, [_i64, _i64]),
     "fp8_cast_amax_transpose": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fp8_cast_amax_transpose_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
     "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mxfp8_gemm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
@@ -222,6 +223,19 @@ def fp8_cast_amax_transpose(x: torch.Tensor, out_dtype: int, scale, out=None, ou
     _check(_lib.fp8_cast_amax_transpose(_p(x), _hp(x), rows, cols, out_dtype, _p(scale), _p(out), _p(out_t),
                                         _p(amax), _p(dbias), _p(workspace), ws_bytes, _stream(stream)),
            "fp8_cast_amax_transpose")
+
+
+def fp8_cast_amax_transpose_noalloc(x: torch.Tensor, out_dtype: int, scale, out=None, out_t=None, amax=None,
+                                    dbias=None, stream=None) -> None:
+    """fp8_cast_amax_transpose for callers that cannot allocate device memory:
+    the bias-gradient scratch is the library's own 4 MiB static device array
+    (ceil(rows/128) * cols * 4 bytes must fit).  Calls on one device share
+    that array, so concurrent calls must be ordered on one stream."""
+    assert x.dim() == 2 and x.is_contiguous()
+    rows, cols = x.shape
+    _check(_lib.fp8_cast_amax_transpose_noalloc(_p(x), _hp(x), rows, cols, out_dtype, _p(scale), _p(out),
+                                                _p(out_t), _p(amax), _p(dbias), _stream(stream)),
+           "fp8_cast_amax_transpose_noalloc")
 
 
 def fp8_gemm(A: torch.Tensor, a_dtype: int, B: torch.Tensor, b_dtype: int, a_scale_inv, b_scale_inv, D: torch.Tensor,

@@ -236,3 +236,84 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.
+//
+// Some callers only hand this library their input and output buffers: a
+// plugin or custom-op interface with a fixed signature has no workspace
+// argument, and a process whose device memory is owned by another allocator
+// may not be allowed to call cudaMalloc itself.  Such callers cannot supply
+// the bias-gradient workspace of fp8_cast_amax_transpose.  This variant takes
+// that workspace from a fixed-size array in the library's own static device
+// memory instead; it allocates nothing.
+// ---------------------------------------------------------------------------
+namespace fp8dl {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB, held on every device that loads the library
+static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
+static float *g_static_scratch_addr[64];  // device address of g_static_scratch, per device index
+
+// The array's name in host code is a host-side stand-in, not a device address:
+// look the address up once per device, with that device current.
+static fp8dl_status static_scratch_address(int dev, float **out) {
+    if (g_static_scratch_addr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(FP8DL_ERR_CUDA, "cudaGetSymbolAddress(static scratch) failed: %s", cudaGetErrorString(e));
+        g_static_scratch_addr[dev] = static_cast<float *>(p);
+    }
+    *out = g_static_scratch_addr[dev];
+    return FP8DL_OK;
+}
+
+}  // namespace fp8dl
+
+extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
+                                                        int32_t out_dtype, const float *scale, uint8_t *out,
+                                                        uint8_t *out_t, float *amax, float *dbias,
+                                                        fp8dl_stream_t stream) {
+    FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
+    FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
+    FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "out_dtype must be E4M3 or E5M2");
+    FP8DL_CHECK_ARG(!(out || out_t) || scale != nullptr, "scale is NULL but an FP8 output was requested");
+    FP8DL_CHECK_ARG(out || out_t || amax || dbias, "nothing to compute: all outputs are NULL");
+    if (!dim_ok(rows, 16) || !dim_ok(cols, 16))
+        return fail(FP8DL_ERR_SHAPE, "rows (%lld) and cols (%lld) must be positive multiples of 16",
+                    (long long)rows, (long long)cols);
+    if (!aligned16(x) || !aligned16(out) || !aligned16(out_t) || !aligned16(dbias))
+        return fail(FP8DL_ERR_ALIGN, "x, out, out_t and dbias must be 16-byte aligned");
+    if (dbias && fp8_cast_workspace_size(rows, cols) > kStaticScratchBytes)
+        return fail(FP8DL_ERR_WORKSPACE,
+                    "fp8_cast_amax_transpose_noalloc: dbias of a %lld x %lld tensor needs %zu bytes of scratch, "
+                    "more than the %zu-byte static array (ceil(rows/128) * cols * 4 must be <= %zu)",
+                    (long long)rows, (long long)cols, fp8_cast_workspace_size(rows, cols), kStaticScratchBytes,
+                    kStaticScratchBytes);
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
+    float *ws = nullptr;
+    if (dbias) FP8DL_TRY(static_scratch_address(dev, &ws));
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    const int64_t max_ctas = (int64_t)sms * 8;
+    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
+    if (x_dtype == FP8DL_BF16) {
+        if (out_dtype == FP8DL_E4M3)
+            launch_cast<FP8DL_BF16, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+        else
+            launch_cast<FP8DL_BF16, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+    } else {
+        if (out_dtype == FP8DL_E4M3)
+            launch_cast<FP8DL_F32, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+        else
+            launch_cast<FP8DL_F32, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+    }
+    FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc"));
+    if (dbias) {
+        const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
+        colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws, n_tiles, cols, dbias);
+        FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc(dbias reduce)"));
+    }
+    return FP8DL_OK;
+}

@@ -156,6 +156,34 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
                                      uint8_t *out_t, float *amax, float *dbias, void *workspace,
                                      size_t workspace_bytes, fp8dl_stream_t stream);
 
+/* The same cast for callers that cannot allocate device memory.  The paper
+ * has no counterpart to this call: it exists for callers that only hand the
+ * library their input and output buffers (a plugin or custom-op interface
+ * whose fixed signature has no workspace argument, or a process whose device
+ * memory belongs to another allocator that does not let it call cudaMalloc),
+ * so they can neither pass the bias-gradient workspace nor allocate one.
+ *   Arguments, layouts and results are those of fp8_cast_amax_transpose,
+ *   without workspace/workspace_bytes.
+ *   Scratch: the dbias workspace is a 4 MiB array in the library's static
+ *   device memory (every GPU that loads the library holds it until the
+ *   process exits).  Calls with dbias != NULL need
+ *   fp8_cast_workspace_size(rows, cols) <= 4 MiB, i.e.
+ *   ceil(rows/128) * cols * 4 <= 4194304; larger ones return
+ *   FP8DL_ERR_WORKSPACE before any launch.  The call allocates nothing
+ *   (no cudaMalloc, cudaFree or allocating library routine).
+ *   First call per device: looks up the array's device address with
+ *   cudaGetSymbolAddress (that device current) and caches it; make that first
+ *   call before any stream capture.
+ *   Sharing: all calls on a device share the one array, which keeps the last
+ *   call's contents; each call writes every scratch entry it reads, so no
+ *   clearing is needed.  Calls that overlap on the GPU (different streams, or
+ *   host threads without ordering) race on the array and give wrong dbias:
+ *   order them on one stream. */
+fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
+                                             int32_t out_dtype, const float *scale, uint8_t *out,
+                                             uint8_t *out_t, float *amax, float *dbias,
+                                             fp8dl_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * FP8 GEMM with dequantising epilogue (§三.3 fp8_gemm; §三.4 high-precision
  * output, dims multiple of 16):
