@@ -50,6 +50,7 @@ _SIGS = {
     "fp8_cast_amax_transpose": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fp8_cast_amax_transpose_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
+    "mxfp8_scale_bytes": (_sz, [_i64, _i64]),
     "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mxfp8_gemm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
     "fp8dl_device_supported": (_i32, [_i32]),
@@ -247,6 +248,11 @@ def fp8_gemm(A: torch.Tensor, a_dtype: int, B: torch.Tensor, b_dtype: int, a_sca
     _check(_lib.fp8_gemm(_p(A), a_dtype, _p(B), b_dtype, M, N, K, _p(a_scale_inv), _p(b_scale_inv), _p(bias),
                          _hp(bias) if bias is not None else BF16, _p(D), _hp(D), _p(dev_status), _stream(stream)),
            "fp8_gemm")
+
+
+def mxfp8_scale_bytes(rows: int, cols: int) -> int:
+    """Bytes of the tiled E8M0 scale buffer of an MXFP8 [rows x cols] matrix (blocks along cols)."""
+    return _lib.mxfp8_scale_bytes(rows, cols)
 
 
 def mxfp8_quantize(x: torch.Tensor, row_q=None, row_s=None, col_q=None, col_s=None, stream=None) -> None:

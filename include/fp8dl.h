@@ -206,18 +206,33 @@ fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32
  * elements; per block: e = the smallest integer with amax_b * 2^-e <= 448,
  * clamped to [-127, 127] (amax_b = 0 gives e = 0); scale byte = e + 127 (E8M0);
  * data = enc_e4m3(fl32(x * 2^-e)).
- *   row_q [rows x cols], row_s [rows x cols/32]: blocks along each row, or NULL
- *   col_q [cols x rows], col_s [cols x rows/32]: blocks along each column,
- *         stored transposed (row j of col_q is column j of x), or NULL
- * rows and cols must be multiples of 32. */
+ *   row_q [rows x cols]: blocks along each row, or NULL
+ *   row_s  scales of row_q in the tiled layout below (R = rows, NB = cols/32)
+ *   col_q [cols x rows]: blocks along each column, stored transposed (row j
+ *         of col_q is column j of x), or NULL
+ *   col_s  scales of col_q in the tiled layout (R = cols, NB = rows/32)
+ * rows and cols must be multiples of 32.
+ *
+ * Tiled scale layout (the order the tensor cores read block scales in).  For
+ * a matrix of R rows with NB blocks per row, S[r][b] is the scale byte of
+ * block b of row r.  Rows are grouped by 128 and blocks by 4; each
+ * (row group g, block group h) is one 512-byte tile at byte offset
+ * (g * ceil(NB/4) + h) * 512, and inside the tile
+ *     byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4)  holds  S[r][b].
+ * Total size: mxfp8_scale_bytes(R, 32*NB).  Entries for rows >= R or blocks
+ * >= NB (padding) are written as 127 (2^0). */
+size_t mxfp8_scale_bytes(int64_t rows, int64_t cols);
+
 fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
                             uint8_t *row_q, uint8_t *row_s, uint8_t *col_q, uint8_t *col_s,
                             fp8dl_stream_t stream);
 
 /* MXFP8 GEMM: D[m,n] = round_d( sum_b 2^(ea[m,b]+eb[n,b]) * sum_{k in b} A[m,k]*B[n,k]
  *                               + bias[n] )
- * A [M x K] E4M3, A_s [M x K/32] E8M0; B [N x K] E4M3, B_s [N x K/32] E8M0
- * (layouts as produced by mxfp8_quantize).  M, N, K multiples of 32.
+ * A [M x K] E4M3 with scales A_s (tiled layout, R = M, NB = K/32);
+ * B [N x K] E4M3 with scales B_s (tiled layout, R = N, NB = K/32), as produced
+ * by mxfp8_quantize (row_q/row_s of X and W for the forward GEMM; col_q/col_s
+ * for the operands of the gradient GEMMs).  M, N, K multiples of 32.
  * bias, D, dev_status as for fp8_gemm. */
 fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, const uint8_t *B_s,
                         int64_t M, int64_t N, int64_t K, const void *bias, int32_t bias_dtype,
