@@ -338,3 +338,87 @@ def mx_gemm_elems(A, As, B, Bs, bias, ms, ns, threads: int | None = None):
     with ThreadPoolExecutor(t) as ex:
         list(ex.map(run, range(t)))
     return ref, absr
+
+
+# --------------------------------------------------------------------------
+# LayerNormMLP pieces (fp64)
+# --------------------------------------------------------------------------
+def _sig_lnmlp(L):
+    if getattr(L, "_lnmlp", False):
+        return
+    L.orc_layernorm_fwd.restype = None
+    L.orc_layernorm_fwd.argtypes = [_vp, ctypes.c_int, _i64, _i64, _vp, _vp, ctypes.c_int, ctypes.c_double,
+                                    _vp, _vp, _vp]
+    L.orc_gelu.restype = None
+    L.orc_gelu.argtypes = [_vp, ctypes.c_int, _i64, _vp]
+    L.orc_dgelu.restype = None
+    L.orc_dgelu.argtypes = [_vp, _vp, ctypes.c_int, _i64, _vp]
+    L.orc_layernorm_bwd.restype = None
+    L.orc_layernorm_bwd.argtypes = [_vp, _vp, ctypes.c_int, _i64, _i64, _vp, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _vp]
+    L._lnmlp = True
+
+
+def layernorm_fwd(x: np.ndarray, gamma: np.ndarray, beta: np.ndarray, eps: float = 1e-5):
+    """(y, mu, rsigma) in fp64 for a 2-D x (float32 or bf16 bits)."""
+    L = lib()
+    _sig_lnmlp(L)
+    x = np.ascontiguousarray(x)
+    gamma, beta = np.ascontiguousarray(gamma), np.ascontiguousarray(beta)
+    assert _kind(gamma) == _kind(beta)
+    R, C = x.shape
+    y = np.empty((R, C), np.float64)
+    mu = np.empty(R, np.float64)
+    rs = np.empty(R, np.float64)
+    t = _threads(R * C, None)
+    bounds = [R * i // t for i in range(t + 1)]
+
+    def run(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        if hi > lo:
+            L.orc_layernorm_fwd(x.ctypes.data + lo * C * x.itemsize, _kind(x), hi - lo, C, _ptr(gamma), _ptr(beta),
+                                _kind(gamma), float(eps), y.ctypes.data + lo * C * 8, mu.ctypes.data + lo * 8,
+                                rs.ctypes.data + lo * 8)
+
+    with ThreadPoolExecutor(t) as ex:
+        list(ex.map(run, range(t)))
+    return y, mu, rs
+
+
+def gelu(h: np.ndarray) -> np.ndarray:
+    L = lib()
+    _sig_lnmlp(L)
+    h = np.ascontiguousarray(h)
+    out = np.empty(h.shape, np.float64)
+    L.orc_gelu(_ptr(h), _kind(h), h.size, _ptr(out))
+    return out
+
+
+def dgelu(dg: np.ndarray, h: np.ndarray) -> np.ndarray:
+    L = lib()
+    _sig_lnmlp(L)
+    dg, h = np.ascontiguousarray(dg), np.ascontiguousarray(h)
+    assert dg.shape == h.shape and _kind(dg) == _kind(h)
+    out = np.empty(h.shape, np.float64)
+    L.orc_dgelu(_ptr(dg), _ptr(h), _kind(h), h.size, _ptr(out))
+    return out
+
+
+def layernorm_bwd(dy: np.ndarray, x: np.ndarray, gamma: np.ndarray, mu: np.ndarray, rsigma: np.ndarray):
+    """(dx, dgamma, dbeta, dx_abs, dgamma_abs, dbeta_abs) in fp64."""
+    L = lib()
+    _sig_lnmlp(L)
+    dy, x, gamma = np.ascontiguousarray(dy), np.ascontiguousarray(x), np.ascontiguousarray(gamma)
+    mu = np.ascontiguousarray(mu, dtype=np.float64)
+    rsigma = np.ascontiguousarray(rsigma, dtype=np.float64)
+    assert _kind(dy) == _kind(x)
+    R, C = x.shape
+    dx = np.empty((R, C), np.float64)
+    dxa = np.empty((R, C), np.float64)
+    dg = np.empty(C, np.float64)
+    db = np.empty(C, np.float64)
+    dga = np.empty(C, np.float64)
+    dba = np.empty(C, np.float64)
+    L.orc_layernorm_bwd(_ptr(dy), _ptr(x), _kind(x), R, C, _ptr(gamma), _kind(gamma), _ptr(mu), _ptr(rsigma),
+                        _ptr(dx), _ptr(dg), _ptr(db), _ptr(dxa), _ptr(dga), _ptr(dba))
+    return dx, dg, db, dxa, dga, dba

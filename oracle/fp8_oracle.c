@@ -367,3 +367,100 @@ void orc_mx_gemm_elems(const uint8_t *A, const uint8_t *As, const uint8_t *B, co
         abs_ref[e] = aacc;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* LayerNormMLP pieces — [TE-tutor]: te.LayerNormMLP (LayerNorm, fc1, GELU,   */
+/* fc2), whose plain-PyTorch mirror uses nn.LayerNorm and nn.GELU (the erf  */
+/* form).  Textbook definitions in fp64; the pages fix no precision or eps  */
+/* beyond the workload's eps = 1e-5 and the biased variance of LayerNorm.   */
+/* Parameters gamma/beta use the same kinds as the inputs (fp32 or bf16).   */
+/* ------------------------------------------------------------------------ */
+/* y = (x - mu) / sqrt(var + eps) * gamma + beta per row, var biased;
+ * also mu and rsigma = 1/sqrt(var + eps) per row. */
+void orc_layernorm_fwd(const void *x, int kind, int64_t rows, int64_t cols, const void *gamma, const void *beta,
+                       int pkind, double eps, double *y, double *mu, double *rsigma)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; r++) {
+        double m = 0.0, v = 0.0, rs;
+        for (c = 0; c < cols; c++)
+            m += (double)orc_load(x, kind, r * cols + c);
+        m /= (double)cols;
+        for (c = 0; c < cols; c++) {
+            double d = (double)orc_load(x, kind, r * cols + c) - m;
+            v += d * d;
+        }
+        v /= (double)cols;
+        rs = 1.0 / sqrt(v + eps);
+        mu[r] = m;
+        rsigma[r] = rs;
+        for (c = 0; c < cols; c++)
+            y[r * cols + c] = ((double)orc_load(x, kind, r * cols + c) - m) * rs * (double)orc_load(gamma, pkind, c) +
+                              (double)orc_load(beta, pkind, c);
+    }
+}
+
+/* GELU, erf form: g = 0.5 * h * (1 + erf(h / sqrt(2))). */
+void orc_gelu(const void *h, int kind, int64_t n, double *g)
+{
+    int64_t i;
+    for (i = 0; i < n; i++) {
+        double v = (double)orc_load(h, kind, i);
+        g[i] = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
+    }
+}
+
+/* Backward of GELU: dh = dg * (0.5 * (1 + erf(h/sqrt2)) + h * exp(-h^2/2) / sqrt(2 pi)). */
+void orc_dgelu(const void *dg, const void *h, int kind, int64_t n, double *dh)
+{
+    const double inv_sqrt_2pi = 0.3989422804014327;
+    int64_t i;
+    for (i = 0; i < n; i++) {
+        double v = (double)orc_load(h, kind, i);
+        double d = 0.5 * (1.0 + erf(v / sqrt(2.0))) + v * exp(-0.5 * v * v) * inv_sqrt_2pi;
+        dh[i] = (double)orc_load(dg, kind, i) * d;
+    }
+}
+
+/* Backward of LayerNorm given the forward's per-row mu and rsigma:
+ *   xhat = (x - mu) * rsigma, g = dy * gamma
+ *   dx = rsigma * (g - mean(g) - xhat * mean(g * xhat))
+ *   dgamma = sum_rows dy * xhat,  dbeta = sum_rows dy
+ * The *_abs outputs are the same expressions over absolute values (for error
+ * bounds of an fp32 implementation). */
+void orc_layernorm_bwd(const void *dy, const void *x, int kind, int64_t rows, int64_t cols, const void *gamma,
+                       int pkind, const double *mu, const double *rsigma, double *dx, double *dgamma, double *dbeta,
+                       double *dx_abs, double *dgamma_abs, double *dbeta_abs)
+{
+    int64_t r, c;
+    for (c = 0; c < cols; c++) {
+        dgamma[c] = dbeta[c] = dgamma_abs[c] = dbeta_abs[c] = 0.0;
+    }
+    for (r = 0; r < rows; r++) {
+        double s1 = 0.0, s2 = 0.0, a1 = 0.0, a2 = 0.0;
+        for (c = 0; c < cols; c++) {
+            double d = (double)orc_load(dy, kind, r * cols + c);
+            double xh = ((double)orc_load(x, kind, r * cols + c) - mu[r]) * rsigma[r];
+            double g = d * (double)orc_load(gamma, pkind, c);
+            s1 += g;
+            s2 += g * xh;
+            a1 += fabs(g);
+            a2 += fabs(g * xh);
+            dgamma[c] += d * xh;
+            dbeta[c] += d;
+            dgamma_abs[c] += fabs(d * xh);
+            dbeta_abs[c] += fabs(d);
+        }
+        s1 /= (double)cols;
+        s2 /= (double)cols;
+        a1 /= (double)cols;
+        a2 /= (double)cols;
+        for (c = 0; c < cols; c++) {
+            double d = (double)orc_load(dy, kind, r * cols + c);
+            double xh = ((double)orc_load(x, kind, r * cols + c) - mu[r]) * rsigma[r];
+            double g = d * (double)orc_load(gamma, pkind, c);
+            dx[r * cols + c] = rsigma[r] * (g - s1 - xh * s2);
+            dx_abs[r * cols + c] = rsigma[r] * (fabs(g) + a1 + fabs(xh) * a2);
+        }
+    }
+}
