@@ -53,6 +53,12 @@ _SIGS = {
     "mxfp8_scale_bytes": (_sz, [_i64, _i64]),
     "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mxfp8_gemm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
+    "fp8_layernorm_cast": (_i32, [_vp, _i64, _i64, _vp, _vp, ctypes.c_float, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _vp, _vp]),
+    "fp8_gelu_cast": (_i32, [_vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fp8_dgelu_cast": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "fp8_layernorm_bwd_workspace_size": (_sz, [_i64, _i64]),
+    "fp8_layernorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fp8dl_device_supported": (_i32, [_i32]),
     "fp8dl_last_error": (ctypes.c_char_p, []),
     "fp8dl_version": (_i32, []),
@@ -271,3 +277,49 @@ def mxfp8_gemm(A, A_s, B, B_s, D: torch.Tensor, bias: torch.Tensor | None = None
     _check(_lib.mxfp8_gemm(_p(A), _p(A_s), _p(B), _p(B_s), M, N, K, _p(bias),
                            _hp(bias) if bias is not None else BF16, _p(D), _hp(D), _p(dev_status), _stream(stream)),
            "mxfp8_gemm")
+
+
+# --------------------------------------------------------------------------
+# LayerNormMLP pieces (bf16 tensors)
+# --------------------------------------------------------------------------
+def _nbytes(t):
+    return t.numel() * t.element_size() if isinstance(t, torch.Tensor) else 0
+
+
+def fp8_layernorm_cast(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float, out_dtype: int, scale,
+                       mu: torch.Tensor, rsigma: torch.Tensor, out=None, out_t=None, amax=None, y=None,
+                       stream=None) -> None:
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    rows, cols = x.shape
+    _check(_lib.fp8_layernorm_cast(_p(x), rows, cols, _p(gamma), _p(beta), float(eps), out_dtype, _p(scale),
+                                   _p(out), _p(out_t), _p(amax), _p(mu), _p(rsigma), _p(y), _stream(stream)),
+           "fp8_layernorm_cast")
+
+
+def fp8_gelu_cast(h: torch.Tensor, out_dtype: int, scale, out=None, out_t=None, amax=None, g=None,
+                  stream=None) -> None:
+    assert h.dtype == torch.bfloat16 and h.dim() == 2 and h.is_contiguous()
+    rows, cols = h.shape
+    _check(_lib.fp8_gelu_cast(_p(h), rows, cols, out_dtype, _p(scale), _p(out), _p(out_t), _p(amax), _p(g),
+                              _stream(stream)), "fp8_gelu_cast")
+
+
+def fp8_dgelu_cast(dg: torch.Tensor, h: torch.Tensor, out_dtype: int, scale, out=None, out_t=None, amax=None,
+                   dbias=None, workspace=None, dh=None, stream=None) -> None:
+    assert dg.dtype == torch.bfloat16 and h.dtype == torch.bfloat16 and dg.shape == h.shape
+    rows, cols = h.shape
+    _check(_lib.fp8_dgelu_cast(_p(dg), _p(h), rows, cols, out_dtype, _p(scale), _p(out), _p(out_t), _p(amax),
+                               _p(dbias), _p(workspace), _nbytes(workspace), _p(dh), _stream(stream)),
+           "fp8_dgelu_cast")
+
+
+def fp8_layernorm_bwd_workspace_size(rows: int, cols: int) -> int:
+    return _lib.fp8_layernorm_bwd_workspace_size(rows, cols)
+
+
+def fp8_layernorm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mu, rsigma, dx: torch.Tensor,
+                      dgamma: torch.Tensor, dbeta: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    rows, cols = x.shape
+    _check(_lib.fp8_layernorm_bwd(_p(dy), _p(x), _p(gamma), _p(mu), _p(rsigma), rows, cols, _p(dx), _p(dgamma),
+                                  _p(dbeta), _p(workspace), _nbytes(workspace), _stream(stream)),
+           "fp8_layernorm_bwd")

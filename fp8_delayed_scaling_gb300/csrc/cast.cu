@@ -20,6 +20,8 @@
 //   amax: |x| max per thread -> warp shuffle -> one atomicMax per CTA.
 //   dbias: per-tile column sums (fp32, fixed order) to a workspace row per
 //          128-row tile, then a second kernel sums the tile rows in order.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace fp8dl {
@@ -59,11 +61,28 @@ struct RowSeg16<FP8DL_F32> {
 // Byte offset of 16-byte chunk `chunk` of staged row `r` (rows are 128 bytes).
 __device__ __forceinline__ int stage_off(int r, int chunk) { return r * CT_COLS + ((chunk ^ ((r >> 2) & 7)) << 4); }
 
-template <int XKIND, int FMT>
-__global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict__ x, int64_t rows, int64_t cols,
+// Element operation fused in front of the cast.
+enum CastOp { OP_NONE = 0, OP_GELU = 1, OP_DGELU = 2 };
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// GELU, erf form (the nn.GELU of the Transformer Engine tutorial's LayerNormMLP
+// mirror), in fp32 and rounded to bf16 like the tensor it stands for.
+__device__ __forceinline__ float gelu_bf16(float h) { return bf16_round(0.5f * h * (1.0f + erff(h * 0.70710678118654752f))); }
+
+// dh = dg * GELU'(h) = dg * (0.5 * (1 + erf(h/sqrt2)) + h * exp(-h^2/2) / sqrt(2 pi)), rounded to bf16.
+__device__ __forceinline__ float dgelu_bf16(float dg, float h) {
+    const float d = 0.5f * (1.0f + erff(h * 0.70710678118654752f)) + h * expf(-0.5f * h * h) * 0.39894228040143268f;
+    return bf16_round(dg * d);
+}
+
+template <int XKIND, int FMT, int OP>
+__global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict__ x, const void *__restrict__ aux,
+                                                          int64_t rows, int64_t cols,
                                                           const float *__restrict__ scale_p,
                                                           uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
-                                                          float *__restrict__ amax_p, float *__restrict__ ws) {
+                                                          float *__restrict__ amax_p, float *__restrict__ ws,
+                                                          uint16_t *__restrict__ pre_out) {
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
     __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
     __shared__ float red[32][CT_COLS + 1];
@@ -85,18 +104,29 @@ __global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict
         for (int j = 0; j < 16; j++) csum[j] = 0.0f;
         if (p1_ok) {
             RowSeg16<XKIND> seg[4];
-            const char *base = static_cast<const char *>(x) + ((r0 + 4 * rb) * cols + c0 + 16 * cb) * ESZ;
+            RowSeg16<XKIND> hseg[OP == OP_DGELU ? 4 : 1];
+            const int64_t eoff = (r0 + 4 * rb) * cols + c0 + 16 * cb;
+            const char *base = static_cast<const char *>(x) + eoff * ESZ;
 #pragma unroll
             for (int i = 0; i < 4; i++) seg[i].load(base + i * cols * ESZ);
+            if (OP == OP_DGELU) {
+                const char *hbase = static_cast<const char *>(aux) + eoff * ESZ;
+#pragma unroll
+                for (int i = 0; i < 4; i++) hseg[OP == OP_DGELU ? i : 0].load(hbase + i * cols * ESZ);
+            }
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 uint32_t w[4];
+                float pre[16];
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     float v[4];
 #pragma unroll
                     for (int j = 0; j < 4; j++) {
-                        const float xv = seg[i].get(4 * q + j);
+                        float xv = seg[i].get(4 * q + j);
+                        if (OP == OP_GELU) xv = gelu_bf16(xv);
+                        if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(4 * q + j));
+                        pre[4 * q + j] = xv;
                         amax = fmaxf(amax, fabsf(xv));
                         csum[4 * q + j] += xv;
                         v[j] = __fmul_rn(xv, scale);
@@ -105,6 +135,17 @@ __global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict
                 }
                 const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
                 const int r = 4 * rb + i;
+                if (OP != OP_NONE && pre_out) {
+                    uint32_t pw[8];
+#pragma unroll
+                    for (int p = 0; p < 8; p++) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(pre[2 * p], pre[2 * p + 1]);
+                        pw[p] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb);
+                    dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+                }
                 if (out) *reinterpret_cast<uint4 *>(out + (r0 + r) * cols + c0 + 16 * cb) = codes;
                 if (out_t) *reinterpret_cast<uint4 *>(stage + stage_off(r, cb)) = codes;
             }
@@ -175,7 +216,20 @@ __global__ void colsum_reduce_kernel(const float *__restrict__ ws, int64_t n_til
 template <int XKIND, int FMT>
 static void launch_cast(dim3 grid, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
                         uint8_t *out, uint8_t *out_t, float *amax, float *ws) {
-    cast_kernel<XKIND, FMT><<<grid, CT_THREADS, 0, st>>>(x, rows, cols, scale, out, out_t, amax, ws);
+    cast_kernel<XKIND, FMT, OP_NONE>
+        <<<grid, CT_THREADS, 0, st>>>(x, nullptr, rows, cols, scale, out, out_t, amax, ws, nullptr);
+}
+
+template <int OP>
+static void launch_op_cast(dim3 grid, cudaStream_t st, int fmt, const void *x, const void *aux, int64_t rows,
+                           int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *ws,
+                           uint16_t *pre_out) {
+    if (fmt == FP8DL_E4M3)
+        cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP>
+            <<<grid, CT_THREADS, 0, st>>>(x, aux, rows, cols, scale, out, out_t, amax, ws, pre_out);
+    else
+        cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP>
+            <<<grid, CT_THREADS, 0, st>>>(x, aux, rows, cols, scale, out, out_t, amax, ws, pre_out);
 }
 
 }  // namespace fp8dl
@@ -236,6 +290,69 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// GELU + cast and dGELU + cast (the LayerNormMLP activation, fused in front of
+// the FP8 cast of its output / of the gradient of its input).
+// ---------------------------------------------------------------------------
+namespace fp8dl {
+
+static fp8dl_status op_cast_common(int op, const void *x, const void *aux, int64_t rows, int64_t cols,
+                                   int32_t out_dtype, const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
+                                   float *dbias, void *workspace, size_t workspace_bytes, void *pre_out,
+                                   fp8dl_stream_t stream, const char *name) {
+    FP8DL_CHECK_ARG(x != nullptr && (op != OP_DGELU || aux != nullptr), "%s: input is NULL", name);
+    FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "%s: out_dtype must be E4M3 or E5M2", name);
+    FP8DL_CHECK_ARG(!(out || out_t) || scale != nullptr, "%s: scale is NULL but an FP8 output was requested", name);
+    FP8DL_CHECK_ARG(out || out_t || amax || dbias || pre_out, "%s: nothing to compute", name);
+    if (!dim_ok(rows, 16) || !dim_ok(cols, 16))
+        return fail(FP8DL_ERR_SHAPE, "%s: rows (%lld) and cols (%lld) must be positive multiples of 16", name,
+                    (long long)rows, (long long)cols);
+    if (!aligned16(x) || !aligned16(aux) || !aligned16(out) || !aligned16(out_t) || !aligned16(dbias) ||
+        !aligned16(pre_out))
+        return fail(FP8DL_ERR_ALIGN, "%s: pointers must be 16-byte aligned", name);
+    if (dbias) {
+        if (!workspace || workspace_bytes < fp8_cast_workspace_size(rows, cols))
+            return fail(FP8DL_ERR_WORKSPACE, "%s: dbias needs a workspace of %zu bytes", name,
+                        fp8_cast_workspace_size(rows, cols));
+        if (!aligned16(workspace)) return fail(FP8DL_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
+    }
+    int sms = 0;
+    FP8DL_TRY(current_device(nullptr, &sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    const int64_t max_ctas = (int64_t)sms * 8;
+    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
+    float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
+    uint16_t *pre = static_cast<uint16_t *>(pre_out);
+    if (op == OP_GELU)
+        launch_op_cast<OP_GELU>(grid, st, out_dtype, x, nullptr, rows, cols, scale, out, out_t, amax, ws, pre);
+    else
+        launch_op_cast<OP_DGELU>(grid, st, out_dtype, x, aux, rows, cols, scale, out, out_t, amax, ws, pre);
+    FP8DL_TRY(check_launch(name));
+    if (dbias) {
+        const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
+        colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws, n_tiles, cols, dbias);
+        FP8DL_TRY(check_launch(name));
+    }
+    return FP8DL_OK;
+}
+
+}  // namespace fp8dl
+
+extern "C" fp8dl_status fp8_gelu_cast(const void *h, int64_t rows, int64_t cols, int32_t out_dtype,
+                                      const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *g,
+                                      fp8dl_stream_t stream) {
+    return fp8dl::op_cast_common(fp8dl::OP_GELU, h, nullptr, rows, cols, out_dtype, scale, out, out_t, amax, nullptr,
+                                 nullptr, 0, g, stream, "fp8_gelu_cast");
+}
+
+extern "C" fp8dl_status fp8_dgelu_cast(const void *dg, const void *h, int64_t rows, int64_t cols, int32_t out_dtype,
+                                       const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *dbias,
+                                       void *workspace, size_t workspace_bytes, void *dh, fp8dl_stream_t stream) {
+    return fp8dl::op_cast_common(fp8dl::OP_DGELU, dg, h, rows, cols, out_dtype, scale, out, out_t, amax, dbias,
+                                 workspace, workspace_bytes, dh, stream, "fp8_dgelu_cast");
+}
 
 // ---------------------------------------------------------------------------
 // Entry point for callers that cannot allocate device memory.

@@ -239,6 +239,55 @@ fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, 
                         void *D, int32_t d_dtype, int32_t *dev_status, fp8dl_stream_t stream);
 
 /* ----------------------------------------------------------------------------
+ * LayerNormMLP pieces.  The Transformer Engine tutorial builds its blocks
+ * from te.LayerNormMLP (LayerNorm -> fc1 -> GELU -> fc2), mirrored in plain
+ * PyTorch by nn.LayerNorm and nn.GELU (erf form).  Under delayed scaling the
+ * scale of each activation's FP8 cast is known before the activation runs
+ * ("FP8 低精度训练：Transformer Engine 简析" §三.1), so each activation is fused
+ * with the cast of its output (cast semantics as fp8_cast_amax_transpose).
+ * All high-precision tensors here are bf16; mu and rsigma are fp32.
+ */
+
+/* LayerNorm forward + cast, per row of x [rows x cols] (cols <= 8192):
+ *   mu = mean(x), var = mean((x - mu)^2) (biased), rsigma = 1/sqrt(var + eps)
+ *   y = bf16((x - mu) * rsigma * gamma + beta)       (fp32 arithmetic)
+ *   out = enc(fl32(y * scale)), out_t = out^T, amax max-ed with max |y|
+ * gamma, beta [cols] bf16; mu, rsigma [rows] fp32 (for the backward);
+ * y [rows x cols] bf16 or NULL; out/out_t/amax nullable as for the cast. */
+fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const void *gamma,
+                                const void *beta, float eps, int32_t out_dtype, const float *scale,
+                                uint8_t *out, uint8_t *out_t, float *amax, float *mu, float *rsigma,
+                                void *y, fp8dl_stream_t stream);
+
+/* GELU + cast: g = bf16(0.5 * h * (1 + erf(h / sqrt2))) in fp32 arithmetic, then the
+ * cast of g (out, out_t, amax of g).  h [rows x cols] bf16 (the fc1 output);
+ * g [rows x cols] bf16 or NULL. */
+fp8dl_status fp8_gelu_cast(const void *h, int64_t rows, int64_t cols, int32_t out_dtype,
+                           const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *g,
+                           fp8dl_stream_t stream);
+
+/* dGELU + cast: dh = bf16(dg * (0.5 * (1 + erf(h/sqrt2)) + h * exp(-h^2/2) / sqrt(2 pi))),
+ * then the cast of dh (E5M2 in HYBRID) with amax, transposed copy and the
+ * bias gradient dbias = column sums of dh (workspace as for the cast).
+ * dg, h [rows x cols] bf16; dh [rows x cols] bf16 or NULL. */
+fp8dl_status fp8_dgelu_cast(const void *dg, const void *h, int64_t rows, int64_t cols, int32_t out_dtype,
+                            const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *dbias,
+                            void *workspace, size_t workspace_bytes, void *dh, fp8dl_stream_t stream);
+
+/* LayerNorm backward from the forward's mu and rsigma:
+ *   xhat = (x - mu) * rsigma, g = dy * gamma
+ *   dx = bf16(rsigma * (g - mean(g) - xhat * mean(g * xhat)))
+ *   dgamma = sum_rows dy * xhat, dbeta = sum_rows dy   (fp32 [cols], overwritten)
+ * dy, x [rows x cols] bf16, gamma [cols] bf16; workspace of
+ * fp8_layernorm_bwd_workspace_size(rows, cols) bytes. */
+size_t fp8_layernorm_bwd_workspace_size(int64_t rows, int64_t cols);
+
+fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma, const float *mu,
+                               const float *rsigma, int64_t rows, int64_t cols, void *dx, float *dgamma,
+                               float *dbeta, void *workspace, size_t workspace_bytes,
+                               fp8dl_stream_t stream);
+
+/* ----------------------------------------------------------------------------
  * Library state. */
 /* 1 if `device` is an sm_103 GPU this library can run on, else 0. */
 int32_t fp8dl_device_supported(int32_t device);
