@@ -61,6 +61,10 @@ WORKLOADS = {
     "linear_hybrid": dict(desc="te.Linear 2048 tokens 768->3072 fwd+bwd, HYBRID, history 16",
                           tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="hybrid",
                           x_dtype=torch.float32, training=True),
+    "ln_mlp": dict(desc="LayerNormMLP fwd+bwd under HYBRID delayed scaling, history 16: x bf16 [16384 x 4096], "
+                        "LayerNorm -> E4M3 cast -> fc1 4096->16384 -> GELU -> E4M3 cast -> fc2 16384->4096",
+                   tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
+                   x_dtype=torch.bfloat16, training=True, kind="lnmlp"),
     "linear_fwd": dict(desc="te.Linear 2048 tokens 768->3072 forward, E4M3, history 16",
                        tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="e4m3", x_dtype=torch.float32,
                        training=False),
@@ -76,6 +80,13 @@ def step_flops(cfg):
 def cast_bytes(cfg):
     """Algorithmic HBM bytes of all casts in one step (read once, write each output once)."""
     M = cfg["tokens"]
+    if cfg.get("kind") == "lnmlp":
+        H, F = cfg["layers"][0][1], cfg["layers"][0][2]
+        return (M * H * (2 + 2) + F * H * (2 + 2) * 2      # LN+cast of x; casts of W1 and W2 (+T)
+                + M * F * (2 + 2)                          # GELU+cast of h (+T)
+                + M * H * (2 + 2) + 4 * H                  # cast of dY (+T, dbias)
+                + M * F * (2 + 2 + 2) + 4 * F              # dGELU+cast of (dg, h) (+T, dbias)
+                + M * H * (2 + 2 + 2))                     # LayerNorm backward: read dy and x, write dx
     esz_x = 2 if cfg["x_dtype"] == torch.bfloat16 else 4
     tot = 0
     for _, k, n in cfg["layers"]:
@@ -145,6 +156,50 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+class LnMlpModel:
+    """One LayerNormMLP block (fwd+bwd) per step."""
+
+    def __init__(self, cfg, dev, seed):
+        import fp8_delayed_scaling_gb300 as fd
+        from fp8_delayed_scaling_gb300.lnmlp import Fp8LayerNormMLP, make_state
+        self.fd = fd
+        self.cfg = cfg
+        self.recipe = fd.Recipe(margin=0, interval=1, fp8_format=fd.FORMAT_HYBRID, amax_history_len=cfg["hist"])
+        self.state = make_state(self.recipe, 1, device=dev)
+        M = cfg["tokens"]
+        H, F = cfg["layers"][0][1], cfg["layers"][0][2]
+        gamma = (1.0 + wl.normal((H,), 0.1, wl.generator(seed, "gamma"))).to(torch.bfloat16).to(dev)
+        beta = torch.zeros(H, dtype=torch.bfloat16, device=dev)
+        w1 = wl.normal((F, H), 0.02, wl.generator(seed, "W1"), torch.bfloat16).to(dev)
+        w2 = wl.normal((H, F), 0.02, wl.generator(seed, "W2"), torch.bfloat16).to(dev)
+        b1 = torch.zeros(F, dtype=torch.bfloat16, device=dev)
+        b2 = torch.zeros(H, dtype=torch.bfloat16, device=dev)
+        self.blk = Fp8LayerNormMLP(self.state, 0, gamma, beta, w1, b1, w2, b2, M)
+        self.layers = [self.blk]
+        self.x = [wl.normal((M, H), 1.0, wl.generator(seed, "x"), torch.bfloat16).to(dev)]
+        self.dy = [wl.normal((M, H), 1e-3, wl.generator(seed, "dY"), torch.bfloat16).to(dev)]
+        self.step_no = 0
+        self.blk.forward(self.x[0], seed=True)
+        self.blk.backward(self.x[0], self.dy[0], seed=True)
+        self.state.update(self.step_no)
+        self.step_no += 1
+
+    def launches_per_step(self):
+        # LN+cast, W1 cast, fc1, GELU+cast, W2 cast, fc2 | dY cast+reduce, 2 GEMMs, dGELU cast+reduce,
+        # 2 GEMMs, LN bwd (3 kernels) | update
+        return 6 + 2 + 2 + 2 + 2 + 3 + 1
+
+    def step(self):
+        self.blk.forward(self.x[0])
+        self.blk.backward(self.x[0], self.dy[0])
+        self.state.update(self.step_no)
+        self.step_no += 1
+
+    def outputs(self):
+        b = self.blk
+        return [b.dw1, b.dw2, b.db1, b.db2, b.dgamma, b.dbeta, b.dx]
+
+
 class Model:
     def __init__(self, cfg, dev, seed):
         import fp8_delayed_scaling_gb300 as fd
@@ -177,6 +232,15 @@ class Model:
         per = 3 if not self.cfg["training"] else 3 + 1 + 1 + 2  # casts X, W, gemm; cast dY (+reduce), 2 gemms
         return per * len(self.layers) + 1
 
+    def outputs(self):
+        out = []
+        for lin in self.layers:
+            if self.cfg["training"]:
+                out += [lin.dw] + ([lin.db] if lin.db is not None else [])
+            else:
+                out.append(lin.y)
+        return out
+
     def step(self, timers=None):
         for lin, x in zip(self.layers, self.x):
             lin.forward(x)
@@ -187,8 +251,8 @@ class Model:
 
 
 def run_ours(args, cfg, dev, rank, world):
-    seed = 2
-    model = Model(cfg, dev, seed)
+    seed = wl.SEEDS.get(args.workload, 2)
+    model = (LnMlpModel if cfg.get("kind") == "lnmlp" else Model)(cfg, dev, seed)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -228,11 +292,15 @@ def run_ours(args, cfg, dev, rank, world):
 
 def profile_kernels(model, flush, stream, reps=5):
     """Average device time per launch class (cast / gemm / update) over `reps` steps."""
-    fd = model.fd
     import fp8_delayed_scaling_gb300.linear as L
+    import fp8_delayed_scaling_gb300.lnmlp as LM
     times = {"gemm": [], "cast": [], "update": []}
     flops_per_gemm_step = step_flops(model.cfg)
-    orig_gemm, orig_cast, orig_update = L.fp8_gemm, L.fp8_cast_amax_transpose, model.state.update
+    cast_names = ["fp8_cast_amax_transpose", "fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast",
+                  "fp8_layernorm_bwd"]
+    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM) for name in ["fp8_gemm"] + cast_names
+             if hasattr(mod, name)]
+    orig_update = model.state.update
 
     def timed(kind, fn):
         def w(*a, **k):
@@ -244,8 +312,8 @@ def profile_kernels(model, flush, stream, reps=5):
             times[kind].append((e0, e1))
         return w
 
-    L.fp8_gemm = timed("gemm", orig_gemm)
-    L.fp8_cast_amax_transpose = timed("cast", orig_cast)
+    for mod, name, fn in saved:
+        setattr(mod, name, timed("gemm" if name == "fp8_gemm" else "cast", fn))
     model.state.update = timed("update", orig_update)
     try:
         for _ in range(reps):
@@ -253,7 +321,8 @@ def profile_kernels(model, flush, stream, reps=5):
             model.step()
         torch.cuda.synchronize()
     finally:
-        L.fp8_gemm, L.fp8_cast_amax_transpose = orig_gemm, orig_cast
+        for mod, name, fn in saved:
+            setattr(mod, name, fn)
         model.state.update = orig_update
     out = {}
     for k, v in times.items():
@@ -270,14 +339,7 @@ def run_e2e(args, model, dev, stream, world):
     layer's X and dY from pinned memory, the step, D2H of every layer's dW and db."""
     hx = [x.cpu().pin_memory() for x in model.x]
     hdy = [d.cpu().pin_memory() for d in model.dy]
-    outs = []
-    for lin in model.layers:
-        if model.cfg["training"]:
-            outs.append((lin.dw, torch.empty_like(lin.dw, device="cpu").pin_memory()))
-            if lin.db is not None:
-                outs.append((lin.db, torch.empty_like(lin.db, device="cpu").pin_memory()))
-        else:
-            outs.append((lin.y, torch.empty_like(lin.y, device="cpu").pin_memory()))
+    outs = [(t, torch.empty_like(t, device="cpu").pin_memory()) for t in model.outputs()]
     h2d = sum(t.numel() * t.element_size() for t in hx + hdy)
     d2h = sum(h.numel() * h.element_size() for _, h in outs)
     steps = max(1, min(args.steps, 10))

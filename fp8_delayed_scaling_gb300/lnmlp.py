@@ -1,0 +1,146 @@
+"""te.LayerNormMLP under a DelayedScaling recipe, sequenced over the C ABI.
+
+"NVIDIA Transformer Engine 加速训练教程" uses te.LayerNormMLP: LayerNorm ->
+fc1 -> GELU -> fc2.  Under delayed scaling ("FP8 低精度训练：Transformer
+Engine 简析" §三.1, §三.3) every GEMM operand is an FP8 cast with a stored
+scale, so each activation is fused with the cast of its output:
+
+  forward   LN+cast(x)        -> q_ln, q_ln^T      (slot fc1.in)
+            cast W1           -> qW1, qW1^T        (slot fc1.w)
+            h  = fc1(q_ln, qW1) + b1               (bf16)
+            GELU+cast(h)      -> q_g, q_g^T        (slot fc2.in)
+            cast W2           -> qW2, qW2^T        (slot fc2.w)
+            y  = fc2(q_g, qW2) + b2                (bf16)
+  backward  cast dY (+db2)    -> qdY, qdY^T        (slot fc2.grad)
+            dg  = dgrad(qdY, qW2^T);  dW2 = wgrad(qdY^T, q_g^T)
+            dGELU+cast(dg, h) (+db1) -> qdh, qdh^T (slot fc1.grad)
+            dln = dgrad(qdh, qW1^T);  dW1 = wgrad(qdh^T, q_ln^T)
+            LN backward(dln, x) -> dx, dgamma, dbeta
+  update    all six slots, one launch.
+
+On the first step every slot's history is seeded with that step's own amax
+(an amax-only pass) before its cast; because each activation depends on the
+previous GEMM, the seeding is interleaved with the forward and backward.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose, fp8_cast_workspace_size,
+               fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_layernorm_bwd, fp8_layernorm_bwd_workspace_size,
+               fp8_layernorm_cast, fp8_seed_amax_history)
+
+FC1_IN, FC1_W, FC1_GRAD, FC2_IN, FC2_W, FC2_GRAD = range(6)
+SLOTS = 6
+
+
+def slot_dtypes(recipe: Recipe):
+    g = E5M2 if recipe.fp8_format == FORMAT_HYBRID else E4M3
+    return [E4M3, E4M3, g, E4M3, E4M3, g]
+
+
+def make_state(recipe: Recipe, n_blocks: int = 1, device="cuda") -> ScalingState:
+    return ScalingState(recipe, slot_dtypes(recipe) * n_blocks, device=device)
+
+
+class Fp8LayerNormMLP:
+    def __init__(self, state: ScalingState, block_index: int, gamma, beta, w1, b1, w2, b2, tokens: int,
+                 eps: float = 1e-5, keep_activations: bool = False):
+        self.state = state
+        self.base = block_index * SLOTS
+        self.recipe = state.recipe
+        self.gamma, self.beta, self.w1, self.b1, self.w2, self.b2 = gamma, beta, w1, b1, w2, b2
+        self.F, self.H = w1.shape
+        self.M = tokens
+        self.eps = eps
+        self.gfmt = E5M2 if self.recipe.fp8_format == FORMAT_HYBRID else E4M3
+        dev = w1.device
+        M, F, H = self.M, self.F, self.H
+        u8 = dict(dtype=torch.uint8, device=dev)
+        bf = dict(dtype=torch.bfloat16, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.q_ln, self.q_lnT = torch.empty((M, H), **u8), torch.empty((H, M), **u8)
+        self.mu, self.rs = torch.empty(M, **f32), torch.empty(M, **f32)
+        self.qw1, self.qw1T = torch.empty((F, H), **u8), torch.empty((H, F), **u8)
+        self.h = torch.empty((M, F), **bf)
+        self.q_g, self.q_gT = torch.empty((M, F), **u8), torch.empty((F, M), **u8)
+        self.qw2, self.qw2T = torch.empty((H, F), **u8), torch.empty((F, H), **u8)
+        self.y = torch.empty((M, H), **bf)
+        self.qdy, self.qdyT = torch.empty((M, H), **u8), torch.empty((H, M), **u8)
+        self.db2 = torch.empty(H, **f32)
+        self.dg = torch.empty((M, F), **bf)
+        self.dw2 = torch.empty((H, F), **bf)
+        self.qdh, self.qdhT = torch.empty((M, F), **u8), torch.empty((F, M), **u8)
+        self.db1 = torch.empty(F, **f32)
+        self.dln = torch.empty((M, H), **bf)
+        self.dw1 = torch.empty((F, H), **bf)
+        self.dx = torch.empty((M, H), **bf)
+        self.dgamma, self.dbeta = torch.empty(H, **f32), torch.empty(H, **f32)
+        self.ws_cast = torch.empty(max(fp8_cast_workspace_size(M, H), fp8_cast_workspace_size(M, F)), **u8)
+        self.ws_ln = torch.empty(fp8_layernorm_bwd_workspace_size(M, H), **u8)
+        self.keep = keep_activations
+        if keep_activations:  # the bf16 tensors that are cast, for inspection
+            self.y_ln = torch.empty((M, H), **bf)
+            self.g = torch.empty((M, F), **bf)
+            self.dh = torch.empty((M, F), **bf)
+        else:
+            self.y_ln = self.g = self.dh = None
+
+    def slot(self, k: int) -> int:
+        return self.base + k
+
+    def _seed(self, first: int, count: int, stream) -> None:
+        fp8_seed_amax_history(self.recipe, count, self.state.buf.data_ptr() + self.slot(first) * self.state.stride,
+                              stream=stream)
+
+    def forward(self, x: torch.Tensor, seed: bool = False, stream=None) -> torch.Tensor:
+        st = self.state
+        s = self.slot
+        if seed:
+            fp8_layernorm_cast(x, self.gamma, self.beta, self.eps, E4M3, None, self.mu, self.rs,
+                               amax=st.amax(s(FC1_IN)), stream=stream)
+            fp8_cast_amax_transpose(self.w1, E4M3, None, amax=st.amax(s(FC1_W)), stream=stream)
+            self._seed(FC1_IN, 2, stream)
+        fp8_layernorm_cast(x, self.gamma, self.beta, self.eps, E4M3, st.scale(s(FC1_IN)), self.mu, self.rs,
+                           out=self.q_ln, out_t=self.q_lnT, amax=st.amax(s(FC1_IN)), y=self.y_ln, stream=stream)
+        fp8_cast_amax_transpose(self.w1, E4M3, st.scale(s(FC1_W)), out=self.qw1, out_t=self.qw1T,
+                                amax=st.amax(s(FC1_W)), stream=stream)
+        fp8_gemm(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), st.scale_inv(s(FC1_W)), self.h,
+                 bias=self.b1, stream=stream)
+        if seed:
+            fp8_gelu_cast(self.h, E4M3, None, amax=st.amax(s(FC2_IN)), g=None, stream=stream)
+            fp8_cast_amax_transpose(self.w2, E4M3, None, amax=st.amax(s(FC2_W)), stream=stream)
+            self._seed(FC2_IN, 2, stream)
+        fp8_gelu_cast(self.h, E4M3, st.scale(s(FC2_IN)), out=self.q_g, out_t=self.q_gT, amax=st.amax(s(FC2_IN)),
+                      g=self.g, stream=stream)
+        fp8_cast_amax_transpose(self.w2, E4M3, st.scale(s(FC2_W)), out=self.qw2, out_t=self.qw2T,
+                                amax=st.amax(s(FC2_W)), stream=stream)
+        fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), st.scale_inv(s(FC2_W)), self.y,
+                 bias=self.b2, stream=stream)
+        return self.y
+
+    def backward(self, x: torch.Tensor, dy: torch.Tensor, seed: bool = False, stream=None):
+        st = self.state
+        s = self.slot
+        g = self.gfmt
+        if seed:
+            fp8_cast_amax_transpose(dy, g, None, amax=st.amax(s(FC2_GRAD)), stream=stream)
+            self._seed(FC2_GRAD, 1, stream)
+        fp8_cast_amax_transpose(dy, g, st.scale(s(FC2_GRAD)), out=self.qdy, out_t=self.qdyT,
+                                amax=st.amax(s(FC2_GRAD)), dbias=self.db2, workspace=self.ws_cast, stream=stream)
+        fp8_gemm(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_W)), self.dg,
+                 stream=stream)
+        fp8_gemm(self.qdyT, g, self.q_gT, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_IN)), self.dw2,
+                 stream=stream)
+        if seed:
+            fp8_dgelu_cast(self.dg, self.h, g, None, amax=st.amax(s(FC1_GRAD)), stream=stream)
+            self._seed(FC1_GRAD, 1, stream)
+        fp8_dgelu_cast(self.dg, self.h, g, st.scale(s(FC1_GRAD)), out=self.qdh, out_t=self.qdhT,
+                       amax=st.amax(s(FC1_GRAD)), dbias=self.db1, workspace=self.ws_cast, dh=self.dh, stream=stream)
+        fp8_gemm(self.qdh, g, self.qw1T, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_W)), self.dln,
+                 stream=stream)
+        fp8_gemm(self.qdhT, g, self.q_lnT, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_IN)), self.dw1,
+                 stream=stream)
+        fp8_layernorm_bwd(self.dln, x, self.gamma, self.mu, self.rs, self.dx, self.dgamma, self.dbeta, self.ws_ln,
+                          stream=stream)
+        return self.dx
