@@ -2,10 +2,13 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = one pass of the whole hot path over one batch of synthetic input:
-for every layer of the workload, the fused casts (+amax, +transposed copies,
-+bias gradient), the forward, dgrad and wgrad FP8 GEMMs, and one delayed
-scale update of all slots.  Inputs are resident in HBM before timing; the L2
+One step = one pass of the whole hot path over one batch of synthetic input.
+The default workload is the LayerNormMLP block (16384 tokens, 4096 -> 16384 ->
+4096, HYBRID delayed scaling, history 16): LayerNorm+cast, the weight casts,
+fc1, GELU+cast, fc2, the grad_output cast with bias gradient, dgrad and wgrad
+of both GEMMs, dGELU+cast with bias gradient, the LayerNorm backward, and one
+delayed scale update of all six slots.  `--workload llama_proj | mx_mlp |
+linear_hybrid | linear_fwd` selects the other workloads.  Inputs are resident in HBM before timing; the L2
 is flushed (a 512 MB write) between timed steps, outside the step events.
 
 Prints one JSON line (rank 0).  `value` is TFLOP/s of algorithmic GEMM work
@@ -65,6 +68,10 @@ WORKLOADS = {
                         "LayerNorm -> E4M3 cast -> fc1 4096->16384 -> GELU -> E4M3 cast -> fc2 16384->4096",
                    tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
                    x_dtype=torch.bfloat16, training=True, kind="lnmlp"),
+    "mx_mlp": dict(desc="MXFP8 (1x32 E8M0 blocks) MLP fwd+bwd: 16384 tokens, 8192 -> 28672 -> 8192, X with per-channel "
+                        "factors log-uniform in [1e-3, 1e2]", tokens=16384, layers=[("up", 8192, 28672),
+                                                                                ("down", 28672, 8192)],
+                   hist=0, fmt="mxfp8", x_dtype=torch.bfloat16, training=True, kind="mx"),
     "linear_fwd": dict(desc="te.Linear 2048 tokens 768->3072 forward, E4M3, history 16",
                        tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="e4m3", x_dtype=torch.float32,
                        training=False),
@@ -80,6 +87,8 @@ def step_flops(cfg):
 def cast_bytes(cfg):
     """Algorithmic HBM bytes of all casts in one step (read once, write each output once)."""
     M = cfg["tokens"]
+    if cfg.get("kind") == "mx":  # quantise X, W, dY of each layer: read 2 B, write 2 B + 2/32 B of scales
+        return sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) for _, k, n in cfg["layers"])
     if cfg.get("kind") == "lnmlp":
         H, F = cfg["layers"][0][1], cfg["layers"][0][2]
         return (M * H * (2 + 2) + F * H * (2 + 2) * 2      # LN+cast of x; casts of W1 and W2 (+T)
@@ -117,7 +126,7 @@ class ClockSampler:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -200,6 +209,40 @@ class LnMlpModel:
         return [b.dw1, b.dw2, b.db1, b.db2, b.dgamma, b.dbeta, b.dx]
 
 
+class MxModel:
+    """MXFP8 MLP: up (8192->28672) feeding down (28672->8192), fwd+bwd per step."""
+
+    def __init__(self, cfg, dev, seed):
+        import fp8_delayed_scaling_gb300 as fd
+        from fp8_delayed_scaling_gb300.mxlinear import MxLinear
+        self.fd = fd
+        self.cfg = cfg
+        M = cfg["tokens"]
+        (_, H, F), _ = cfg["layers"]
+        self.up = MxLinear(wl.normal((F, H), 0.02, wl.generator(seed, "W1"), torch.bfloat16).to(dev), None, M)
+        self.down = MxLinear(wl.normal((H, F), 0.02, wl.generator(seed, "W2"), torch.bfloat16).to(dev), None, M)
+        self.layers = [self.up, self.down]
+        self.x = [wl.channel_scaled_normal(M, H, wl.generator(seed, "X")).to(dev)]
+        self.dy = [wl.normal((M, H), 1.0, wl.generator(seed, "dY"), torch.bfloat16).to(dev)]
+
+        class _NoState:
+            def update(self, step):
+                pass
+        self.state = _NoState()
+
+    def launches_per_step(self):
+        return 2 * (2 + 1) + 2 * (1 + 2)  # per layer: quantise X, W, GEMM; quantise dY, 2 GEMMs
+
+    def step(self):
+        h = self.up.forward(self.x[0])
+        self.down.forward(h)
+        dh, _, _ = self.down.backward(self.dy[0])
+        self.up.backward(dh)
+
+    def outputs(self):
+        return [self.up.dw, self.down.dw, self.up.dx]
+
+
 class Model:
     def __init__(self, cfg, dev, seed):
         import fp8_delayed_scaling_gb300 as fd
@@ -252,7 +295,7 @@ class Model:
 
 def run_ours(args, cfg, dev, rank, world):
     seed = wl.SEEDS.get(args.workload, 2)
-    model = (LnMlpModel if cfg.get("kind") == "lnmlp" else Model)(cfg, dev, seed)
+    model = {"lnmlp": LnMlpModel, "mx": MxModel}.get(cfg.get("kind"), Model)(cfg, dev, seed)
     stream = torch.cuda.current_stream()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -294,11 +337,12 @@ def profile_kernels(model, flush, stream, reps=5):
     """Average device time per launch class (cast / gemm / update) over `reps` steps."""
     import fp8_delayed_scaling_gb300.linear as L
     import fp8_delayed_scaling_gb300.lnmlp as LM
+    import fp8_delayed_scaling_gb300.mxlinear as MX
     times = {"gemm": [], "cast": [], "update": []}
     flops_per_gemm_step = step_flops(model.cfg)
     cast_names = ["fp8_cast_amax_transpose", "fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast",
-                  "fp8_layernorm_bwd"]
-    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM) for name in ["fp8_gemm"] + cast_names
+                  "fp8_layernorm_bwd", "mxfp8_quantize"]
+    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in ["fp8_gemm", "mxfp8_gemm"] + cast_names
              if hasattr(mod, name)]
     orig_update = model.state.update
 
@@ -313,7 +357,7 @@ def profile_kernels(model, flush, stream, reps=5):
         return w
 
     for mod, name, fn in saved:
-        setattr(mod, name, timed("gemm" if name == "fp8_gemm" else "cast", fn))
+        setattr(mod, name, timed("gemm" if name.endswith("gemm") else "cast", fn))
     model.state.update = timed("update", orig_update)
     try:
         for _ in range(reps):
@@ -484,9 +528,9 @@ def run_only(args, dev):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama_proj", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="ln_mlp", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only", default=None, choices=["gemm", "cast", "mxq", "mxgemm"])
     ap.add_argument("--shape", default="8192,12288,4096")
@@ -538,7 +582,7 @@ def main():
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8(e4m3/e5m2)->fp32acc->bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": config,
-        "roofline": {"bound": "tensor", "kernel": "fp8_gemm", "achieved": round(achieved, 1),
+        "roofline": {"bound": "tensor", "kernel": "mxfp8_gemm" if cfg.get("kind") == "mx" else "fp8_gemm", "achieved": round(achieved, 1),
                      "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
                      "traffic": None,
                      "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},

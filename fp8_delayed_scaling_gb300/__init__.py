@@ -59,6 +59,7 @@ _SIGS = {
     "fp8_dgelu_cast": (_i32, [_vp, _vp, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "fp8_layernorm_bwd_workspace_size": (_sz, [_i64, _i64]),
     "fp8_layernorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fp8dl_wait_selftest": (_i32, [_i64, _i32, _vp, _vp]),
     "fp8dl_device_supported": (_i32, [_i32]),
     "fp8dl_last_error": (ctypes.c_char_p, []),
     "fp8dl_version": (_i32, []),
@@ -117,6 +118,12 @@ def fp8dl_version() -> int:
 
 def fp8dl_device_supported(device: int = 0) -> bool:
     return bool(_lib.fp8dl_device_supported(device))
+
+
+def fp8dl_wait_selftest(budget_cycles: int, arrive_first: bool, dev_status, stream=None) -> None:
+    """Run the bounded-wait self-test; the outcome is written to dev_status (device int32)."""
+    _check(_lib.fp8dl_wait_selftest(int(budget_cycles), 1 if arrive_first else 0, _p(dev_status), _stream(stream)),
+           "fp8dl_wait_selftest")
 
 
 def fp8dl_slot_stride(amax_history_len: int) -> int:

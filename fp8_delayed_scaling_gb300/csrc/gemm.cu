@@ -262,6 +262,22 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounded wait: one thread waits, through mbar_wait, on a
+// barrier phase that completes only if `arrive_first` is set.
+// ---------------------------------------------------------------------------
+__global__ void wait_selftest_kernel(long long budget, int arrive_first, int32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        mbar_fence_init();
+        if (arrive_first) mbar_arrive(smem_u32(&bar));
+        if (mbar_wait(smem_u32(&bar), 0, &abort_flag, status, budget)) atomicExch(reinterpret_cast<int *>(status), 0);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host
 // ---------------------------------------------------------------------------
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
@@ -305,6 +321,17 @@ static fp8dl_status check_gemm_common(int64_t M, int64_t N, int64_t K, int64_t m
 }  // namespace fp8dl
 
 using namespace fp8dl;
+
+extern "C" fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arrive_first, int32_t *dev_status,
+                                            fp8dl_stream_t stream) {
+    FP8DL_CHECK_ARG(dev_status != nullptr, "dev_status is NULL");
+    FP8DL_CHECK_ARG(budget_cycles >= 0 && budget_cycles <= (int64_t(1) << 32), "budget_cycles must be in [0, 2^32]");
+    if (!aligned16(dev_status)) return fail(FP8DL_ERR_ALIGN, "dev_status must be 16-byte aligned");
+    FP8DL_TRY(current_device(nullptr, nullptr));
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)budget_cycles, arrive_first ? 1 : 0,
+                                                             dev_status);
+    return check_launch("fp8dl_wait_selftest");
+}
 
 extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
                                  int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,

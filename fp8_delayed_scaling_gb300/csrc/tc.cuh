@@ -50,7 +50,7 @@ constexpr long long kWaitBudgetCycles = 1ll << 33;
 // reported a timeout through *status, or when the budget runs out — then it
 // sets the abort flag and reports FP8DL_ERR_TIMEOUT.  Never traps.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *status) {
+                                          int32_t *status, long long budget = kWaitBudgetCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t i = 1;; ++i) {
@@ -61,7 +61,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                 *abort_flag = 1;
                 return false;
             }
-            if (clock64() - t0 > kWaitBudgetCycles) {
+            if (clock64() - t0 > budget) {
                 *abort_flag = 1;
                 if (status) atomicExch(reinterpret_cast<int *>(status), (int)FP8DL_ERR_TIMEOUT);
                 return false;

@@ -293,6 +293,15 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
 int32_t fp8dl_device_supported(int32_t device);
 /* Last error message of the calling thread ("" if none). */
 const char *fp8dl_last_error(void);
+/* Self-test of failure detection without a GPU fault.  One thread waits,
+ * through the same bounded wait the GEMM pipelines use, on a shared-memory
+ * barrier phase; if arrive_first is 0 nothing ever completes it, the wait
+ * gives up after budget_cycles SM clock cycles (<= 2^32), writes
+ * FP8DL_ERR_TIMEOUT into *dev_status and the kernel returns; with
+ * arrive_first = 1 the phase completes and *dev_status is set to FP8DL_OK.
+ * The CUDA context stays usable either way. */
+fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arrive_first, int32_t *dev_status,
+                                 fp8dl_stream_t stream);
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t fp8dl_version(void);
 
