@@ -26,6 +26,7 @@
 // Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
 // copies and MMAs, frees TMEM and exits, reporting through *status.
 #include <cuda_bf16.h>
+#include <stdlib.h>
 
 #include "tc.cuh"
 
@@ -261,6 +262,244 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// 2-SM variant: a cluster of two CTAs (one per SM) computes a 256x256 tile with
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=32).  Each CTA TMA-loads only its
+// own halves — 128 rows of A and 128 rows of B (its half of N) — so every SM
+// moves 32 KB per stage instead of 48 KB, and the shared-memory traffic per
+// tensor cycle drops accordingly.  No data is multicast.
+//   - Both CTAs' loads complete on the even ("leader") CTA's full barrier.
+//   - The leader's single MMA thread issues for the pair; its commits arrive on
+//     the empty/accumulator barriers at the same offset in both CTAs.
+//   - Each CTA's epilogue drains its own 128 accumulator rows and releases
+//     the accumulator on the leader's barrier (a remote arrive from the peer).
+// ---------------------------------------------------------------------------
+namespace g2 {
+constexpr int BM = 128, BN = 256, BNH = 128, BK = 128;  // per-CTA rows of A and of B
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK, B_BYTES = BNH * BK, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int GROUP_M = 8;  // in 256-row pair tiles
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+}  // namespace g2
+
+__device__ __forceinline__ void tile_coords2(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t &tm,
+                                             int64_t &tn) {
+    const int64_t per_group = (int64_t)g2::GROUP_M * tiles_n;
+    const int64_t g = tile / per_group;
+    const int64_t first_m = g * g2::GROUP_M;
+    const int64_t gsize = min((int64_t)g2::GROUP_M, tiles_m - first_m);
+    const int64_t local = tile - g * per_group;
+    tm = first_m + local % gsize;
+    tn = local / gsize;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
+    fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                         const GemmArgs args) {
+    using namespace g2;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    uint8_t *bar_area = smem + STAGES * STAGE_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(bar_area);
+    uint64_t *empty = full + STAGES;
+    uint64_t *tfull = empty + STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int64_t tiles_m = (args.M + 2 * BM - 1) / (2 * BM), tiles_n = (args.N + BN - 1) / BN;
+    const int64_t tiles = tiles_m * tiles_n;
+    const int num_kb = (int)((args.K + BK - 1) / BK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; s++) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; a++) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 8);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+        tma_prefetch_map(&tmap_a);
+        tma_prefetch_map(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised before any cross-CTA signal
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {  // ------------------------------------------------ producer (both CTAs)
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
+                int64_t tm, tn;
+                tile_coords2(tile, tiles_m, tiles_n, tm, tn);
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = smem_u32(&full[s]);
+                    const uint32_t fb = mapa_shared(fb_local, 0);
+                    if (leader) mbar_expect_tx(fb_local, 2 * STAGE_BYTES);
+                    uint8_t *sa = smem + s * STAGE_BYTES;
+                    tma_load_2d_pair(smem_u32(sa), &tmap_a, fb, kb * BK, (int32_t)(tm * 2 * BM + rank * BM));
+                    tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmap_b, fb, kb * BK,
+                                     (int32_t)(tn * BN + rank * BNH));
+                    issued++;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+            }
+            if (!ok && leader) {
+                for (int64_t i = issued - 1; i >= 0 && i >= issued - STAGES; i--)
+                    mbar_drain(smem_u32(&full[i % STAGES]), (uint32_t)((i / STAGES) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {  // ----------------------------------------- MMA issuer (leader only)
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            bool ok = true, any = false;
+            uint32_t last_bar = 0, last_par = 0;
+            for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
+                if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1, abort_flag, args.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < num_kb; kb++) {
+                    if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, args.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; kk++)
+                        umma_f8f6f4_pair(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
+                                         args.idesc, (kb | kk) != 0);
+                    umma_commit_pair(smem_u32(&empty[s]), 0x3);
+                    any = true;
+                    last_bar = smem_u32(&empty[s]);
+                    last_par = ph;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(smem_u32(&tfull[acc]), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    aph ^= 1;
+                }
+            }
+            if (!ok && any) mbar_drain(last_bar, last_par);
+        }
+    } else {  // ------------------------------------------------------------ epilogue (both CTAs)
+        const int q = warp & 3;
+        const float sc = __fmul_rn(__ldg(args.a_scale_inv), __ldg(args.b_scale_inv));
+        const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int64_t tile = pair; tile < tiles; tile += npairs) {
+            int64_t tm, tn;
+            tile_coords2(tile, tiles_m, tiles_n, tm, tn);
+            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
+            tc_fence_after();
+            const int64_t row = tm * 2 * BM + rank * BM + 32 * q + lane;
+            const bool row_ok = row < args.M;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; c++) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * BN + c * 32) + ((uint32_t)(32 * q) << 16), r);
+                tmem_ld_wait();
+                const int64_t n0 = tn * BN + c * 32;
+                if (row_ok && n0 < args.N) {
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * sc;
+                    if (args.bias_dtype >= 0) {
+#pragma unroll
+                        for (int j = 0; j < 32; j++)
+                            if (n0 + j < args.N) v[j] += load_bias(args.bias, args.bias_dtype, n0 + j);
+                    }
+                    if (args.d_dtype == FP8DL_BF16) {
+                        __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.D) + row * args.N + n0;
+#pragma unroll
+                        for (int g = 0; g < 4; g++) {
+                            if (n0 + 8 * g < args.N) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int p = 0; p < 4; p++) {
+                                    __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * g + 2 * p], v[8 * g + 2 * p + 1]);
+                                    w[p] = *reinterpret_cast<uint32_t *>(&h);
+                                }
+                                *reinterpret_cast<uint4 *>(drow + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    } else {
+                        float *drow = static_cast<float *>(args.D) + row * args.N + n0;
+#pragma unroll
+                        for (int g = 0; g < 8; g++)
+                            if (n0 + 4 * g < args.N)
+                                *reinterpret_cast<float4 *>(drow + 4 * g) =
+                                    make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader)
+                    mbar_arrive(smem_u32(&tempty[acc]));
+                else
+                    mbar_arrive_cluster(tempty_leader[acc]);
+            }
+            if (++acc == 2) {
+                acc = 0;
+                aph ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // the peer's shared memory and TMEM stay live until the pair is done
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Self-test of the bounded wait: one thread waits, through mbar_wait, on a
 // barrier phase that completes only if `arrive_first` is set.
@@ -344,19 +583,24 @@ extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_
     int dev = 0, sms = 0;
     FP8DL_TRY(current_device(&dev, &sms));
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ta2, tb2;
     FP8DL_TRY(encode_tmap_2d_u8(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, g1::BK, g1::BM,
                                 CU_TENSOR_MAP_SWIZZLE_128B));
     FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g1::BK, g1::BN,
+                                CU_TENSOR_MAP_SWIZZLE_128B));
+    ta2 = ta;  // the pair kernel loads 128-row boxes of both operands
+    FP8DL_TRY(encode_tmap_2d_u8(&tb2, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g2::BK, g2::BNH,
                                 CU_TENSOR_MAP_SWIZZLE_128B));
     GemmArgs args;
     args.M = M;
     args.N = N;
     args.K = K;
     // Instruction descriptor, kind::f8f6f4: D fp32 (bit 4), A type bits 7-9, B type bits 10-12
-    // (0 = E4M3, 1 = E5M2), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28.
-    args.idesc = (1u << 4) | ((uint32_t)a_dtype << 7) | ((uint32_t)b_dtype << 10) | ((uint32_t)(g1::BN >> 3) << 17) |
-                 ((uint32_t)(g1::BM >> 4) << 24);
+    // (0 = E4M3, 1 = E5M2), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28
+    // (M = 128 for one CTA, 256 for a CTA pair; N = 256 either way).
+    const uint32_t idesc_base = (1u << 4) | ((uint32_t)a_dtype << 7) | ((uint32_t)b_dtype << 10) |
+                                ((uint32_t)(g1::BN >> 3) << 17);
+    args.idesc = idesc_base | ((uint32_t)(g1::BM >> 4) << 24);
     args.a_scale_inv = a_scale_inv;
     args.b_scale_inv = b_scale_inv;
     args.bias = bias;
@@ -366,11 +610,40 @@ extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_
     args.status = dev_status;
 
     static bool attr_set[64] = {};
+    static int pair_clusters[64] = {};
     if (!attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              g1::SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     g2::SMEM_BYTES);
         if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        // how many CTA pairs can be resident at once
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(sms / 2 * 2), 1, 1);
+        cfg.blockDim = dim3(g2::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = g2::SMEM_BYTES;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_pair_kernel, &cfg);
+        if (e != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            clusters = 0;  // the pair kernel is not used on this device
+        }
+        pair_clusters[dev] = clusters;
         attr_set[dev] = true;
+    }
+    // Variant: the 2-SM pair kernel when the problem has two 128-row halves per tile
+    // and pairs can be resident; FP8DL_GEMM_VARIANT=1sm|2sm overrides (testing).
+    const char *v = getenv("FP8DL_GEMM_VARIANT");
+    const int forced = (v && v[0] == '1') ? 1 : (v && v[0] == '2') ? 2 : 0;
+    const bool use_pair = pair_clusters[dev] > 0 && (forced == 2 || (forced == 0 && M > g1::BM));
+    if (use_pair) {
+        args.idesc = idesc_base | ((uint32_t)(2 * g2::BM >> 4) << 24);
+        const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
+        const int64_t pairs = tiles < pair_clusters[dev] ? tiles : pair_clusters[dev];
+        fp8_gemm_pair_kernel<<<(unsigned)(2 * pairs), g2::THREADS, g2::SMEM_BYTES, (cudaStream_t)stream>>>(ta2, tb2,
+                                                                                                             args);
+        return check_launch("fp8_gemm(pair)");
     }
     const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);

@@ -38,9 +38,16 @@ SHAPES = [(128, 256, 128), (16, 16, 16), (48, 80, 32), (144, 272, 400), (256, 51
           (2048, 3072, 768), (1000 // 16 * 16, 2000 // 16 * 16, 1024)]
 
 
+@pytest.fixture(params=["1sm", "2sm"])
+def variant(request, monkeypatch):
+    """Run a test with the one-CTA kernel and with the CTA-pair kernel."""
+    monkeypatch.setenv("FP8DL_GEMM_VARIANT", request.param)
+    return request.param
+
+
 @pytest.mark.parametrize("M,N,K", SHAPES)
 @pytest.mark.parametrize("afmt,bfmt", [(0, 0), (1, 0), (0, 1)])
-def test_gemm_full_parity(M, N, K, afmt, bfmt):
+def test_gemm_full_parity(M, N, K, afmt, bfmt, variant):
     dev = gpu()
     rng = np.random.default_rng(M * 7 + N * 3 + K + 10 * afmt + bfmt)
     A = _codes(rng, afmt, (M, K))
@@ -58,7 +65,7 @@ def test_gemm_full_parity(M, N, K, afmt, bfmt):
 
 @pytest.mark.parametrize("bias_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("d_dtype", [torch.bfloat16, torch.float32])
-def test_gemm_bias_and_output_types(bias_dtype, d_dtype):
+def test_gemm_bias_and_output_types(bias_dtype, d_dtype, variant):
     dev = gpu()
     rng = np.random.default_rng(3)
     M, N, K = 272, 528, 256
@@ -74,7 +81,7 @@ def test_gemm_bias_and_output_types(bias_dtype, d_dtype):
     check_gemm(D, ref, absr, ms.ravel(), ns.ravel())
 
 
-def test_gemm_identity_is_exact():
+def test_gemm_identity_is_exact(variant):
     """A * I^T with I = identity in E4M3 (code 0x38 = 1.0) returns A exactly."""
     dev = gpu()
     rng = np.random.default_rng(5)
@@ -86,7 +93,7 @@ def test_gemm_identity_is_exact():
     assert np.array_equal(D.cpu().numpy().astype(np.float64), oracle.decode_table(0)[A])
 
 
-def test_gemm_large_sampled():
+def test_gemm_large_sampled(variant):
     """A full-size projection shape (8192 x 12288 x 4096), sampled output elements."""
     dev = gpu()
     rng = np.random.default_rng(8)
