@@ -486,6 +486,43 @@ def run_only(args, dev):
             Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, generator=g).to(dev)
             fn = lambda: fd.mxfp8_gemm(A, As, B, Bs, D)  # noqa: E731
         work, unit = 2.0 * M * N * K, "TFLOP/s"
+    elif args.only in ("gelu", "dgelu", "ln", "lnbwd"):
+        R, C = shape
+        x = wl.normal((R, C), 2.0, g, torch.bfloat16).to(dev)
+        sc = torch.ones(1, dtype=torch.float32, device=dev)
+        am = torch.zeros(1, dtype=torch.float32, device=dev)
+        q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+        qt = torch.empty((C, R), dtype=torch.uint8, device=dev)
+        if args.only == "gelu":
+            fn = lambda: fd.fp8_gelu_cast(x, fd.E4M3, sc, out=q, out_t=qt, amax=am)  # noqa: E731
+            work = R * C * (2 + 1 + 1)
+        elif args.only == "dgelu":
+            dgt = wl.normal((R, C), 1e-3, g, torch.bfloat16).to(dev)
+            db = torch.empty(C, dtype=torch.float32, device=dev)
+            ws = torch.empty(fd.fp8_cast_workspace_size(R, C), dtype=torch.uint8, device=dev)
+            fn = lambda: fd.fp8_dgelu_cast(dgt, x, fd.E5M2, sc, out=q, out_t=qt, amax=am, dbias=db,  # noqa: E731
+                                           workspace=ws)
+            work = R * C * (2 + 2 + 1 + 1) + 4 * C
+        elif args.only == "ln":
+            gam = torch.ones(C, dtype=torch.bfloat16, device=dev)
+            bet = torch.zeros(C, dtype=torch.bfloat16, device=dev)
+            mu = torch.empty(R, dtype=torch.float32, device=dev)
+            rs = torch.empty(R, dtype=torch.float32, device=dev)
+            fn = lambda: fd.fp8_layernorm_cast(x, gam, bet, 1e-5, fd.E4M3, sc, mu, rs, out=q, out_t=qt,  # noqa: E731
+                                               amax=am)
+            work = R * C * (2 + 1 + 1) + 8 * R
+        else:
+            gam = torch.ones(C, dtype=torch.bfloat16, device=dev)
+            mu = torch.zeros(R, dtype=torch.float32, device=dev)
+            rs = torch.ones(R, dtype=torch.float32, device=dev)
+            dyt = wl.normal((R, C), 1e-3, g, torch.bfloat16).to(dev)
+            dx = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
+            dgm = torch.empty(C, dtype=torch.float32, device=dev)
+            dbt = torch.empty(C, dtype=torch.float32, device=dev)
+            ws = torch.empty(fd.fp8_layernorm_bwd_workspace_size(R, C), dtype=torch.uint8, device=dev)
+            fn = lambda: fd.fp8_layernorm_bwd(dyt, x, gam, mu, rs, dx, dgm, dbt, ws)  # noqa: E731
+            work = R * C * (2 + 2 + 2) + 8 * C
+        unit = "GB/s"
     else:
         R, C = shape
         x = wl.normal((R, C), 1.0, g, torch.bfloat16).to(dev)
@@ -532,7 +569,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="ln_mlp", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default=None, choices=["gemm", "cast", "mxq", "mxgemm"])
+    ap.add_argument("--only", default=None, choices=["gemm", "cast", "mxq", "mxgemm", "gelu", "dgelu", "ln", "lnbwd"])
     ap.add_argument("--shape", default="8192,12288,4096")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -62,22 +62,54 @@ struct RowSeg16<FP8DL_F32> {
 __device__ __forceinline__ int stage_off(int r, int chunk) { return r * CT_COLS + ((chunk ^ ((r >> 2) & 7)) << 4); }
 
 // Element operation fused in front of the cast.
-enum CastOp { OP_NONE = 0, OP_GELU = 1, OP_DGELU = 2 };
+enum CastOp { OP_NONE = 0, OP_GELU = 1, OP_DGELU = 2, OP_LAYERNORM = 3 };
+
+// Extra inputs of the element operation: h for dGELU; per-row mean/rsigma and
+// per-column gamma/beta (bf16) for LayerNorm.
+struct OpArgs {
+    const void *aux;
+    const float *mu, *rs;
+    const uint16_t *gamma, *beta;
+};
 
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-// GELU, erf form (the nn.GELU of the Transformer Engine tutorial's LayerNormMLP
-// mirror), in fp32 and rounded to bf16 like the tensor it stands for.
-__device__ __forceinline__ float gelu_bf16(float h) { return bf16_round(0.5f * h * (1.0f + erff(h * 0.70710678118654752f))); }
+// Standard normal CDF Phi(x) and density phi(x), the two pieces of the erf
+// GELU (GELU(h) = h * Phi(h), Phi(h) = (1 + erf(h / sqrt2)) / 2) and of its
+// derivative (Phi(h) + h * phi(h)).  Phi by Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 26.2.17: for x >= 0,
+//   Phi(x) = 1 - phi(x) * (b1 t + b2 t^2 + b3 t^3 + b4 t^4 + b5 t^5) + eps,
+//   t = 1 / (1 + p x),  |eps| < 7.5e-8,
+// and Phi(-x) = 1 - Phi(x).  With the fast exponential and reciprocal the total
+// absolute error of Phi stays below 3e-7; the result is rounded to bf16.
+__device__ __forceinline__ void normal_cdf_pdf(float x, float &cdf, float &pdf) {
+    const float ax = fabsf(x);
+    pdf = 0.3989422804f * __expf(-0.5f * x * x);
+    const float t = __fdividef(1.0f, fmaf(0.2316419f, ax, 1.0f));
+    float poly = fmaf(t, 1.330274429f, -1.821255978f);
+    poly = fmaf(t, poly, 1.781477937f);
+    poly = fmaf(t, poly, -0.356563782f);
+    poly = fmaf(t, poly, 0.319381530f);
+    const float tail = pdf * poly * t;  // = Phi(-|x|)
+    cdf = x >= 0.0f ? 1.0f - tail : tail;
+}
 
-// dh = dg * GELU'(h) = dg * (0.5 * (1 + erf(h/sqrt2)) + h * exp(-h^2/2) / sqrt(2 pi)), rounded to bf16.
+// GELU(h) = h * Phi(h), rounded to bf16 like the tensor it stands for.
+__device__ __forceinline__ float gelu_bf16(float h) {
+    float cdf, pdf;
+    normal_cdf_pdf(h, cdf, pdf);
+    return bf16_round(h * cdf);
+}
+
+// dh = dg * GELU'(h) = dg * (Phi(h) + h * phi(h)), rounded to bf16.
 __device__ __forceinline__ float dgelu_bf16(float dg, float h) {
-    const float d = 0.5f * (1.0f + erff(h * 0.70710678118654752f)) + h * expf(-0.5f * h * h) * 0.39894228040143268f;
-    return bf16_round(dg * d);
+    float cdf, pdf;
+    normal_cdf_pdf(h, cdf, pdf);
+    return bf16_round(dg * fmaf(h, pdf, cdf));
 }
 
 template <int XKIND, int FMT, int OP>
-__global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict__ x, const void *__restrict__ aux,
+__global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_NONE ? 3 : (XKIND == FP8DL_BF16 ? 4 : 2)) cast_kernel(const void *__restrict__ x, const OpArgs op,
                                                           int64_t rows, int64_t cols,
                                                           const float *__restrict__ scale_p,
                                                           uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
@@ -85,7 +117,7 @@ __global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict
                                                           uint16_t *__restrict__ pre_out) {
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
     __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
-    __shared__ float red[32][CT_COLS + 1];
+    __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // per-warp column partials (dbias)
 
     const int t = threadIdx.x;
     const int cb = t & 7, rb = t >> 3;                               // phase 1
@@ -109,50 +141,84 @@ __global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict
             const char *base = static_cast<const char *>(x) + eoff * ESZ;
 #pragma unroll
             for (int i = 0; i < 4; i++) seg[i].load(base + i * cols * ESZ);
+            float ln_mu[4], ln_rs[4];
+            uint32_t ln_g[8], ln_b[8];
+            if (OP == OP_LAYERNORM) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    ln_mu[i] = __ldg(op.mu + r0 + 4 * rb + i);
+                    ln_rs[i] = __ldg(op.rs + r0 + 4 * rb + i);
+                }
+                const uint4 g0 = __ldg(reinterpret_cast<const uint4 *>(op.gamma + c0 + 16 * cb));
+                const uint4 g1 = __ldg(reinterpret_cast<const uint4 *>(op.gamma + c0 + 16 * cb + 8));
+                const uint4 b0 = __ldg(reinterpret_cast<const uint4 *>(op.beta + c0 + 16 * cb));
+                const uint4 b1 = __ldg(reinterpret_cast<const uint4 *>(op.beta + c0 + 16 * cb + 8));
+                ln_g[0] = g0.x; ln_g[1] = g0.y; ln_g[2] = g0.z; ln_g[3] = g0.w;
+                ln_g[4] = g1.x; ln_g[5] = g1.y; ln_g[6] = g1.z; ln_g[7] = g1.w;
+                ln_b[0] = b0.x; ln_b[1] = b0.y; ln_b[2] = b0.z; ln_b[3] = b0.w;
+                ln_b[4] = b1.x; ln_b[5] = b1.y; ln_b[6] = b1.z; ln_b[7] = b1.w;
+            }
             if (OP == OP_DGELU) {
-                const char *hbase = static_cast<const char *>(aux) + eoff * ESZ;
+                const char *hbase = static_cast<const char *>(op.aux) + eoff * ESZ;
 #pragma unroll
                 for (int i = 0; i < 4; i++) hseg[OP == OP_DGELU ? i : 0].load(hbase + i * cols * ESZ);
             }
 #pragma unroll
             for (int i = 0; i < 4; i++) {
                 uint32_t w[4];
-                float pre[16];
+                const int r = 4 * rb + i;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    float v[4];
+                for (int hh = 0; hh < 2; hh++) {  // two halves of 8 elements
+                    float v[8];
 #pragma unroll
-                    for (int j = 0; j < 4; j++) {
-                        float xv = seg[i].get(4 * q + j);
+                    for (int j = 0; j < 8; j++) {
+                        float xv = seg[i].get(8 * hh + j);
                         if (OP == OP_GELU) xv = gelu_bf16(xv);
-                        if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(4 * q + j));
-                        pre[4 * q + j] = xv;
+                        if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(8 * hh + j));
+                        if (OP == OP_LAYERNORM) {
+                            const int k = 8 * hh + j;  // y = bf16((x - mu) * rs * gamma + beta)
+                            const float gk = (k & 1) ? bf16_hi(ln_g[k >> 1]) : bf16_lo(ln_g[k >> 1]);
+                            const float bk = (k & 1) ? bf16_hi(ln_b[k >> 1]) : bf16_lo(ln_b[k >> 1]);
+                            xv = bf16_round(fmaf((xv - ln_mu[i]) * ln_rs[i], gk, bk));
+                        }
+                        v[j] = xv;
                         amax = fmaxf(amax, fabsf(xv));
-                        csum[4 * q + j] += xv;
-                        v[j] = __fmul_rn(xv, scale);
+                        if (OP == OP_NONE || OP == OP_DGELU) csum[8 * hh + j] += xv;  // dbias only there
                     }
-                    w[q] = pack4<FMT>(v[0], v[1], v[2], v[3]);
+                    w[2 * hh] = pack4<FMT>(__fmul_rn(v[0], scale), __fmul_rn(v[1], scale), __fmul_rn(v[2], scale),
+                                           __fmul_rn(v[3], scale));
+                    w[2 * hh + 1] = pack4<FMT>(__fmul_rn(v[4], scale), __fmul_rn(v[5], scale),
+                                               __fmul_rn(v[6], scale), __fmul_rn(v[7], scale));
+                    if (OP != OP_NONE && pre_out) {
+                        uint32_t pw[4];
+#pragma unroll
+                        for (int p = 0; p < 4; p++) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * p], v[2 * p + 1]);
+                            pw[p] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb + 8 * hh) =
+                            make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    }
                 }
                 const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
-                const int r = 4 * rb + i;
-                if (OP != OP_NONE && pre_out) {
-                    uint32_t pw[8];
-#pragma unroll
-                    for (int p = 0; p < 8; p++) {
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(pre[2 * p], pre[2 * p + 1]);
-                        pw[p] = *reinterpret_cast<uint32_t *>(&b2);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb);
-                    dst[0] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                    dst[1] = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-                }
                 if (out) *reinterpret_cast<uint4 *>(out + (r0 + r) * cols + c0 + 16 * cb) = codes;
                 if (out_t) *reinterpret_cast<uint4 *>(stage + stage_off(r, cb)) = codes;
             }
         }
         if (ws) {
+            // lanes l, l+8, l+16, l+24 share a column block: reduce over them, then lanes 0-7
+            // hold the warp's 16-row partial of columns 16*cb .. 16*cb+15
 #pragma unroll
-            for (int j = 0; j < 16; j++) red[rb][16 * cb + j] = csum[j];
+            for (int j = 0; j < 16; j++) {
+                csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 8);
+                csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 16);
+            }
+            if (lane < 8) {
+                float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    dst[j] = make_float4(csum[4 * j], csum[4 * j + 1], csum[4 * j + 2], csum[4 * j + 3]);
+            }
         }
         if (out_t || ws) __syncthreads();
         if (out_t) {
@@ -184,7 +250,8 @@ __global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict
             const int64_t tr = r0 / CT_ROWS;
             if (t < CT_COLS && c0 + t < cols) {
                 float s = 0.0f;
-                for (int k = 0; k < 32; k++) s += red[k][t];
+#pragma unroll
+                for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
                 ws[tr * cols + c0 + t] = s;
             }
         }
@@ -203,33 +270,67 @@ __global__ void __launch_bounds__(CT_THREADS) cast_kernel(const void *__restrict
     }
 }
 
-// dbias[c] = sum over row tiles (in order) of ws[tile][c].
-__global__ void colsum_reduce_kernel(const float *__restrict__ ws, int64_t n_tiles, int64_t cols,
-                                     float *__restrict__ dbias) {
-    const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (c >= cols) return;
+// dbias[c] = sum over row tiles of ws[tile][c], in a fixed order: CTA = 32
+// columns x 8 warps; warp w sums tiles w, w+8, ... (lane = column), then the 8
+// partials are added in warp order.
+constexpr int RED_COLS = 32, RED_WARPS = 8;
+
+__global__ void __launch_bounds__(RED_COLS *RED_WARPS) colsum_reduce_kernel(const float *__restrict__ ws,
+                                                                            int64_t n_tiles, int64_t cols,
+                                                                            float *__restrict__ dbias) {
+    __shared__ float part[RED_WARPS][RED_COLS];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t c = blockIdx.x * (int64_t)RED_COLS + lane;
     float s = 0.0f;
-    for (int64_t k = 0; k < n_tiles; k++) s += ws[k * cols + c];
-    dbias[c] = s;
+    if (c < cols)
+        for (int64_t k = w; k < n_tiles; k += RED_WARPS) s += ws[k * cols + c];
+    part[w][lane] = s;
+    __syncthreads();
+    if (w == 0 && c < cols) {
+        float t = 0.0f;
+#pragma unroll
+        for (int k = 0; k < RED_WARPS; k++) t += part[k][lane];
+        dbias[c] = t;
+    }
+}
+
+static void launch_colsum_reduce(const float *ws, int64_t n_tiles, int64_t cols, float *dbias, cudaStream_t st) {
+    colsum_reduce_kernel<<<(unsigned)((cols + RED_COLS - 1) / RED_COLS), RED_COLS * RED_WARPS, 0, st>>>(ws, n_tiles,
+                                                                                                       cols, dbias);
 }
 
 template <int XKIND, int FMT>
 static void launch_cast(dim3 grid, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
                         uint8_t *out, uint8_t *out_t, float *amax, float *ws) {
     cast_kernel<XKIND, FMT, OP_NONE>
-        <<<grid, CT_THREADS, 0, st>>>(x, nullptr, rows, cols, scale, out, out_t, amax, ws, nullptr);
+        <<<grid, CT_THREADS, 0, st>>>(x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, nullptr);
 }
 
 template <int OP>
-static void launch_op_cast(dim3 grid, cudaStream_t st, int fmt, const void *x, const void *aux, int64_t rows,
+static void launch_op_cast(dim3 grid, cudaStream_t st, int fmt, const void *x, const OpArgs &op, int64_t rows,
                            int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *ws,
                            uint16_t *pre_out) {
     if (fmt == FP8DL_E4M3)
         cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP>
-            <<<grid, CT_THREADS, 0, st>>>(x, aux, rows, cols, scale, out, out_t, amax, ws, pre_out);
+            <<<grid, CT_THREADS, 0, st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
     else
         cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP>
-            <<<grid, CT_THREADS, 0, st>>>(x, aux, rows, cols, scale, out, out_t, amax, ws, pre_out);
+            <<<grid, CT_THREADS, 0, st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+}
+
+// LayerNorm + cast over 128 x 128 tiles, given the per-row statistics (used by
+// fp8_layernorm_cast after its row-statistics pass).
+fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const float *rs, const void *gamma,
+                                        const void *beta, int64_t rows, int64_t cols, int fmt, const float *scale,
+                                        uint8_t *out, uint8_t *out_t, float *amax, void *y, int sms,
+                                        cudaStream_t st) {
+    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    const int64_t max_ctas = (int64_t)sms * 8;
+    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
+    OpArgs op{nullptr, mu, rs, static_cast<const uint16_t *>(gamma), static_cast<const uint16_t *>(beta)};
+    launch_op_cast<OP_LAYERNORM>(grid, st, fmt, x, op, rows, cols, scale, out, out_t, amax, nullptr,
+                                 static_cast<uint16_t *>(y));
+    return check_launch("fp8_layernorm_cast(tiles)");
 }
 
 }  // namespace fp8dl
@@ -283,7 +384,7 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose"));
     if (dbias) {
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws, n_tiles, cols, dbias);
+        launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(dbias reduce)"));
     }
     return FP8DL_OK;
@@ -326,13 +427,14 @@ static fp8dl_status op_cast_common(int op, const void *x, const void *aux, int64
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     uint16_t *pre = static_cast<uint16_t *>(pre_out);
     if (op == OP_GELU)
-        launch_op_cast<OP_GELU>(grid, st, out_dtype, x, nullptr, rows, cols, scale, out, out_t, amax, ws, pre);
+        launch_op_cast<OP_GELU>(grid, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre);
     else
-        launch_op_cast<OP_DGELU>(grid, st, out_dtype, x, aux, rows, cols, scale, out, out_t, amax, ws, pre);
+        launch_op_cast<OP_DGELU>(grid, st, out_dtype, x, OpArgs{aux, nullptr, nullptr, nullptr, nullptr}, rows, cols,
+                                 scale, out, out_t, amax, ws, pre);
     FP8DL_TRY(check_launch(name));
     if (dbias) {
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws, n_tiles, cols, dbias);
+        launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
         FP8DL_TRY(check_launch(name));
     }
     return FP8DL_OK;
@@ -429,7 +531,7 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc"));
     if (dbias) {
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        colsum_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(ws, n_tiles, cols, dbias);
+        launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc(dbias reduce)"));
     }
     return FP8DL_OK;

@@ -6,7 +6,9 @@
 // nn.LayerNorm (biased variance).  Under delayed scaling ("FP8 低精度训练：
 // Transformer Engine 简析" §三.1/§三.3) the LayerNorm output is what fc1 casts,
 // and its scale is known before the LayerNorm runs, so normalisation, bf16
-// rounding, the FP8 cast, the amax and the transposed copy are one pass.
+// rounding, the FP8 cast, the amax and the transposed copy are one pass over
+// 128x128 tiles (the cast kernel with a LayerNorm element operation, in
+// cast.cu), after a pass that computes the per-row statistics.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -22,133 +24,55 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 // ---------------------------------------------------------------------------
-// LayerNorm forward + cast.  One CTA = 16 rows (8 warps x 2 rows); a warp
-// holds its row in registers as 16-byte chunks (CPL per lane, cols <= 256*CPL):
-//   mu = sum(x)/C; var = sum((x-mu)^2)/C; rs = 1/sqrt(var+eps)   (fp32)
-//   y = bf16( (x-mu)*rs*gamma + beta );  q = enc(fl32(y*scale))
-// Codes are written row-major and staged in shared memory; the CTA then writes
-// 16 bytes (its 16 rows) of every transposed row.
+// Row statistics of LayerNorm: warp per row, the row held in registers,
+//   mu = sum(x)/C, var = sum((x-mu)^2)/C (two passes over the registers), rs = 1/sqrt(var+eps).
 // ---------------------------------------------------------------------------
-constexpr int LN_ROWS = 16, LN_THREADS = 256;
-
-template <int CPL, int FMT>
-__global__ void __launch_bounds__(LN_THREADS) ln_cast_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
-                                                             const uint16_t *__restrict__ gamma,
-                                                             const uint16_t *__restrict__ beta, float eps,
-                                                             const float *__restrict__ scale_p, uint8_t *__restrict__ out,
-                                                             uint8_t *__restrict__ out_t, float *__restrict__ amax_p,
-                                                             float *__restrict__ mu_out, float *__restrict__ rs_out,
-                                                             uint16_t *__restrict__ y_out) {
-    extern __shared__ __align__(16) uint8_t codes[];  // [LN_ROWS][cols]
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+template <int CPL>
+__global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                       float eps, float *__restrict__ mu_out,
+                                                       float *__restrict__ rs_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t nchunks = cols / 8;
-    const float scale = (out || out_t) ? __ldg(scale_p) : 1.0f;
     const float inv_cols = 1.0f / (float)cols;
-    float amax = 0.0f;
-    const int64_t blocks = rows / LN_ROWS;
-    for (int64_t blk = blockIdx.x; blk < blocks; blk += gridDim.x) {
-        const int64_t r0 = blk * LN_ROWS;
-#pragma unroll 1
-        for (int rr = 0; rr < 2; rr++) {
-            const int rl = 2 * warp + rr;
-            const int64_t r = r0 + rl;
-            const uint16_t *xr = x + r * cols;
-            uint4 v[CPL];
+    for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const uint16_t *xr = x + r * cols;
+        uint4 v[CPL];
 #pragma unroll
-            for (int i = 0; i < CPL; i++) {
-                const int64_t c = lane + 32 * i;
-                if (c < nchunks) v[i] = ldg_stream(xr + 8 * c);
+        for (int i = 0; i < CPL; i++)
+            if (lane + 32 * i < nchunks) v[i] = ldg_stream(xr + 8 * (lane + 32 * i));
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < CPL; i++)
+            if (lane + 32 * i < nchunks) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int q = 0; q < 4; q++) s += bf16_lo(w[q]) + bf16_hi(w[q]);
             }
-            float s = 0.0f;
+        const float mean = warp_sum(s) * inv_cols;
+        float ss = 0.0f;
 #pragma unroll
-            for (int i = 0; i < CPL; i++) {
-                if (lane + 32 * i < nchunks) {
-                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        for (int i = 0; i < CPL; i++)
+            if (lane + 32 * i < nchunks) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-                    for (int q = 0; q < 4; q++) s += bf16_lo(w[q]) + bf16_hi(w[q]);
+                for (int q = 0; q < 4; q++) {
+                    const float a = bf16_lo(w[q]) - mean, b = bf16_hi(w[q]) - mean;
+                    ss += a * a + b * b;
                 }
             }
-            const float mean = warp_sum(s) * inv_cols;
-            float ss = 0.0f;
-#pragma unroll
-            for (int i = 0; i < CPL; i++) {
-                if (lane + 32 * i < nchunks) {
-                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        const float a = bf16_lo(w[q]) - mean, b = bf16_hi(w[q]) - mean;
-                        ss += a * a + b * b;
-                    }
-                }
-            }
-            const float var = warp_sum(ss) * inv_cols;
-            const float rs = 1.0f / sqrtf(var + eps);
-            if (lane == 0) {
-                mu_out[r] = mean;
-                rs_out[r] = rs;
-            }
-#pragma unroll
-            for (int i = 0; i < CPL; i++) {
-                const int64_t c = lane + 32 * i;
-                if (c < nchunks) {
-                    const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gamma + 8 * c));
-                    const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(beta + 8 * c));
-                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
-                    float y[8];
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        y[2 * q] = bf16r(fmaf((bf16_lo(w[q]) - mean) * rs, bf16_lo(gw[q]), bf16_lo(bw[q])));
-                        y[2 * q + 1] = bf16r(fmaf((bf16_hi(w[q]) - mean) * rs, bf16_hi(gw[q]), bf16_hi(bw[q])));
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; j++) amax = fmaxf(amax, fabsf(y[j]));
-                    if (y_out) {
-                        uint32_t pw[4];
-#pragma unroll
-                        for (int p = 0; p < 4; p++) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(y[2 * p], y[2 * p + 1]);
-                            pw[p] = *reinterpret_cast<uint32_t *>(&b2);
-                        }
-                        *reinterpret_cast<uint4 *>(y_out + r * cols + 8 * c) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                    }
-                    if (out || out_t) {
-                        const uint32_t lo = pack4<FMT>(__fmul_rn(y[0], scale), __fmul_rn(y[1], scale),
-                                                       __fmul_rn(y[2], scale), __fmul_rn(y[3], scale));
-                        const uint32_t hi = pack4<FMT>(__fmul_rn(y[4], scale), __fmul_rn(y[5], scale),
-                                                       __fmul_rn(y[6], scale), __fmul_rn(y[7], scale));
-                        if (out) *reinterpret_cast<uint2 *>(out + r * cols + 8 * c) = make_uint2(lo, hi);
-                        if (out_t) *reinterpret_cast<uint2 *>(codes + rl * cols + 8 * c) = make_uint2(lo, hi);
-                    }
-                }
-            }
-        }
-        if (out_t) {
-            __syncthreads();
-            for (int64_t c = t; c < cols; c += LN_THREADS) {
-                uint32_t w[4];
-#pragma unroll
-                for (int g = 0; g < 4; g++)
-                    w[g] = (uint32_t)codes[(4 * g) * cols + c] | ((uint32_t)codes[(4 * g + 1) * cols + c] << 8) |
-                           ((uint32_t)codes[(4 * g + 2) * cols + c] << 16) |
-                           ((uint32_t)codes[(4 * g + 3) * cols + c] << 24);
-                *reinterpret_cast<uint4 *>(out_t + c * rows + r0) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            __syncthreads();
-        }
-    }
-    if (amax_p) {
-        __shared__ float wmax[LN_THREADS / 32];
-        const float m = warp_max(amax);
-        if (lane == 0) wmax[warp] = m;
-        __syncthreads();
-        if (t == 0) {
-            float mm = wmax[0];
-            for (int k = 1; k < LN_THREADS / 32; k++) mm = fmaxf(mm, wmax[k]);
-            atomic_max_nonneg(amax_p, mm);
+        const float var = warp_sum(ss) * inv_cols;
+        if (lane == 0) {
+            mu_out[r] = mean;
+            rs_out[r] = 1.0f / sqrtf(var + eps);
         }
     }
 }
+
+fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const float *rs, const void *gamma,
+                                        const void *beta, int64_t rows, int64_t cols, int fmt, const float *scale,
+                                        uint8_t *out, uint8_t *out_t, float *amax, void *y, int sms,
+                                        cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // LayerNorm backward, given the forward's per-row mu and rs:
@@ -201,9 +125,9 @@ __global__ void __launch_bounds__(256) ln_bwd_tile_kernel(const uint16_t *__rest
                                                           const float *__restrict__ mu, const float *__restrict__ rs,
                                                           const float *__restrict__ c12, int64_t rows, int64_t cols,
                                                           uint16_t *__restrict__ dx, float *__restrict__ part) {
-    __shared__ float red_g[32][LB_COLS + 1];
-    __shared__ float red_b[32][LB_COLS + 1];
-    const int t = threadIdx.x, cb = t & 7, rb = t >> 3;
+    __shared__ __align__(16) float red_g[8][LB_COLS];
+    __shared__ __align__(16) float red_b[8][LB_COLS];
+    const int t = threadIdx.x, cb = t & 7, rb = t >> 3, lane = t & 31, wi = t >> 5;
     const int64_t tiles_c = (cols + LB_COLS - 1) / LB_COLS;
     const int64_t tiles = ((rows + LB_ROWS - 1) / LB_ROWS) * tiles_c;
     const int64_t n_rt = (rows + LB_ROWS - 1) / LB_ROWS;
@@ -246,13 +170,25 @@ __global__ void __launch_bounds__(256) ln_bwd_tile_kernel(const uint16_t *__rest
         }
 #pragma unroll
         for (int j = 0; j < 16; j++) {
-            red_g[rb][16 * cb + j] = pg[j];
-            red_b[rb][16 * cb + j] = pb[j];
+            pg[j] += __shfl_xor_sync(0xffffffffu, pg[j], 8);
+            pg[j] += __shfl_xor_sync(0xffffffffu, pg[j], 16);
+            pb[j] += __shfl_xor_sync(0xffffffffu, pb[j], 8);
+            pb[j] += __shfl_xor_sync(0xffffffffu, pb[j], 16);
+        }
+        if (lane < 8) {
+            float4 *dg4 = reinterpret_cast<float4 *>(&red_g[wi][16 * cb]);
+            float4 *db4 = reinterpret_cast<float4 *>(&red_b[wi][16 * cb]);
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                dg4[j] = make_float4(pg[4 * j], pg[4 * j + 1], pg[4 * j + 2], pg[4 * j + 3]);
+                db4[j] = make_float4(pb[4 * j], pb[4 * j + 1], pb[4 * j + 2], pb[4 * j + 3]);
+            }
         }
         __syncthreads();
         if (t < LB_COLS && c0 + t < cols) {
             float sg = 0.0f, sb = 0.0f;
-            for (int k = 0; k < 32; k++) {
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
                 sg += red_g[k][t];
                 sb += red_b[k][t];
             }
@@ -264,45 +200,31 @@ __global__ void __launch_bounds__(256) ln_bwd_tile_kernel(const uint16_t *__rest
     }
 }
 
-__global__ void ln_bwd_reduce_kernel(const float *__restrict__ part, int64_t n_rt, int64_t cols,
-                                     float *__restrict__ dgamma, float *__restrict__ dbeta) {
-    const int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-    if (c >= cols) return;
+// dgamma/dbeta[c] = sum over row tiles of the partials, fixed order (see colsum_reduce_kernel).
+__global__ void __launch_bounds__(256) ln_bwd_reduce_kernel(const float *__restrict__ part, int64_t n_rt, int64_t cols,
+                                                            float *__restrict__ dgamma, float *__restrict__ dbeta) {
+    __shared__ float pg[8][32], pb[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t c = blockIdx.x * (int64_t)32 + lane;
     float sg = 0.0f, sb = 0.0f;
-    for (int64_t k = 0; k < n_rt; k++) {
-        sg += part[k * cols + c];
-        sb += part[(n_rt + k) * cols + c];
+    if (c < cols)
+        for (int64_t k = w; k < n_rt; k += 8) {
+            sg += part[k * cols + c];
+            sb += part[(n_rt + k) * cols + c];
+        }
+    pg[w][lane] = sg;
+    pb[w][lane] = sb;
+    __syncthreads();
+    if (w == 0 && c < cols) {
+        float a = 0.0f, b = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            a += pg[k][lane];
+            b += pb[k][lane];
+        }
+        dgamma[c] = a;
+        dbeta[c] = b;
     }
-    dgamma[c] = sg;
-    dbeta[c] = sb;
-}
-
-template <int CPL>
-static void launch_ln_cast(int fmt, unsigned grid, size_t smem, cudaStream_t st, const uint16_t *x, int64_t rows,
-                           int64_t cols, const uint16_t *gamma, const uint16_t *beta, float eps, const float *scale,
-                           uint8_t *out, uint8_t *out_t, float *amax, float *mu, float *rs, uint16_t *y) {
-    if (fmt == FP8DL_E4M3)
-        ln_cast_kernel<CPL, FP8DL_E4M3>
-            <<<grid, LN_THREADS, smem, st>>>(x, rows, cols, gamma, beta, eps, scale, out, out_t, amax, mu, rs, y);
-    else
-        ln_cast_kernel<CPL, FP8DL_E5M2>
-            <<<grid, LN_THREADS, smem, st>>>(x, rows, cols, gamma, beta, eps, scale, out, out_t, amax, mu, rs, y);
-}
-
-template <int CPL>
-static fp8dl_status set_ln_smem(int dev, size_t smem) {
-    static size_t set_to[64] = {};
-    if (set_to[dev] < smem) {
-        cudaError_t e1 = cudaFuncSetAttribute(ln_cast_kernel<CPL, FP8DL_E4M3>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        cudaError_t e2 = cudaFuncSetAttribute(ln_cast_kernel<CPL, FP8DL_E5M2>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e1 != cudaSuccess || e2 != cudaSuccess)
-            return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute(ln_cast_kernel): %s",
-                        cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
-        set_to[dev] = smem;
-    }
-    return FP8DL_OK;
 }
 
 }  // namespace fp8dl
@@ -326,32 +248,24 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
         return fail(FP8DL_ERR_ALIGN, "x, gamma, beta, out, out_t and y must be 16-byte aligned");
     int dev = 0, sms = 0;
     FP8DL_TRY(current_device(&dev, &sms));
-    const size_t smem = out_t ? (size_t)LN_ROWS * (size_t)cols : 0;
-    const int64_t blocks = rows / LN_ROWS;
-    const int per_sm = smem > 65536 ? 1 : 3;
-    const unsigned grid = (unsigned)(blocks < (int64_t)sms * per_sm ? blocks : (int64_t)sms * per_sm);
     cudaStream_t st = (cudaStream_t)stream;
-    auto X = static_cast<const uint16_t *>(x);
-    auto G = static_cast<const uint16_t *>(gamma);
-    auto B = static_cast<const uint16_t *>(beta);
-    auto Y = static_cast<uint16_t *>(y);
+    // pass 1: per-row statistics (one read of x); pass 2: normalise + cast in 128x128 tiles
     const int64_t chunks_per_lane = (cols / 8 + 31) / 32;
-    if (chunks_per_lane <= 4) {
-        FP8DL_TRY(set_ln_smem<4>(dev, smem));
-        launch_ln_cast<4>(out_dtype, grid, smem, st, X, rows, cols, G, B, eps, scale, out, out_t, amax, mu, rsigma, Y);
-    } else if (chunks_per_lane <= 8) {
-        FP8DL_TRY(set_ln_smem<8>(dev, smem));
-        launch_ln_cast<8>(out_dtype, grid, smem, st, X, rows, cols, G, B, eps, scale, out, out_t, amax, mu, rsigma, Y);
-    } else if (chunks_per_lane <= 16) {
-        FP8DL_TRY(set_ln_smem<16>(dev, smem));
-        launch_ln_cast<16>(out_dtype, grid, smem, st, X, rows, cols, G, B, eps, scale, out, out_t, amax, mu, rsigma,
-                           Y);
-    } else {
-        FP8DL_TRY(set_ln_smem<32>(dev, smem));
-        launch_ln_cast<32>(out_dtype, grid, smem, st, X, rows, cols, G, B, eps, scale, out, out_t, amax, mu, rsigma,
-                           Y);
-    }
-    return check_launch("fp8_layernorm_cast");
+    const int64_t row_ctas = (rows + 7) / 8;
+    const unsigned g1 = (unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8);
+    auto X = static_cast<const uint16_t *>(x);
+    if (chunks_per_lane <= 4)
+        ln_stats_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+    else if (chunks_per_lane <= 8)
+        ln_stats_kernel<8><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+    else if (chunks_per_lane <= 16)
+        ln_stats_kernel<16><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+    else
+        ln_stats_kernel<32><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+    FP8DL_TRY(check_launch("fp8_layernorm_cast(statistics)"));
+    if (!(out || out_t || amax || y)) return FP8DL_OK;
+    return launch_layernorm_tile_cast(x, mu, rsigma, gamma, beta, rows, cols, out_dtype, scale, out, out_t, amax, y,
+                                      sms, st);
 }
 
 size_t fp8_layernorm_bwd_workspace_size(int64_t rows, int64_t cols) {
@@ -390,7 +304,7 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
     ln_bwd_tile_kernel<<<(unsigned)(tiles < (int64_t)sms * 4 ? tiles : (int64_t)sms * 4), 256, 0, st>>>(
         DY, X, G, mu, rsigma, c12, rows, cols, static_cast<uint16_t *>(dx), part);
     FP8DL_TRY(check_launch("fp8_layernorm_bwd(dx)"));
-    ln_bwd_reduce_kernel<<<(unsigned)((cols + 255) / 256), 256, 0, st>>>(part, n_rt, cols, dgamma, dbeta);
+    ln_bwd_reduce_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(part, n_rt, cols, dgamma, dbeta);
     return check_launch("fp8_layernorm_bwd(reduce)");
 }
 
