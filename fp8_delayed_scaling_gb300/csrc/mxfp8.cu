@@ -17,30 +17,20 @@ namespace fp8dl {
 // quantisation
 // ---------------------------------------------------------------------------
 // Smallest e with amax * 2^-e <= 448 (= 1.75 * 2^8), clamped to [-127, 127];
-// amax = 0 gives 0.  Computed exactly from the bits: amax = (1 + m/2^23) * 2^E,
-// and 1 + m/2^23 <= 1.75 exactly when m <= 0x600000.
+// amax = 0 gives 0.  From the bits: a normal amax = (1 + m/2^23) * 2^(E-127)
+// with 1 + m/2^23 <= 1.75 exactly when m <= 0x600000, so e = E - 135 + (m >
+// 0x600000).  Every subnormal amax (E = 0) gives e <= -134, i.e. -127 after
+// the clamp, and the largest amax (E = 255) gives e <= 121, so only the lower
+// clamp is ever active.
 __device__ __forceinline__ int e8m0_exponent(float amax) {
     const uint32_t bits = __float_as_uint(amax);
-    if (bits == 0u) return 0;
-    int E;
-    uint32_t m;
-    const uint32_t ef = bits >> 23;
-    if (ef == 0u) {  // subnormal: bits * 2^-149
-        const int p = 31 - __clz(bits);
-        E = p - 149;
-        m = (bits << (23 - p)) & 0x7FFFFFu;
-    } else {
-        E = (int)ef - 127;
-        m = bits & 0x7FFFFFu;
-    }
-    int e = (m <= 0x600000u) ? E - 8 : E - 7;
-    return max(-127, min(127, e));
+    int e = (int)(bits >> 23) - 135 + ((bits & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    e = max(e, -127);
+    return bits == 0u ? 0 : e;
 }
 
-// 2^-e as an exact fp32 (2^-127 is subnormal).
-__device__ __forceinline__ float pow2_neg(int e) {
-    return e <= 126 ? __int_as_float((127 - e) << 23) : __int_as_float(0x00400000);
-}
+// 2^-e as an exact fp32 for e in [-127, 121] (the exponents e8m0_exponent gives).
+__device__ __forceinline__ float pow2_neg(int e) { return __int_as_float((127 - e) << 23); }
 
 // Byte offset of scale S[r][b] in the tiled scale layout (128-row x 4-block
 // tiles of 512 bytes; kg = number of 4-block groups per row = ceil(NB / 4)).
@@ -51,52 +41,57 @@ __host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t b, int6
     return ((r >> 7) * kg + (b >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (b & 3);
 }
 
-constexpr int MQ_ROWS = 32, MQ_COLS = 256, MQ_THREADS = 256;
+// ---------------------------------------------------------------------------
+// Quantisation kernel.  A CTA tile is 128 x 128 elements; the CTA streams its
+// tiles through a three-stage shared-memory ring filled with cp.async by all
+// threads, so the next two tiles are in flight while one is converted.
+// Each warp converts a 32-row x 64-column part of the tile (two 32 x 32
+// blocks side by side).  From shared memory each lane
+// takes 8 rows x 8 columns: lane bits 0-1 = 8-column chunk, bits 2-3 = 8-row
+// chunk, bit 4 = which 32 x 32 block.  Row-block amaxes reduce over lane bits
+// 0-1, column-block amaxes over bits 2-3 (shuffles within each block's 16
+// lanes).  Row-wise codes leave as 8-byte row pieces, column-wise codes after
+// an in-register 8 x 8 byte transpose as 8-byte pieces of the transposed rows
+// (four lanes fill each 32-byte sector).
+// ---------------------------------------------------------------------------
+constexpr int MQ_THREADS = 256, MQ_WARPS = MQ_THREADS / 32, MQ_STAGES = 3;
 
-// Shared-memory staging of a 32 x 256 tile, rows of 256*ESZ bytes.  16-byte
-// chunks are XOR-swizzled by their 32-element block index so that the row pass
-// (8 threads reading 8 different blocks of one row) and the column pass (32
-// threads reading one row's consecutive elements) are both conflict free.
+// Transpose a 4x4 byte block held as 4 row words: word c of the result holds
+// column c, rows in byte order.
+__device__ __forceinline__ void transpose4x4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t (&o)[4]) {
+    const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(c, d, 0x5140);
+    const uint32_t t2 = __byte_perm(a, b, 0x7362), t3 = __byte_perm(c, d, 0x7362);
+    o[0] = __byte_perm(t0, t1, 0x5410);
+    o[1] = __byte_perm(t0, t1, 0x7632);
+    o[2] = __byte_perm(t2, t3, 0x5410);
+    o[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Stage one CTA tile (128 rows x 128 columns) into shared memory with 16-byte
+// cp.async chunks; rows and columns past the matrix are skipped.
 template <int ESZ>
-__device__ __forceinline__ int mq_chunk(int cc) {
-    constexpr int PER_BLOCK = 32 * ESZ / 16;
-    return cc ^ ((cc / PER_BLOCK) & 7);
-}
-
-template <int XKIND>
-__device__ __forceinline__ float mq_load(const uint8_t *tile, int r, int c) {
-    constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
-    const int byte = c * ESZ;
-    const uint8_t *p = tile + r * MQ_COLS * ESZ + mq_chunk<ESZ>(byte >> 4) * 16 + (byte & 15);
-    if (XKIND == FP8DL_BF16) return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
-    return *reinterpret_cast<const float *>(p);
-}
-
-// 32 consecutive elements of row r starting at block b, as fp32.
-template <int XKIND>
-__device__ __forceinline__ void mq_load_block(const uint8_t *tile, int r, int b, float (&v)[32]) {
-    constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
-    constexpr int PER_BLOCK = 32 * ESZ / 16;
+__device__ __forceinline__ void mq_stage(uint8_t *buf, const void *x, int64_t rows, int64_t cols, int64_t r0,
+                                         int64_t c0) {
+    constexpr int ROW_BYTES = 128 * ESZ, PER_ROW = ROW_BYTES / 16, CHUNKS = 128 * PER_ROW;
+    const uint32_t sbuf = (uint32_t)__cvta_generic_to_shared(buf);
 #pragma unroll
-    for (int j = 0; j < PER_BLOCK; j++) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(tile + r * MQ_COLS * ESZ +
-                                                         mq_chunk<ESZ>(b * PER_BLOCK + j) * 16);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            if (XKIND == FP8DL_BF16) {
-                v[8 * j + 2 * q] = bf16_lo(w[q]);
-                v[8 * j + 2 * q + 1] = bf16_hi(w[q]);
-            } else {
-                v[4 * j + q] = __uint_as_float(w[q]);
-            }
-        }
+    for (int k = 0; k < CHUNKS / MQ_THREADS; k++) {
+        const int ch = threadIdx.x + MQ_THREADS * k, r = ch / PER_ROW, c = ch % PER_ROW;
+        if (r0 + r < rows && c0 + c * 16 / ESZ < cols)
+            cp_async16(sbuf + r * ROW_BYTES + c * 16,
+                       static_cast<const char *>(x) + ((r0 + r) * cols + c0) * ESZ + c * 16);
     }
 }
 
-// One tile = 32 rows x 256 cols.  Phase 1 stages the tile in shared memory
-// with coalesced 16-byte loads; the row pass gives each thread one 1x32
-// block, the column pass one 32x1 block (one column of the tile).
 template <int XKIND>
 __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *__restrict__ x, int64_t rows,
                                                                     int64_t cols, uint8_t *__restrict__ row_q,
@@ -104,67 +99,141 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
                                                                     uint8_t *__restrict__ col_q,
                                                                     uint8_t *__restrict__ col_s) {
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
-    constexpr int CHUNKS_PER_ROW = MQ_COLS * ESZ / 16;
-    constexpr int CHUNKS = MQ_ROWS * CHUNKS_PER_ROW;
-    __shared__ __align__(16) uint8_t tile[MQ_ROWS * MQ_COLS * ESZ];
-    const int t = threadIdx.x;
-    const int64_t tiles_c = (cols + MQ_COLS - 1) / MQ_COLS;
-    const int64_t tiles = (rows / MQ_ROWS) * tiles_c;
-    for (int64_t tl = blockIdx.x; tl < tiles; tl += gridDim.x) {
-        const int64_t r0 = (tl / tiles_c) * MQ_ROWS, c0 = (tl % tiles_c) * MQ_COLS;
-        const int valid_cols = (int)min((int64_t)MQ_COLS, cols - c0);
-        for (int k = t; k < CHUNKS; k += MQ_THREADS) {
-            const int r = k / CHUNKS_PER_ROW, cc = k % CHUNKS_PER_ROW;
-            if (cc * 16 / ESZ < valid_cols) {
-                const uint8_t *src = static_cast<const uint8_t *>(x) + ((r0 + r) * cols + c0) * ESZ + cc * 16;
-                *reinterpret_cast<uint4 *>(tile + (r * MQ_COLS) * ESZ + mq_chunk<ESZ>(cc) * 16) = ldg_stream(src);
-            }
+    constexpr int ROW_BYTES = 128 * ESZ, STAGE = 128 * ROW_BYTES;
+    extern __shared__ __align__(16) uint8_t mq_smem[];
+    // Scales of one CTA tile: exactly one 512-byte tile of the tiled scale layout per
+    // orientation (128 rows x 4 blocks).  Double-buffered; written out one iteration later.
+    __shared__ __align__(16) uint8_t sf_tile[2][2][512];  // [buffer][row-wise, column-wise]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cc = lane & 3, rr = (lane >> 2) & 3, sub = lane >> 4;
+    const int wr = warp >> 1, wc = warp & 1;  // this warp's 32-row band and 64-column half of the tile
+    const int64_t tiles_c = (cols + 127) / 128, tiles = ((rows + 127) / 128) * tiles_c;
+    const int64_t kg_row = (cols / 32 + 3) / 4, kg_col = (rows / 32 + 3) / 4;
+    // in-tile position of this lane's 8 x 8 piece
+    const int prow = 32 * wr + 8 * rr, pcol = 64 * wc + 32 * sub + 8 * cc;
+    // byte of the in-tile scale layout for (row r, block b) of a 128-row x 4-block tile
+    auto sf_byte = [](int r, int b) { return (r & 31) * 16 + (r >> 5) * 4 + b; };
+    for (int k = threadIdx.x; k < 2 * 2 * 512 / 4; k += MQ_THREADS) reinterpret_cast<uint32_t *>(sf_tile)[k] = 0x7F7F7F7Fu;
+#pragma unroll
+    for (int k = 0; k < MQ_STAGES - 1; k++) {
+        const int64_t t0 = blockIdx.x + (int64_t)k * gridDim.x;
+        if (t0 < tiles) mq_stage<ESZ>(mq_smem + k * STAGE, x, rows, cols, (t0 / tiles_c) * 128, (t0 % tiles_c) * 128);
+        cp_async_commit();
+    }
+    int stage = 0, sfb = 0;
+    int64_t prev_tile = -1;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int64_t nt = tile + (int64_t)(MQ_STAGES - 1) * gridDim.x;
+        const int ns = stage == 0 ? MQ_STAGES - 1 : stage - 1;  // the stage consumed one iteration ago
+        if (nt < tiles) mq_stage<ESZ>(mq_smem + ns * STAGE, x, rows, cols, (nt / tiles_c) * 128, (nt % tiles_c) * 128);
+        cp_async_commit();
+        cp_async_wait<MQ_STAGES - 1>();
+        __syncthreads();  // the current stage is complete for every thread; the previous tile's scales are final
+        if (prev_tile >= 0 && threadIdx.x < 64) {  // write the previous tile's two scale tiles, 16 bytes per thread
+            const int o = threadIdx.x & 31, which = threadIdx.x >> 5;
+            const int64_t ptr = prev_tile / tiles_c, ptc = prev_tile % tiles_c;
+            uint8_t *dst = which == 0 ? row_s + (ptr * kg_row + ptc) * 512 : col_s + (ptc * kg_col + ptr) * 512;
+            uint4 *src = reinterpret_cast<uint4 *>(sf_tile[sfb ^ 1][which]) + o;
+            if ((which == 0 ? row_q : col_q) != nullptr) *(reinterpret_cast<uint4 *>(dst) + o) = *src;
+            *src = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);  // padding default for reuse
         }
-        __syncthreads();
-        if (row_q) {  // row pass: thread -> (row r, block b)
-            const int r = t >> 3, b = t & 7;
-            if (32 * b < valid_cols) {
-                float v[32];
-                float amax = 0.0f;
-                mq_load_block<XKIND>(tile, r, b, v);
+        const int64_t tr0 = (tile / tiles_c) * 128, tc0 = (tile % tiles_c) * 128;
+        const bool ok = tr0 + 32 * wr < rows && tc0 + 64 * wc + 32 * sub < cols;  // whole 32 x 32 block present
+        const uint8_t *sb = mq_smem + stage * STAGE + prow * ROW_BYTES + pcol * ESZ;
+        float v[8][8];
 #pragma unroll
-                for (int j = 0; j < 32; j++) amax = fmaxf(amax, fabsf(v[j]));
-                const int e = e8m0_exponent(amax);
-                const float mult = pow2_neg(e);
-                uint32_t w[8];
+        for (int i = 0; i < 8; i++) {
+            const uint8_t *p = sb + i * ROW_BYTES;
+            if (ESZ == 2) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(p);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int q = 0; q < 8; q++)
-                    w[q] = pack4<FP8DL_E4M3>(__fmul_rn(v[4 * q], mult), __fmul_rn(v[4 * q + 1], mult),
-                                             __fmul_rn(v[4 * q + 2], mult), __fmul_rn(v[4 * q + 3], mult));
-                uint8_t *dst = row_q + (r0 + r) * cols + c0 + 32 * b;
-                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                row_s[sf_offset(r0 + r, c0 / 32 + b, (cols / 32 + 3) / 4)] = (uint8_t)(e + 127);
-            }
-        }
-        if (col_q) {  // column pass: thread -> column t of the tile
-            if (t < valid_cols) {
-                float v[32];
-                float amax = 0.0f;
-#pragma unroll
-                for (int j = 0; j < 32; j++) {
-                    v[j] = mq_load<XKIND>(tile, j, t);
-                    amax = fmaxf(amax, fabsf(v[j]));
+                for (int q = 0; q < 4; q++) {
+                    v[i][2 * q] = bf16_lo(w4[q]);
+                    v[i][2 * q + 1] = bf16_hi(w4[q]);
                 }
-                const int e = e8m0_exponent(amax);
-                const float mult = pow2_neg(e);
-                uint32_t w[8];
-#pragma unroll
-                for (int q = 0; q < 8; q++)
-                    w[q] = pack4<FP8DL_E4M3>(__fmul_rn(v[4 * q], mult), __fmul_rn(v[4 * q + 1], mult),
-                                             __fmul_rn(v[4 * q + 2], mult), __fmul_rn(v[4 * q + 3], mult));
-                uint8_t *dst = col_q + (c0 + t) * rows + r0;
-                reinterpret_cast<uint4 *>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                reinterpret_cast<uint4 *>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                col_s[sf_offset(c0 + t, r0 / 32, (rows / 32 + 3) / 4)] = (uint8_t)(e + 127);
+            } else {
+                const uint4 u0 = *reinterpret_cast<const uint4 *>(p), u1 = *reinterpret_cast<const uint4 *>(p + 16);
+                v[i][0] = __uint_as_float(u0.x); v[i][1] = __uint_as_float(u0.y);
+                v[i][2] = __uint_as_float(u0.z); v[i][3] = __uint_as_float(u0.w);
+                v[i][4] = __uint_as_float(u1.x); v[i][5] = __uint_as_float(u1.y);
+                v[i][6] = __uint_as_float(u1.z); v[i][7] = __uint_as_float(u1.w);
             }
         }
-        __syncthreads();
+        __syncthreads();  // the stage may be refilled once every thread has read it
+        float rmax[8], cmax[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            rmax[i] = 0.0f;
+            cmax[i] = 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const float a = fabsf(v[i][j]);
+                rmax[i] = fmaxf(rmax[i], a);
+                cmax[j] = fmaxf(cmax[j], a);
+            }
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 1));
+            rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 2));
+            cmax[i] = fmaxf(cmax[i], __shfl_xor_sync(0xffffffffu, cmax[i], 4));
+            cmax[i] = fmaxf(cmax[i], __shfl_xor_sync(0xffffffffu, cmax[i], 8));
+        }
+        if (ok && row_q) {
+            uint8_t *qrow = row_q + (tr0 + prow) * cols + tc0 + pcol;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int e = e8m0_exponent(rmax[i]);
+                const float m = pow2_neg(e);
+                const uint32_t lo = pack4<FP8DL_E4M3>(__fmul_rn(v[i][0], m), __fmul_rn(v[i][1], m),
+                                                      __fmul_rn(v[i][2], m), __fmul_rn(v[i][3], m));
+                const uint32_t hi = pack4<FP8DL_E4M3>(__fmul_rn(v[i][4], m), __fmul_rn(v[i][5], m),
+                                                      __fmul_rn(v[i][6], m), __fmul_rn(v[i][7], m));
+                *reinterpret_cast<uint2 *>(qrow + i * cols) = make_uint2(lo, hi);
+                if (cc == 0) sf_tile[sfb][0][sf_byte(prow + i, pcol >> 5)] = (uint8_t)(e + 127);
+            }
+        }
+        if (ok && col_q) {
+            float m[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                const int e = e8m0_exponent(cmax[j]);
+                m[j] = pow2_neg(e);
+                if (rr == 0) sf_tile[sfb][1][sf_byte(pcol + j, prow >> 5)] = (uint8_t)(e + 127);
+            }
+            uint8_t *qcol = col_q + (tc0 + pcol) * rows + tr0 + prow;
+#pragma unroll
+            for (int half = 0; half < 2; half++) {  // columns 4*half .. 4*half+3
+                uint32_t wcode[8];
+#pragma unroll
+                for (int i = 0; i < 8; i++)
+                    wcode[i] = pack4<FP8DL_E4M3>(__fmul_rn(v[i][4 * half], m[4 * half]),
+                                                 __fmul_rn(v[i][4 * half + 1], m[4 * half + 1]),
+                                                 __fmul_rn(v[i][4 * half + 2], m[4 * half + 2]),
+                                                 __fmul_rn(v[i][4 * half + 3], m[4 * half + 3]));
+                uint32_t lo[4], hi[4];
+                transpose4x4(wcode[0], wcode[1], wcode[2], wcode[3], lo);
+                transpose4x4(wcode[4], wcode[5], wcode[6], wcode[7], hi);
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    *reinterpret_cast<uint2 *>(qcol + (4 * half + j) * rows) = make_uint2(lo[j], hi[j]);
+            }
+        }
+        stage = stage == MQ_STAGES - 1 ? 0 : stage + 1;
+        prev_tile = tile;
+        sfb ^= 1;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    if (prev_tile >= 0 && threadIdx.x < 64) {  // the last tile's scales
+        const int o = threadIdx.x & 31, which = threadIdx.x >> 5;
+        const int64_t ptr = prev_tile / tiles_c, ptc = prev_tile % tiles_c;
+        uint8_t *dst = which == 0 ? row_s + (ptr * kg_row + ptc) * 512 : col_s + (ptc * kg_col + ptr) * 512;
+        if ((which == 0 ? row_q : col_q) != nullptr)
+            *(reinterpret_cast<uint4 *>(dst) + o) = *(reinterpret_cast<const uint4 *>(sf_tile[sfb ^ 1][which]) + o);
     }
 }
 
@@ -487,15 +556,26 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
         return fail(FP8DL_ERR_ALIGN, "x, row_q and col_q must be 16-byte aligned");
     int sms = 0;
     FP8DL_TRY(current_device(nullptr, &sms));
-    const int64_t tiles = (rows / MQ_ROWS) * ((cols + MQ_COLS - 1) / MQ_COLS);
-    const int64_t max_ctas = (int64_t)sms * 8;
+    const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+    const int64_t max_ctas = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(tiles < max_ctas ? tiles : max_ctas);
+    const size_t smem = (size_t)MQ_STAGES * 128 * 128 * (x_dtype == FP8DL_BF16 ? 2 : 4);
+    static bool attr[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr[dev]) {
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MQ_STAGES * 128 * 128 * 2);
+        cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MQ_STAGES * 128 * 128 * 4);
+        attr[dev] = true;
+    }
     if (x_dtype == FP8DL_BF16)
-        mxfp8_quantize_kernel<FP8DL_BF16><<<grid, MQ_THREADS, 0, (cudaStream_t)stream>>>(x, rows, cols, row_q, row_s,
-                                                                                          col_q, col_s);
+        mxfp8_quantize_kernel<FP8DL_BF16><<<grid, MQ_THREADS, smem, (cudaStream_t)stream>>>(x, rows, cols, row_q,
+                                                                                             row_s, col_q, col_s);
     else
-        mxfp8_quantize_kernel<FP8DL_F32><<<grid, MQ_THREADS, 0, (cudaStream_t)stream>>>(x, rows, cols, row_q, row_s,
-                                                                                         col_q, col_s);
+        mxfp8_quantize_kernel<FP8DL_F32><<<grid, MQ_THREADS, smem, (cudaStream_t)stream>>>(x, rows, cols, row_q,
+                                                                                            row_s, col_q, col_s);
     FP8DL_TRY(check_launch("mxfp8_quantize"));
     if (row_s) launch_sf_pad(row_s, rows, cols / 32, (cudaStream_t)stream);
     if (col_s) launch_sf_pad(col_s, cols, rows / 32, (cudaStream_t)stream);
