@@ -21,8 +21,8 @@
 //   warps 2-5   epilogue: tcgen05.ld 32 columns at a time, scale, bias,
 //               round, store.  Two accumulators let the epilogue of one tile
 //               overlap the main loop of the next.
-// Tile order: groups of up to 16 row-tiles sweep all column-tiles, so the
-// tiles in flight share A and B panels in L2.
+// Tile order: groups of row tiles (see pick_raster), so the tiles in flight
+// form a square-ish block and share A and B panels in L2.
 // Every wait is bounded (see mbar_wait); on a timeout the CTA drains its
 // copies and MMAs, frees TMEM and exits, reporting through *status.
 #include <cuda_bf16.h>
@@ -38,12 +38,13 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK, B_BYTES = BN * BK, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;
-constexpr int GROUP_M = 16;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /* barriers */ + 1024 /* alignment slack */;
 }  // namespace g1
 
 struct GemmArgs {
     int64_t M, N, K;
+    int raster_n;    // 1: groups of `group` column tiles, rows outer (B panels stay in L2)
+    int64_t group;   // tiles per group along the grouped dimension
     uint32_t idesc;
     const float *a_scale_inv, *b_scale_inv;
     const void *bias;
@@ -53,15 +54,22 @@ struct GemmArgs {
     int32_t *status;
 };
 
-__device__ __forceinline__ void tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t &tm,
-                                            int64_t &tn) {
-    const int64_t per_group = (int64_t)g1::GROUP_M * tiles_n;
+// Tile order.  Tiles come in groups of `group` tiles along one dimension; inside
+// a group that dimension varies fastest.  The grouped dimension's operand
+// panels stay resident in L2 while the other operand streams through once per
+// group (pick_raster chooses the dimension and the group size).
+__device__ __forceinline__ void tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int raster_n,
+                                            int64_t group, int64_t &tm, int64_t &tn) {
+    const int64_t outer = raster_n ? tiles_m : tiles_n;  // tiles along the ungrouped dimension
+    const int64_t inner = raster_n ? tiles_n : tiles_m;
+    const int64_t per_group = group * outer;
     const int64_t g = tile / per_group;
-    const int64_t first_m = g * g1::GROUP_M;
-    const int64_t gsize = min((int64_t)g1::GROUP_M, tiles_m - first_m);
+    const int64_t first = g * group;
+    const int64_t gsize = min(group, inner - first);
     const int64_t local = tile - g * per_group;
-    tm = first_m + local % gsize;
-    tn = local / gsize;
+    const int64_t a = first + local % gsize, b = local / gsize;
+    tm = raster_n ? b : a;
+    tn = raster_n ? a : b;
 }
 
 __device__ __forceinline__ float load_bias(const void *bias, int dtype, int64_t n) {
@@ -122,7 +130,7 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
                 int64_t tm, tn;
-                tile_coords(tile, tiles_m, tiles_n, tm, tn);
+                tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
                 for (int kb = 0; kb < num_kb; kb++) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, args.status)) {
                         ok = false;
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
         uint32_t aph = 0;
         for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
             int64_t tm, tn;
-            tile_coords(tile, tiles_m, tiles_n, tm, tn);
+            tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
             if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
             tc_fence_after();
             const int64_t row = tm * BM + 32 * q + lane;
@@ -281,20 +289,8 @@ constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK, B_BYTES = BNH * BK, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;
-constexpr int GROUP_M = 8;  // in 256-row pair tiles
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
 }  // namespace g2
-
-__device__ __forceinline__ void tile_coords2(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t &tm,
-                                             int64_t &tn) {
-    const int64_t per_group = (int64_t)g2::GROUP_M * tiles_n;
-    const int64_t g = tile / per_group;
-    const int64_t first_m = g * g2::GROUP_M;
-    const int64_t gsize = min((int64_t)g2::GROUP_M, tiles_m - first_m);
-    const int64_t local = tile - g * per_group;
-    tm = first_m + local % gsize;
-    tn = local / gsize;
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -351,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
             bool ok = true;
             for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
                 int64_t tm, tn;
-                tile_coords2(tile, tiles_m, tiles_n, tm, tn);
+                tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
                 for (int kb = 0; kb < num_kb; kb++) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, args.status)) {
                         ok = false;
@@ -429,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
         uint32_t aph = 0;
         for (int64_t tile = pair; tile < tiles; tile += npairs) {
             int64_t tm, tn;
-            tile_coords2(tile, tiles_m, tiles_n, tm, tn);
+            tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
             if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
             tc_fence_after();
             const int64_t row = tm * 2 * BM + rank * BM + 32 * q + lane;
@@ -543,6 +539,21 @@ fp8dl_status encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inne
     return FP8DL_OK;
 }
 
+// Tile order: groups of `group` row tiles, rows fastest inside a group.  The
+// tiles in flight step through K together, so what one wave reads from DRAM
+// grows with the number of distinct A and B panels it spans; a square-ish
+// block of concurrent tiles (group ~ sqrt of the tiles in flight, counted in
+// elements) keeps that smallest.  Measured: ordering that keeps a whole
+// operand "resident" instead streams the other operand's panels through L2 and
+// raised DRAM reads (16384x16384x4096: 601 MB -> 927 MB).
+void pick_raster(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n, int &raster_n, int64_t &group) {
+    (void)M;
+    (void)N;
+    (void)K;
+    raster_n = 0;
+    group = tile_m >= tile_n ? 8 : 16;  // 256x256 pair tiles: 8; 128x256 single-CTA tiles: 16
+}
+
 static fp8dl_status check_gemm_common(int64_t M, int64_t N, int64_t K, int64_t mult, const void *A, const void *B,
                                       const void *bias, int32_t bias_dtype, const void *D, int32_t d_dtype) {
     FP8DL_CHECK_ARG(A && B && D, "A, B and D must be non-NULL");
@@ -639,12 +650,14 @@ extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_
     const bool use_pair = pair_clusters[dev] > 0 && (forced == 2 || (forced == 0 && M > g1::BM));
     if (use_pair) {
         args.idesc = idesc_base | ((uint32_t)(2 * g2::BM >> 4) << 24);
+        pick_raster(M, N, K, 2 * g2::BM, g2::BN, args.raster_n, args.group);
         const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
         const int64_t pairs = tiles < pair_clusters[dev] ? tiles : pair_clusters[dev];
         fp8_gemm_pair_kernel<<<(unsigned)(2 * pairs), g2::THREADS, g2::SMEM_BYTES, (cudaStream_t)stream>>>(ta2, tb2,
                                                                                                              args);
         return check_launch("fp8_gemm(pair)");
     }
+    pick_raster(M, N, K, g1::BM, g1::BN, args.raster_n, args.group);
     const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
     fp8_gemm_kernel<<<grid, g1::THREADS, g1::SMEM_BYTES, (cudaStream_t)stream>>>(ta, tb, args);

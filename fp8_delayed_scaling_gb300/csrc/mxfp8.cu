@@ -13,6 +13,8 @@
 
 namespace fp8dl {
 
+void pick_raster(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n, int &raster_n, int64_t &group);
+
 // ---------------------------------------------------------------------------
 // quantisation
 // ---------------------------------------------------------------------------
@@ -290,12 +292,13 @@ constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256, SF_COLS_PER_STAGE = 16;
-constexpr int GROUP_M = 16;
 constexpr int SMEM_BYTES = STAGES * AB_BYTES + STAGES * SF_BYTES + 1024 /* barriers */ + 1024 /* alignment */;
 }  // namespace mx
 
 struct MxArgs {
     int64_t M, N, K;
+    int raster_n;
+    int64_t group;
     const uint8_t *sfa, *sfb;
     int64_t kg;       // 4-block groups per row of the scale layout = ceil(K / 128)
     int64_t sfb_rows; // 128-row scale tiles of B = ceil(N / 128)
@@ -307,15 +310,18 @@ struct MxArgs {
     int32_t *status;
 };
 
-__device__ __forceinline__ void mx_tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t &tm,
-                                               int64_t &tn) {
-    const int64_t per_group = (int64_t)mx::GROUP_M * tiles_n;
+__device__ __forceinline__ void mx_tile_coords(int64_t tile, int64_t tiles_m, int64_t tiles_n, int raster_n,
+                                               int64_t group, int64_t &tm, int64_t &tn) {
+    const int64_t outer = raster_n ? tiles_m : tiles_n;
+    const int64_t inner = raster_n ? tiles_n : tiles_m;
+    const int64_t per_group = group * outer;
     const int64_t g = tile / per_group;
-    const int64_t first_m = g * mx::GROUP_M;
-    const int64_t gsize = min((int64_t)mx::GROUP_M, tiles_m - first_m);
+    const int64_t first = g * group;
+    const int64_t gsize = min(group, inner - first);
     const int64_t local = tile - g * per_group;
-    tm = first_m + local % gsize;
-    tn = local / gsize;
+    const int64_t a = first + local % gsize, b = local / gsize;
+    tm = raster_n ? b : a;
+    tn = raster_n ? a : b;
 }
 
 __device__ __forceinline__ float mx_bias(const void *bias, int dtype, int64_t n) {
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
             bool ok = true;
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
                 int64_t tm, tn;
-                mx_tile_coords(tile, tiles_m, tiles_n, tm, tn);
+                mx_tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
                 const bool sfb1 = 2 * tn + 1 < args.sfb_rows;
                 for (int kb = 0; kb < num_kb; kb++) {
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, args.status)) {
@@ -453,7 +459,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
         uint32_t aph = 0;
         for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
             int64_t tm, tn;
-            mx_tile_coords(tile, tiles_m, tiles_n, tm, tn);
+            mx_tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
             if (!mbar_wait(smem_u32(tfull), aph, abort_flag, args.status)) break;
             tc_fence_after();
             const int64_t row = tm * BM + 32 * q + lane;
@@ -618,6 +624,7 @@ fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, 
     args.D = D;
     args.d_dtype = d_dtype;
     args.status = dev_status;
+    pick_raster(M, N, K, mx::BM, mx::BN, args.raster_n, args.group);
     static bool attr_set[64] = {};
     if (!attr_set[dev]) {
         cudaError_t e =
