@@ -68,6 +68,10 @@ WORKLOADS = {
                         "LayerNorm -> E4M3 cast -> fc1 4096->16384 -> GELU -> E4M3 cast -> fc2 16384->4096",
                    tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
                    x_dtype=torch.bfloat16, training=True, kind="lnmlp"),
+    "ln_mlp_current": dict(desc="The ln_mlp block with just-in-time (current) scaling instead of delayed scaling: "
+                                "each activation is written in bf16 with its amax, then cast in a second pass",
+                           tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
+                           x_dtype=torch.bfloat16, training=True, kind="lnmlp", scaling="current"),
     "mx_mlp": dict(desc="MXFP8 (1x32 E8M0 blocks) MLP fwd+bwd: 16384 tokens, 8192 -> 28672 -> 8192, X with per-channel "
                         "factors log-uniform in [1e-3, 1e2]", tokens=16384, layers=[("up", 8192, 28672),
                                                                                 ("down", 28672, 8192)],
@@ -183,17 +187,23 @@ class LnMlpModel:
         w2 = wl.normal((H, F), 0.02, wl.generator(seed, "W2"), torch.bfloat16).to(dev)
         b1 = torch.zeros(F, dtype=torch.bfloat16, device=dev)
         b2 = torch.zeros(H, dtype=torch.bfloat16, device=dev)
-        self.blk = Fp8LayerNormMLP(self.state, 0, gamma, beta, w1, b1, w2, b2, M)
+        self.current = cfg.get("scaling") == "current"
+        self.blk = Fp8LayerNormMLP(self.state, 0, gamma, beta, w1, b1, w2, b2, M,
+                                   scaling="current" if self.current else "delayed")
         self.layers = [self.blk]
         self.x = [wl.normal((M, H), 1.0, wl.generator(seed, "x"), torch.bfloat16).to(dev)]
         self.dy = [wl.normal((M, H), 1e-3, wl.generator(seed, "dY"), torch.bfloat16).to(dev)]
         self.step_no = 0
         self.blk.forward(self.x[0], seed=True)
         self.blk.backward(self.x[0], self.dy[0], seed=True)
-        self.state.update(self.step_no)
+        if not self.current:
+            self.state.update(self.step_no)
         self.step_no += 1
 
     def launches_per_step(self):
+        if self.current:
+            # per cast: producer (+amax) pass, scale, cast; LN stats; GEMMs; reduces; LN bwd
+            return (2 + 1 + 1) + 3 + 1 + (3 + 1) + 3 + 1 + 3 + 1 + 2 + (1 + 3 + 2) + (1 + 3 + 2) + 2 + 3
         # LN+cast, W1 cast, fc1, GELU+cast, W2 cast, fc2 | dY cast+reduce, 2 GEMMs, dGELU cast+reduce,
         # 2 GEMMs, LN bwd (3 kernels) | update
         return 6 + 2 + 2 + 2 + 2 + 3 + 1
@@ -201,7 +211,8 @@ class LnMlpModel:
     def step(self):
         self.blk.forward(self.x[0])
         self.blk.backward(self.x[0], self.dy[0])
-        self.state.update(self.step_no)
+        if not self.current:  # current scaling keeps no history to update
+            self.state.update(self.step_no)
         self.step_no += 1
 
     def outputs(self):
@@ -341,7 +352,7 @@ def profile_kernels(model, flush, stream, reps=5):
     times = {"gemm": [], "cast": [], "update": []}
     flops_per_gemm_step = step_flops(model.cfg)
     cast_names = ["fp8_cast_amax_transpose", "fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast",
-                  "fp8_layernorm_bwd", "mxfp8_quantize"]
+                  "fp8_layernorm_bwd", "mxfp8_quantize", "fp8_seed_amax_history"]
     saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in ["fp8_gemm", "mxfp8_gemm"] + cast_names
              if hasattr(mod, name)]
     orig_update = model.state.update

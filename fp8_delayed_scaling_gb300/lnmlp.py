@@ -21,6 +21,13 @@ scale, so each activation is fused with the cast of its output:
 On the first step every slot's history is seeded with that step's own amax
 (an amax-only pass) before its cast; because each activation depends on the
 previous GEMM, the seeding is interleaved with the forward and backward.
+
+scaling="current" runs the just-in-time alternative the same page contrasts
+with delayed scaling (§三.1): each tensor's scale comes from its own amax of
+this step, so every cast needs that amax first.  The producing kernel writes
+the bf16 tensor and its amax, the seed call turns the amax into the current
+scale (a history of length 1), and a separate cast pass reads the tensor
+again — the extra HBM round trip that delayed scaling avoids.
 """
 from __future__ import annotations
 
@@ -45,7 +52,9 @@ def make_state(recipe: Recipe, n_blocks: int = 1, device="cuda") -> ScalingState
 
 class Fp8LayerNormMLP:
     def __init__(self, state: ScalingState, block_index: int, gamma, beta, w1, b1, w2, b2, tokens: int,
-                 eps: float = 1e-5, keep_activations: bool = False):
+                 eps: float = 1e-5, keep_activations: bool = False, scaling: str = "delayed"):
+        assert scaling in ("delayed", "current")
+        self.scaling = scaling
         self.state = state
         self.base = block_index * SLOTS
         self.recipe = state.recipe
@@ -79,7 +88,7 @@ class Fp8LayerNormMLP:
         self.ws_cast = torch.empty(max(fp8_cast_workspace_size(M, H), fp8_cast_workspace_size(M, F)), **u8)
         self.ws_ln = torch.empty(fp8_layernorm_bwd_workspace_size(M, H), **u8)
         self.keep = keep_activations
-        if keep_activations:  # the bf16 tensors that are cast, for inspection
+        if keep_activations or scaling == "current":  # the bf16 tensors that are cast
             self.y_ln = torch.empty((M, H), **bf)
             self.g = torch.empty((M, F), **bf)
             self.dh = torch.empty((M, F), **bf)
@@ -93,7 +102,16 @@ class Fp8LayerNormMLP:
         fp8_seed_amax_history(self.recipe, count, self.state.buf.data_ptr() + self.slot(first) * self.state.stride,
                               stream=stream)
 
+    def _current_cast(self, t: torch.Tensor, fmt: int, slot: int, out, out_t, stream, dbias=None) -> None:
+        """Just-in-time cast: the slot's amax was recorded by the producer; turn it into
+        this step's scale, then cast."""
+        self._seed(slot - self.base, 1, stream)
+        fp8_cast_amax_transpose(t, fmt, self.state.scale(slot), out=out, out_t=out_t, dbias=dbias,
+                                workspace=self.ws_cast if dbias is not None else None, stream=stream)
+
     def forward(self, x: torch.Tensor, seed: bool = False, stream=None) -> torch.Tensor:
+        if self.scaling == "current":
+            return self._forward_current(x, stream)
         st = self.state
         s = self.slot
         if seed:
@@ -119,7 +137,44 @@ class Fp8LayerNormMLP:
                  bias=self.b2, stream=stream)
         return self.y
 
+    def _forward_current(self, x, stream):
+        st, s = self.state, self.slot
+        fp8_layernorm_cast(x, self.gamma, self.beta, self.eps, E4M3, None, self.mu, self.rs, amax=st.amax(s(FC1_IN)),
+                           y=self.y_ln, stream=stream)
+        self._current_cast(self.y_ln, E4M3, s(FC1_IN), self.q_ln, self.q_lnT, stream)
+        fp8_cast_amax_transpose(self.w1, E4M3, None, amax=st.amax(s(FC1_W)), stream=stream)
+        self._current_cast(self.w1, E4M3, s(FC1_W), self.qw1, self.qw1T, stream)
+        fp8_gemm(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), st.scale_inv(s(FC1_W)), self.h,
+                 bias=self.b1, stream=stream)
+        fp8_gelu_cast(self.h, E4M3, None, amax=st.amax(s(FC2_IN)), g=self.g, stream=stream)
+        self._current_cast(self.g, E4M3, s(FC2_IN), self.q_g, self.q_gT, stream)
+        fp8_cast_amax_transpose(self.w2, E4M3, None, amax=st.amax(s(FC2_W)), stream=stream)
+        self._current_cast(self.w2, E4M3, s(FC2_W), self.qw2, self.qw2T, stream)
+        fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), st.scale_inv(s(FC2_W)), self.y,
+                 bias=self.b2, stream=stream)
+        return self.y
+
+    def _backward_current(self, x, dy, stream):
+        st, s, g = self.state, self.slot, self.gfmt
+        fp8_cast_amax_transpose(dy, g, None, amax=st.amax(s(FC2_GRAD)), stream=stream)
+        self._current_cast(dy, g, s(FC2_GRAD), self.qdy, self.qdyT, stream, dbias=self.db2)
+        fp8_gemm(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_W)), self.dg,
+                 stream=stream)
+        fp8_gemm(self.qdyT, g, self.q_gT, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_IN)), self.dw2,
+                 stream=stream)
+        fp8_dgelu_cast(self.dg, self.h, g, None, amax=st.amax(s(FC1_GRAD)), dh=self.dh, stream=stream)
+        self._current_cast(self.dh, g, s(FC1_GRAD), self.qdh, self.qdhT, stream, dbias=self.db1)
+        fp8_gemm(self.qdh, g, self.qw1T, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_W)), self.dln,
+                 stream=stream)
+        fp8_gemm(self.qdhT, g, self.q_lnT, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_IN)), self.dw1,
+                 stream=stream)
+        fp8_layernorm_bwd(self.dln, x, self.gamma, self.mu, self.rs, self.dx, self.dgamma, self.dbeta, self.ws_ln,
+                          stream=stream)
+        return self.dx
+
     def backward(self, x: torch.Tensor, dy: torch.Tensor, seed: bool = False, stream=None):
+        if self.scaling == "current":
+            return self._backward_current(x, dy, stream)
         st = self.state
         s = self.slot
         g = self.gfmt

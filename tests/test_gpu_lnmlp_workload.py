@@ -130,3 +130,53 @@ def test_ln_mlp_two_steps():
         got = state.read()
         assert np.array_equal(got["scale"], ost.scale) and np.array_equal(got["scale_inv"], ost.scale_inv)
         assert np.array_equal(got["hist"], ost.hist) and np.array_equal(got["pos"], ost.pos)
+
+
+def test_ln_mlp_current_scaling_step():
+    """Just-in-time (current) scaling variant: each cast uses FP8_MAX/amax of the
+    tensor it casts, from this step; codes bit-exact, GEMMs within bound."""
+    import fp8_delayed_scaling_gb300 as fd
+    from fp8_delayed_scaling_gb300.lnmlp import Fp8LayerNormMLP, make_state
+    dev = gpu()
+    Ms, Hs, Fs = 512, 256, 1024
+    g = wl.generator(60, "current")
+    gamma = (1.0 + wl.normal((Hs,), 0.1, g)).to(torch.bfloat16)
+    beta = torch.zeros(Hs, dtype=torch.bfloat16)
+    w1 = wl.normal((Fs, Hs), 0.02, g, torch.bfloat16)
+    w2 = wl.normal((Hs, Fs), 0.02, g, torch.bfloat16)
+    b1, b2 = torch.zeros(Fs, dtype=torch.bfloat16), torch.zeros(Hs, dtype=torch.bfloat16)
+    x = wl.normal((Ms, Hs), 1.0, g, torch.bfloat16)
+    dy = wl.normal((Ms, Hs), 1e-3, g, torch.bfloat16)
+    recipe = fd.Recipe(margin=0, interval=1, fp8_format=fd.FORMAT_HYBRID, amax_history_len=16)
+    state = make_state(recipe, 1, device=dev)
+    blk = Fp8LayerNormMLP(state, 0, gamma.to(dev), beta.to(dev), w1.to(dev), b1.to(dev), w2.to(dev), b2.to(dev), Ms,
+                          scaling="current")
+    xd = x.to(dev)
+    blk.forward(xd)
+    blk.backward(xd, dy.to(dev))
+    torch.cuda.synchronize()
+    got = state.read()
+    pre = [host(blk.y_ln), host(w1), host(blk.dh), host(blk.g), host(w2), host(dy)]
+    ost = oracle.ScalingState([0, 0, 1, 0, 0, 1], hist_len=16)
+    for i, t in enumerate(pre):
+        ost.record_amax(i, oracle.amax(t))
+    ost.seed()  # the current scale of every tensor
+    assert np.array_equal(got["scale"], ost.scale)
+    sc, si = ost.scale, ost.scale_inv
+    qs = [(blk.q_ln, blk.q_lnT, 0), (blk.qw1, blk.qw1T, 0), (blk.qdh, blk.qdhT, 1), (blk.q_g, blk.q_gT, 0),
+          (blk.qw2, blk.qw2T, 0), (blk.qdy, blk.qdyT, 1)]
+    for i, (q, qT, fmt) in enumerate(qs):
+        ref = oracle.quantize(fmt, pre[i], sc[i])
+        assert np.array_equal(q.cpu().numpy(), ref), i
+        assert np.array_equal(qT.cpu().numpy(), ref.T), i
+    rng = np.random.default_rng(3)
+    qln, qw1, qg, qw2 = (blk.q_ln.cpu().numpy(), blk.qw1.cpu().numpy(), blk.q_g.cpu().numpy(), blk.qw2.cpu().numpy())
+    qdy, qdh = blk.qdy.cpu().numpy(), blk.qdh.cpu().numpy()
+    for name, D, A, af, B, bf, sa, sb in (
+            ("fc1", blk.h, qln, 0, qw1, 0, si[0], si[1]),
+            ("fc2", blk.y, qg, 0, qw2, 0, si[3], si[4]),
+            ("fc2 dgrad", blk.dg, qdy, 1, np.ascontiguousarray(qw2.T), 0, si[5], si[4]),
+            ("fc1 wgrad", blk.dw1, np.ascontiguousarray(qdh.T), 1, np.ascontiguousarray(qln.T), 0, si[2], si[0])):
+        ms, ns = sample_elems(D.shape[0], D.shape[1], rng, n=1024)
+        ref, absr = oracle.gemm_elems(A, af, B, bf, sa, sb, None, ms, ns)
+        check_gemm(D, ref, absr, ms, ns, what=name)
