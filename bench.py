@@ -68,6 +68,10 @@ WORKLOADS = {
                         "LayerNorm -> E4M3 cast -> fc1 4096->16384 -> GELU -> E4M3 cast -> fc2 16384->4096",
                    tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
                    x_dtype=torch.bfloat16, training=True, kind="lnmlp"),
+    "ln_mlp_separate": dict(desc="The ln_mlp block with GELU + E4M3 cast of h as its own kernel after the fc1 GEMM "
+                                 "instead of in the GEMM's epilogue",
+                            tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
+                            x_dtype=torch.bfloat16, training=True, kind="lnmlp", gelu_epilogue="separate"),
     "ln_mlp_current": dict(desc="The ln_mlp block with just-in-time (current) scaling instead of delayed scaling: "
                                 "each activation is written in bf16 with its amax, then cast in a second pass",
                            tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
@@ -88,15 +92,16 @@ def step_flops(cfg):
     return per * (3 if cfg["training"] else 1)
 
 
-def cast_bytes(cfg):
-    """Algorithmic HBM bytes of all casts in one step (read once, write each output once)."""
+def cast_bytes(cfg, fused_gelu=False):
+    """Algorithmic HBM bytes of the HBM-bound kernels of one step (read once, write each output once).
+    With the GELU + cast fused into the fc1 GEMM (fused_gelu), that pass is no longer a separate kernel."""
     M = cfg["tokens"]
     if cfg.get("kind") == "mx":  # quantise X, W, dY of each layer: read 2 B, write 2 B + 2/32 B of scales
         return sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) for _, k, n in cfg["layers"])
     if cfg.get("kind") == "lnmlp":
         H, F = cfg["layers"][0][1], cfg["layers"][0][2]
         return (M * H * (2 + 2) + F * H * (2 + 2) * 2      # LN+cast of x; casts of W1 and W2 (+T)
-                + M * F * (2 + 2)                          # GELU+cast of h (+T)
+                + (0 if fused_gelu else M * F * (2 + 2))    # GELU+cast of h (+T)
                 + M * H * (2 + 2) + 4 * H                  # cast of dY (+T, dbias)
                 + M * F * (2 + 2 + 2) + 4 * F              # dGELU+cast of (dg, h) (+T, dbias)
                 + M * H * (2 + 2 + 2))                     # LayerNorm backward: read dy and x, write dx
@@ -189,7 +194,8 @@ class LnMlpModel:
         b2 = torch.zeros(H, dtype=torch.bfloat16, device=dev)
         self.current = cfg.get("scaling") == "current"
         self.blk = Fp8LayerNormMLP(self.state, 0, gamma, beta, w1, b1, w2, b2, M,
-                                   scaling="current" if self.current else "delayed")
+                                   scaling="current" if self.current else "delayed",
+                                   fused=cfg.get("gelu_epilogue", "fused") == "fused")
         self.layers = [self.blk]
         self.x = [wl.normal((M, H), 1.0, wl.generator(seed, "x"), torch.bfloat16).to(dev)]
         self.dy = [wl.normal((M, H), 1e-3, wl.generator(seed, "dY"), torch.bfloat16).to(dev)]
@@ -201,6 +207,10 @@ class LnMlpModel:
         self.step_no += 1
 
     def launches_per_step(self):
+        if self.blk.fused and not self.current:
+            # LN stats+cast, W1 cast, fc1+GELU+cast, W2 cast, fc2 | dY cast+reduce, 2 GEMMs,
+            # dGELU cast+reduce, 2 GEMMs, LN bwd (3 kernels) | update
+            return 2 + 1 + 1 + 1 + 1 + 2 + 2 + 2 + 2 + 3 + 1
         if self.current:
             # per cast: producer (+amax) pass, scale, cast; LN stats; GEMMs; reduces; LN bwd
             return (2 + 1 + 1) + 3 + 1 + (3 + 1) + 3 + 1 + 3 + 1 + 2 + (1 + 3 + 2) + (1 + 3 + 2) + 2 + 3
@@ -353,7 +363,8 @@ def profile_kernels(model, flush, stream, reps=5):
     flops_per_gemm_step = step_flops(model.cfg)
     cast_names = ["fp8_cast_amax_transpose", "fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast",
                   "fp8_layernorm_bwd", "mxfp8_quantize", "fp8_seed_amax_history"]
-    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in ["fp8_gemm", "mxfp8_gemm"] + cast_names
+    gemm_names = ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast"]
+    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in gemm_names + cast_names
              if hasattr(mod, name)]
     orig_update = model.state.update
 
@@ -368,7 +379,7 @@ def profile_kernels(model, flush, stream, reps=5):
         return w
 
     for mod, name, fn in saved:
-        setattr(mod, name, timed("gemm" if name.endswith("gemm") else "cast", fn))
+        setattr(mod, name, timed("gemm" if name in gemm_names else "cast", fn))
     model.state.update = timed("update", orig_update)
     try:
         for _ in range(reps):
@@ -385,7 +396,8 @@ def profile_kernels(model, flush, stream, reps=5):
         out[k] = {"ms_per_step": tot / reps, "launches_per_step": len(v) // reps,
                   "avg_launch_ms": tot / max(1, len(v))}
     out["gemm"]["flops_per_step"] = flops_per_gemm_step
-    out["cast"]["bytes_per_step"] = cast_bytes(model.cfg)
+    fused = getattr(getattr(model, "blk", None), "fused", False) and not getattr(model, "current", False)
+    out["cast"]["bytes_per_step"] = cast_bytes(model.cfg, fused_gelu=fused)
     return out
 
 
@@ -484,7 +496,7 @@ def run_only(args, dev):
     shape = [int(v) for v in args.shape.split(",")]
     g = torch.Generator(device="cpu").manual_seed(1)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    if args.only in ("gemm", "mxgemm"):
+    if args.only in ("gemm", "gemm_gelu", "mxgemm"):
         M, N, K = shape
         A = torch.randint(0, 0x70, (M, K), dtype=torch.uint8, generator=g).to(dev)
         B = torch.randint(0, 0x70, (N, K), dtype=torch.uint8, generator=g).to(dev)
@@ -492,6 +504,12 @@ def run_only(args, dev):
         one = torch.ones(1, dtype=torch.float32, device=dev)
         if args.only == "gemm":
             fn = lambda: fd.fp8_gemm(A, fd.E4M3, B, fd.E4M3, one, one, D)  # noqa: E731
+        elif args.only == "gemm_gelu":
+            q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            qt = torch.empty((N, M), dtype=torch.uint8, device=dev)
+            am = torch.zeros(1, dtype=torch.float32, device=dev)
+            fn = lambda: fd.fp8_gemm_gelu_cast(A, fd.E4M3, B, fd.E4M3, one, one, D, fd.E4M3, one, q, qt,  # noqa: E731
+                                               q_amax=am)
         else:
             As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, generator=g).to(dev)
             Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, generator=g).to(dev)
@@ -580,7 +598,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="ln_mlp", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default=None, choices=["gemm", "cast", "mxq", "mxgemm", "gelu", "dgelu", "ln", "lnbwd"])
+    ap.add_argument("--only", default=None, choices=["gemm", "gemm_gelu", "cast", "mxq", "mxgemm", "gelu", "dgelu",
+                                                          "ln", "lnbwd"])
     ap.add_argument("--shape", default="8192,12288,4096")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -50,6 +50,8 @@ _SIGS = {
     "fp8_cast_amax_transpose": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fp8_cast_amax_transpose_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
+    "fp8_gemm_gelu_cast": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
+                                  _vp, _vp, _vp, _vp, _vp]),
     "mxfp8_scale_bytes": (_sz, [_i64, _i64]),
     "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mxfp8_gemm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
@@ -261,6 +263,18 @@ def fp8_gemm(A: torch.Tensor, a_dtype: int, B: torch.Tensor, b_dtype: int, a_sca
     _check(_lib.fp8_gemm(_p(A), a_dtype, _p(B), b_dtype, M, N, K, _p(a_scale_inv), _p(b_scale_inv), _p(bias),
                          _hp(bias) if bias is not None else BF16, _p(D), _hp(D), _p(dev_status), _stream(stream)),
            "fp8_gemm")
+
+
+def fp8_gemm_gelu_cast(A: torch.Tensor, a_dtype: int, B: torch.Tensor, b_dtype: int, a_scale_inv, b_scale_inv,
+                       H: torch.Tensor, q_dtype: int, q_scale, q: torch.Tensor, q_t: torch.Tensor, q_amax=None,
+                       bias: torch.Tensor | None = None, g=None, dev_status=None, stream=None) -> None:
+    """H = A*B^T*sa_inv*sb_inv + bias (bf16); q, q^T = FP8 codes of GELU(H) at q_scale; amax of GELU(H)."""
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2 and tuple(H.shape) == (M, N) and H.dtype == torch.bfloat16
+    _check(_lib.fp8_gemm_gelu_cast(_p(A), a_dtype, _p(B), b_dtype, M, N, K, _p(a_scale_inv), _p(b_scale_inv), _p(bias),
+                                   _hp(bias) if bias is not None else BF16, _p(H), q_dtype, _p(q_scale), _p(q), _p(q_t),
+                                   _p(q_amax), _p(g), _p(dev_status), _stream(stream)), "fp8_gemm_gelu_cast")
 
 
 def mxfp8_scale_bytes(rows: int, cols: int) -> int:

@@ -72,42 +72,6 @@ struct OpArgs {
     const uint16_t *gamma, *beta;
 };
 
-__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
-
-// Standard normal CDF Phi(x) and density phi(x), the two pieces of the erf
-// GELU (GELU(h) = h * Phi(h), Phi(h) = (1 + erf(h / sqrt2)) / 2) and of its
-// derivative (Phi(h) + h * phi(h)).  Phi by Abramowitz & Stegun, Handbook of
-// Mathematical Functions, formula 26.2.17: for x >= 0,
-//   Phi(x) = 1 - phi(x) * (b1 t + b2 t^2 + b3 t^3 + b4 t^4 + b5 t^5) + eps,
-//   t = 1 / (1 + p x),  |eps| < 7.5e-8,
-// and Phi(-x) = 1 - Phi(x).  With the fast exponential and reciprocal the total
-// absolute error of Phi stays below 3e-7; the result is rounded to bf16.
-__device__ __forceinline__ void normal_cdf_pdf(float x, float &cdf, float &pdf) {
-    const float ax = fabsf(x);
-    pdf = 0.3989422804f * __expf(-0.5f * x * x);
-    const float t = __fdividef(1.0f, fmaf(0.2316419f, ax, 1.0f));
-    float poly = fmaf(t, 1.330274429f, -1.821255978f);
-    poly = fmaf(t, poly, 1.781477937f);
-    poly = fmaf(t, poly, -0.356563782f);
-    poly = fmaf(t, poly, 0.319381530f);
-    const float tail = pdf * poly * t;  // = Phi(-|x|)
-    cdf = x >= 0.0f ? 1.0f - tail : tail;
-}
-
-// GELU(h) = h * Phi(h), rounded to bf16 like the tensor it stands for.
-__device__ __forceinline__ float gelu_bf16(float h) {
-    float cdf, pdf;
-    normal_cdf_pdf(h, cdf, pdf);
-    return bf16_round(h * cdf);
-}
-
-// dh = dg * GELU'(h) = dg * (Phi(h) + h * phi(h)), rounded to bf16.
-__device__ __forceinline__ float dgelu_bf16(float dg, float h) {
-    float cdf, pdf;
-    normal_cdf_pdf(h, cdf, pdf);
-    return bf16_round(dg * fmaf(h, pdf, cdf));
-}
-
 template <int XKIND, int FMT, int OP>
 __global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_NONE ? 3 : (XKIND == FP8DL_BF16 ? 4 : 2)) cast_kernel(const void *__restrict__ x, const OpArgs op,
                                                           int64_t rows, int64_t cols,

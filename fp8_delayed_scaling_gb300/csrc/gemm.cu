@@ -52,6 +52,13 @@ struct GemmArgs {
     void *D;
     int d_dtype;
     int32_t *status;
+    // fused GELU + FP8 cast of the output (pair kernel, EPI = 1)
+    uint8_t *q;            // [M x N] codes of g = GELU(D)
+    uint8_t *q_t;          // [N x M] the same codes transposed (written by TMA from the CTA's staging)
+    int q_fmt;             // fp8dl_fp8_dtype
+    const float *q_scale;  // device float
+    float *q_amax;         // device float, max-ed with max |g|, or NULL
+    void *g_out;           // [M x N] bf16 g, or NULL
 };
 
 // Tile order.  Tiles come in groups of `group` tiles along one dimension; inside
@@ -287,14 +294,46 @@ namespace g2 {
 constexpr int BM = 128, BN = 256, BNH = 128, BK = 128;  // per-CTA rows of A and of B
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK, B_BYTES = BNH * BK, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+// epilogue warps: 4 (one per TMEM lane quarter) for the plain epilogue; 16 for the
+// fused GELU + cast one, whose per-element work needs four warps per SM
+// sub-partition to hide its arithmetic latency (each warp drains 2 of the 8
+// 32-column chunks of its lane quarter)
+__host__ __device__ constexpr int epi_warps(int epi) { return epi ? 16 : 4; }
+__host__ __device__ constexpr int threads(int epi) { return 64 + 32 * epi_warps(epi); }
+constexpr int QT_BYTES = BN * BM;  // transposed FP8 codes of one CTA's 128 x 256 output (fused epilogue)
+constexpr int smem_bytes(int epi) { return STAGES * STAGE_BYTES + 1024 + (epi ? QT_BYTES : 0) + 1024; }
 }  // namespace g2
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
+// EPI = 0: D = round(acc * s + bias).  EPI = 1 (fc1 of the LayerNormMLP): also
+// g = bf16(GELU(D)), codes q = enc(fl32(g * scale)) row-major and transposed
+// (the transposed codes of the CTA's 128 x 256 output are staged in shared
+// memory and written with one TMA tensor store), and amax |g| — the cast that
+// delayed scaling lets run inside the GEMM, its scale being known in advance.
+// Bias of 32 consecutive output columns starting at n0 (0 beyond N).
+__device__ __forceinline__ void load_bias32(const void *bias, int dtype, int64_t n0, int64_t N, float (&b)[32]) {
+    if (n0 + 32 <= N && dtype == FP8DL_BF16) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(bias) + n0);
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            const uint4 u = __ldg(p + k);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                b[8 * k + 2 * q] = bf16_lo(w[q]);
+                b[8 * k + 2 * q + 1] = bf16_hi(w[q]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j++) b[j] = n0 + j < N ? load_bias(bias, dtype, n0 + j) : 0.0f;
+    }
+}
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                         const GemmArgs args) {
+                         const __grid_constant__ CUtensorMap tmap_qt, const GemmArgs args) {
     using namespace g2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -306,6 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint8_t *qt_stage = bar_area + 1024;  // EPI = 1 only: [256 columns][128 rows] codes
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -322,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
         }
         for (int a = 0; a < 2; a++) {
             mbar_init(smem_u32(&tfull[a]), 1);
-            mbar_init(smem_u32(&tempty[a]), 8);
+            mbar_init(smem_u32(&tempty[a]), 2 * epi_warps(EPI));  // the epilogue warps of both CTAs
         }
         *abort_flag = 0;
         mbar_fence_init();
@@ -418,11 +458,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
             if (!ok && any) mbar_drain(last_bar, last_par);
         }
     } else {  // ------------------------------------------------------------ epilogue (both CTAs)
-        const int q = warp & 3;
+        const int q = warp & 3;                              // TMEM lane quarter
+        const int part = (warp - 2) >> 2;                    // column part of the quarter
+        constexpr int CHUNKS = BN / 32 / (epi_warps(EPI) / 4);  // 32-column chunks per warp
+        constexpr int NEPI = 32 * epi_warps(EPI);            // epilogue threads
         const float sc = __fmul_rn(__ldg(args.a_scale_inv), __ldg(args.b_scale_inv));
+        const float qscale = EPI ? __ldg(args.q_scale) : 0.0f;
+        float gmax = 0.0f;
         const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
         int acc = 0;
         uint32_t aph = 0;
+        bool stored = false;
         for (int64_t tile = pair; tile < tiles; tile += npairs) {
             int64_t tm, tn;
             tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
@@ -430,35 +476,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
             tc_fence_after();
             const int64_t row = tm * 2 * BM + rank * BM + 32 * q + lane;
             const bool row_ok = row < args.M;
+            if (EPI && stored) {  // the previous tile's transposed codes must have left shared memory
+                if (threadIdx.x == 64) bulk_wait_read();
+                named_barrier(1, NEPI);
+            }
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; c++) {
+            for (int cc = 0; cc < CHUNKS; cc++) {
+                const int c = part * CHUNKS + cc;  // chunk of 32 columns within the tile
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * BN + c * 32) + ((uint32_t)(32 * q) << 16), r);
                 tmem_ld_wait();
                 const int64_t n0 = tn * BN + c * 32;
-                if (row_ok && n0 < args.N) {
-                    float v[32];
+                float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * sc;
-                    if (args.bias_dtype >= 0) {
+                for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * sc;
+                if (args.bias_dtype >= 0) {
+                    float b[32];
+                    load_bias32(args.bias, args.bias_dtype, n0, args.N, b);
 #pragma unroll
-                        for (int j = 0; j < 32; j++)
-                            if (n0 + j < args.N) v[j] += load_bias(args.bias, args.bias_dtype, n0 + j);
+                    for (int j = 0; j < 32; j++) v[j] += b[j];
+                }
+                uint32_t hw[16];  // the bf16 output as packed pairs (also the GELU's input)
+                if (EPI || args.d_dtype == FP8DL_BF16) {
+#pragma unroll
+                    for (int p = 0; p < 16; p++) {
+                        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * p], v[2 * p + 1]);
+                        hw[p] = *reinterpret_cast<uint32_t *>(&h);
                     }
-                    if (args.d_dtype == FP8DL_BF16) {
+                }
+                if (row_ok && n0 < args.N) {
+                    if (EPI || args.d_dtype == FP8DL_BF16) {
                         __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.D) + row * args.N + n0;
 #pragma unroll
-                        for (int g = 0; g < 4; g++) {
-                            if (n0 + 8 * g < args.N) {
-                                uint32_t w[4];
-#pragma unroll
-                                for (int p = 0; p < 4; p++) {
-                                    __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * g + 2 * p], v[8 * g + 2 * p + 1]);
-                                    w[p] = *reinterpret_cast<uint32_t *>(&h);
-                                }
-                                *reinterpret_cast<uint4 *>(drow + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
-                            }
-                        }
+                        for (int g = 0; g < 4; g++)
+                            if (n0 + 8 * g < args.N)
+                                *reinterpret_cast<uint4 *>(drow + 8 * g) =
+                                    make_uint4(hw[4 * g], hw[4 * g + 1], hw[4 * g + 2], hw[4 * g + 3]);
                     } else {
                         float *drow = static_cast<float *>(args.D) + row * args.N + n0;
 #pragma unroll
@@ -467,6 +520,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
                                 *reinterpret_cast<float4 *>(drow + 4 * g) =
                                     make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
                     }
+                }
+                if (EPI) {
+                    // g = GELU of the bf16 output, its codes, and the transposed staging.
+                    // Columns beyond N hold exact zeros (zero-filled B rows, zero bias), so
+                    // g = 0 there; rows beyond M are kept out of the amax below.
+                    uint32_t code[8], gw[16];  // codes; bf16 g as packed pairs
+                    float cmax = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 8; k++) {
+                        float gg[4];
+#pragma unroll
+                        for (int p = 0; p < 2; p++) {
+                            const uint32_t w = hw[2 * k + p];
+                            __nv_bfloat162 g2 = __floats2bfloat162_rn(gelu_f32(bf16_lo(w)), gelu_f32(bf16_hi(w)));
+                            gw[2 * k + p] = *reinterpret_cast<uint32_t *>(&g2);
+                            gg[2 * p] = bf16_lo(gw[2 * k + p]);
+                            gg[2 * p + 1] = bf16_hi(gw[2 * k + p]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; j++) cmax = fmaxf(cmax, fabsf(gg[j]));
+                        code[k] = args.q_fmt == FP8DL_E4M3
+                                      ? pack4<FP8DL_E4M3>(__fmul_rn(gg[0], qscale), __fmul_rn(gg[1], qscale),
+                                                          __fmul_rn(gg[2], qscale), __fmul_rn(gg[3], qscale))
+                                      : pack4<FP8DL_E5M2>(__fmul_rn(gg[0], qscale), __fmul_rn(gg[1], qscale),
+                                                          __fmul_rn(gg[2], qscale), __fmul_rn(gg[3], qscale));
+                    }
+                    if (row_ok) gmax = fmaxf(gmax, cmax);
+                    if (row_ok && n0 < args.N) {
+                        uint8_t *qrow = args.q + row * args.N + n0;
+                        if (n0 + 16 <= args.N) *reinterpret_cast<uint4 *>(qrow) = make_uint4(code[0], code[1], code[2], code[3]);
+                        if (n0 + 32 <= args.N)
+                            *reinterpret_cast<uint4 *>(qrow + 16) = make_uint4(code[4], code[5], code[6], code[7]);
+                        if (args.g_out) {
+                            __nv_bfloat16 *grow = static_cast<__nv_bfloat16 *>(args.g_out) + row * args.N + n0;
+#pragma unroll
+                            for (int g = 0; g < 4; g++)
+                                if (n0 + 8 * g < args.N)
+                                    *reinterpret_cast<uint4 *>(grow + 8 * g) =
+                                        make_uint4(gw[4 * g], gw[4 * g + 1], gw[4 * g + 2], gw[4 * g + 3]);
+                        }
+                    }
+                    uint8_t *st = qt_stage + (c * 32) * BM + 32 * q + lane;  // column (c*32 + j), row (32q + lane)
+#pragma unroll
+                    for (int j = 0; j < 32; j++) st[j * BM] = (uint8_t)(code[j >> 2] >> (8 * (j & 3)));
                 }
             }
             tc_fence_before();
@@ -477,10 +574,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::THREADS, 1)
                 else
                     mbar_arrive_cluster(tempty_leader[acc]);
             }
+            if (EPI) {  // the CTA's transposed codes: one TMA store of [256 columns x 128 rows]
+                fence_proxy_async_smem();
+                named_barrier(1, NEPI);
+                if (threadIdx.x == 64) {
+                    tma_store_2d(&tmap_qt, smem_u32(qt_stage), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * BN));
+                    bulk_commit();
+                }
+                stored = true;
+            }
             if (++acc == 2) {
                 acc = 0;
                 aph ^= 1;
             }
+        }
+        if (EPI) {
+            if (threadIdx.x == 64) bulk_wait_all();
+            const float m = warp_max(gmax);
+            if (lane == 0 && args.q_amax) atomic_max_nonneg(args.q_amax, m);
         }
     }
 
@@ -583,35 +694,103 @@ extern "C" fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arriv
     return check_launch("fp8dl_wait_selftest");
 }
 
-extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
-                                 int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
-                                 const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype, int32_t *dev_status,
-                                 fp8dl_stream_t stream) {
-    FP8DL_TRY(check_gemm_common(M, N, K, 16, A, B, bias, bias_dtype, D, d_dtype));
-    FP8DL_CHECK_ARG((a_dtype == FP8DL_E4M3 || a_dtype == FP8DL_E5M2) && (b_dtype == FP8DL_E4M3 || b_dtype == FP8DL_E5M2),
-                    "a_dtype and b_dtype must be E4M3 or E5M2");
-    FP8DL_CHECK_ARG(a_scale_inv && b_scale_inv, "a_scale_inv and b_scale_inv must be non-NULL");
-    int dev = 0, sms = 0;
-    FP8DL_TRY(current_device(&dev, &sms));
+namespace fp8dl {
 
-    CUtensorMap ta, tb, ta2, tb2;
-    FP8DL_TRY(encode_tmap_2d_u8(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, g1::BK, g1::BM,
-                                CU_TENSOR_MAP_SWIZZLE_128B));
-    FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g1::BK, g1::BN,
-                                CU_TENSOR_MAP_SWIZZLE_128B));
-    ta2 = ta;  // the pair kernel loads 128-row boxes of both operands
-    FP8DL_TRY(encode_tmap_2d_u8(&tb2, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g2::BK, g2::BNH,
-                                CU_TENSOR_MAP_SWIZZLE_128B));
-    GemmArgs args;
-    args.M = M;
-    args.N = N;
-    args.K = K;
+// Per-device launch state of the GEMM kernels.
+static bool g_attr_set[64];
+static int g_pair_clusters[64];
+
+static fp8dl_status gemm_device_setup(int dev, int sms) {
+    if (g_attr_set[dev]) return FP8DL_OK;
+    cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g1::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g2::smem_bytes(0));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g2::smem_bytes(1));
+    if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    // how many CTA pairs can be resident at once (both pair kernels hold one CTA per SM)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(sms / 2 * 2), 1, 1);
+    cfg.blockDim = dim3(g2::threads(1), 1, 1);
+    cfg.dynamicSmemBytes = g2::smem_bytes(1);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_pair_kernel<1>, &cfg);
+    if (e != cudaSuccess || clusters < 1) {
+        cudaGetLastError();
+        clusters = 0;  // the pair kernels are not used on this device
+    }
+    g_pair_clusters[dev] = clusters;
+    g_attr_set[dev] = true;
+    return FP8DL_OK;
+}
+
+// The 2-SM pair kernel runs when the problem has two 128-row halves per tile and
+// pairs can be resident; FP8DL_GEMM_VARIANT=1sm|2sm overrides (testing).
+static bool gemm_use_pair(int dev, int64_t M) {
+    const char *v = getenv("FP8DL_GEMM_VARIANT");
+    const int forced = (v && v[0] == '1') ? 1 : (v && v[0] == '2') ? 2 : 0;
+    return g_pair_clusters[dev] > 0 && (forced == 2 || (forced == 0 && M > g1::BM));
+}
+
+// Shared launch path of fp8_gemm (epi = 0) and fp8_gemm_gelu_cast (epi = 1, pair kernel only).
+static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
+                                int64_t N, int64_t K, GemmArgs &args, int epi, int dev, int sms, bool use_pair,
+                                cudaStream_t stream) {
+    CUtensorMap ta, tb, tq;
     // Instruction descriptor, kind::f8f6f4: D fp32 (bit 4), A type bits 7-9, B type bits 10-12
     // (0 = E4M3, 1 = E5M2), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28
     // (M = 128 for one CTA, 256 for a CTA pair; N = 256 either way).
     const uint32_t idesc_base = (1u << 4) | ((uint32_t)a_dtype << 7) | ((uint32_t)b_dtype << 10) |
                                 ((uint32_t)(g1::BN >> 3) << 17);
+    FP8DL_TRY(encode_tmap_2d_u8(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, g1::BK, g1::BM,
+                                CU_TENSOR_MAP_SWIZZLE_128B));
+    if (use_pair) {
+        // both operands in 128-row boxes: each CTA of a pair loads its own halves
+        FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g2::BK, g2::BNH,
+                                    CU_TENSOR_MAP_SWIZZLE_128B));
+        if (epi) {
+            // q^T [N x M] codes, stored in boxes of 128 rows of the output (inner) x 256 columns
+            FP8DL_TRY(encode_tmap_2d_u8(&tq, args.q_t, (uint64_t)M, (uint64_t)N, (uint64_t)M, g2::BM, g2::BN,
+                                        CU_TENSOR_MAP_SWIZZLE_NONE));
+        } else {
+            tq = ta;  // unused
+        }
+        args.idesc = idesc_base | ((uint32_t)(2 * g2::BM >> 4) << 24);
+        pick_raster(M, N, K, 2 * g2::BM, g2::BN, args.raster_n, args.group);
+        const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
+        const int64_t pairs = tiles < g_pair_clusters[dev] ? tiles : g_pair_clusters[dev];
+        if (epi)
+            fp8_gemm_pair_kernel<1>
+                <<<(unsigned)(2 * pairs), g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
+        else
+            fp8_gemm_pair_kernel<0>
+                <<<(unsigned)(2 * pairs), g2::threads(0), g2::smem_bytes(0), stream>>>(ta, tb, tq, args);
+        return check_launch(epi ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");
+    }
+    FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g1::BK, g1::BN,
+                                CU_TENSOR_MAP_SWIZZLE_128B));
     args.idesc = idesc_base | ((uint32_t)(g1::BM >> 4) << 24);
+    pick_raster(M, N, K, g1::BM, g1::BN, args.raster_n, args.group);
+    const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
+    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+    fp8_gemm_kernel<<<grid, g1::THREADS, g1::SMEM_BYTES, stream>>>(ta, tb, args);
+    return check_launch("fp8_gemm");
+}
+
+static fp8dl_status gemm_args(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
+                              int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
+                              const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype, int32_t *dev_status,
+                              GemmArgs &args) {
+    FP8DL_TRY(check_gemm_common(M, N, K, 16, A, B, bias, bias_dtype, D, d_dtype));
+    FP8DL_CHECK_ARG((a_dtype == FP8DL_E4M3 || a_dtype == FP8DL_E5M2) && (b_dtype == FP8DL_E4M3 || b_dtype == FP8DL_E5M2),
+                    "a_dtype and b_dtype must be E4M3 or E5M2");
+    FP8DL_CHECK_ARG(a_scale_inv && b_scale_inv, "a_scale_inv and b_scale_inv must be non-NULL");
+    args = GemmArgs{};
+    args.M = M;
+    args.N = N;
+    args.K = K;
     args.a_scale_inv = a_scale_inv;
     args.b_scale_inv = b_scale_inv;
     args.bias = bias;
@@ -619,47 +798,49 @@ extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_
     args.D = D;
     args.d_dtype = d_dtype;
     args.status = dev_status;
+    return FP8DL_OK;
+}
 
-    static bool attr_set[64] = {};
-    static int pair_clusters[64] = {};
-    if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             g1::SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fp8_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     g2::SMEM_BYTES);
-        if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        // how many CTA pairs can be resident at once
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(sms / 2 * 2), 1, 1);
-        cfg.blockDim = dim3(g2::THREADS, 1, 1);
-        cfg.dynamicSmemBytes = g2::SMEM_BYTES;
-        int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_pair_kernel, &cfg);
-        if (e != cudaSuccess || clusters < 1) {
-            cudaGetLastError();
-            clusters = 0;  // the pair kernel is not used on this device
-        }
-        pair_clusters[dev] = clusters;
-        attr_set[dev] = true;
+}  // namespace fp8dl
+
+extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
+                                 int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
+                                 const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype, int32_t *dev_status,
+                                 fp8dl_stream_t stream) {
+    GemmArgs args;
+    FP8DL_TRY(gemm_args(A, a_dtype, B, b_dtype, M, N, K, a_scale_inv, b_scale_inv, bias, bias_dtype, D, d_dtype,
+                        dev_status, args));
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
+    FP8DL_TRY(gemm_device_setup(dev, sms));
+    return launch_gemm(A, a_dtype, B, b_dtype, M, N, K, args, 0, dev, sms, gemm_use_pair(dev, M), (cudaStream_t)stream);
+}
+
+extern "C" fp8dl_status fp8_gemm_gelu_cast(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype,
+                                           int64_t M, int64_t N, int64_t K, const float *a_scale_inv,
+                                           const float *b_scale_inv, const void *bias, int32_t bias_dtype, void *H,
+                                           int32_t q_dtype, const float *q_scale, uint8_t *q, uint8_t *q_t,
+                                           float *q_amax, void *g, int32_t *dev_status, fp8dl_stream_t stream) {
+    GemmArgs args;
+    FP8DL_TRY(gemm_args(A, a_dtype, B, b_dtype, M, N, K, a_scale_inv, b_scale_inv, bias, bias_dtype, H, FP8DL_BF16,
+                        dev_status, args));
+    FP8DL_CHECK_ARG(q_dtype == FP8DL_E4M3 || q_dtype == FP8DL_E5M2, "q_dtype must be E4M3 or E5M2");
+    FP8DL_CHECK_ARG(q && q_t && q_scale, "q, q_t and q_scale must be non-NULL");
+    if (!aligned16(q) || !aligned16(q_t) || !aligned16(g))
+        return fail(FP8DL_ERR_ALIGN, "q, q_t and g must be 16-byte aligned");
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
+    FP8DL_TRY(gemm_device_setup(dev, sms));
+    if (!gemm_use_pair(dev, M)) {
+        // one-CTA kernel: the GEMM, then the GELU + cast kernel over its output
+        FP8DL_TRY(launch_gemm(A, a_dtype, B, b_dtype, M, N, K, args, 0, dev, sms, false, (cudaStream_t)stream));
+        return fp8_gelu_cast(H, M, N, q_dtype, q_scale, q, q_t, q_amax, g, stream);
     }
-    // Variant: the 2-SM pair kernel when the problem has two 128-row halves per tile
-    // and pairs can be resident; FP8DL_GEMM_VARIANT=1sm|2sm overrides (testing).
-    const char *v = getenv("FP8DL_GEMM_VARIANT");
-    const int forced = (v && v[0] == '1') ? 1 : (v && v[0] == '2') ? 2 : 0;
-    const bool use_pair = pair_clusters[dev] > 0 && (forced == 2 || (forced == 0 && M > g1::BM));
-    if (use_pair) {
-        args.idesc = idesc_base | ((uint32_t)(2 * g2::BM >> 4) << 24);
-        pick_raster(M, N, K, 2 * g2::BM, g2::BN, args.raster_n, args.group);
-        const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
-        const int64_t pairs = tiles < pair_clusters[dev] ? tiles : pair_clusters[dev];
-        fp8_gemm_pair_kernel<<<(unsigned)(2 * pairs), g2::THREADS, g2::SMEM_BYTES, (cudaStream_t)stream>>>(ta2, tb2,
-                                                                                                             args);
-        return check_launch("fp8_gemm(pair)");
-    }
-    pick_raster(M, N, K, g1::BM, g1::BN, args.raster_n, args.group);
-    const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
-    const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-    fp8_gemm_kernel<<<grid, g1::THREADS, g1::SMEM_BYTES, (cudaStream_t)stream>>>(ta, tb, args);
-    return check_launch("fp8_gemm");
+    args.q = q;
+    args.q_t = q_t;
+    args.q_fmt = q_dtype;
+    args.q_scale = q_scale;
+    args.q_amax = q_amax;
+    args.g_out = g;
+    return launch_gemm(A, a_dtype, B, b_dtype, M, N, K, args, 1, dev, sms, true, (cudaStream_t)stream);
 }

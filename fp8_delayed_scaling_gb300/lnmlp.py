@@ -8,7 +8,8 @@ scale, so each activation is fused with the cast of its output:
   forward   LN+cast(x)        -> q_ln, q_ln^T      (slot fc1.in)
             cast W1           -> qW1, qW1^T        (slot fc1.w)
             h  = fc1(q_ln, qW1) + b1               (bf16)
-            GELU+cast(h)      -> q_g, q_g^T        (slot fc2.in)
+            GELU+cast(h)      -> q_g, q_g^T        (slot fc2.in; fused into
+                                                    the fc1 epilogue after step 0)
             cast W2           -> qW2, qW2^T        (slot fc2.w)
             y  = fc2(q_g, qW2) + b2                (bf16)
   backward  cast dY (+db2)    -> qdY, qdY^T        (slot fc2.grad)
@@ -34,8 +35,8 @@ from __future__ import annotations
 import torch
 
 from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose, fp8_cast_workspace_size,
-               fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_layernorm_bwd, fp8_layernorm_bwd_workspace_size,
-               fp8_layernorm_cast, fp8_seed_amax_history)
+               fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_gemm_gelu_cast, fp8_layernorm_bwd,
+               fp8_layernorm_bwd_workspace_size, fp8_layernorm_cast, fp8_seed_amax_history)
 
 FC1_IN, FC1_W, FC1_GRAD, FC2_IN, FC2_W, FC2_GRAD = range(6)
 SLOTS = 6
@@ -52,9 +53,10 @@ def make_state(recipe: Recipe, n_blocks: int = 1, device="cuda") -> ScalingState
 
 class Fp8LayerNormMLP:
     def __init__(self, state: ScalingState, block_index: int, gamma, beta, w1, b1, w2, b2, tokens: int,
-                 eps: float = 1e-5, keep_activations: bool = False, scaling: str = "delayed"):
+                 eps: float = 1e-5, keep_activations: bool = False, scaling: str = "delayed", fused: bool = True):
         assert scaling in ("delayed", "current")
         self.scaling = scaling
+        self.fused = fused  # GELU + cast inside the fc1 GEMM's epilogue (delayed scaling, after step 0)
         self.state = state
         self.base = block_index * SLOTS
         self.recipe = state.recipe
@@ -123,6 +125,15 @@ class Fp8LayerNormMLP:
                            out=self.q_ln, out_t=self.q_lnT, amax=st.amax(s(FC1_IN)), y=self.y_ln, stream=stream)
         fp8_cast_amax_transpose(self.w1, E4M3, st.scale(s(FC1_W)), out=self.qw1, out_t=self.qw1T,
                                 amax=st.amax(s(FC1_W)), stream=stream)
+        if self.fused and not seed:
+            fp8_gemm_gelu_cast(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), st.scale_inv(s(FC1_W)), self.h,
+                               E4M3, st.scale(s(FC2_IN)), self.q_g, self.q_gT, q_amax=st.amax(s(FC2_IN)),
+                               bias=self.b1, g=self.g, stream=stream)
+            fp8_cast_amax_transpose(self.w2, E4M3, st.scale(s(FC2_W)), out=self.qw2, out_t=self.qw2T,
+                                    amax=st.amax(s(FC2_W)), stream=stream)
+            fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), st.scale_inv(s(FC2_W)), self.y,
+                     bias=self.b2, stream=stream)
+            return self.y
         fp8_gemm(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), st.scale_inv(s(FC1_W)), self.h,
                  bias=self.b1, stream=stream)
         if seed:

@@ -200,6 +200,22 @@ fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32
                       const float *b_scale_inv, const void *bias, int32_t bias_dtype, void *D,
                       int32_t d_dtype, int32_t *dev_status, fp8dl_stream_t stream);
 
+/* FP8 GEMM whose epilogue also applies GELU and the FP8 cast of the result
+ * (the fc1 GEMM of a LayerNormMLP).  Delayed scaling knows the cast's scale
+ * before the GEMM runs ("FP8 低精度训练：Transformer Engine 简析" §三.1: with the
+ * scale known in advance the computation stays in one kernel), so the GELU
+ * output never makes an HBM round trip:
+ *   H[m,n] = bf16( acc[m,n] * fl32(a_scale_inv * b_scale_inv) + bias[n] )   (as fp8_gemm)
+ *   G = bf16( GELU(H) )  (erf form; see fp8_gelu_cast)
+ *   q = enc(fl32(G * q_scale)) [M x N], q_t = q^T [N x M], *q_amax max-ed with max |G|
+ *   g [M x N] bf16 receives G, or NULL.
+ * H is bf16.  Results are identical to fp8_gemm followed by fp8_gelu_cast. */
+fp8dl_status fp8_gemm_gelu_cast(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype,
+                                int64_t M, int64_t N, int64_t K, const float *a_scale_inv,
+                                const float *b_scale_inv, const void *bias, int32_t bias_dtype, void *H,
+                                int32_t q_dtype, const float *q_scale, uint8_t *q, uint8_t *q_t,
+                                float *q_amax, void *g, int32_t *dev_status, fp8dl_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * MXFP8 quantisation (block-scaled FP8, named by the Transformer Engine
  * README).  x [rows x cols] (bf16 or fp32).  Blocks are 32 consecutive
