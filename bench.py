@@ -61,6 +61,13 @@ WORKLOADS = {
                             "8192 tokens; QKV 4096->12288, out 4096->4096, up 4096->11008, down 11008->4096",
                        tokens=8192, layers=llama_layers(), hist=1024, fmt="hybrid", x_dtype=torch.bfloat16,
                        training=True),
+    "llama_proj_mb4": dict(desc="llama_proj as 4 micro-batches of 2048 tokens with the FP8 weight cache: the weights "
+                                "are cast on the first micro-batch only; scale update after every micro-batch",
+                           tokens=8192, layers=llama_layers(), hist=1024, fmt="hybrid", x_dtype=torch.bfloat16,
+                           training=True, micro_batches=4, weight_cache=True),
+    "llama_proj_mb4_nocache": dict(desc="llama_proj_mb4 without the weight cache: every micro-batch casts the weights",
+                                   tokens=8192, layers=llama_layers(), hist=1024, fmt="hybrid",
+                                   x_dtype=torch.bfloat16, training=True, micro_batches=4, weight_cache=False),
     "linear_hybrid": dict(desc="te.Linear 2048 tokens 768->3072 fwd+bwd, HYBRID, history 16",
                           tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="hybrid",
                           x_dtype=torch.float32, training=True),
@@ -106,11 +113,12 @@ def cast_bytes(cfg, fused_gelu=False):
                 + M * F * (2 + 2 + 2) + 4 * F              # dGELU+cast of (dg, h) (+T, dbias)
                 + M * H * (2 + 2 + 2))                     # LayerNorm backward: read dy and x, write dx
     esz_x = 2 if cfg["x_dtype"] == torch.bfloat16 else 4
+    w_casts = 1 if cfg.get("weight_cache") else cfg.get("micro_batches", 1)  # weight casts per step
     tot = 0
     for _, k, n in cfg["layers"]:
         t = 2 if cfg["training"] else 1
         tot += M * k * esz_x + M * k * t          # X -> qX (+ qX^T)
-        tot += n * k * esz_x + n * k * t          # W -> qW (+ qW^T)
+        tot += (n * k * esz_x + n * k * t) * w_casts  # W -> qW (+ qW^T)
         if cfg["training"]:
             tot += M * n * 2 + 2 * M * n + 4 * n  # dY bf16 -> qdY + qdY^T + dbias
     return tot
@@ -274,11 +282,14 @@ class Model:
         self.recipe = fd.Recipe(margin=0, interval=1, fp8_format=fmt, amax_history_len=cfg["hist"])
         self.state = make_state(self.recipe, len(cfg["layers"]), device=dev)
         M = cfg["tokens"]
+        self.mb = cfg.get("micro_batches", 1)
+        self.cache = cfg.get("weight_cache", False)
+        self.Mmb = M // self.mb  # tokens per micro-batch
         self.layers, self.x, self.dy = [], [], []
         for i, (name, k, n) in enumerate(cfg["layers"]):
             w = wl.normal((n, k), 0.02, wl.generator(seed, "W/" + name), cfg["x_dtype"]).to(dev)
             b = torch.zeros(n, dtype=cfg["x_dtype"], device=dev)
-            self.layers.append(Fp8Linear(self.state, i, w, b, M, training=cfg["training"]))
+            self.layers.append(Fp8Linear(self.state, i, w, b, self.Mmb, training=cfg["training"]))
             if cfg["x_dtype"] == torch.bfloat16:
                 x = wl.student_t3((M, k), 0.5, wl.generator(seed, "X/" + name))
             else:
@@ -288,13 +299,18 @@ class Model:
                 self.dy.append(wl.normal((M, n), 1e-3, wl.generator(seed, "dY/" + name), torch.bfloat16).to(dev))
         self.step_no = 0
         for lin, x in zip(self.layers, self.x):
-            lin.seed_forward(x)
+            lin.seed_forward(x[:self.Mmb])
         for lin, dy in zip(self.layers, self.dy):
-            lin.seed_backward(dy)
+            lin.seed_backward(dy[:self.Mmb])
 
     def launches_per_step(self):
         per = 3 if not self.cfg["training"] else 3 + 1 + 1 + 2  # casts X, W, gemm; cast dY (+reduce), 2 gemms
-        return per * len(self.layers) + 1
+        if self.mb == 1:
+            return per * len(self.layers) + 1
+        # with the cache: the first micro-batch also writes the decode factor, the others skip the W cast
+        first = per + 1 if self.cache else per
+        rest = per - 1 if self.cache else per
+        return (first + rest * (self.mb - 1)) * len(self.layers) + self.mb
 
     def outputs(self):
         out = []
@@ -306,12 +322,15 @@ class Model:
         return out
 
     def step(self, timers=None):
-        for lin, x in zip(self.layers, self.x):
-            lin.forward(x)
-        for lin, dy in zip(self.layers, self.dy):
-            lin.backward(dy)
-        self.state.update(self.step_no)
-        self.step_no += 1
+        m = self.Mmb
+        for j in range(self.mb):  # one scale update per micro-batch, as at each autocast exit
+            first = (j == 0) if self.cache else None
+            for lin, x in zip(self.layers, self.x):
+                lin.forward(x[j * m:(j + 1) * m], is_first_microbatch=first)
+            for lin, dy in zip(self.layers, self.dy):
+                lin.backward(dy[j * m:(j + 1) * m])
+            self.state.update(self.step_no)
+            self.step_no += 1
 
 
 def run_ours(args, cfg, dev, rank, world):

@@ -47,7 +47,7 @@ _SIGS = {
     "fp8_update_scale": (_i32, [ctypes.POINTER(fp8dl_recipe), _i32, _vp, _i64, _vp]),
     "fp8_seed_amax_history": (_i32, [ctypes.POINTER(fp8dl_recipe), _i32, _vp, _vp]),
     "fp8_cast_workspace_size": (_sz, [_i64, _i64]),
-    "fp8_cast_amax_transpose": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "fp8_cast_amax_transpose": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fp8_cast_amax_transpose_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "fp8_gemm": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
     "fp8_gemm_gelu_cast": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
@@ -232,12 +232,13 @@ class ScalingState:
 # kernels
 # --------------------------------------------------------------------------
 def fp8_cast_amax_transpose(x: torch.Tensor, out_dtype: int, scale, out=None, out_t=None, amax=None, dbias=None,
-                            workspace=None, stream=None) -> None:
+                            workspace=None, scale_inv_out=None, stream=None) -> None:
     assert x.dim() == 2 and x.is_contiguous()
     rows, cols = x.shape
     ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
     _check(_lib.fp8_cast_amax_transpose(_p(x), _hp(x), rows, cols, out_dtype, _p(scale), _p(out), _p(out_t),
-                                        _p(amax), _p(dbias), _p(workspace), ws_bytes, _stream(stream)),
+                                        _p(amax), _p(scale_inv_out), _p(dbias), _p(workspace), ws_bytes,
+                                        _stream(stream)),
            "fp8_cast_amax_transpose")
 
 

@@ -297,6 +297,12 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
     return check_launch("fp8_layernorm_cast(tiles)");
 }
 
+// The decode factor of codes cast at *scale: fl32(1 / scale), the same
+// rounding as the scale_inv the scale update stores beside the scale.
+__global__ void scale_inv_snapshot_kernel(const float *scale, float *scale_inv) {
+    if (threadIdx.x == 0) *scale_inv = __frcp_rn(*scale);
+}
+
 }  // namespace fp8dl
 
 using namespace fp8dl;
@@ -309,9 +315,11 @@ size_t fp8_cast_workspace_size(int64_t rows, int64_t cols) {
 }
 
 fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, int32_t out_dtype,
-                                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *dbias,
-                                     void *workspace, size_t workspace_bytes, fp8dl_stream_t stream) {
+                                     const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
+                                     float *scale_inv_out, float *dbias, void *workspace, size_t workspace_bytes,
+                                     fp8dl_stream_t stream) {
     FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
+    FP8DL_CHECK_ARG(!scale_inv_out || scale != nullptr, "scale_inv_out needs scale");
     FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
     FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "out_dtype must be E4M3 or E5M2");
     FP8DL_CHECK_ARG(!(out || out_t) || scale != nullptr, "scale is NULL but an FP8 output was requested");
@@ -350,6 +358,10 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
         launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(dbias reduce)"));
+    }
+    if (scale_inv_out) {
+        scale_inv_snapshot_kernel<<<1, 32, 0, st>>>(scale, scale_inv_out);
+        FP8DL_TRY(check_launch("fp8_cast_amax_transpose(scale_inv)"));
     }
     return FP8DL_OK;
 }

@@ -17,6 +17,14 @@ Per step, for D = X W^T + b with X [M x K], W [N x K]:
             dX[M,K] = fp8_gemm(qdY, qW^T)        * sdy_inv * sw_inv
             dW[N,K] = fp8_gemm(qdY^T, qX^T)      * sdy_inv * sx_inv
   update    fp8_update_scale over all slots (one launch)
+
+FP8 weight cache (§三.3: the weight cast is skipped while a cached FP8 copy
+exists).  forward(..., is_first_microbatch=True) casts the weight and keeps the
+codes together with the decode factor they were cast at; later micro-batches
+(is_first_microbatch=False) reuse both and launch no weight cast.  The decode
+factor must travel with the codes: the scale update after each forward may
+already have moved the slot's scale_inv on (a new weight amax entered the
+history).  A skipped cast records no weight amax for that step.
 """
 from __future__ import annotations
 
@@ -27,6 +35,36 @@ from . import (BF16, E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_a
 
 SLOTS_PER_LAYER = 3
 IN, WEIGHT, GRAD = 0, 1, 2
+
+
+class WeightCache:
+    """The FP8 codes of one weight (row-major and transposed) and the scale_inv
+    they decode with.  `valid` says the codes stand for the current weight."""
+
+    def __init__(self, q: torch.Tensor, q_t: torch.Tensor | None):
+        self.q, self.q_t = q, q_t
+        self.scale_inv = torch.empty(1, dtype=torch.float32, device=q.device)
+        self.valid = False
+
+    def check(self, is_first_microbatch) -> None:
+        """Raise before any launch when a reuse is asked for and nothing is cached."""
+        if is_first_microbatch is False and not self.valid:
+            raise RuntimeError("is_first_microbatch=False, but no FP8 copy of the weight is cached: "
+                               "cast it first with is_first_microbatch=True")
+
+    def cast(self, w: torch.Tensor, state: ScalingState, slot: int, is_first_microbatch, stream=None):
+        """Cast w into the cache (or reuse it) and return the scale_inv to decode with:
+        None -> cast, decode with the slot's scale_inv, nothing kept;
+        True -> cast, keep the codes and their decode factor;
+        False -> no launch, the kept codes and factor."""
+        self.check(is_first_microbatch)
+        if is_first_microbatch is False:
+            return self.scale_inv
+        keep = bool(is_first_microbatch)
+        fp8_cast_amax_transpose(w, E4M3, state.scale(slot), out=self.q, out_t=self.q_t, amax=state.amax(slot),
+                                scale_inv_out=self.scale_inv if keep else None, stream=stream)
+        self.valid = keep
+        return self.scale_inv if keep else state.scale_inv(slot)
 
 
 def layer_slot_dtypes(recipe: Recipe):
@@ -66,6 +104,8 @@ class Fp8Linear:
             self.db = torch.empty((N,), dtype=torch.float32, device=dev) if bias is not None else None
             self.ws = torch.empty(fp8_cast_workspace_size(M, N), dtype=torch.uint8, device=dev)
         self.bwd_dtype = E5M2 if self.recipe.fp8_format == FORMAT_HYBRID else E4M3
+        self.wcache = WeightCache(self.qw, self.qwT if training else None)
+        self.w_sinv = None  # the weight's decode factor used by this step's forward
 
     def slot(self, k: int) -> int:
         return self.base + k
@@ -85,15 +125,15 @@ class Fp8Linear:
         fp8_cast_amax_transpose(dy, self.bwd_dtype, None, amax=st.amax(self.slot(GRAD)), stream=stream)
         fp8_seed_amax_history(self.recipe, 1, self._state_at(GRAD), stream=stream)
 
-    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, stream=None, is_first_microbatch=None) -> torch.Tensor:
         st = self.state
         tr = self.training
+        self.wcache.check(is_first_microbatch)
         fp8_cast_amax_transpose(x, E4M3, st.scale(self.slot(IN)), out=self.qx, out_t=self.qxT if tr else None,
                                 amax=st.amax(self.slot(IN)), stream=stream)
-        fp8_cast_amax_transpose(self.w, E4M3, st.scale(self.slot(WEIGHT)), out=self.qw,
-                                out_t=self.qwT if tr else None, amax=st.amax(self.slot(WEIGHT)), stream=stream)
-        fp8_gemm(self.qx, E4M3, self.qw, E4M3, st.scale_inv(self.slot(IN)), st.scale_inv(self.slot(WEIGHT)),
-                 self.y, bias=self.b, stream=stream)
+        self.w_sinv = self.wcache.cast(self.w, st, self.slot(WEIGHT), is_first_microbatch, stream)
+        fp8_gemm(self.qx, E4M3, self.qw, E4M3, st.scale_inv(self.slot(IN)), self.w_sinv, self.y, bias=self.b,
+                 stream=stream)
         return self.y
 
     def backward(self, dy: torch.Tensor, stream=None):
@@ -101,8 +141,7 @@ class Fp8Linear:
         g = self.slot(GRAD)
         fp8_cast_amax_transpose(dy, self.bwd_dtype, st.scale(g), out=self.qdy, out_t=self.qdyT, amax=st.amax(g),
                                 dbias=self.db, workspace=self.ws if self.db is not None else None, stream=stream)
-        fp8_gemm(self.qdy, self.bwd_dtype, self.qwT, E4M3, st.scale_inv(g), st.scale_inv(self.slot(WEIGHT)),
-                 self.dx, stream=stream)
+        fp8_gemm(self.qdy, self.bwd_dtype, self.qwT, E4M3, st.scale_inv(g), self.w_sinv, self.dx, stream=stream)
         fp8_gemm(self.qdyT, self.bwd_dtype, self.qxT, E4M3, st.scale_inv(g), st.scale_inv(self.slot(IN)),
                  self.dw, stream=stream)
         return self.dx, self.dw, self.db

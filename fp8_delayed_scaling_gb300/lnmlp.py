@@ -29,6 +29,9 @@ this step, so every cast needs that amax first.  The producing kernel writes
 the bf16 tensor and its amax, the seed call turns the amax into the current
 scale (a history of length 1), and a separate cast pass reads the tensor
 again — the extra HBM round trip that delayed scaling avoids.
+
+Under delayed scaling the two weights can be cached across micro-batches
+(is_first_microbatch, as for te.Linear in linear.py).
 """
 from __future__ import annotations
 
@@ -37,6 +40,7 @@ import torch
 from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose, fp8_cast_workspace_size,
                fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_gemm_gelu_cast, fp8_layernorm_bwd,
                fp8_layernorm_bwd_workspace_size, fp8_layernorm_cast, fp8_seed_amax_history)
+from .linear import WeightCache
 
 FC1_IN, FC1_W, FC1_GRAD, FC2_IN, FC2_W, FC2_GRAD = range(6)
 SLOTS = 6
@@ -89,6 +93,8 @@ class Fp8LayerNormMLP:
         self.dgamma, self.dbeta = torch.empty(H, **f32), torch.empty(H, **f32)
         self.ws_cast = torch.empty(max(fp8_cast_workspace_size(M, H), fp8_cast_workspace_size(M, F)), **u8)
         self.ws_ln = torch.empty(fp8_layernorm_bwd_workspace_size(M, H), **u8)
+        self.w1cache, self.w2cache = WeightCache(self.qw1, self.qw1T), WeightCache(self.qw2, self.qw2T)
+        self.w1_sinv = self.w2_sinv = None  # the weights' decode factors used by this step's forward
         self.keep = keep_activations
         if keep_activations or scaling == "current":  # the bf16 tensors that are cast
             self.y_ln = torch.empty((M, H), **bf)
@@ -111,9 +117,17 @@ class Fp8LayerNormMLP:
         fp8_cast_amax_transpose(t, fmt, self.state.scale(slot), out=out, out_t=out_t, dbias=dbias,
                                 workspace=self.ws_cast if dbias is not None else None, stream=stream)
 
-    def forward(self, x: torch.Tensor, seed: bool = False, stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, seed: bool = False, stream=None, is_first_microbatch=None) -> torch.Tensor:
+        """is_first_microbatch: the FP8 weight cache of te modules (None: cast the
+        weights every call; True: cast and keep them; False: reuse the kept codes)."""
         if self.scaling == "current":
+            if is_first_microbatch is not None:
+                raise ValueError("the FP8 weight cache is defined for delayed scaling only")
             return self._forward_current(x, stream)
+        if seed and is_first_microbatch is False:
+            raise ValueError("the seeding step casts the weights; it cannot reuse a cached copy")
+        self.w1cache.check(is_first_microbatch)
+        self.w2cache.check(is_first_microbatch)
         st = self.state
         s = self.slot
         if seed:
@@ -123,18 +137,16 @@ class Fp8LayerNormMLP:
             self._seed(FC1_IN, 2, stream)
         fp8_layernorm_cast(x, self.gamma, self.beta, self.eps, E4M3, st.scale(s(FC1_IN)), self.mu, self.rs,
                            out=self.q_ln, out_t=self.q_lnT, amax=st.amax(s(FC1_IN)), y=self.y_ln, stream=stream)
-        fp8_cast_amax_transpose(self.w1, E4M3, st.scale(s(FC1_W)), out=self.qw1, out_t=self.qw1T,
-                                amax=st.amax(s(FC1_W)), stream=stream)
+        self.w1_sinv = self.w1cache.cast(self.w1, st, s(FC1_W), is_first_microbatch, stream)
         if self.fused and not seed:
-            fp8_gemm_gelu_cast(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), st.scale_inv(s(FC1_W)), self.h,
+            fp8_gemm_gelu_cast(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), self.w1_sinv, self.h,
                                E4M3, st.scale(s(FC2_IN)), self.q_g, self.q_gT, q_amax=st.amax(s(FC2_IN)),
                                bias=self.b1, g=self.g, stream=stream)
-            fp8_cast_amax_transpose(self.w2, E4M3, st.scale(s(FC2_W)), out=self.qw2, out_t=self.qw2T,
-                                    amax=st.amax(s(FC2_W)), stream=stream)
-            fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), st.scale_inv(s(FC2_W)), self.y,
+            self.w2_sinv = self.w2cache.cast(self.w2, st, s(FC2_W), is_first_microbatch, stream)
+            fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), self.w2_sinv, self.y,
                      bias=self.b2, stream=stream)
             return self.y
-        fp8_gemm(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), st.scale_inv(s(FC1_W)), self.h,
+        fp8_gemm(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), self.w1_sinv, self.h,
                  bias=self.b1, stream=stream)
         if seed:
             fp8_gelu_cast(self.h, E4M3, None, amax=st.amax(s(FC2_IN)), g=None, stream=stream)
@@ -142,9 +154,8 @@ class Fp8LayerNormMLP:
             self._seed(FC2_IN, 2, stream)
         fp8_gelu_cast(self.h, E4M3, st.scale(s(FC2_IN)), out=self.q_g, out_t=self.q_gT, amax=st.amax(s(FC2_IN)),
                       g=self.g, stream=stream)
-        fp8_cast_amax_transpose(self.w2, E4M3, st.scale(s(FC2_W)), out=self.qw2, out_t=self.qw2T,
-                                amax=st.amax(s(FC2_W)), stream=stream)
-        fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), st.scale_inv(s(FC2_W)), self.y,
+        self.w2_sinv = self.w2cache.cast(self.w2, st, s(FC2_W), is_first_microbatch, stream)
+        fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), self.w2_sinv, self.y,
                  bias=self.b2, stream=stream)
         return self.y
 
@@ -194,8 +205,7 @@ class Fp8LayerNormMLP:
             self._seed(FC2_GRAD, 1, stream)
         fp8_cast_amax_transpose(dy, g, st.scale(s(FC2_GRAD)), out=self.qdy, out_t=self.qdyT,
                                 amax=st.amax(s(FC2_GRAD)), dbias=self.db2, workspace=self.ws_cast, stream=stream)
-        fp8_gemm(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_W)), self.dg,
-                 stream=stream)
+        fp8_gemm(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), self.w2_sinv, self.dg, stream=stream)
         fp8_gemm(self.qdyT, g, self.q_gT, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_IN)), self.dw2,
                  stream=stream)
         if seed:
@@ -203,8 +213,7 @@ class Fp8LayerNormMLP:
             self._seed(FC1_GRAD, 1, stream)
         fp8_dgelu_cast(self.dg, self.h, g, st.scale(s(FC1_GRAD)), out=self.qdh, out_t=self.qdhT,
                        amax=st.amax(s(FC1_GRAD)), dbias=self.db1, workspace=self.ws_cast, dh=self.dh, stream=stream)
-        fp8_gemm(self.qdh, g, self.qw1T, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_W)), self.dln,
-                 stream=stream)
+        fp8_gemm(self.qdh, g, self.qw1T, E4M3, st.scale_inv(s(FC1_GRAD)), self.w1_sinv, self.dln, stream=stream)
         fp8_gemm(self.qdhT, g, self.q_lnT, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_IN)), self.dw1,
                  stream=stream)
         fp8_layernorm_bwd(self.dln, x, self.gamma, self.mu, self.rs, self.dx, self.dgamma, self.dbeta, self.ws_ln,

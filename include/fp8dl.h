@@ -142,6 +142,12 @@ fp8dl_status fp8_seed_amax_history(const fp8dl_recipe *recipe, int32_t n_slots, 
  *   out      [rows x cols] FP8 codes, out[i,j] = enc(fl32(x[i,j] * scale)), or NULL
  *   out_t    [cols x rows] FP8 codes, out_t[j,i] = out[i,j], or NULL
  *   amax     device float, atomically max-ed with max |x| (pre-scale), or NULL
+ *   scale_inv_out  device float receiving fl32(1 / *scale), the factor that
+ *            decodes these codes, or NULL.  Codes kept past the next scale
+ *            update (a weight cast once and reused over micro-batches, §三.3:
+ *            the cast is skipped while a cached FP8 copy exists) carry their
+ *            own decode factor this way, since the update rewrites the slot's
+ *            scale_inv.  Written by a one-thread kernel after the cast.
  *   dbias    [cols] fp32 column sums of x (the bias gradient when x is
  *            grad_output), or NULL; overwritten, not accumulated
  *   workspace/workspace_bytes  scratch of fp8_cast_workspace_size(rows, cols)
@@ -153,8 +159,8 @@ size_t fp8_cast_workspace_size(int64_t rows, int64_t cols);
 
 fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
                                      int32_t out_dtype, const float *scale, uint8_t *out,
-                                     uint8_t *out_t, float *amax, float *dbias, void *workspace,
-                                     size_t workspace_bytes, fp8dl_stream_t stream);
+                                     uint8_t *out_t, float *amax, float *scale_inv_out, float *dbias,
+                                     void *workspace, size_t workspace_bytes, fp8dl_stream_t stream);
 
 /* The same cast for callers that cannot allocate device memory.  The paper
  * has no counterpart to this call: it exists for callers that only hand the

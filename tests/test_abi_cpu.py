@@ -60,14 +60,16 @@ def test_host_validation_without_gpu(lib):
     L = _raw(lib)
     a16 = 1 << 20  # a fake, 16-byte aligned address: validation fails before any use
     # NULL input
-    assert L.fp8_cast_amax_transpose(None, 1, 32, 32, 0, a16, a16, None, None, None, None, 0, None) == lib.ERR_INVALID_ARG
+    assert L.fp8_cast_amax_transpose(None, 1, 32, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_INVALID_ARG
     # dimension not a multiple of 16
-    assert L.fp8_cast_amax_transpose(a16, 1, 33, 32, 0, a16, a16, None, None, None, None, 0, None) == lib.ERR_SHAPE
+    assert L.fp8_cast_amax_transpose(a16, 1, 33, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_SHAPE
     assert L.fp8_gemm(a16, 0, a16, 0, 16, 24, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
     # misaligned pointer
-    assert L.fp8_cast_amax_transpose(a16 + 8, 1, 32, 32, 0, a16, a16, None, None, None, None, 0, None) == lib.ERR_ALIGN
+    assert L.fp8_cast_amax_transpose(a16 + 8, 1, 32, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_ALIGN
     # dbias without workspace
-    assert L.fp8_cast_amax_transpose(a16, 1, 32, 32, 0, a16, a16, None, None, a16, None, 0, None) == lib.ERR_WORKSPACE
+    assert L.fp8_cast_amax_transpose(a16, 1, 32, 32, 0, a16, a16, None, None, None, a16, None, 0, None) == lib.ERR_WORKSPACE
+    # a decode-factor output without a scale
+    assert L.fp8_cast_amax_transpose(a16, 1, 32, 32, 0, None, None, None, a16, a16, None, None, 0, None) == lib.ERR_INVALID_ARG
     # bad dtype enums
     assert L.fp8_gemm(a16, 2, a16, 0, 16, 16, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_INVALID_ARG
     assert L.mxfp8_quantize(a16, 1, 48, 32, a16, a16, None, None, None) == lib.ERR_SHAPE
@@ -88,6 +90,23 @@ def test_valid_call_without_gpu_fails_loudly(lib):
         pytest.skip("a GPU is present")
     L = _raw(lib)
     a16 = 1 << 20
-    st = L.fp8_cast_amax_transpose(a16, 1, 32, 32, 0, a16, a16, None, None, None, None, 0, None)
+    st = L.fp8_cast_amax_transpose(a16, 1, 32, 32, 0, a16, a16, None, None, None, None, None, 0, None)
     assert st in (lib.ERR_CUDA, lib.ERR_UNSUPPORTED_DEVICE)
     assert lib.fp8dl_device_supported(0) is False
+
+
+def test_weight_cache_reuse_without_a_cast_raises_before_any_launch(lib):
+    """is_first_microbatch=False with nothing cached is a host-side error (no launch)."""
+    import torch
+    from fp8_delayed_scaling_gb300.linear import Fp8Linear, WeightCache
+    wc = WeightCache(torch.empty((32, 16), dtype=torch.uint8), None)
+    wc.check(None)
+    wc.check(True)
+    with pytest.raises(RuntimeError):
+        wc.check(False)
+    import types
+    recipe = lib.Recipe(margin=0, interval=1, fp8_format=lib.FORMAT_HYBRID, amax_history_len=4)
+    state = types.SimpleNamespace(recipe=recipe)  # never touched: the check comes first
+    lin = Fp8Linear(state, 0, torch.zeros((32, 16), dtype=torch.bfloat16), None, 16)
+    with pytest.raises(RuntimeError):
+        lin.forward(torch.zeros((16, 16), dtype=torch.bfloat16), is_first_microbatch=False)
