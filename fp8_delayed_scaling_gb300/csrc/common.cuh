@@ -92,26 +92,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-// Standard normal CDF Phi(x) and density phi(x), the two pieces of the erf
-// GELU (GELU(h) = h * Phi(h), Phi(h) = (1 + erf(h / sqrt2)) / 2) and of its
-// derivative (Phi(h) + h * phi(h)).  Phi by Abramowitz & Stegun, Handbook of
-// Mathematical Functions, formula 26.2.17: for x >= 0,
-//   Phi(x) = 1 - phi(x) * (b1 t + b2 t^2 + b3 t^3 + b4 t^4 + b5 t^5) + eps,
-//   t = 1 / (1 + p x),  |eps| < 7.5e-8,
-// and Phi(-x) = 1 - Phi(x).  With the fast exponential and reciprocal the total
-// absolute error of Phi stays below 3e-7; the result is rounded to bf16.
-__device__ __forceinline__ void normal_cdf_pdf(float x, float &cdf, float &pdf) {
-    const float ax = fabsf(x);
-    pdf = 0.3989422804f * __expf(-0.5f * x * x);
-    const float t = __fdividef(1.0f, fmaf(0.2316419f, ax, 1.0f));
-    float poly = fmaf(t, 1.330274429f, -1.821255978f);
-    poly = fmaf(t, poly, 1.781477937f);
-    poly = fmaf(t, poly, -0.356563782f);
-    poly = fmaf(t, poly, 0.319381530f);
-    const float tail = pdf * poly * t;  // = Phi(-|x|)
-    cdf = x >= 0.0f ? 1.0f - tail : tail;
-}
-
 __device__ __forceinline__ float ex2_approx_ftz(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -123,24 +103,37 @@ __device__ __forceinline__ float rcp_approx_ftz(float x) {
     return y;
 }
 
-// GELU(h) = h * Phi(h) in fp32 (before the bf16 rounding), written as
-//   GELU(h) = max(h, 0) - |h| * Phi(-|h|),
-// which is h * (1 - Phi(-h)) for h >= 0 and h * Phi(h) for h < 0: one fused
-// multiply-add instead of a select.  Phi(-|h|) is the tail of formula 26.2.17
-// above, phi(h) * t * (b1 + b2 t + ... + b5 t^4), with the density's factor
-// 1/sqrt(2 pi) folded into the coefficients and exp(-h^2/2) = 2^(-h^2 log2(e)/2).
-// Flushing a subnormal exponential to zero (|h| > 13) changes the result by
-// less than |h| * 2^-126.
-__device__ __forceinline__ float gelu_f32(float h) {
+// The erf GELU, GELU(h) = h * Phi(h) with Phi the standard normal CDF, and its
+// derivative GELU'(h) = Phi(h) + h * phi(h), phi the density.  Both take the
+// lower tail T(h) = Phi(-|h|) from Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 26.2.17: for x >= 0
+//   Phi(-x) = phi(x) * (b1 t + b2 t^2 + b3 t^3 + b4 t^4 + b5 t^5) + eps,
+//   t = 1 / (1 + p x),  |eps| < 7.5e-8,
+// with the density's factor 1/sqrt(2 pi) folded into the b's and
+// exp(-h^2/2) = 2^(-h^2 log2(e) / 2) from the hardware approximations (total
+// |dPhi| < 3e-7).  Flushing a subnormal exponential to zero (|h| > 13) changes
+// a result by less than |h| * 2^-126.
+struct NormalTail {
+    float e;     // exp(-h^2 / 2)
+    float tail;  // Phi(-|h|)
+};
+__device__ __forceinline__ NormalTail normal_tail(float h) {
     constexpr float K = 0.3989422804f;  // 1 / sqrt(2 pi)
-    const float ah = fabsf(h);
     const float e = ex2_approx_ftz(h * h * -0.7213475204f);
-    const float t = rcp_approx_ftz(fmaf(0.2316419f, ah, 1.0f));
+    const float t = rcp_approx_ftz(fmaf(0.2316419f, fabsf(h), 1.0f));
     float poly = fmaf(t, 1.330274429f * K, -1.821255978f * K);
     poly = fmaf(t, poly, 1.781477937f * K);
     poly = fmaf(t, poly, -0.356563782f * K);
     poly = fmaf(t, poly, 0.319381530f * K);
-    return fmaf(-ah, e * poly * t, fmaxf(h, 0.0f));
+    return {e, e * poly * t};
+}
+
+// GELU(h) in fp32 (before the bf16 rounding), written as
+//   GELU(h) = max(h, 0) - |h| * Phi(-|h|),
+// which is h * (1 - Phi(-h)) for h >= 0 and h * Phi(h) for h < 0: one fused
+// multiply-add instead of a select.
+__device__ __forceinline__ float gelu_f32(float h) {
+    return fmaf(-fabsf(h), normal_tail(h).tail, fmaxf(h, 0.0f));
 }
 
 // GELU(h) rounded to bf16 like the tensor it stands for.
@@ -148,9 +141,10 @@ __device__ __forceinline__ float gelu_bf16(float h) { return bf16_round(gelu_f32
 
 // dh = dg * GELU'(h) = dg * (Phi(h) + h * phi(h)), rounded to bf16.
 __device__ __forceinline__ float dgelu_bf16(float dg, float h) {
-    float cdf, pdf;
-    normal_cdf_pdf(h, cdf, pdf);
-    return bf16_round(dg * fmaf(h, pdf, cdf));
+    const NormalTail n = normal_tail(h);
+    const float cdf = h >= 0.0f ? 1.0f - n.tail : n.tail;
+    return bf16_round(dg * fmaf(h * 0.3989422804f, n.e, cdf));
 }
+
 
 }  // namespace fp8dl
