@@ -37,6 +37,10 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
+# DRAM bytes (read + write) per GEMM launch, the mean over one step's launches,
+# from one ncu capture of this workload with the kernels as they are now
+# (profiles/fp8_gemm_traffic_ln_mlp.md).  Workloads without a capture report null.
+GEMM_TRAFFIC = {"ln_mlp": 1.376e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -670,7 +674,7 @@ def main():
         "config": config,
         "roofline": {"bound": "tensor", "kernel": "mxfp8_gemm" if cfg.get("kind") == "mx" else "fp8_gemm", "achieved": round(achieved, 1),
                      "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
-                     "traffic": None,
+                     "traffic": GEMM_TRAFFIC.get(args.workload),
                      "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},
         "cast": {"achieved_gbs": round(cast_gbs, 1), "peak_gbs": hbm, "frac": round(cast_gbs / hbm, 4),
                  "ms_per_step": round(c["ms_per_step"], 4), "launches_per_step": c["launches_per_step"]},
