@@ -220,9 +220,9 @@ class LnMlpModel:
 
     def launches_per_step(self):
         if self.blk.fused and not self.current:
-            # LN stats+cast, W1 cast, fc1+GELU+cast, W2 cast, fc2 | dY cast+reduce, 2 GEMMs,
-            # dGELU cast+reduce, 2 GEMMs, LN bwd (3 kernels) | update
-            return 2 + 1 + 1 + 1 + 1 + 2 + 2 + 2 + 2 + 3 + 1
+            # LN stats+cast, W1 cast, fc1+GELU+cast, W2 cast, fc2 | dY cast+reduce, fc2 wgrad,
+            # fc2 dgrad+dGELU+cast and its dbias reduce, 2 GEMMs, LN bwd (3 kernels) | update
+            return 2 + 1 + 1 + 1 + 1 + 2 + 1 + 2 + 2 + 3 + 1
         if self.current:
             # per cast: producer (+amax) pass, scale, cast; LN stats; GEMMs; reduces; LN bwd
             return (2 + 1 + 1) + 3 + 1 + (3 + 1) + 3 + 1 + 3 + 1 + 2 + (1 + 3 + 2) + (1 + 3 + 2) + 2 + 3
@@ -383,15 +383,17 @@ def profile_kernels(model, flush, stream, reps=5):
     import fp8_delayed_scaling_gb300.lnmlp as LM
     import fp8_delayed_scaling_gb300.mxlinear as MX
     times = {"gemm": [], "cast": [], "update": []}
+    by_entry = {}  # entry point -> [(start, end) events]
+    seq = []        # (entry point, start, end) in call order, all reps
     flops_per_gemm_step = step_flops(model.cfg)
     cast_names = ["fp8_cast_amax_transpose", "fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast",
                   "fp8_layernorm_bwd", "mxfp8_quantize", "fp8_seed_amax_history"]
-    gemm_names = ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast"]
+    gemm_names = ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast", "fp8_gemm_dgelu_cast"]
     saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in gemm_names + cast_names
              if hasattr(mod, name)]
     orig_update = model.state.update
 
-    def timed(kind, fn):
+    def timed(kind, fn, name):
         def w(*a, **k):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
@@ -399,11 +401,13 @@ def profile_kernels(model, flush, stream, reps=5):
             fn(*a, **k)
             e1.record(stream)
             times[kind].append((e0, e1))
+            by_entry.setdefault(name, []).append((e0, e1))
+            seq.append((name, e0, e1))
         return w
 
     for mod, name, fn in saved:
-        setattr(mod, name, timed("gemm" if name in gemm_names else "cast", fn))
-    model.state.update = timed("update", orig_update)
+        setattr(mod, name, timed("gemm" if name in gemm_names else "cast", fn, name))
+    model.state.update = timed("update", orig_update, "fp8_update_scale")
     try:
         for _ in range(reps):
             flush.fill_(1)
@@ -418,6 +422,11 @@ def profile_kernels(model, flush, stream, reps=5):
         tot = sum(a.elapsed_time(b) for a, b in v)
         out[k] = {"ms_per_step": tot / reps, "launches_per_step": len(v) // reps,
                   "avg_launch_ms": tot / max(1, len(v))}
+    out["by_entry"] = {k: {"ms_per_step": round(sum(a.elapsed_time(b) for a, b in v) / reps, 5),
+                           "calls_per_step": len(v) // reps} for k, v in by_entry.items()}
+    per = len(seq) // reps  # the calls of one step, in order, averaged over the reps
+    out["by_call"] = [[seq[i][0], round(sum(seq[r * per + i][1].elapsed_time(seq[r * per + i][2])
+                                            for r in range(reps)) / reps, 5)] for i in range(per)]
     out["gemm"]["flops_per_step"] = flops_per_gemm_step
     fused = getattr(getattr(model, "blk", None), "fused", False) and not getattr(model, "current", False)
     out["cast"]["bytes_per_step"] = cast_bytes(model.cfg, fused_gelu=fused)
@@ -519,7 +528,7 @@ def run_only(args, dev):
     shape = [int(v) for v in args.shape.split(",")]
     g = torch.Generator(device="cpu").manual_seed(1)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    if args.only in ("gemm", "gemm_gelu", "mxgemm"):
+    if args.only in ("gemm", "gemm_gelu", "gemm_dgelu", "mxgemm"):
         M, N, K = shape
         A = torch.randint(0, 0x70, (M, K), dtype=torch.uint8, generator=g).to(dev)
         B = torch.randint(0, 0x70, (N, K), dtype=torch.uint8, generator=g).to(dev)
@@ -533,6 +542,15 @@ def run_only(args, dev):
             am = torch.zeros(1, dtype=torch.float32, device=dev)
             fn = lambda: fd.fp8_gemm_gelu_cast(A, fd.E4M3, B, fd.E4M3, one, one, D, fd.E4M3, one, q, qt,  # noqa: E731
                                                q_amax=am)
+        elif args.only == "gemm_dgelu":
+            h = wl.normal((M, N), 2.0, g, torch.bfloat16).to(dev)
+            q = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            qt = torch.empty((N, M), dtype=torch.uint8, device=dev)
+            am = torch.zeros(1, dtype=torch.float32, device=dev)
+            db = torch.empty(N, dtype=torch.float32, device=dev)
+            ws = torch.empty(fd.fp8_gemm_dgelu_workspace_size(M, N), dtype=torch.uint8, device=dev)
+            fn = lambda: fd.fp8_gemm_dgelu_cast(A, fd.E5M2, B, fd.E4M3, one, one, h, fd.E5M2, one, q, qt,  # noqa: E731
+                                                q_amax=am, dbias=db, workspace=ws)
         else:
             As = torch.randint(120, 134, (M, K // 32), dtype=torch.uint8, generator=g).to(dev)
             Bs = torch.randint(120, 134, (N, K // 32), dtype=torch.uint8, generator=g).to(dev)
@@ -621,7 +639,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="ln_mlp", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default=None, choices=["gemm", "gemm_gelu", "cast", "mxq", "mxgemm", "gelu", "dgelu",
+    ap.add_argument("--only", default=None, choices=["gemm", "gemm_gelu", "gemm_dgelu", "cast", "mxq", "mxgemm", "gelu", "dgelu",
                                                           "ln", "lnbwd"])
     ap.add_argument("--shape", default="8192,12288,4096")
     args = ap.parse_args()
@@ -678,8 +696,8 @@ def main():
                      "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},
         "cast": {"achieved_gbs": round(cast_gbs, 1), "peak_gbs": hbm, "frac": round(cast_gbs / hbm, 4),
                  "ms_per_step": round(c["ms_per_step"], 4), "launches_per_step": c["launches_per_step"]},
-        "kernels": {k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
-                    for k, v in kt.items()},
+        "kernels": {k: ({kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        if isinstance(v, dict) else v) for k, v in kt.items()},
         "gpu_launches": model.launches_per_step() * args.steps,
         "e2e": {"value": round(flops * world / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

@@ -52,6 +52,9 @@ _SIGS = {
     "fp8_gemm": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
     "fp8_gemm_gelu_cast": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]),
+    "fp8_gemm_dgelu_workspace_size": (_sz, [_i64, _i64]),
+    "fp8_gemm_dgelu_cast": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _sz, _vp, _vp, _vp]),
     "mxfp8_scale_bytes": (_sz, [_i64, _i64]),
     "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "mxfp8_gemm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
@@ -276,6 +279,25 @@ def fp8_gemm_gelu_cast(A: torch.Tensor, a_dtype: int, B: torch.Tensor, b_dtype: 
     _check(_lib.fp8_gemm_gelu_cast(_p(A), a_dtype, _p(B), b_dtype, M, N, K, _p(a_scale_inv), _p(b_scale_inv), _p(bias),
                                    _hp(bias) if bias is not None else BF16, _p(H), q_dtype, _p(q_scale), _p(q), _p(q_t),
                                    _p(q_amax), _p(g), _p(dev_status), _stream(stream)), "fp8_gemm_gelu_cast")
+
+
+def fp8_gemm_dgelu_workspace_size(M: int, N: int) -> int:
+    return _lib.fp8_gemm_dgelu_workspace_size(M, N)
+
+
+def fp8_gemm_dgelu_cast(A: torch.Tensor, a_dtype: int, B: torch.Tensor, b_dtype: int, a_scale_inv, b_scale_inv,
+                        h: torch.Tensor, q_dtype: int, q_scale, q: torch.Tensor, q_t: torch.Tensor, q_amax=None,
+                        dbias=None, workspace=None, dg=None, dh=None, dev_status=None, stream=None) -> None:
+    """dg = A*B^T*sa_inv*sb_inv (bf16, not stored unless dg is given); q, q^T = FP8 codes of
+    dh = bf16(dg * GELU'(h)) at q_scale; amax |dh|; dbias = column sums of dh."""
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2 and tuple(h.shape) == (M, N) and h.dtype == torch.bfloat16
+    ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
+    _check(_lib.fp8_gemm_dgelu_cast(_p(A), a_dtype, _p(B), b_dtype, M, N, K, _p(a_scale_inv), _p(b_scale_inv), _p(h),
+                                    _p(dg), q_dtype, _p(q_scale), _p(q), _p(q_t), _p(q_amax), _p(dbias),
+                                    _p(workspace), ws_bytes, _p(dh), _p(dev_status), _stream(stream)),
+           "fp8_gemm_dgelu_cast")
 
 
 def mxfp8_scale_bytes(rows: int, cols: int) -> int:

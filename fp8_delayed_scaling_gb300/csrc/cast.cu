@@ -263,6 +263,10 @@ static void launch_colsum_reduce(const float *ws, int64_t n_tiles, int64_t cols,
                                                                                                        cols, dbias);
 }
 
+void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, cudaStream_t st) {
+    launch_colsum_reduce(ws, n_rows, cols, dbias, st);
+}
+
 template <int XKIND, int FMT>
 static void launch_cast(dim3 grid, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
                         uint8_t *out, uint8_t *out_t, float *amax, float *ws) {

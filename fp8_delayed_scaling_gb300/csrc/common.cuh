@@ -20,6 +20,9 @@ fp8dl_status check_launch(const char *what);
 // Validates the current device (sm_103) once per device and caches the SM count.
 fp8dl_status current_device(int *dev, int *num_sms);
 
+// dbias[c] = sum over r of ws[r * cols + c] (fp32, a fixed order), one launch on st.
+void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, cudaStream_t st);
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool dim_ok(int64_t d, int64_t mult) { return d > 0 && d % mult == 0 && d <= (int64_t(1) << 31); }
 
@@ -139,12 +142,13 @@ __device__ __forceinline__ float gelu_f32(float h) {
 // GELU(h) rounded to bf16 like the tensor it stands for.
 __device__ __forceinline__ float gelu_bf16(float h) { return bf16_round(gelu_f32(h)); }
 
-// dh = dg * GELU'(h) = dg * (Phi(h) + h * phi(h)), rounded to bf16.
-__device__ __forceinline__ float dgelu_bf16(float dg, float h) {
+// dh = dg * GELU'(h) = dg * (Phi(h) + h * phi(h)) in fp32, and rounded to bf16.
+__device__ __forceinline__ float dgelu_f32(float dg, float h) {
     const NormalTail n = normal_tail(h);
     const float cdf = h >= 0.0f ? 1.0f - n.tail : n.tail;
-    return bf16_round(dg * fmaf(h * 0.3989422804f, n.e, cdf));
+    return dg * fmaf(h * 0.3989422804f, n.e, cdf);
 }
+__device__ __forceinline__ float dgelu_bf16(float dg, float h) { return bf16_round(dgelu_f32(dg, h)); }
 
 
 }  // namespace fp8dl

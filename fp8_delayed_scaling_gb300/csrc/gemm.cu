@@ -59,6 +59,9 @@ struct GemmArgs {
     const float *q_scale;  // device float
     float *q_amax;         // device float, max-ed with max |g|, or NULL
     void *g_out;           // [M x N] bf16 g, or NULL
+    // fused dGELU (EPI = 2): dh = dGELU(D, h) takes the place of g above
+    const void *h_in;      // [M x N] bf16 h, the forward's GELU input
+    float *ws;             // [ceil(M/32) x N] column sums of dh per 32-row group, or NULL
 };
 
 // Tile order.  Tiles come in groups of `group` tiles along one dimension; inside
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
                 if (row_ok && n0 < args.N) {
                     float v[32];
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * s;
+                    for (int j = 0; j < 32; j++) v[j] = __fmul_rn(__uint_as_float(r[j]), s);  // not fused with + bias
                     if (args.bias_dtype >= 0) {
 #pragma unroll
                         for (int j = 0; j < 32; j++)
@@ -310,6 +313,9 @@ constexpr int smem_bytes(int epi) { return STAGES * STAGE_BYTES + 1024 + (epi ? 
 // (the transposed codes of the CTA's 128 x 256 output are staged in shared
 // memory and written with one TMA tensor store), and amax |g| — the cast that
 // delayed scaling lets run inside the GEMM, its scale being known in advance.
+// EPI = 2 (fc2 dgrad): the same with dh = bf16(dD * GELU'(h)) from the
+// forward's h, D = dD optional, plus per-32-row column sums of dh (the fc1
+// bias gradient before its final reduction).
 // Bias of 32 consecutive output columns starting at n0 (0 beyond N).
 __device__ __forceinline__ void load_bias32(const void *bias, int dtype, int64_t n0, int64_t N, float (&b)[32]) {
     if (n0 + 32 <= N && dtype == FP8DL_BF16) {
@@ -327,6 +333,20 @@ __device__ __forceinline__ void load_bias32(const void *bias, int dtype, int64_t
     } else {
 #pragma unroll
         for (int j = 0; j < 32; j++) b[j] = n0 + j < N ? load_bias(bias, dtype, n0 + j) : 0.0f;
+    }
+}
+
+// One step of a reduce-scatter over the 32 lanes: lane l keeps the half of
+// y[0 .. 2O) selected by bit O of l and adds the partner's (lane l ^ O) copy
+// of that half, leaving the sums in y[0 .. O).
+template <int O, int L>
+__device__ __forceinline__ void reduce_scatter_step(float (&y)[L], int lane) {
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int i = 0; i < O; i++) {
+        const float send = up ? y[i] : y[i + O];
+        const float keep = up ? y[i + O] : y[i];
+        y[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
     }
 }
 
@@ -472,10 +492,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
         for (int64_t tile = pair; tile < tiles; tile += npairs) {
             int64_t tm, tn;
             tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
-            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
-            tc_fence_after();
             const int64_t row = tm * 2 * BM + rank * BM + 32 * q + lane;
             const bool row_ok = row < args.M;
+            const __nv_bfloat16 *hrow =
+                EPI == 2 ? static_cast<const __nv_bfloat16 *>(args.h_in) + row * args.N : nullptr;
+            if (EPI == 2 && row_ok && tn * BN + part * CHUNKS * 32 < args.N)  // this thread's h: one 128-byte line
+                prefetch_l2(hrow + tn * BN + part * CHUNKS * 32);
+            if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
+            tc_fence_after();
             if (EPI && stored) {  // the previous tile's transposed codes must have left shared memory
                 if (threadIdx.x == 64) bulk_wait_read();
                 named_barrier(1, NEPI);
@@ -483,20 +507,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
 #pragma unroll 1
             for (int cc = 0; cc < CHUNKS; cc++) {
                 const int c = part * CHUNKS + cc;  // chunk of 32 columns within the tile
+                const int64_t n0 = tn * BN + c * 32;
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * BN + c * 32) + ((uint32_t)(32 * q) << 16), r);
-                tmem_ld_wait();
-                const int64_t n0 = tn * BN + c * 32;
                 float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * sc;
                 if (args.bias_dtype >= 0) {
                     float b[32];
                     load_bias32(args.bias, args.bias_dtype, n0, args.N, b);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] += b[j];
+                    for (int j = 0; j < 32; j++) v[j] = __fmul_rn(__uint_as_float(r[j]), sc) + b[j];  // two roundings
+                } else {
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * sc;
                 }
-                uint32_t hw[16];  // the bf16 output as packed pairs (also the GELU's input)
+                uint32_t hw[16];  // the bf16 output as packed pairs (also the activation's input)
                 if (EPI || args.d_dtype == FP8DL_BF16) {
 #pragma unroll
                     for (int p = 0; p < 16; p++) {
@@ -504,7 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                         hw[p] = *reinterpret_cast<uint32_t *>(&h);
                     }
                 }
-                if (row_ok && n0 < args.N) {
+                if (row_ok && n0 < args.N && args.D) {
                     if (EPI || args.d_dtype == FP8DL_BF16) {
                         __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.D) + row * args.N + n0;
 #pragma unroll
@@ -522,48 +548,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     }
                 }
                 if (EPI) {
-                    // g = GELU of the bf16 output, its codes, and the transposed staging.
-                    // Columns beyond N hold exact zeros (zero-filled B rows, zero bias), so
-                    // g = 0 there; rows beyond M are kept out of the amax below.
-                    uint32_t code[8], gw[16];  // codes; bf16 g as packed pairs
+                    // y = GELU(D) (EPI 1) or dGELU(D, h) (EPI 2) in bf16, its codes, amax and the
+                    // transposed staging.  Columns beyond N hold exact zeros (zero-filled B rows,
+                    // zero bias) and so do rows beyond M in EPI 2 (no bias, h = 0); rows beyond M
+                    // are kept out of the EPI 1 amax below.
+                    // Groups of 8 columns: y, its bf16 store, codes and transposed staging; the
+                    // EPI 2 column sums start at once (first reduce-scatter step, below).
+                    uint32_t code[8];
+                    float ys[16];  // EPI 2: y of columns 0-15, then the pair sums (j, j + 16)
                     float cmax = 0.0f;
+                    const bool row_store = row_ok && n0 < args.N;
+                    uint8_t *st = qt_stage + (c * 32) * BM + 32 * q + lane;  // column (c*32 + j), row (32q + lane)
+                    // EPI 2: h of 8 columns per group, loaded one group ahead (0 outside the matrix)
+                    auto load_h8 = [&](int g) -> uint4 {
+                        return (EPI == 2 && row_ok && n0 + 8 * g < args.N)
+                                   ? __ldg(reinterpret_cast<const uint4 *>(hrow + n0 + 8 * g))
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                    };
+                    uint4 hcur = load_h8(0);
 #pragma unroll
-                    for (int k = 0; k < 8; k++) {
-                        float gg[4];
+                    for (int g = 0; g < 4; g++) {
+                        const uint4 hnext = g < 3 ? load_h8(g + 1) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t hv[4] = {hcur.x, hcur.y, hcur.z, hcur.w};
+                        uint32_t gw[4];
+                        float y8[8];
 #pragma unroll
-                        for (int p = 0; p < 2; p++) {
-                            const uint32_t w = hw[2 * k + p];
-                            __nv_bfloat162 g2 = __floats2bfloat162_rn(gelu_f32(bf16_lo(w)), gelu_f32(bf16_hi(w)));
-                            gw[2 * k + p] = *reinterpret_cast<uint32_t *>(&g2);
-                            gg[2 * p] = bf16_lo(gw[2 * k + p]);
-                            gg[2 * p + 1] = bf16_hi(gw[2 * k + p]);
+                        for (int p = 0; p < 4; p++) {
+                            const uint32_t w = hw[4 * g + p];
+                            float lo, hi;
+                            if (EPI == 1) {
+                                lo = gelu_f32(bf16_lo(w));
+                                hi = gelu_f32(bf16_hi(w));
+                            } else {
+                                lo = dgelu_f32(bf16_lo(w), bf16_lo(hv[p]));
+                                hi = dgelu_f32(bf16_hi(w), bf16_hi(hv[p]));
+                            }
+                            __nv_bfloat162 y2 = __floats2bfloat162_rn(lo, hi);
+                            gw[p] = *reinterpret_cast<uint32_t *>(&y2);
+                            y8[2 * p] = bf16_lo(gw[p]);
+                            y8[2 * p + 1] = bf16_hi(gw[p]);
                         }
 #pragma unroll
-                        for (int j = 0; j < 4; j++) cmax = fmaxf(cmax, fabsf(gg[j]));
-                        code[k] = args.q_fmt == FP8DL_E4M3
-                                      ? pack4<FP8DL_E4M3>(__fmul_rn(gg[0], qscale), __fmul_rn(gg[1], qscale),
-                                                          __fmul_rn(gg[2], qscale), __fmul_rn(gg[3], qscale))
-                                      : pack4<FP8DL_E5M2>(__fmul_rn(gg[0], qscale), __fmul_rn(gg[1], qscale),
-                                                          __fmul_rn(gg[2], qscale), __fmul_rn(gg[3], qscale));
+                        for (int j = 0; j < 8; j++) cmax = fmaxf(cmax, fabsf(y8[j]));
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; h2++) {
+                            const float *y4 = y8 + 4 * h2;
+                            code[2 * g + h2] =
+                                args.q_fmt == FP8DL_E4M3
+                                    ? pack4<FP8DL_E4M3>(__fmul_rn(y4[0], qscale), __fmul_rn(y4[1], qscale),
+                                                        __fmul_rn(y4[2], qscale), __fmul_rn(y4[3], qscale))
+                                    : pack4<FP8DL_E5M2>(__fmul_rn(y4[0], qscale), __fmul_rn(y4[1], qscale),
+                                                        __fmul_rn(y4[2], qscale), __fmul_rn(y4[3], qscale));
+                        }
+                        if (args.g_out && row_store && n0 + 8 * g < args.N)
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.g_out) + row * args.N + n0 +
+                                                       8 * g) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+#pragma unroll
+                        for (int j = 0; j < 8; j++)
+                            st[(8 * g + j) * BM] = (uint8_t)(code[2 * g + (j >> 2)] >> (8 * (j & 3)));
+                        if (EPI == 2) {
+                            const bool up = (lane & 16) != 0;
+#pragma unroll
+                            for (int j = 0; j < 8; j++) {
+                                if (g < 2) {
+                                    ys[8 * g + j] = y8[j];
+                                } else {  // column i + 16 meets column i: lane keeps one, trades the other
+                                    const int i = 8 * (g - 2) + j;
+                                    const float send = up ? ys[i] : y8[j];
+                                    const float keep = up ? y8[j] : ys[i];
+                                    ys[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                                }
+                            }
+                        }
+                        hcur = hnext;
                     }
                     if (row_ok) gmax = fmaxf(gmax, cmax);
-                    if (row_ok && n0 < args.N) {
+                    if (row_store) {
                         uint8_t *qrow = args.q + row * args.N + n0;
                         if (n0 + 16 <= args.N) *reinterpret_cast<uint4 *>(qrow) = make_uint4(code[0], code[1], code[2], code[3]);
                         if (n0 + 32 <= args.N)
                             *reinterpret_cast<uint4 *>(qrow + 16) = make_uint4(code[4], code[5], code[6], code[7]);
-                        if (args.g_out) {
-                            __nv_bfloat16 *grow = static_cast<__nv_bfloat16 *>(args.g_out) + row * args.N + n0;
-#pragma unroll
-                            for (int g = 0; g < 4; g++)
-                                if (n0 + 8 * g < args.N)
-                                    *reinterpret_cast<uint4 *>(grow + 8 * g) =
-                                        make_uint4(gw[4 * g], gw[4 * g + 1], gw[4 * g + 2], gw[4 * g + 3]);
-                        }
                     }
-                    uint8_t *st = qt_stage + (c * 32) * BM + 32 * q + lane;  // column (c*32 + j), row (32q + lane)
-#pragma unroll
-                    for (int j = 0; j < 32; j++) st[j * BM] = (uint8_t)(code[j >> 2] >> (8 * (j & 3)));
+                    if (EPI == 2 && args.ws) {
+                        // the rest of the reduce-scatter: lane l ends with column n0 + l summed
+                        // over the warp's 32 rows
+                        reduce_scatter_step<8>(ys, lane);
+                        reduce_scatter_step<4>(ys, lane);
+                        reduce_scatter_step<2>(ys, lane);
+                        reduce_scatter_step<1>(ys, lane);
+                        const int64_t row32 = tm * (2 * BM / 32) + rank * (BM / 32) + q;  // 32-row group
+                        if (row32 * 32 < args.M && n0 + lane < args.N) args.ws[row32 * args.N + n0 + lane] = ys[0];
+                    }
                 }
             }
             tc_fence_before();
@@ -577,7 +652,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
             if (EPI) {  // the CTA's transposed codes: one TMA store of [256 columns x 128 rows]
                 fence_proxy_async_smem();
                 named_barrier(1, NEPI);
-                if (threadIdx.x == 64) {
+                if (threadIdx.x == 64 && tm * 2 * BM + rank * BM < args.M) {  // no store when all rows lie beyond M
                     tma_store_2d(&tmap_qt, smem_u32(qt_stage), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * BN));
                     bulk_commit();
                 }
@@ -666,8 +741,9 @@ void pick_raster(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n
 }
 
 static fp8dl_status check_gemm_common(int64_t M, int64_t N, int64_t K, int64_t mult, const void *A, const void *B,
-                                      const void *bias, int32_t bias_dtype, const void *D, int32_t d_dtype) {
-    FP8DL_CHECK_ARG(A && B && D, "A, B and D must be non-NULL");
+                                      const void *bias, int32_t bias_dtype, const void *D, int32_t d_dtype,
+                                      bool d_required = true) {
+    FP8DL_CHECK_ARG(A && B && (D || !d_required), "A, B and D must be non-NULL");
     FP8DL_CHECK_ARG(d_dtype == FP8DL_BF16 || d_dtype == FP8DL_F32, "d_dtype must be FP8DL_BF16 or FP8DL_F32");
     FP8DL_CHECK_ARG(!bias || bias_dtype == FP8DL_BF16 || bias_dtype == FP8DL_F32,
                     "bias_dtype must be FP8DL_BF16 or FP8DL_F32");
@@ -709,6 +785,9 @@ static fp8dl_status gemm_device_setup(int dev, int sms) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  g2::smem_bytes(1));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g2::smem_bytes(2));
     if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     // how many CTA pairs can be resident at once (both pair kernels hold one CTA per SM)
     cudaLaunchConfig_t cfg = {};
@@ -734,7 +813,8 @@ static bool gemm_use_pair(int dev, int64_t M) {
     return g_pair_clusters[dev] > 0 && (forced == 2 || (forced == 0 && M > g1::BM));
 }
 
-// Shared launch path of fp8_gemm (epi = 0) and fp8_gemm_gelu_cast (epi = 1, pair kernel only).
+// Shared launch path of fp8_gemm (epi = 0), fp8_gemm_gelu_cast (epi = 1) and
+// fp8_gemm_dgelu_cast (epi = 2); the fused epilogues exist in the pair kernel only.
 static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
                                 int64_t N, int64_t K, GemmArgs &args, int epi, int dev, int sms, bool use_pair,
                                 cudaStream_t stream) {
@@ -761,13 +841,17 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
         pick_raster(M, N, K, 2 * g2::BM, g2::BN, args.raster_n, args.group);
         const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
         const int64_t pairs = tiles < g_pair_clusters[dev] ? tiles : g_pair_clusters[dev];
-        if (epi)
+        if (epi == 2)
+            fp8_gemm_pair_kernel<2>
+                <<<(unsigned)(2 * pairs), g2::threads(2), g2::smem_bytes(2), stream>>>(ta, tb, tq, args);
+        else if (epi == 1)
             fp8_gemm_pair_kernel<1>
                 <<<(unsigned)(2 * pairs), g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
         else
             fp8_gemm_pair_kernel<0>
                 <<<(unsigned)(2 * pairs), g2::threads(0), g2::smem_bytes(0), stream>>>(ta, tb, tq, args);
-        return check_launch(epi ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");
+        return check_launch(epi == 2 ? "fp8_gemm_dgelu_cast(pair)"
+                                     : epi == 1 ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");
     }
     FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g1::BK, g1::BN,
                                 CU_TENSOR_MAP_SWIZZLE_128B));
@@ -782,8 +866,8 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
 static fp8dl_status gemm_args(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype, int64_t M,
                               int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
                               const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype, int32_t *dev_status,
-                              GemmArgs &args) {
-    FP8DL_TRY(check_gemm_common(M, N, K, 16, A, B, bias, bias_dtype, D, d_dtype));
+                              GemmArgs &args, bool d_required = true) {
+    FP8DL_TRY(check_gemm_common(M, N, K, 16, A, B, bias, bias_dtype, D, d_dtype, d_required));
     FP8DL_CHECK_ARG((a_dtype == FP8DL_E4M3 || a_dtype == FP8DL_E5M2) && (b_dtype == FP8DL_E4M3 || b_dtype == FP8DL_E5M2),
                     "a_dtype and b_dtype must be E4M3 or E5M2");
     FP8DL_CHECK_ARG(a_scale_inv && b_scale_inv, "a_scale_inv and b_scale_inv must be non-NULL");
@@ -843,4 +927,50 @@ extern "C" fp8dl_status fp8_gemm_gelu_cast(const uint8_t *A, int32_t a_dtype, co
     args.q_amax = q_amax;
     args.g_out = g;
     return launch_gemm(A, a_dtype, B, b_dtype, M, N, K, args, 1, dev, sms, true, (cudaStream_t)stream);
+}
+
+extern "C" size_t fp8_gemm_dgelu_workspace_size(int64_t M, int64_t N) {
+    if (M <= 0 || N <= 0) return 0;
+    return (size_t)((M + 31) / 32) * (size_t)N * sizeof(float);
+}
+
+extern "C" fp8dl_status fp8_gemm_dgelu_cast(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype,
+                                            int64_t M, int64_t N, int64_t K, const float *a_scale_inv,
+                                            const float *b_scale_inv, const void *h, void *dg, int32_t q_dtype,
+                                            const float *q_scale, uint8_t *q, uint8_t *q_t, float *q_amax,
+                                            float *dbias, void *workspace, size_t workspace_bytes, void *dh,
+                                            int32_t *dev_status, fp8dl_stream_t stream) {
+    GemmArgs args;
+    FP8DL_TRY(gemm_args(A, a_dtype, B, b_dtype, M, N, K, a_scale_inv, b_scale_inv, nullptr, FP8DL_BF16, dg, FP8DL_BF16,
+                        dev_status, args, /*d_required=*/false));
+    FP8DL_CHECK_ARG(q_dtype == FP8DL_E4M3 || q_dtype == FP8DL_E5M2, "q_dtype must be E4M3 or E5M2");
+    FP8DL_CHECK_ARG(h && q && q_t && q_scale, "h, q, q_t and q_scale must be non-NULL");
+    if (!aligned16(h) || !aligned16(q) || !aligned16(q_t) || !aligned16(dh))
+        return fail(FP8DL_ERR_ALIGN, "h, q, q_t and dh must be 16-byte aligned");
+    if (dbias) {
+        if (!workspace || workspace_bytes < fp8_gemm_dgelu_workspace_size(M, N))
+            return fail(FP8DL_ERR_WORKSPACE, "dbias needs a workspace of %zu bytes (got %zu)",
+                        fp8_gemm_dgelu_workspace_size(M, N), workspace ? workspace_bytes : (size_t)0);
+        if (!aligned16(workspace)) return fail(FP8DL_ERR_ALIGN, "workspace must be 16-byte aligned");
+    }
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
+    FP8DL_TRY(gemm_device_setup(dev, sms));
+    if (g_pair_clusters[dev] < 1)
+        return fail(FP8DL_ERR_UNSUPPORTED_DEVICE, "fp8_gemm_dgelu_cast needs resident CTA-pair clusters");
+    args.q = q;
+    args.q_t = q_t;
+    args.q_fmt = q_dtype;
+    args.q_scale = q_scale;
+    args.q_amax = q_amax;
+    args.g_out = dh;
+    args.h_in = h;
+    args.ws = dbias ? static_cast<float *>(workspace) : nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    FP8DL_TRY(launch_gemm(A, a_dtype, B, b_dtype, M, N, K, args, 2, dev, sms, true, st));
+    if (dbias) {
+        colsum_reduce(args.ws, (M + 31) / 32, N, dbias, st);
+        FP8DL_TRY(check_launch("fp8_gemm_dgelu_cast(dbias reduce)"));
+    }
+    return FP8DL_OK;
 }

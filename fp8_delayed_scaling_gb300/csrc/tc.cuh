@@ -9,6 +9,11 @@
 
 namespace fp8dl {
 
+// Prefetch the global line holding p into L2 (no register, no completion).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

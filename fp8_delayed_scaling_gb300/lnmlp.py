@@ -13,8 +13,10 @@ scale, so each activation is fused with the cast of its output:
             cast W2           -> qW2, qW2^T        (slot fc2.w)
             y  = fc2(q_g, qW2) + b2                (bf16)
   backward  cast dY (+db2)    -> qdY, qdY^T        (slot fc2.grad)
-            dg  = dgrad(qdY, qW2^T);  dW2 = wgrad(qdY^T, q_g^T)
-            dGELU+cast(dg, h) (+db1) -> qdh, qdh^T (slot fc1.grad)
+            dW2 = wgrad(qdY^T, q_g^T);  dg = dgrad(qdY, qW2^T)
+            dGELU+cast(dg, h) (+db1) -> qdh, qdh^T (slot fc1.grad; fused into
+                                                    the dgrad epilogue after step 0,
+                                                    so dg never reaches HBM)
             dln = dgrad(qdh, qW1^T);  dW1 = wgrad(qdh^T, q_ln^T)
             LN backward(dln, x) -> dx, dgamma, dbeta
   update    all six slots, one launch.
@@ -38,7 +40,8 @@ from __future__ import annotations
 import torch
 
 from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose, fp8_cast_workspace_size,
-               fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_gemm_gelu_cast, fp8_layernorm_bwd,
+               fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_gemm_dgelu_cast, fp8_gemm_dgelu_workspace_size,
+               fp8_gemm_gelu_cast, fp8_layernorm_bwd,
                fp8_layernorm_bwd_workspace_size, fp8_layernorm_cast, fp8_seed_amax_history)
 from .linear import WeightCache
 
@@ -60,7 +63,9 @@ class Fp8LayerNormMLP:
                  eps: float = 1e-5, keep_activations: bool = False, scaling: str = "delayed", fused: bool = True):
         assert scaling in ("delayed", "current")
         self.scaling = scaling
-        self.fused = fused  # GELU + cast inside the fc1 GEMM's epilogue (delayed scaling, after step 0)
+        # GELU + cast inside the fc1 GEMM's epilogue and dGELU + cast (+ db1) inside the fc2
+        # dgrad's (delayed scaling, after step 0)
+        self.fused = fused
         self.state = state
         self.base = block_index * SLOTS
         self.recipe = state.recipe
@@ -93,6 +98,8 @@ class Fp8LayerNormMLP:
         self.dgamma, self.dbeta = torch.empty(H, **f32), torch.empty(H, **f32)
         self.ws_cast = torch.empty(max(fp8_cast_workspace_size(M, H), fp8_cast_workspace_size(M, F)), **u8)
         self.ws_ln = torch.empty(fp8_layernorm_bwd_workspace_size(M, H), **u8)
+        # fused dGELU epilogue: fc1 bias-gradient partials per 32-row group
+        self.ws_dgelu = torch.empty(fp8_gemm_dgelu_workspace_size(M, F), **u8) if fused else None
         self.w1cache, self.w2cache = WeightCache(self.qw1, self.qw1T), WeightCache(self.qw2, self.qw2T)
         self.w1_sinv = self.w2_sinv = None  # the weights' decode factors used by this step's forward
         self.keep = keep_activations
@@ -205,14 +212,25 @@ class Fp8LayerNormMLP:
             self._seed(FC2_GRAD, 1, stream)
         fp8_cast_amax_transpose(dy, g, st.scale(s(FC2_GRAD)), out=self.qdy, out_t=self.qdyT,
                                 amax=st.amax(s(FC2_GRAD)), dbias=self.db2, workspace=self.ws_cast, stream=stream)
-        fp8_gemm(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), self.w2_sinv, self.dg, stream=stream)
         fp8_gemm(self.qdyT, g, self.q_gT, E4M3, st.scale_inv(s(FC2_GRAD)), st.scale_inv(s(FC2_IN)), self.dw2,
                  stream=stream)
+        if self.fused and not seed:  # dgrad with dGELU + cast + dbias in its epilogue; dg stays on chip
+            fp8_gemm_dgelu_cast(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), self.w2_sinv, self.h, g,
+                                st.scale(s(FC1_GRAD)), self.qdh, self.qdhT, q_amax=st.amax(s(FC1_GRAD)),
+                                dbias=self.db1, workspace=self.ws_dgelu, dg=self.dg if self.keep else None,
+                                dh=self.dh, stream=stream)
+            return self._backward_fc1(x, stream)
+        fp8_gemm(self.qdy, g, self.qw2T, E4M3, st.scale_inv(s(FC2_GRAD)), self.w2_sinv, self.dg, stream=stream)
         if seed:
             fp8_dgelu_cast(self.dg, self.h, g, None, amax=st.amax(s(FC1_GRAD)), stream=stream)
             self._seed(FC1_GRAD, 1, stream)
         fp8_dgelu_cast(self.dg, self.h, g, st.scale(s(FC1_GRAD)), out=self.qdh, out_t=self.qdhT,
                        amax=st.amax(s(FC1_GRAD)), dbias=self.db1, workspace=self.ws_cast, dh=self.dh, stream=stream)
+        return self._backward_fc1(x, stream)
+
+    def _backward_fc1(self, x: torch.Tensor, stream):
+        """fc1 dgrad and wgrad from the dh codes, then the LayerNorm backward."""
+        st, s, g = self.state, self.slot, self.gfmt
         fp8_gemm(self.qdh, g, self.qw1T, E4M3, st.scale_inv(s(FC1_GRAD)), self.w1_sinv, self.dln, stream=stream)
         fp8_gemm(self.qdhT, g, self.q_lnT, E4M3, st.scale_inv(s(FC1_GRAD)), st.scale_inv(s(FC1_IN)), self.dw1,
                  stream=stream)

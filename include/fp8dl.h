@@ -222,6 +222,29 @@ fp8dl_status fp8_gemm_gelu_cast(const uint8_t *A, int32_t a_dtype, const uint8_t
                                 int32_t q_dtype, const float *q_scale, uint8_t *q, uint8_t *q_t,
                                 float *q_amax, void *g, int32_t *dev_status, fp8dl_stream_t stream);
 
+/* FP8 GEMM whose epilogue applies dGELU and the FP8 cast of the result (the
+ * fc2 dgrad GEMM of a LayerNormMLP feeding the fc1 backward), with the fc1
+ * bias gradient.  As for fp8_gemm_gelu_cast, the delayed scale of the output
+ * is known before the GEMM, so dg never makes an HBM round trip:
+ *   dg[m,n] = bf16( acc[m,n] * fl32(a_scale_inv * b_scale_inv) )   (no bias)
+ *   dh = bf16( dg * GELU'(h) )  (erf form; see fp8_dgelu_cast), h [M x N] bf16
+ *   q = enc(fl32(dh * q_scale)) [M x N], q_t = q^T [N x M], *q_amax max-ed with max |dh|
+ *   dbias[n] = sum over m of dh[m,n] (fp32, a fixed order), or NULL
+ *   dg and dh [M x N] bf16 receive those tensors, or NULL.
+ * workspace: fp8_gemm_dgelu_workspace_size(M, N) bytes (16-byte aligned),
+ * needed only when dbias != NULL.  Codes, amax, dg and dh are identical to
+ * fp8_gemm followed by fp8_dgelu_cast; dbias agrees within its summation
+ * bound (the order of the sum differs).  Needs CTA-pair clusters
+ * (FP8DL_ERR_UNSUPPORTED_DEVICE otherwise). */
+size_t fp8_gemm_dgelu_workspace_size(int64_t M, int64_t N);
+
+fp8dl_status fp8_gemm_dgelu_cast(const uint8_t *A, int32_t a_dtype, const uint8_t *B, int32_t b_dtype,
+                                 int64_t M, int64_t N, int64_t K, const float *a_scale_inv,
+                                 const float *b_scale_inv, const void *h, void *dg, int32_t q_dtype,
+                                 const float *q_scale, uint8_t *q, uint8_t *q_t, float *q_amax,
+                                 float *dbias, void *workspace, size_t workspace_bytes, void *dh,
+                                 int32_t *dev_status, fp8dl_stream_t stream);
+
 /* ----------------------------------------------------------------------------
  * MXFP8 quantisation (block-scaled FP8, named by the Transformer Engine
  * README).  x [rows x cols] (bf16 or fp32).  Blocks are 32 consecutive

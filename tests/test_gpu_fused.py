@@ -62,3 +62,67 @@ def test_fused_gelu_epilogue_matches_unfused_and_oracle(M, N, K):
     qo = oracle.quantize(0, gb, 37.0)
     assert np.array_equal(q1.cpu().numpy(), qo) and np.array_equal(t1.cpu().numpy(), qo.T)
     assert a1.item() == oracle.amax(gb)
+
+
+def _codes_fmt(rng, fmt, shape, lim=8.0):
+    tab = oracle.decode_table(fmt)
+    ok = np.array([c for c in range(256) if np.isfinite(tab[c]) and abs(tab[c]) <= lim], np.uint8)
+    return ok[rng.integers(0, ok.size, shape)]
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 128), (384, 768, 1040), (2048, 4096, 1024), (128, 256, 64),
+                                   (272, 528, 256), (48, 80, 32)])
+def test_fused_dgelu_epilogue_matches_unfused_and_oracle(M, N, K, monkeypatch):
+    """fp8_gemm_dgelu_cast (fc2 dgrad with dGELU + E5M2 cast + amax + db1 in its epilogue)
+    against fp8_gemm + fp8_dgelu_cast on the same pair kernel, and against the oracle."""
+    import fp8_delayed_scaling_gb300 as fd
+    monkeypatch.setenv("FP8DL_GEMM_VARIANT", "2sm")  # the unfused GEMM on the fused one's kernel
+    dev = gpu()
+    rng = np.random.default_rng(3 * M + 5 * N + K)
+    A = torch.from_numpy(_codes_fmt(rng, 1, (M, K))).to(dev)  # qdY, E5M2
+    B = torch.from_numpy(_codes_fmt(rng, 0, (N, K))).to(dev)  # qW2^T, E4M3
+    h = wl.normal((M, N), 2.0, wl.generator(71, "fh/%d/%d" % (M, N)), torch.bfloat16)
+    hd = h.to(dev)
+    sa = torch.tensor([0.05], device=dev)
+    sb = torch.tensor([0.03], device=dev)
+    qs = torch.tensor([1024.0], device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    ws_f = torch.empty(fd.fp8_gemm_dgelu_workspace_size(M, N), **u8)
+    ws_u = torch.empty(fd.fp8_cast_workspace_size(M, N), **u8)
+    dg1, dg2 = torch.full((M, N), float("nan"), **bf), torch.full((M, N), float("nan"), **bf)
+    dh1, dh2 = torch.empty((M, N), **bf), torch.empty((M, N), **bf)
+    q1, q2, q3 = (torch.full((M, N), 0xAA, **u8) for _ in range(3))
+    t1, t2, t3 = (torch.full((N, M), 0xAA, **u8) for _ in range(3))
+    a1, a2, a3 = (torch.zeros(1, device=dev) for _ in range(3))
+    db1, db2, db3 = (torch.full((N,), float("nan"), device=dev) for _ in range(3))
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    fd.fp8_gemm_dgelu_cast(A, fd.E5M2, B, fd.E4M3, sa, sb, hd, fd.E5M2, qs, q1, t1, a1, dbias=db1, workspace=ws_f,
+                           dg=dg1, dh=dh1, dev_status=st)
+    fd.fp8_gemm(A, fd.E5M2, B, fd.E4M3, sa, sb, dg2)
+    fd.fp8_dgelu_cast(dg2, hd, fd.E5M2, qs, out=q2, out_t=t2, amax=a2, dbias=db2, workspace=ws_u, dh=dh2)
+    # the production form: neither dg nor dh leaves the chip
+    fd.fp8_gemm_dgelu_cast(A, fd.E5M2, B, fd.E4M3, sa, sb, hd, fd.E5M2, qs, q3, t3, a3, dbias=db3, workspace=ws_f)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(dg1, dg2) and torch.equal(dh1, dh2)
+    assert torch.equal(q1, q2) and torch.equal(t1, t2) and a1.item() == a2.item()
+    assert torch.equal(q3, q1) and torch.equal(t3, t1) and a3.item() == a1.item()
+    assert torch.equal(db3, db1)  # a fixed summation order
+    dhb = host(dh1)
+    s, sabs = oracle.colsum(dhb)
+    for db in (db1, db2):
+        assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= M * 2.0 ** -24 * sabs + 1e-30)
+    # against the oracle: the GEMM within bound, dGELU within bound, codes bit-exact from dh
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    ms, ns = ms.ravel(), ns.ravel()
+    if ms.size > 200000:
+        sel = rng.choice(ms.size, 200000, replace=False)
+        ms, ns = ms[sel], ns[sel]
+    ref, absr = oracle.gemm_elems(A.cpu().numpy(), 1, B.cpu().numpy(), 0, 0.05, 0.03, None, ms, ns)
+    check_gemm(dg1, ref, absr, ms, ns, what="fused dg")
+    dr = oracle.dgelu(host(dg1), host(h))
+    assert np.all(np.abs(as_f64(dh1) - dr) <= 2.0 ** -7 * np.abs(dr) + 2.0 ** -21 * np.abs(as_f64(dg1)))
+    qo = oracle.quantize(1, dhb, 1024.0)
+    assert np.array_equal(q1.cpu().numpy(), qo) and np.array_equal(t1.cpu().numpy(), qo.T)
+    assert a1.item() == oracle.amax(dhb)
