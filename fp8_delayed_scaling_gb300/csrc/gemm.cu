@@ -305,7 +305,10 @@ constexpr int TMEM_COLS = 512;
 __host__ __device__ constexpr int epi_warps(int epi) { return epi ? 16 : 4; }
 __host__ __device__ constexpr int threads(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int QT_BYTES = BN * BM;  // transposed FP8 codes of one CTA's 128 x 256 output (fused epilogue)
-constexpr int smem_bytes(int epi) { return STAGES * STAGE_BYTES + 1024 + (epi ? QT_BYTES : 0) + 1024; }
+// The fused epilogues double-buffer their transposed-code tile, paid for with one operand stage.
+__host__ __device__ constexpr int stages(int epi) { return epi ? STAGES - 1 : STAGES; }
+__host__ __device__ constexpr int qt_bufs(int epi) { return epi ? 2 : 0; }
+constexpr int smem_bytes(int epi) { return stages(epi) * STAGE_BYTES + 1024 + qt_bufs(epi) * QT_BYTES + 1024; }
 }  // namespace g2
 
 // EPI = 0: D = round(acc * s + bias).  EPI = 1 (fc1 of the LayerNormMLP): also
@@ -350,22 +353,23 @@ __device__ __forceinline__ void reduce_scatter_step(float (&y)[L], int lane) {
     }
 }
 
-template <int EPI>
+template <int EPI, int QF>  // QF: FP8 format of the fused epilogue's codes
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_qt, const GemmArgs args) {
     using namespace g2;
+    constexpr int NST = stages(EPI);  // operand stages
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    uint8_t *bar_area = smem + STAGES * STAGE_BYTES;
+    uint8_t *bar_area = smem + NST * STAGE_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(bar_area);
-    uint64_t *empty = full + STAGES;
-    uint64_t *tfull = empty + STAGES;
+    uint64_t *empty = full + NST;
+    uint64_t *tfull = empty + NST;
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint8_t *qt_stage = bar_area + 1024;  // EPI = 1 only: [256 columns][128 rows] codes
+    uint8_t *qt_stage = bar_area + 1024;  // EPI >= 1: two [256 columns][128 rows] code tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -376,7 +380,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     const int num_kb = (int)((args.K + BK - 1) / BK);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; s++) {
+        for (int s = 0; s < NST; s++) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -421,15 +425,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmap_b, fb, kb * BK,
                                      (int32_t)(tn * BN + rank * BNH));
                     issued++;
-                    if (++s == STAGES) {
+                    if (++s == NST) {
                         s = 0;
                         ph ^= 1;
                     }
                 }
             }
             if (!ok && leader) {
-                for (int64_t i = issued - 1; i >= 0 && i >= issued - STAGES; i--)
-                    mbar_drain(smem_u32(&full[i % STAGES]), (uint32_t)((i / STAGES) & 1));
+                for (int64_t i = issued - 1; i >= 0 && i >= issued - NST; i--)
+                    mbar_drain(smem_u32(&full[i % NST]), (uint32_t)((i / NST) & 1));
             }
         }
     } else if (warp == 1) {
@@ -463,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     any = true;
                     last_bar = smem_u32(&empty[s]);
                     last_par = ph;
-                    if (++s == STAGES) {
+                    if (++s == NST) {
                         s = 0;
                         ph ^= 1;
                     }
@@ -484,11 +488,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
         constexpr int NEPI = 32 * epi_warps(EPI);            // epilogue threads
         const float sc = __fmul_rn(__ldg(args.a_scale_inv), __ldg(args.b_scale_inv));
         const float qscale = EPI ? __ldg(args.q_scale) : 0.0f;
+        // Transposed staging of the fused epilogue: qt_stage holds the CTA's q^T block as 256
+        // rows of 128 bytes (one per output column) in the TMA 128-byte swizzle (16-byte chunk
+        // k of row R at chunk k ^ (R & 7)).  A 4x4 byte transpose across each lane quad leaves
+        // lane l with column 2(l & 1) + ((l >> 1) & 1) of its 4-column word for the quad's
+        // rows 32q + 4(l >> 2) .. +3: one 32-bit store per word.
+
         float gmax = 0.0f;
         const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty[0]), 0), mapa_shared(smem_u32(&tempty[1]), 0)};
         int acc = 0;
         uint32_t aph = 0;
-        bool stored = false;
+        int jt = 0;  // tiles drained by this CTA
         for (int64_t tile = pair; tile < tiles; tile += npairs) {
             int64_t tm, tn;
             tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
@@ -500,10 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                 prefetch_l2(hrow + tn * BN + part * CHUNKS * 32);
             if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
             tc_fence_after();
-            if (EPI && stored) {  // the previous tile's transposed codes must have left shared memory
-                if (threadIdx.x == 64) bulk_wait_read();
-                named_barrier(1, NEPI);
-            }
+            uint8_t *qt_buf = qt_stage + (jt & 1) * QT_BYTES;  // free: see the barrier at the tile's end
 #pragma unroll 1
             for (int cc = 0; cc < CHUNKS; cc++) {
                 const int c = part * CHUNKS + cc;  // chunk of 32 columns within the tile
@@ -558,7 +565,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     float ys[16];  // EPI 2: y of columns 0-15, then the pair sums (j, j + 16)
                     float cmax = 0.0f;
                     const bool row_store = row_ok && n0 < args.N;
-                    uint8_t *st = qt_stage + (c * 32) * BM + 32 * q + lane;  // column (c*32 + j), row (32q + lane)
                     // EPI 2: h of 8 columns per group, loaded one group ahead (0 outside the matrix)
                     auto load_h8 = [&](int g) -> uint4 {
                         return (EPI == 2 && row_ok && n0 + 8 * g < args.N)
@@ -593,19 +599,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
 #pragma unroll
                         for (int h2 = 0; h2 < 2; h2++) {
                             const float *y4 = y8 + 4 * h2;
-                            code[2 * g + h2] =
-                                args.q_fmt == FP8DL_E4M3
-                                    ? pack4<FP8DL_E4M3>(__fmul_rn(y4[0], qscale), __fmul_rn(y4[1], qscale),
-                                                        __fmul_rn(y4[2], qscale), __fmul_rn(y4[3], qscale))
-                                    : pack4<FP8DL_E5M2>(__fmul_rn(y4[0], qscale), __fmul_rn(y4[1], qscale),
-                                                        __fmul_rn(y4[2], qscale), __fmul_rn(y4[3], qscale));
+                            code[2 * g + h2] = pack4<QF>(__fmul_rn(y4[0], qscale), __fmul_rn(y4[1], qscale),
+                                                         __fmul_rn(y4[2], qscale), __fmul_rn(y4[3], qscale));
                         }
                         if (args.g_out && row_store && n0 + 8 * g < args.N)
                             *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.g_out) + row * args.N + n0 +
                                                        8 * g) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
 #pragma unroll
-                        for (int j = 0; j < 8; j++)
-                            st[(8 * g + j) * BM] = (uint8_t)(code[2 * g + (j >> 2)] >> (8 * (j & 3)));
+                        for (int h2 = 0; h2 < 2; h2++) {
+                            // 4x4 byte transpose across the lane quad (rows), then one 32-bit store
+                            const uint32_t w = code[2 * g + h2];
+                            const uint32_t a1 =
+                                __byte_perm(w, __shfl_xor_sync(0xffffffffu, w, 1), (lane & 1) ? 0x3726u : 0x5140u);
+                            const uint32_t t =
+                                __byte_perm(a1, __shfl_xor_sync(0xffffffffu, a1, 2), (lane & 2) ? 0x3276u : 0x5410u);
+                            const int col = c * 32 + 8 * g + 4 * h2 + (((lane & 1) << 1) | ((lane >> 1) & 1));
+                            const int rb = 32 * q + 4 * (lane >> 2);  // first of the word's 4 rows
+                            *reinterpret_cast<uint32_t *>(qt_buf + col * BM + (((rb >> 4) ^ (col & 7)) << 4) + (rb & 15)) = t;
+                        }
                         if (EPI == 2) {
                             const bool up = (lane & 16) != 0;
 #pragma unroll
@@ -651,13 +662,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
             }
             if (EPI) {  // the CTA's transposed codes: one TMA store of [256 columns x 128 rows]
                 fence_proxy_async_smem();
+                // The previous tile's store (the other buffer, issued a tile ago) has finished reading
+                // before anyone passes this barrier, so the next tile may overwrite that buffer.
+                if (threadIdx.x == 64) bulk_wait_read();
                 named_barrier(1, NEPI);
                 if (threadIdx.x == 64 && tm * 2 * BM + rank * BM < args.M) {  // no store when all rows lie beyond M
-                    tma_store_2d(&tmap_qt, smem_u32(qt_stage), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * BN));
+                    tma_store_2d(&tmap_qt, smem_u32(qt_buf), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * BN));
                     bulk_commit();
                 }
-                stored = true;
             }
+            jt++;
             if (++acc == 2) {
                 acc = 0;
                 aph ^= 1;
@@ -779,15 +793,15 @@ static int g_pair_clusters[64];
 static fp8dl_status gemm_device_setup(int dev, int sms) {
     if (g_attr_set[dev]) return FP8DL_OK;
     cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g1::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 g2::smem_bytes(0));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 g2::smem_bytes(1));
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 g2::smem_bytes(2));
+    const void *pair_kernels[] = {(const void *)fp8_gemm_pair_kernel<0, 0>,
+                                  (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3>,
+                                  (const void *)fp8_gemm_pair_kernel<1, FP8DL_E5M2>,
+                                  (const void *)fp8_gemm_pair_kernel<2, FP8DL_E4M3>,
+                                  (const void *)fp8_gemm_pair_kernel<2, FP8DL_E5M2>};
+    const int pair_epi[] = {0, 1, 1, 2, 2};
+    for (int k = 0; k < 5 && e == cudaSuccess; k++)
+        e = cudaFuncSetAttribute(pair_kernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 g2::smem_bytes(pair_epi[k]));
     if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     // how many CTA pairs can be resident at once (both pair kernels hold one CTA per SM)
     cudaLaunchConfig_t cfg = {};
@@ -795,7 +809,7 @@ static fp8dl_status gemm_device_setup(int dev, int sms) {
     cfg.blockDim = dim3(g2::threads(1), 1, 1);
     cfg.dynamicSmemBytes = g2::smem_bytes(1);
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, fp8_gemm_pair_kernel<1>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3>, &cfg);
     if (e != cudaSuccess || clusters < 1) {
         cudaGetLastError();
         clusters = 0;  // the pair kernels are not used on this device
@@ -833,7 +847,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
         if (epi) {
             // q^T [N x M] codes, stored in boxes of 128 rows of the output (inner) x 256 columns
             FP8DL_TRY(encode_tmap_2d_u8(&tq, args.q_t, (uint64_t)M, (uint64_t)N, (uint64_t)M, g2::BM, g2::BN,
-                                        CU_TENSOR_MAP_SWIZZLE_NONE));
+                                        CU_TENSOR_MAP_SWIZZLE_128B));
         } else {
             tq = ta;  // unused
         }
@@ -841,15 +855,18 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
         pick_raster(M, N, K, 2 * g2::BM, g2::BN, args.raster_n, args.group);
         const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
         const int64_t pairs = tiles < g_pair_clusters[dev] ? tiles : g_pair_clusters[dev];
-        if (epi == 2)
-            fp8_gemm_pair_kernel<2>
-                <<<(unsigned)(2 * pairs), g2::threads(2), g2::smem_bytes(2), stream>>>(ta, tb, tq, args);
+        const unsigned grid = (unsigned)(2 * pairs);
+        const bool e4 = args.q_fmt == FP8DL_E4M3;
+        if (epi == 2 && e4)
+            fp8_gemm_pair_kernel<2, FP8DL_E4M3><<<grid, g2::threads(2), g2::smem_bytes(2), stream>>>(ta, tb, tq, args);
+        else if (epi == 2)
+            fp8_gemm_pair_kernel<2, FP8DL_E5M2><<<grid, g2::threads(2), g2::smem_bytes(2), stream>>>(ta, tb, tq, args);
+        else if (epi == 1 && e4)
+            fp8_gemm_pair_kernel<1, FP8DL_E4M3><<<grid, g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
         else if (epi == 1)
-            fp8_gemm_pair_kernel<1>
-                <<<(unsigned)(2 * pairs), g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
+            fp8_gemm_pair_kernel<1, FP8DL_E5M2><<<grid, g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
         else
-            fp8_gemm_pair_kernel<0>
-                <<<(unsigned)(2 * pairs), g2::threads(0), g2::smem_bytes(0), stream>>>(ta, tb, tq, args);
+            fp8_gemm_pair_kernel<0, 0><<<grid, g2::threads(0), g2::smem_bytes(0), stream>>>(ta, tb, tq, args);
         return check_launch(epi == 2 ? "fp8_gemm_dgelu_cast(pair)"
                                      : epi == 1 ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");
     }
