@@ -40,7 +40,7 @@ FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 # DRAM bytes (read + write) per GEMM launch, the mean over one step's launches,
 # from one ncu capture of this workload with the kernels as they are now
 # (profiles/fp8_gemm_traffic_ln_mlp.md).  Workloads without a capture report null.
-GEMM_TRAFFIC = {"ln_mlp": 1.376e9}
+GEMM_TRAFFIC = {"ln_mlp": 1.375e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -103,18 +103,19 @@ def step_flops(cfg):
     return per * (3 if cfg["training"] else 1)
 
 
-def cast_bytes(cfg, fused_gelu=False):
+def cast_bytes(cfg, fused=False):
     """Algorithmic HBM bytes of the HBM-bound kernels of one step (read once, write each output once).
-    With the GELU + cast fused into the fc1 GEMM (fused_gelu), that pass is no longer a separate kernel."""
+    With the activations fused into the GEMM epilogues (fused: GELU + cast in fc1, dGELU + cast + db1
+    in the fc2 dgrad), those passes are no longer separate kernels."""
     M = cfg["tokens"]
     if cfg.get("kind") == "mx":  # quantise X, W, dY of each layer: read 2 B, write 2 B + 2/32 B of scales
         return sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) for _, k, n in cfg["layers"])
     if cfg.get("kind") == "lnmlp":
         H, F = cfg["layers"][0][1], cfg["layers"][0][2]
         return (M * H * (2 + 2) + F * H * (2 + 2) * 2      # LN+cast of x; casts of W1 and W2 (+T)
-                + (0 if fused_gelu else M * F * (2 + 2))    # GELU+cast of h (+T)
+                + (0 if fused else M * F * (2 + 2))         # GELU+cast of h (+T)
                 + M * H * (2 + 2) + 4 * H                  # cast of dY (+T, dbias)
-                + M * F * (2 + 2 + 2) + 4 * F              # dGELU+cast of (dg, h) (+T, dbias)
+                + (0 if fused else M * F * (2 + 2 + 2) + 4 * F)  # dGELU+cast of (dg, h) (+T, dbias)
                 + M * H * (2 + 2 + 2))                     # LayerNorm backward: read dy and x, write dx
     esz_x = 2 if cfg["x_dtype"] == torch.bfloat16 else 4
     w_casts = 1 if cfg.get("weight_cache") else cfg.get("micro_batches", 1)  # weight casts per step
@@ -429,7 +430,7 @@ def profile_kernels(model, flush, stream, reps=5):
                                             for r in range(reps)) / reps, 5)] for i in range(per)]
     out["gemm"]["flops_per_step"] = flops_per_gemm_step
     fused = getattr(getattr(model, "blk", None), "fused", False) and not getattr(model, "current", False)
-    out["cast"]["bytes_per_step"] = cast_bytes(model.cfg, fused_gelu=fused)
+    out["cast"]["bytes_per_step"] = cast_bytes(model.cfg, fused=fused)
     return out
 
 
