@@ -367,3 +367,6 @@ def fp8_layernorm_bwd(dy: torch.Tensor, x: torch.Tensor, gamma: torch.Tensor, mu
     _check(_lib.fp8_layernorm_bwd(_p(dy), _p(x), _p(gamma), _p(mu), _p(rsigma), rows, cols, _p(dx), _p(dgamma),
                                   _p(dbeta), _p(workspace), _nbytes(workspace), _stream(stream)),
            "fp8_layernorm_bwd")
+
+
+from .autocast import fp8_autocast  # noqa: E402  (the step region; see autocast.py)

@@ -76,3 +76,56 @@ def test_amax_max_allreduce_matches_single_process():
     for rank, scale, scale_inv, tmax in res:
         assert np.array_equal(scale, ref.scale) and np.array_equal(scale_inv, ref.scale_inv)
         assert tmax == 2.5
+
+
+class _HostState:
+    """A scaling-state block in host memory with the library's slot layout; update() is
+    recorded instead of launched (the reduce under test runs before it)."""
+
+    def __init__(self, n_slots, hist_len=16):
+        import fp8_delayed_scaling_gb300 as fd
+        self.n_slots = n_slots
+        self.stride = fd.fp8dl_slot_stride(hist_len)
+        self.buf = torch.zeros(n_slots * self.stride, dtype=torch.uint8)
+        self.updates = []
+
+    def update(self, step, stream=None):
+        self.updates.append((step, self.amaxes().tolist()))
+
+    def amaxes(self):
+        from fp8_delayed_scaling_gb300.autocast import amax_view
+        return amax_view(self.buf, self.n_slots, self.stride).clone()
+
+
+def _autocast_worker(rank, world, port, q):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    from fp8_delayed_scaling_gb300.autocast import amax_view, fp8_autocast
+    st = _HostState(3)
+    rows = st.buf.view(3, st.stride)
+    rows[:, 12:].fill_(7)  # bytes other than the amaxes must survive the reduce
+    for step in range(2):
+        with fp8_autocast(st, group=dist.group.WORLD):
+            amax_view(st.buf, 3, st.stride).copy_(torch.tensor([1.0 + rank, 5.0 - rank, 0.25 * (step + 1)]))
+    untouched = bool((rows[:, 12:] == 7).all())
+    q.put((rank, st.updates, untouched))
+    dist.destroy_process_group()
+
+
+def test_autocast_exit_reduces_amax_over_the_group_then_updates():
+    """fp8_autocast(group=...) exit: MAX all-reduce of the amax fields in place, then one update."""
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_autocast_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, updates, untouched in res:
+        assert untouched
+        assert updates == [(0, [2.0, 5.0, 0.25]), (1, [2.0, 5.0, 0.5])]
