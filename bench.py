@@ -435,25 +435,30 @@ def profile_kernels(model, flush, stream, reps=5):
 
 
 def run_e2e(args, model, dev, stream, world):
-    """Same step through the C ABI with HOST inputs and outputs: per step, H2D of every
-    layer's X and dY from pinned memory, the step, D2H of every layer's dW and db."""
-    hx = [x.cpu().pin_memory() for x in model.x]
-    hdy = [d.cpu().pin_memory() for d in model.dy]
-    outs = [(t, torch.empty_like(t, device="cpu").pin_memory()) for t in model.outputs()]
-    h2d = sum(t.numel() * t.element_size() for t in hx + hdy)
-    d2h = sum(h.numel() * h.element_size() for _, h in outs)
-    steps = max(1, min(args.steps, 10))
+    """Same step through the C ABI with HOST inputs and outputs: every step copies every
+    layer's X and dY from pinned memory to the device and the step's products (weight and
+    bias gradients, dx, ...) back to pinned memory.  The copies run through
+    HostStepPipeline: on two copy streams, overlapped with the neighbouring steps' compute."""
+    from fp8_delayed_scaling_gb300.pipeline import HostStepPipeline
+    nx = len(model.x)
+    host_in = [x.cpu().pin_memory() for x in model.x] + [d.cpu().pin_memory() for d in model.dy]
+    dev_out = model.outputs()
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    pipe = HostStepPipeline(model.x + model.dy, dev_out)
+
+    def step(ins):
+        model.x[:] = ins[:nx]
+        model.dy[:] = ins[nx:]
+        model.step()
+
+    steps = max(1, min(args.steps, 20))
+    pipe.run(2, step, lambda i: host_in, lambda i: host_out)  # settle the streams and buffers
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        for d, h in zip(model.x, hx):
-            d.copy_(h, non_blocking=True)
-        for d, h in zip(model.dy, hdy):
-            d.copy_(h, non_blocking=True)
-        model.step()
-        for d, h in outs:
-            h.copy_(d, non_blocking=True)
-        torch.cuda.synchronize()
+    pipe.run(steps, step, lambda i: host_in, lambda i: host_out)
+    torch.cuda.synchronize()
     sec = (time.perf_counter() - t0) / steps
     if world > 1:
         t = torch.tensor([sec], device=dev)
