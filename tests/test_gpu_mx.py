@@ -108,7 +108,7 @@ def _codes(rng, shape):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (32, 32, 32), (96, 160, 64), (256, 512, 384), (160, 288, 96),
-                                   (384, 768, 1024), (1024, 2048, 512)])
+                                   (384, 768, 1024), (1024, 2048, 512), (288, 544, 320), (640, 416, 2080)])
 def test_mx_gemm_parity(M, N, K):
     dev = gpu()
     rng = np.random.default_rng(M + 3 * N + 7 * K)
