@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
+METRIC = "FP8 linear fwd+bwd TFLOP/s & cast/amax GB/s, % of GB300 FP8/HBM peak"
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 # DRAM bytes (read + write) per GEMM launch, the mean over one step's launches,
 # from one ncu capture of this workload with the kernels as they are now
@@ -491,56 +492,93 @@ def run_e2e(args, model, dev, stream, world):
 # ---------------------------------------------------------------------------
 # oracle (CPU baseline / reference arm)
 # ---------------------------------------------------------------------------
-def run_oracle_sample(cfg, seed, budget_s=15.0):
-    """Time the oracle on a bounded sample of one step; returns (TFLOP/s-equivalent, cores, sample text).
+def run_oracle_sample(cfg, seed, rows=64, gemm_rows=8, gemm_cols=None):
+    """Time the oracle on a bounded sample of one step; returns (TFLOP/s-equivalent, cores, sample text,
+    estimated seconds for the whole step).
 
-    Sample: for every layer, the casts of a 64-row slab of X, W and dY, and the
-    GEMM reference on 8 output rows of each of the three GEMMs; time is scaled
-    to a whole step by algorithmic work (elements for casts, FLOPs for GEMMs)."""
+    The sample follows the workload's kind.  Per layer: the casts (per-tensor: amax + quantise;
+    MX: row- and column-wise block quantisation) of `rows`-row slabs of X, W and dY, and the
+    GEMM reference (per-tensor or block-scaled) of `gemm_rows` output rows (their first
+    `gemm_cols` columns, all by default).  The LayerNormMLP
+    adds the LayerNorm forward and backward, GELU and dGELU references on slabs.  Each part is
+    scaled to the whole step by its own work (elements for element-wise parts, FLOPs for
+    GEMMs), and the parts are summed."""
     import oracle
     cores = os.cpu_count() or 1
     M = cfg["tokens"]
-    rows = 64
-    gemm_rows = 8
-    t_cast = 0.0
-    cast_elems_done = 0
-    cast_elems_total = 0
-    t_gemm = 0.0
+    kind = cfg.get("kind")
+    est = 0.0
     flops_done = 0
-    t_begin = time.perf_counter()
+    elem_done = 0
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def elementwise(fn, sampled, total):
+        nonlocal est, elem_done
+        est += timed(fn) * total / max(1, sampled)
+        elem_done += sampled
+
+    rng = np.random.default_rng(0)
+    if kind == "mx":  # column-wise blocks need whole 32-row groups
+        rows = max(32, rows // 32 * 32)
     for name, k, n in cfg["layers"]:
-        if time.perf_counter() - t_begin > budget_s:
-            break
         gx = wl.generator(seed, "X/" + name)
         x = (wl.student_t3((rows, k), 0.5, gx) if cfg["x_dtype"] == torch.bfloat16
              else wl.normal((rows, k), 1.0, gx))
         w = wl.normal((rows, k), 0.02, wl.generator(seed, "W/" + name), cfg["x_dtype"])
         dy = wl.normal((rows, n), 1e-3, wl.generator(seed, "dY/" + name), torch.bfloat16)
-        arrs = [wl.host_array(x), wl.host_array(w)] + ([wl.bf16_bits(dy)] if cfg["training"] else [])
-        t0 = time.perf_counter()
-        for a in arrs:
-            am = oracle.amax(a)
-            oracle.quantize(0, a, float(448.0 / max(float(am), 1e-30)))
-        t_cast += time.perf_counter() - t0
-        cast_elems_done += sum(a.size for a in arrs)
-        cast_elems_total += M * k + n * k + (M * n if cfg["training"] else 0)
-        # GEMM: full K reduction for gemm_rows output rows of [rows x n] against a random [n x k] B
-        rng = np.random.default_rng(0)
-        A = rng.integers(0, 0x7E, (gemm_rows, k), dtype=np.uint8)
-        B = rng.integers(0, 0x7E, (n, k), dtype=np.uint8)
-        ms, ns = np.meshgrid(np.arange(gemm_rows), np.arange(n), indexing="ij")
-        t0 = time.perf_counter()
-        oracle.gemm_elems(A, 0, B, 0, 1.0, 1.0, None, ms.ravel(), ns.ravel())
-        t_gemm += time.perf_counter() - t0
-        flops_done += 2 * gemm_rows * n * k
+        xa, wa, dya = wl.host_array(x), wl.host_array(w), wl.bf16_bits(dy)
+        parts = [(xa, M * k), (wa, n * k)] + ([(dya, M * n)] if cfg["training"] else [])
+        for arr, total in parts:
+            if kind == "mx":
+                elementwise(lambda: (oracle.mx_quantize_rows(arr), oracle.mx_quantize_cols(arr)), arr.size, total)
+            else:
+                elementwise(lambda: oracle.quantize(0, arr, float(448.0 / max(float(oracle.amax(arr)), 1e-30))),
+                            arr.size, total)
+        # GEMM reference: gemm_rows output rows with the full K reduction, scaled by FLOPs
+        nc = n if gemm_cols is None else min(n, gemm_cols)
+
+        def codes(r, c):  # finite E4M3 codes (0x00-0x7D), only the B rows the sample reads
+            return (np.frombuffer(rng.bytes(r * c), np.uint8) % 0x7E).reshape(r, c).astype(np.uint8)
+
+        A, B = codes(gemm_rows, k), codes(nc, k)
+        ms, ns = np.meshgrid(np.arange(gemm_rows), np.arange(nc), indexing="ij")
+        if kind == "mx":
+            As = rng.integers(120, 134, (gemm_rows, k // 32), dtype=np.uint8)
+            Bs = rng.integers(120, 134, (nc, k // 32), dtype=np.uint8)
+            t = timed(lambda: oracle.mx_gemm_elems(A, As, B, Bs, None, ms.ravel(), ns.ravel()))
+        else:
+            t = timed(lambda: oracle.gemm_elems(A, 0, B, 0, 1.0, 1.0, None, ms.ravel(), ns.ravel()))
+        flops = 2 * gemm_rows * nc * k
+        est += t * (2 * M * n * k * (3 if cfg["training"] else 1)) / flops
+        flops_done += flops
+    if kind == "lnmlp":  # the LayerNorm and activation references on slabs
+        H, F = cfg["layers"][0][1], cfg["layers"][0][2]
+        g = wl.generator(seed, "lnmlp-sample")
+        xs = wl.bf16_bits(wl.normal((rows, H), 1.0, g, torch.bfloat16))
+        hs = wl.bf16_bits(wl.normal((rows, F), 1.0, g, torch.bfloat16))
+        dgs = wl.bf16_bits(wl.normal((rows, F), 1e-3, g, torch.bfloat16))
+        dys = wl.bf16_bits(wl.normal((rows, H), 1e-3, g, torch.bfloat16))
+        gam = wl.bf16_bits(torch.ones(H, dtype=torch.bfloat16))
+        bet = wl.bf16_bits(torch.zeros(H, dtype=torch.bfloat16))
+        stats = {}
+        elementwise(lambda: stats.update(fwd=oracle.layernorm_fwd(xs, gam, bet, 1e-5)), xs.size, M * H)
+        elementwise(lambda: oracle.gelu(hs), hs.size, M * F)
+        elementwise(lambda: oracle.dgelu(dgs, hs), hs.size, M * F)
+        _, mu, rs = stats["fwd"]
+        elementwise(lambda: oracle.layernorm_bwd(dys, xs, gam, mu, rs), xs.size, M * H)
     total_flops = step_flops(cfg)
-    # seconds for a whole step = cast part scaled by elements + GEMM part scaled by FLOPs
-    layers_frac = cast_elems_done / max(1, cast_elems_total)
-    step_s = t_cast / max(layers_frac, 1e-12) + t_gemm * total_flops / max(1, flops_done)
-    sample = ("oracle on %d host threads: casts+amax of %d-row slabs of X/W/dY and the fp64 GEMM reference of %d "
-              "output rows per layer GEMM (%.1f MFLOP), scaled to one step by elements and FLOPs"
-              % (cores, rows, gemm_rows, flops_done / 1e6))
-    return total_flops / step_s / 1e12, cores, sample, step_s
+    what = {"mx": "MX block quantisation (rows and columns) and the block-scaled GEMM reference",
+            "lnmlp": "casts, LayerNorm fwd/bwd, GELU and dGELU references and the GEMM reference"}.get(
+                kind, "casts (amax + quantise) and the GEMM reference")
+    sample = ("oracle on %d host threads: %s; %d-row slabs, %d output rows per GEMM%s (%.1f MFLOP, %.2f M "
+              "elements), each part scaled to one step by its elements or FLOPs"
+              % (cores, what, rows, gemm_rows, "" if gemm_cols is None else " (first %d columns)" % gemm_cols,
+                 flops_done / 1e6, elem_done / 1e6))
+    return total_flops / est / 1e12, cores, sample, est
 
 
 # ---------------------------------------------------------------------------
@@ -683,8 +721,23 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        val, cores, sample, step_s = run_oracle_sample(cfg, 2)
-        line = {"impl": "reference", "metric": "FP8 linear fwd+bwd TFLOP/s (oracle, CPU)", "value": val,
+        # the oracle as it stands on the host cores: W untimed and K timed steps, each a bounded
+        # sample of the step scaled to the whole step.  The sample is the cpu_baseline one
+        # (64-row slabs, 8 output rows per GEMM) unless W + K of those would take more than
+        # ~150 s; then 16-row slabs and 2048 columns of one output row per GEMM.
+        t0 = time.perf_counter()
+        run_oracle_sample(cfg, 2)
+        small = (time.perf_counter() - t0) * (args.steps + args.warmup) > 150.0
+        kw = dict(rows=16, gemm_rows=1, gemm_cols=2048) if small else {}
+        for _ in range(args.warmup - 1):
+            run_oracle_sample(cfg, 2, **kw)
+        est = []
+        for _ in range(args.steps):
+            val, cores, sample, step_s = run_oracle_sample(cfg, 2, **kw)
+            est.append(step_s)
+        step_s = sum(est) / len(est)
+        val = step_flops(cfg) / step_s / 1e12
+        line = {"impl": "reference", "metric": METRIC, "value": val,
                 "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64", "data": "synthetic", "config": config,
@@ -712,7 +765,7 @@ def main():
     cast_gbs = c["bytes_per_step"] / (c["ms_per_step"] * 1e-3) / 1e9
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     line = {
-        "metric": "FP8 linear fwd+bwd TFLOP/s & cast/amax GB/s, % of GB300 FP8/HBM peak",
+        "metric": METRIC,
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8(e4m3/e5m2)->fp32acc->bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
