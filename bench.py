@@ -199,6 +199,19 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+# Data-parallel replicas (torchrun, N > 1): the process group whose replicas share the
+# scales.  Each step ends as an fp8_autocast exit does: the recorded amaxes are MAX-reduced
+# over the group (one all-reduce of n_slots floats), then the scales are updated, so every
+# replica casts the next step with the same scales.
+GROUP = None
+
+
+def close_step(state, step_no):
+    if GROUP is not None:
+        from fp8_delayed_scaling_gb300.autocast import reduce_amax_
+        reduce_amax_(state.buf, state.n_slots, state.stride, GROUP)
+    state.update(step_no)
+
 class LnMlpModel:
     """One LayerNormMLP block (fwd+bwd) per step."""
 
@@ -228,7 +241,7 @@ class LnMlpModel:
         self.blk.forward(self.x[0], seed=True)
         self.blk.backward(self.x[0], self.dy[0], seed=True)
         if not self.current:
-            self.state.update(self.step_no)
+            close_step(self.state, self.step_no)
         self.step_no += 1
 
     def launches_per_step(self):
@@ -247,7 +260,7 @@ class LnMlpModel:
         self.blk.forward(self.x[0])
         self.blk.backward(self.x[0], self.dy[0])
         if not self.current:  # current scaling keeps no history to update
-            self.state.update(self.step_no)
+            close_step(self.state, self.step_no)
         self.step_no += 1
 
     def outputs(self):
@@ -346,7 +359,7 @@ class Model:
                 lin.forward(x[j * m:(j + 1) * m], is_first_microbatch=first)
             for lin, dy in zip(self.layers, self.dy):
                 lin.backward(dy[j * m:(j + 1) * m])
-            self.state.update(self.step_no)
+            close_step(self.state, self.step_no)
             self.step_no += 1
 
 
@@ -746,9 +759,11 @@ def main():
         print(json.dumps(line))
         return
 
-    if world > 1:
-        torch.distributed.init_process_group("nccl")
     torch.cuda.set_device(local)
+    if world > 1:
+        global GROUP
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+        GROUP = torch.distributed.group.WORLD
     dev = torch.device("cuda", local)
     if args.only:
         if rank == 0:
