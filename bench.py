@@ -104,20 +104,32 @@ def step_flops(cfg):
     return per * (3 if cfg["training"] else 1)
 
 
-def cast_bytes(cfg, fused=False):
-    """Algorithmic HBM bytes of the HBM-bound kernels of one step (read once, write each output once).
-    With the activations fused into the GEMM epilogues (fused: GELU + cast in fc1, dGELU + cast + db1
-    in the fc2 dgrad), those passes are no longer separate kernels."""
+def hbm_bytes(cfg, fused=False):
+    """Algorithmic HBM bytes of one step's HBM-bound kernels, by class (each input read once,
+    each output written once):
+      cast     — cast + amax (+ transposed copy, + bias gradient) and MX quantisation;
+      norm_act — LayerNorm forward and backward and the GELU / dGELU casts.
+    With the activations fused into the GEMM epilogues (fused: GELU + cast in fc1, dGELU + cast
+    + db1 in the fc2 dgrad), those passes belong to the GEMMs."""
     M = cfg["tokens"]
     if cfg.get("kind") == "mx":  # quantise X, W, dY of each layer: read 2 B, write 2 B + 2/32 B of scales
-        return sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) for _, k, n in cfg["layers"])
+        return {"cast": sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) for _, k, n in cfg["layers"])}
     if cfg.get("kind") == "lnmlp":
         H, F = cfg["layers"][0][1], cfg["layers"][0][2]
-        return (M * H * (2 + 2) + F * H * (2 + 2) * 2      # LN+cast of x; casts of W1 and W2 (+T)
-                + (0 if fused else M * F * (2 + 2))         # GELU+cast of h (+T)
-                + M * H * (2 + 2) + 4 * H                  # cast of dY (+T, dbias)
-                + (0 if fused else M * F * (2 + 2 + 2) + 4 * F)  # dGELU+cast of (dg, h) (+T, dbias)
-                + M * H * (2 + 2 + 2))                     # LayerNorm backward: read dy and x, write dx
+        if cfg.get("scaling") == "current":  # amax passes first, casts of the bf16 tensors after
+            cast = (M * H * (2 + 2)                          # cast of the LayerNorm output y (+T)
+                    + F * H * (2 + 2 + 2) * 2                # W1, W2: amax pass, cast (+T)
+                    + M * F * (2 + 2)                        # cast of g (+T)
+                    + M * H * (2 + 2 + 2) + 4 * H            # dY: amax pass, cast (+T, dbias)
+                    + M * F * (2 + 2) + 4 * F)               # cast of dh (+T, dbias)
+            norm_act = (M * H * (2 + 2) + M * F * (2 + 2) + M * F * (2 + 2 + 2) + M * H * (2 + 2 + 2))
+            return {"cast": cast, "norm_act": norm_act}
+        cast = F * H * (2 + 2) * 2 + M * H * (2 + 2) + 4 * H  # W1, W2 (+T); dY (+T, dbias)
+        norm_act = (M * H * (2 + 2)                            # LayerNorm + cast of x (+T)
+                    + (0 if fused else M * F * (2 + 2))        # GELU + cast of h (+T)
+                    + (0 if fused else M * F * (2 + 2 + 2) + 4 * F)  # dGELU + cast of (dg, h) (+T, db1)
+                    + M * H * (2 + 2 + 2))                     # LayerNorm backward: read dy and x, write dx
+        return {"cast": cast, "norm_act": norm_act}
     esz_x = 2 if cfg["x_dtype"] == torch.bfloat16 else 4
     w_casts = 1 if cfg.get("weight_cache") else cfg.get("micro_batches", 1)  # weight casts per step
     tot = 0
@@ -127,7 +139,7 @@ def cast_bytes(cfg, fused=False):
         tot += (n * k * esz_x + n * k * t) * w_casts  # W -> qW (+ qW^T)
         if cfg["training"]:
             tot += M * n * 2 + 2 * M * n + 4 * n  # dY bf16 -> qdY + qdY^T + dbias
-    return tot
+    return {"cast": tot}
 
 
 # ---------------------------------------------------------------------------
@@ -418,15 +430,16 @@ def profile_kernels(model, flush, stream, reps=5):
     import fp8_delayed_scaling_gb300.linear as L
     import fp8_delayed_scaling_gb300.lnmlp as LM
     import fp8_delayed_scaling_gb300.mxlinear as MX
-    times = {"gemm": [], "cast": [], "update": []}
+    times = {"gemm": [], "cast": [], "norm_act": [], "update": []}
     by_entry = {}  # entry point -> [(start, end) events]
     seq = []        # (entry point, start, end) in call order, all reps
     flops_per_gemm_step = step_flops(model.cfg)
-    cast_names = ["fp8_cast_amax_transpose", "fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast",
-                  "fp8_layernorm_bwd", "mxfp8_quantize", "fp8_seed_amax_history"]
-    gemm_names = ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast", "fp8_gemm_dgelu_cast"]
-    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in gemm_names + cast_names
-             if hasattr(mod, name)]
+    classes = {"gemm": ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast", "fp8_gemm_dgelu_cast"],
+               "cast": ["fp8_cast_amax_transpose", "mxfp8_quantize"],
+               "norm_act": ["fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast", "fp8_layernorm_bwd"],
+               "update": ["fp8_seed_amax_history"]}  # the just-in-time scale computation
+    kind_of = {name: k for k, names in classes.items() for name in names}
+    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in kind_of if hasattr(mod, name)]
     orig_update = model.state.update
 
     def timed(kind, fn, name):
@@ -442,7 +455,7 @@ def profile_kernels(model, flush, stream, reps=5):
         return w
 
     for mod, name, fn in saved:
-        setattr(mod, name, timed("gemm" if name in gemm_names else "cast", fn, name))
+        setattr(mod, name, timed(kind_of[name], fn, name))
     model.state.update = timed("update", orig_update, "fp8_update_scale")
     try:
         for _ in range(reps):
@@ -465,7 +478,10 @@ def profile_kernels(model, flush, stream, reps=5):
                                             for r in range(reps)) / reps, 5)] for i in range(per)]
     out["gemm"]["flops_per_step"] = flops_per_gemm_step
     fused = getattr(getattr(model, "blk", None), "fused", False) and not getattr(model, "current", False)
-    out["cast"]["bytes_per_step"] = cast_bytes(model.cfg, fused=fused)
+    for k, v in hbm_bytes(model.cfg, fused=fused).items():
+        out[k]["bytes_per_step"] = v
+    if not times["norm_act"]:
+        del out["norm_act"]
     return out
 
 
@@ -776,9 +792,12 @@ def main():
     gemm_ms = g["ms_per_step"]
     achieved = g["flops_per_step"] / (gemm_ms * 1e-3) / 1e12
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP8_PER_BF16
-    c = kt["cast"]
-    cast_gbs = c["bytes_per_step"] / (c["ms_per_step"] * 1e-3) / 1e9
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+
+    def hbm_class(c):  # achieved GB/s of algorithmic bytes against the HBM peak
+        gbs = c["bytes_per_step"] / (c["ms_per_step"] * 1e-3) / 1e9
+        return {"achieved_gbs": round(gbs, 1), "peak_gbs": hbm, "frac": round(gbs / hbm, 4),
+                "ms_per_step": round(c["ms_per_step"], 4), "launches_per_step": c["launches_per_step"]}
     line = {
         "metric": METRIC,
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -789,14 +808,15 @@ def main():
                      "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
                      "traffic": GEMM_TRAFFIC.get(args.workload),
                      "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},
-        "cast": {"achieved_gbs": round(cast_gbs, 1), "peak_gbs": hbm, "frac": round(cast_gbs / hbm, 4),
-                 "ms_per_step": round(c["ms_per_step"], 4), "launches_per_step": c["launches_per_step"]},
+        "cast": hbm_class(kt["cast"]),
         "kernels": {k: ({kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         if isinstance(v, dict) else v) for k, v in kt.items()},
         "gpu_launches": model.launches_per_step() * args.steps,
         "e2e": {"value": round(flops * world / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
     }
+    if "norm_act" in kt:
+        line["norm_act"] = hbm_class(kt["norm_act"])
     if clk:
         line["clocks"] = clk
     if rank == 0 and world == 1:
