@@ -498,7 +498,8 @@ def run_e2e(args, model, dev, stream, world):
     """Same step through the C ABI with HOST inputs and outputs: every step copies every
     layer's X and dY from pinned memory to the device and the step's products (weight and
     bias gradients, dx, ...) back to pinned memory.  The copies run through
-    HostStepPipeline: on two copy streams, overlapped with the neighbouring steps' compute."""
+    HostStepPipeline: on two copy streams, overlapped with the neighbouring steps' compute.
+    On one GPU the step itself is replayed from a CUDA graph captured for each input set."""
     from fp8_delayed_scaling_gb300.pipeline import HostStepPipeline
     nx = len(model.x)
     host_in = [x.cpu().pin_memory() for x in model.x] + [d.cpu().pin_memory() for d in model.dy]
@@ -508,10 +509,21 @@ def run_e2e(args, model, dev, stream, world):
     d2h = sum(h.numel() * h.element_size() for h in host_out)
     pipe = HostStepPipeline(model.x + model.dy, dev_out)
 
-    def step(ins):
+    def eager(ins):
         model.x[:] = ins[:nx]
         model.dy[:] = ins[nx:]
         model.step()
+
+    step = eager
+    if world == 1 and not args.no_graph:  # one captured step per input buffer set
+        from fp8_delayed_scaling_gb300.graph import StepGraph
+        graphs = []
+        for k in range(2):
+            ins = pipe.sets[k]
+            graphs.append(StepGraph(lambda n, ins=ins: eager(ins), interval=1, warmup=1))
+
+        def step(ins):
+            graphs[0 if ins is pipe.sets[0] else 1].replay()
 
     steps = max(1, min(args.steps, 20))
     pipe.run(2, step, lambda i: host_in, lambda i: host_out)  # settle the streams and buffers
