@@ -61,6 +61,13 @@ def test_host_validation_without_gpu(lib):
     a16 = 1 << 20  # a fake, 16-byte aligned address: validation fails before any use
     # NULL input
     assert L.fp8_cast_amax_transpose(None, 1, 32, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_INVALID_ARG
+    # empty inputs: rejected before any launch (every dimension must be a positive multiple of 16)
+    assert L.fp8_cast_amax_transpose(a16, 1, 0, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_SHAPE
+    assert L.fp8_cast_amax_transpose(a16, 1, 32, 0, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_SHAPE
+    assert L.fp8_gemm(a16, 0, a16, 0, 0, 16, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
+    assert L.fp8_gemm(a16, 0, a16, 0, 16, 16, 0, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
+    assert L.mxfp8_quantize(a16, 1, 0, 32, a16, a16, None, None, None) == lib.ERR_SHAPE
+    assert L.mxfp8_gemm(a16, a16, a16, a16, 32, 0, 32, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
     # dimension not a multiple of 16
     assert L.fp8_cast_amax_transpose(a16, 1, 33, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_SHAPE
     assert L.fp8_gemm(a16, 0, a16, 0, 16, 24, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_SHAPE

@@ -150,3 +150,35 @@ def test_update_scale_parity_random_sequences():
             assert np.array_equal(got["hist"], ost.hist), (L, step)
             assert np.array_equal(got["pos"], ost.pos), (L, step)
             assert np.all(got["amax"] == 0)
+
+
+@pytest.mark.parametrize("margin", [0, 7, 126])
+def test_update_scale_degenerate_amaxes(margin):
+    """Amaxes at the edges of fp32 against the oracle, bit for bit: subnormal and tiny
+    amaxes (FP8_MAX/amax overflows: the scale is kept), a huge amax with a large margin (the
+    scale underflows: kept), an amax whose scale_inv is subnormal, NaN (ignored by the window
+    max) and infinity (kept)."""
+    fd = _fd()
+    dev = gpu()
+    seq = [1.0, 1e-45, 1e-38, 3.0e38, 2e-36, float("nan"), 7.5, float("inf"), 0.0, 1e-37, 5e-3, 2.0 ** -126]
+    for L in (1, 3):
+        recipe = fd.Recipe(margin=margin, interval=1, fp8_format=fd.FORMAT_HYBRID, amax_history_len=L)
+        fmts = [0, 1]
+        st = fd.ScalingState(recipe, fmts, device=dev)
+        ost = oracle.ScalingState(fmts, hist_len=L, margin=margin, interval=1)
+        view = st.buf.view(torch.float32).view(len(fmts), st.stride // 4)
+        for step, a0 in enumerate(seq):
+            a = np.array([a0, a0], np.float32)
+            # the amax fields are written directly on both sides (a cast's max would drop a NaN)
+            view[:, 2] = torch.from_numpy(a).to(dev)
+            ost.amax_cur[:] = a
+            if step == 0:
+                st.seed()
+                ost.seed()
+            else:
+                st.update(step)
+                ost.update(step)
+            got = st.read()
+            assert np.array_equal(got["scale"], ost.scale), (margin, L, step)
+            assert np.array_equal(got["scale_inv"], ost.scale_inv), (margin, L, step)
+            assert np.array_equal(got["hist"], ost.hist, equal_nan=True), (margin, L, step)
