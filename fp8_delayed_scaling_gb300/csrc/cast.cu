@@ -322,6 +322,7 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
                                      const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
                                      float *scale_inv_out, float *dbias, void *workspace, size_t workspace_bytes,
                                      fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_cast_amax_transpose");
     FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
     FP8DL_CHECK_ARG(!scale_inv_out || scale != nullptr, "scale_inv_out needs scale");
     FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
@@ -425,6 +426,7 @@ static fp8dl_status op_cast_common(int op, const void *x, const void *aux, int64
 extern "C" fp8dl_status fp8_gelu_cast(const void *h, int64_t rows, int64_t cols, int32_t out_dtype,
                                       const float *scale, uint8_t *out, uint8_t *out_t, float *amax, void *g,
                                       fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_gelu_cast");
     return fp8dl::op_cast_common(fp8dl::OP_GELU, h, nullptr, rows, cols, out_dtype, scale, out, out_t, amax, nullptr,
                                  nullptr, 0, g, stream, "fp8_gelu_cast");
 }
@@ -432,6 +434,7 @@ extern "C" fp8dl_status fp8_gelu_cast(const void *h, int64_t rows, int64_t cols,
 extern "C" fp8dl_status fp8_dgelu_cast(const void *dg, const void *h, int64_t rows, int64_t cols, int32_t out_dtype,
                                        const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *dbias,
                                        void *workspace, size_t workspace_bytes, void *dh, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_dgelu_cast");
     return fp8dl::op_cast_common(fp8dl::OP_DGELU, dg, h, rows, cols, out_dtype, scale, out, out_t, amax, dbias,
                                  workspace, workspace_bytes, dh, stream, "fp8_dgelu_cast");
 }
@@ -473,6 +476,7 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
                                                         int32_t out_dtype, const float *scale, uint8_t *out,
                                                         uint8_t *out_t, float *amax, float *dbias,
                                                         fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_cast_amax_transpose_noalloc");
     FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
     FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
     FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "out_dtype must be E4M3 or E5M2");

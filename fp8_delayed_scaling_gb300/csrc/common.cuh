@@ -7,6 +7,7 @@
 #include <stdio.h>
 
 #include "fp8dl.h"
+#include <nvtx3/nvToolsExt.h>
 
 namespace fp8dl {
 
@@ -22,6 +23,13 @@ fp8dl_status current_device(int *dev, int *num_sms);
 
 // dbias[c] = sum over r of ws[r * cols + c] (fp32, a fixed order), one launch on st.
 void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, cudaStream_t st);
+
+// An NVTX range over one ABI call (visible to nsys/ncu; nearly free without a tool).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+#define FP8DL_NVTX(name) ::fp8dl::NvtxRange fp8dl_nvtx_range_(name)
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool dim_ok(int64_t d, int64_t mult) { return d > 0 && d % mult == 0 && d <= (int64_t(1) << 31); }

@@ -775,6 +775,7 @@ using namespace fp8dl;
 
 extern "C" fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arrive_first, int32_t *dev_status,
                                             fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8dl_wait_selftest");
     FP8DL_CHECK_ARG(dev_status != nullptr, "dev_status is NULL");
     FP8DL_CHECK_ARG(budget_cycles >= 0 && budget_cycles <= (int64_t(1) << 32), "budget_cycles must be in [0, 2^32]");
     if (!aligned16(dev_status)) return fail(FP8DL_ERR_ALIGN, "dev_status must be 16-byte aligned");
@@ -908,6 +909,7 @@ extern "C" fp8dl_status fp8_gemm(const uint8_t *A, int32_t a_dtype, const uint8_
                                  int64_t N, int64_t K, const float *a_scale_inv, const float *b_scale_inv,
                                  const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype, int32_t *dev_status,
                                  fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_gemm");
     GemmArgs args;
     FP8DL_TRY(gemm_args(A, a_dtype, B, b_dtype, M, N, K, a_scale_inv, b_scale_inv, bias, bias_dtype, D, d_dtype,
                         dev_status, args));
@@ -922,6 +924,7 @@ extern "C" fp8dl_status fp8_gemm_gelu_cast(const uint8_t *A, int32_t a_dtype, co
                                            const float *b_scale_inv, const void *bias, int32_t bias_dtype, void *H,
                                            int32_t q_dtype, const float *q_scale, uint8_t *q, uint8_t *q_t,
                                            float *q_amax, void *g, int32_t *dev_status, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_gemm_gelu_cast");
     GemmArgs args;
     FP8DL_TRY(gemm_args(A, a_dtype, B, b_dtype, M, N, K, a_scale_inv, b_scale_inv, bias, bias_dtype, H, FP8DL_BF16,
                         dev_status, args));
@@ -957,6 +960,7 @@ extern "C" fp8dl_status fp8_gemm_dgelu_cast(const uint8_t *A, int32_t a_dtype, c
                                             const float *q_scale, uint8_t *q, uint8_t *q_t, float *q_amax,
                                             float *dbias, void *workspace, size_t workspace_bytes, void *dh,
                                             int32_t *dev_status, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_gemm_dgelu_cast");
     GemmArgs args;
     FP8DL_TRY(gemm_args(A, a_dtype, B, b_dtype, M, N, K, a_scale_inv, b_scale_inv, nullptr, FP8DL_BF16, dg, FP8DL_BF16,
                         dev_status, args, /*d_required=*/false));

@@ -236,6 +236,7 @@ extern "C" {
 fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const void *gamma, const void *beta,
                                 float eps, int32_t out_dtype, const float *scale, uint8_t *out, uint8_t *out_t,
                                 float *amax, float *mu, float *rsigma, void *y, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_layernorm_cast");
     FP8DL_CHECK_ARG(x && gamma && beta && mu && rsigma, "x, gamma, beta, mu and rsigma must be non-NULL");
     FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "out_dtype must be E4M3 or E5M2");
     FP8DL_CHECK_ARG(!(out || out_t) || scale != nullptr, "scale is NULL but an FP8 output was requested");
@@ -277,6 +278,7 @@ size_t fp8_layernorm_bwd_workspace_size(int64_t rows, int64_t cols) {
 fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma, const float *mu,
                                const float *rsigma, int64_t rows, int64_t cols, void *dx, float *dgamma,
                                float *dbeta, void *workspace, size_t workspace_bytes, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_layernorm_bwd");
     FP8DL_CHECK_ARG(dy && x && gamma && mu && rsigma && dx && dgamma && dbeta,
                     "dy, x, gamma, mu, rsigma, dx, dgamma and dbeta must be non-NULL");
     if (!dim_ok(rows, 16) || !dim_ok(cols, 16))

@@ -550,6 +550,7 @@ size_t mxfp8_scale_bytes(int64_t rows, int64_t cols) {
 
 fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, uint8_t *row_q,
                             uint8_t *row_s, uint8_t *col_q, uint8_t *col_s, fp8dl_stream_t stream) {
+    FP8DL_NVTX("mxfp8_quantize");
     FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
     FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
     FP8DL_CHECK_ARG((row_q == nullptr) == (row_s == nullptr), "row_q and row_s must both be given or both NULL");
@@ -591,6 +592,7 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
 fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, const uint8_t *B_s, int64_t M,
                         int64_t N, int64_t K, const void *bias, int32_t bias_dtype, void *D, int32_t d_dtype,
                         int32_t *dev_status, fp8dl_stream_t stream) {
+    FP8DL_NVTX("mxfp8_gemm");
     FP8DL_CHECK_ARG(A && A_s && B && B_s && D, "A, A_s, B, B_s and D must be non-NULL");
     FP8DL_CHECK_ARG(d_dtype == FP8DL_BF16 || d_dtype == FP8DL_F32, "d_dtype must be FP8DL_BF16 or FP8DL_F32");
     FP8DL_CHECK_ARG(!bias || bias_dtype == FP8DL_BF16 || bias_dtype == FP8DL_F32,

@@ -132,6 +132,7 @@ size_t fp8dl_scaling_state_bytes(int32_t amax_history_len, int32_t n_slots) {
 
 fp8dl_status fp8_scaling_state_init(const fp8dl_recipe *recipe, int32_t n_slots, const int32_t *slot_fp8_dtype,
                                     void *state, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_scaling_state_init");
     FP8DL_TRY(check_recipe(recipe, n_slots, state));
     FP8DL_CHECK_ARG(slot_fp8_dtype != nullptr, "slot_fp8_dtype is NULL");
     for (int i = 0; i < n_slots; i++)
@@ -153,11 +154,13 @@ fp8dl_status fp8_scaling_state_init(const fp8dl_recipe *recipe, int32_t n_slots,
 
 fp8dl_status fp8_update_scale(const fp8dl_recipe *recipe, int32_t n_slots, void *state, int64_t step,
                               fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_update_scale");
     return launch_update(recipe, n_slots, state, step, 0, (cudaStream_t)stream);
 }
 
 fp8dl_status fp8_seed_amax_history(const fp8dl_recipe *recipe, int32_t n_slots, void *state,
                                    fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_seed_amax_history");
     return launch_update(recipe, n_slots, state, 0, 1, (cudaStream_t)stream);
 }
 
