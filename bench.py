@@ -14,8 +14,8 @@ is flushed (a 512 MB write) between timed steps, outside the step events.
 Prints one JSON line (rank 0).  `value` is TFLOP/s of algorithmic GEMM work
 (2*M*N*K per GEMM) over the step time; `roofline` is the dominant kernel (the
 GEMM) against the dense FP8 peak derived from the measured bf16 peak.
-`--impl reference` times the CPU oracle (the reference arm of this build) on a
-bounded sample of the same workload.
+`--impl reference` times the CPU oracle (the reference arm: a plain CPU implementation
+of the same computation) on bounded samples of the same workload.
 """
 from __future__ import annotations
 
