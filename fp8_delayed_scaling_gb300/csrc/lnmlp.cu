@@ -6,12 +6,22 @@
 // nn.LayerNorm (biased variance).  Under delayed scaling ("FP8 低精度训练：
 // Transformer Engine 简析" §三.1/§三.3) the LayerNorm output is what fc1 casts,
 // and its scale is known before the LayerNorm runs, so normalisation, bf16
-// rounding, the FP8 cast, the amax and the transposed copy are one pass over
-// 128x128 tiles (the cast kernel with a LayerNorm element operation, in
-// cast.cu), after a pass that computes the per-row statistics.
+// rounding, the FP8 cast, the amax and the transposed copy happen in the pass
+// that reads x.
+//
+// Two implementations of each direction:
+//  - cluster path (cols a multiple of 512, at most 16 x 512): a thread-block
+//    cluster owns blocks of 32 rows; CTA k of the cluster keeps columns
+//    [512k, 512k + 512) of the block in registers, the CTAs exchange per-row
+//    partial sums through distributed shared memory, and x (and dy) are read
+//    from HBM once;
+//  - tile path (any other width): a warp-per-row statistics pass, then 128 x 128
+//    tiles (the cast kernel with a LayerNorm element operation, in cast.cu).
 #include <cuda_bf16.h>
+#include <stdlib.h>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace fp8dl {
 
@@ -73,6 +83,289 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
                                         const void *beta, int64_t rows, int64_t cols, int fmt, const float *scale,
                                         uint8_t *out, uint8_t *out_t, float *amax, void *y, int sms,
                                         cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// Cluster path.  CTA `rank` of a cluster covers columns [LC_COLS*rank,
+// LC_COLS*rank + LC_COLS) of every row block the cluster owns; the cluster's
+// blocks are cid, cid + n_clusters, ... (block j of the cluster below).  The
+// block is staged in shared memory with cp.async (three buffers).
+//
+// Software pipeline, per CTA, in iteration j:
+//   - block j+2 is copied into shared memory;
+//   - the row partials of block j+1 are reduced over the CTA and published in
+//     this CTA's exchange slot;
+//   - the CTA waits on the cluster barrier for block j (arrived one iteration
+//     earlier), arrives for block j+1, and warp 0 gathers block j's partials
+//     from every CTA of the cluster, in rank order; block j is normalised and
+//     written.
+// The barrier's latency is thus hidden behind a whole block's work.  Exchange
+// slots rotate over four blocks: a CTA writes the slot of block j+4 only after
+// its wait for block j+2, which needs every peer's arrival for block j+2, which
+// each peer makes after gathering block j.
+// A barrier at the top of every iteration separates the refill of a buffer
+// from the previous block's reads of it.
+// ---------------------------------------------------------------------------
+constexpr int LC_COLS = 512, LC_THREADS = 256, LC_WARPS = LC_THREADS / 32, LC_MAX_CLUSTER = 16, LC_NBUF = 3;
+constexpr int LC_SLOTS = 4;  // exchange slots, by block number modulo 4
+constexpr int LF_ROWS = 32;  // forward block: two halves of 16 rows, 32-byte column segments of out_t
+constexpr int LB_BLK = 16;   // backward block: 4 rows per thread
+constexpr int LB_CTAS = 2;   // backward CTAs per SM (registers and shared memory sized for it)
+constexpr int LF_BUF = LF_ROWS * LC_COLS * 2;      // one staged x block
+constexpr int LF_SMEM = LC_NBUF * LF_BUF;
+constexpr int LB_SMEM = LC_NBUF * 2 * LB_BLK * LC_COLS * 2;  // three staged (dy, x) blocks
+
+__device__ __forceinline__ int next_buf(int b) { return b == LC_NBUF - 1 ? 0 : b + 1; }
+
+// rows 0..3 x columns 0..3 of bytes (w[k] = row k, column j in byte j) -> column j's 4 rows in col[j].
+__device__ __forceinline__ void transpose4x4_bytes(const uint32_t (&w)[4], uint32_t (&col)[4]) {
+    const uint32_t t0 = __byte_perm(w[0], w[1], 0x5140), t1 = __byte_perm(w[2], w[3], 0x5140);
+    const uint32_t t2 = __byte_perm(w[0], w[1], 0x7362), t3 = __byte_perm(w[2], w[3], 0x7362);
+    col[0] = __byte_perm(t0, t1, 0x5410);
+    col[1] = __byte_perm(t0, t1, 0x7632);
+    col[2] = __byte_perm(t2, t3, 0x5410);
+    col[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+// Asynchronous global -> shared copies (the issuing thread waits for its own groups).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A bf16x2 word as two floats (low half first), and two floats rounded to a bf16x2 word.
+__device__ __forceinline__ float2 bf16x2_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t f2_bf16x2(float2 v) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+    return *reinterpret_cast<uint32_t *>(&b);
+}
+
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int o) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+}
+
+// Mean and sum of squared deviations of two groups of n values each, combined
+// (Chan, Golub and LeVeque's pairwise update with equal counts:
+// M2 = M2_a + M2_b + (m_a - m_b)^2 * n / 2).  Symmetric in a and b.
+__device__ __forceinline__ float2 chan_equal(float2 a, float2 b, float half_n) {
+    const float d = a.x - b.x;
+    return make_float2((a.x + b.x) * 0.5f, (a.y + b.y) + d * d * half_n);
+}
+
+// Reduce-scatter of the (mean, M2) of 16 rows over the 16 lanes of a warp with
+// the same parity, each lane starting from its own 4 values per row: lane l
+// returns row 8*b4 + 4*b3 + 2*b2 + b1 (b = bits of l) merged over those 16
+// lanes (64 values).  Halving exchanges: each level sends the half of the rows
+// the partner keeps.
+__device__ __forceinline__ float2 warp_chan_rows16(const float2 (&s)[16], int lane) {
+    const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
+    float2 k8[8], k4[4], k2[2];
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const float2 send = u4 ? s[i] : s[i + 8], keep = u4 ? s[i + 8] : s[i];
+        k8[i] = chan_equal(keep, shfl_xor2(send, 16), 2.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float2 send = u3 ? k8[i] : k8[i + 4], keep = u3 ? k8[i + 4] : k8[i];
+        k4[i] = chan_equal(keep, shfl_xor2(send, 8), 4.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        const float2 send = u2 ? k4[i] : k4[i + 2], keep = u2 ? k4[i + 2] : k4[i];
+        k2[i] = chan_equal(keep, shfl_xor2(send, 4), 8.0f);
+    }
+    const float2 send = u1 ? k2[0] : k2[1], keep = u1 ? k2[1] : k2[0];
+    return chan_equal(keep, shfl_xor2(send, 2), 16.0f);
+}
+
+// LayerNorm forward + cast.  Thread t holds columns 4*(t >> 1) .. +3 of the
+// CTA's slab for rows 16*(t & 1) .. +15 of the block, so the transposed codes of
+// a column leave a lane pair as one full 32-byte segment (two 16-byte stores).
+// Statistics: each thread takes the mean and M2 of its 4 values of a row; the
+// lanes of equal parity, the eight warps and the cluster's slabs (in rank order, general equal-count form
+// M2 = sum_k M2_k + n sum_k (m_k - mean)^2) are merged; var = M2 / cols,
+// rs = 1/sqrt(var + eps).  Every CTA then normalises its slab:
+// y = bf16((x - mu) * rs * gamma + beta), codes = cvt(y * scale), written
+// row-major (out) and transposed (out_t).
+template <int FMT>
+__global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
+    const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma, const uint16_t *__restrict__ beta,
+    int64_t rows, int64_t cols, float eps, const float *__restrict__ scale_p, uint8_t *__restrict__ out,
+    uint8_t *__restrict__ out_t, float *__restrict__ amax_p, float *__restrict__ mu_out, float *__restrict__ rs_out,
+    uint16_t *__restrict__ y) {
+    extern __shared__ __align__(128) uint8_t lsm[];      // [LC_NBUF][LF_ROWS][LC_COLS] bf16
+    __shared__ float2 wst[LC_WARPS][2][16];              // per-warp (mean, M2) of 64 values of a row
+    __shared__ float2 xch[LC_SLOTS][LF_ROWS];            // slab (mean, M2) of a block, read by the cluster
+    __shared__ float2 stat[LF_ROWS];                     // mean, rsigma
+    __shared__ float wmax[LC_WARPS];
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int cq = t >> 1, h = t & 1;
+    const uint32_t rank = cluster_ctarank(), ncta = cluster_nctarank();
+    const int64_t col0 = (int64_t)rank * LC_COLS, col = col0 + 4 * cq;
+    const int64_t nblk = (rows + LF_ROWS - 1) / LF_ROWS;
+    const int64_t cid = blockIdx.x / ncta, ncl = gridDim.x / ncta;
+    const int64_t nb = cid < nblk ? (nblk - cid + ncl - 1) / ncl : 0;  // this cluster's blocks
+    const float scale = (out || out_t) ? __ldg(scale_p) : 1.0f;
+    const float2 sc2 = make_float2(scale, scale);
+    const uint2 gv = __ldg(reinterpret_cast<const uint2 *>(gamma + col));
+    const uint2 bv = __ldg(reinterpret_cast<const uint2 *>(beta + col));
+    const float2 g2[2] = {bf16x2_f2(gv.x), bf16x2_f2(gv.y)}, b2[2] = {bf16x2_f2(bv.x), bf16x2_f2(bv.y)};
+    // Copy block j into buffer `buf`: 32 rows x 64 chunks of 16 bytes, 8 per thread, a warp per row segment.
+    auto issue = [&](int64_t j, int buf) {
+        if (j < nb) {
+            const int64_t r0 = (cid + j * ncl) * LF_ROWS;
+            for (int i = 0; i < 8; i++) {
+                const int k = t + LC_THREADS * i, r = k >> 6, ch = k & 63;
+                const int64_t row = r0 + r;
+                const bool valid = row < rows;
+                cp_async16(smem_u32(lsm + buf * LF_BUF + (r * LC_COLS + 8 * ch) * 2),
+                           valid ? x + row * cols + col0 + 8 * ch : x, valid);
+            }
+        }
+        cp_async_commit();  // possibly empty: one group per block keeps the wait counts uniform
+    };
+    // this thread's 4 values of row i of its half, as two bf16x2 words
+    auto xrow = [&](int buf, int i) {
+        return *reinterpret_cast<const uint2 *>(lsm + buf * LF_BUF + ((16 * h + i) * LC_COLS + 4 * cq) * 2);
+    };
+    // Per-warp (mean, M2) of the staged block in `buf`, into wst.
+    auto partials = [&](int buf) {
+        float2 st[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            const uint2 q = xrow(buf, i);
+            const float2 v0 = bf16x2_f2(q.x), v1 = bf16x2_f2(q.y);
+            const float2 s = __fadd2_rn(v0, v1);
+            const float m = (s.x + s.y) * 0.25f;
+            const float2 nm = make_float2(-m, -m);
+            const float2 d0 = __fadd2_rn(v0, nm), d1 = __fadd2_rn(v1, nm);
+            const float2 m2 = __ffma2_rn(d1, d1, __fmul2_rn(d0, d0));
+            st[i] = make_float2(m, m2.x + m2.y);
+        }
+        wst[w][h][lane >> 1] = warp_chan_rows16(st, lane);  // row 8*b4 + 4*b3 + 2*b2 + b1 of half h
+    };
+    // After a barrier: the slab (mean, M2) of each row from the eight warps, into xch[slot].
+    auto merge = [&](int slot) {
+        if (t < LF_ROWS) {
+            const int hh = t >> 4, ri = t & 15;  // the row's half, row within it
+            float2 q[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) q[k] = chan_equal(wst[2 * k][hh][ri], wst[2 * k + 1][hh][ri], 32.0f);
+            xch[slot][t] = chan_equal(chan_equal(q[0], q[1], 64.0f), chan_equal(q[2], q[3], 64.0f), 128.0f);
+        }
+    };
+    float amax = 0.0f;
+    if (nb > 0) {  // always, as no more clusters than blocks are launched
+        issue(0, 0);
+        issue(1, 1);
+        cp_async_wait<1>();
+        __syncthreads();  // block 0 was copied by every thread
+        partials(0);
+        __syncthreads();
+        merge(0);
+        cluster_arrive();
+    }
+    int buf = 0, slot = 0;
+    for (int64_t j = 0; j < nb; j++) {
+        const int64_t r0 = (cid + j * ncl) * LF_ROWS;
+        const int nslot = (slot + 1) & (LC_SLOTS - 1);
+        cp_async_wait<0>();  // this thread's copies of block j+1 have landed (the only group in flight)
+        __syncthreads();     // ... everyone's; and every thread is past block j-1, whose buffer is refilled now
+        issue(j + 2, next_buf(next_buf(buf)));
+        if (j + 1 < nb) {
+            partials(next_buf(buf));
+            __syncthreads();
+            merge(nslot);
+        }
+        cluster_wait();                   // every slab of block j is published
+        if (j + 1 < nb) cluster_arrive();  // block j+1's slab is published
+        if (t < LF_ROWS) {
+            const uint32_t a = smem_u32(&xch[slot][t]);
+            float2 p[LC_MAX_CLUSTER];
+#pragma unroll
+            for (int k = 0; k < LC_MAX_CLUSTER; k++)
+                if (k < (int)ncta) p[k] = ld_dsmem_f32x2(mapa_shared(a, (uint32_t)k));
+            float sm = 0.0f;
+#pragma unroll
+            for (int k = 0; k < LC_MAX_CLUSTER; k++)
+                if (k < (int)ncta) sm += p[k].x;
+            const float mean = sm / (float)ncta;
+            float m2 = 0.0f;
+#pragma unroll
+            for (int k = 0; k < LC_MAX_CLUSTER; k++)
+                if (k < (int)ncta) {
+                    const float d = p[k].x - mean;
+                    m2 += p[k].y + d * d * (float)LC_COLS;
+                }
+            const float rsig = 1.0f / sqrtf(m2 / (float)cols + eps);
+            stat[t] = make_float2(mean, rsig);
+            if (rank == 0 && r0 + t < rows) {
+                mu_out[r0 + t] = mean;
+                rs_out[r0 + t] = rsig;
+            }
+        }
+        __syncthreads();
+        if (r0 + 16 * h < rows) {  // rows are a multiple of 16: a half is all in or all out
+            uint32_t codes[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const float2 sr = stat[16 * h + i];
+                const float2 nmu = make_float2(-sr.x, -sr.x), rs2 = make_float2(sr.y, sr.y);
+                const uint2 q = xrow(buf, i);
+                const int64_t row = r0 + 16 * h + i;
+                // y = bf16((x - mu) * rs * gamma + beta), two at a time
+                const uint32_t y0 = f2_bf16x2(__ffma2_rn(__fmul2_rn(__fadd2_rn(bf16x2_f2(q.x), nmu), rs2), g2[0], b2[0]));
+                const uint32_t y1 = f2_bf16x2(__ffma2_rn(__fmul2_rn(__fadd2_rn(bf16x2_f2(q.y), nmu), rs2), g2[1], b2[1]));
+                const float2 yr0 = bf16x2_f2(y0), yr1 = bf16x2_f2(y1);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(yr0.x), fabsf(yr0.y)), fmaxf(fabsf(yr1.x), fabsf(yr1.y))));
+                if (y) *reinterpret_cast<uint2 *>(y + row * cols + col) = make_uint2(y0, y1);
+                const float2 ys0 = __fmul2_rn(yr0, sc2), ys1 = __fmul2_rn(yr1, sc2);
+                codes[i] = pack4<FMT>(ys0.x, ys0.y, ys1.x, ys1.y);
+                if (out) *reinterpret_cast<uint32_t *>(out + row * cols + col) = codes[i];
+            }
+            if (out_t) {
+                uint32_t colw[4][4];  // colw[jj][k]: rows 4k..4k+3 of column 4*cq + jj
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint32_t wr[4] = {codes[4 * k], codes[4 * k + 1], codes[4 * k + 2], codes[4 * k + 3]};
+                    uint32_t cw[4];
+                    transpose4x4_bytes(wr, cw);
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) colw[jj][k] = cw[jj];
+                }
+#pragma unroll
+                for (int jj = 0; jj < 4; jj++)
+                    *reinterpret_cast<uint4 *>(out_t + (col + jj) * rows + r0 + 16 * h) =
+                        make_uint4(colw[jj][0], colw[jj][1], colw[jj][2], colw[jj][3]);
+            }
+        }
+        buf = next_buf(buf);
+        slot = nslot;
+    }
+    cp_async_wait<0>();
+    if (amax_p) {
+        const float m = warp_max(amax);
+        if (lane == 0) wmax[w] = m;
+        __syncthreads();
+        if (t == 0) {
+            float mm = wmax[0];
+            for (int k = 1; k < LC_WARPS; k++) mm = fmaxf(mm, wmax[k]);
+            atomic_max_nonneg(amax_p, mm);
+        }
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its exchange slots
+}
 
 // ---------------------------------------------------------------------------
 // LayerNorm backward, given the forward's per-row mu and rs:
@@ -227,6 +520,310 @@ __global__ void __launch_bounds__(256) ln_bwd_reduce_kernel(const float *__restr
     }
 }
 
+// Sum of the float2 partials of R rows (R = 2 or 4) over a warp, scattered:
+// lane l returns the row given by its top bits (R = 4: 2*b4 + b3; R = 2: b4).
+template <int R>
+__device__ __forceinline__ float2 warp_sum_rows(const float2 (&s)[R], int lane) {
+    static_assert(R == 2 || R == 4, "2 or 4 rows");
+    float2 r;
+    if constexpr (R == 4) {
+        const bool u4 = lane & 16, u3 = lane & 8;
+        float2 k2[2];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const float2 send = u4 ? s[i] : s[i + 2], keep = u4 ? s[i + 2] : s[i];
+            const float2 p = shfl_xor2(send, 16);
+            k2[i] = make_float2(keep.x + p.x, keep.y + p.y);
+        }
+        const float2 send = u3 ? k2[0] : k2[1], keep = u3 ? k2[1] : k2[0];
+        const float2 p = shfl_xor2(send, 8);
+        r = make_float2(keep.x + p.x, keep.y + p.y);
+    } else {
+        const bool u4 = lane & 16;
+        const float2 send = u4 ? s[0] : s[1], keep = u4 ? s[1] : s[0];
+        const float2 p = shfl_xor2(send, 16);
+        r = make_float2(keep.x + p.x, keep.y + p.y);
+#pragma unroll
+        for (int o = 8; o > 4; o >>= 1) {
+            const float2 q = shfl_xor2(r, o);
+            r = make_float2(r.x + q.x, r.y + q.y);
+        }
+    }
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+        const float2 q = shfl_xor2(r, o);
+        r = make_float2(r.x + q.x, r.y + q.y);
+    }
+    return r;
+}
+
+// LayerNorm backward on the cluster layout, with the forward's pipeline.  Per
+// row block of BLK rows, thread t holds the 8 columns starting at
+// LC_COLS*rank + 8*(t & 63) of rows (BLK/4)*(t >> 6) .. +BLK/4-1 and copies and
+// reads only its own 16-byte chunks of dy and x.  Each thread forms
+// g = dy * gamma and xhat = (x - mu) * rs for its slab; the row partials of
+// sum(g) and sum(g * xhat) are published for the cluster (one block ahead),
+// summed over the CTAs in rank order, and
+// dx = rs * (g - mean(g) - xhat * mean(g * xhat)) is written from the staged
+// block.  Each thread keeps the column partials of dgamma (dy * xhat) and dbeta
+// (dy) of its 8 columns across all of the cluster's blocks; at the end the CTA
+// writes one partial row per cluster, part[cluster][col] (dgamma) and
+// part[n_clusters + cluster][col] (dbeta), which ln_bwd_reduce_kernel sums in
+// cluster order.
+template <int BLK>
+__global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
+    const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
+    const float *__restrict__ mu, const float *__restrict__ rs, int64_t rows, int64_t cols,
+    uint16_t *__restrict__ dx, float *__restrict__ part) {
+    constexpr int RPT = BLK / 4;                     // rows per thread
+    constexpr int BUF = 2 * BLK * LC_COLS * 2;       // one staged (dy, x) block
+    extern __shared__ __align__(128) uint8_t lsm[];  // [LC_NBUF][dy, x][BLK][LC_COLS] bf16
+    __shared__ float2 wsum[LC_WARPS][RPT];
+    __shared__ float2 xch[LC_SLOTS][BLK];
+    __shared__ float2 cst[BLK];                      // mean(g), mean(g * xhat)
+    __shared__ float mrs[LC_NBUF][2][BLK];           // [buffer][mu, rs][row]
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    const int c = t & 63, g = t >> 6;
+    const uint32_t rank = cluster_ctarank(), ncta = cluster_nctarank();
+    const int64_t col0 = (int64_t)rank * LC_COLS, col = col0 + 8 * c;
+    const int64_t nblk = (rows + BLK - 1) / BLK;
+    const int64_t cid = blockIdx.x / ncta, ncl = gridDim.x / ncta;
+    const int64_t nb = cid < nblk ? (nblk - cid + ncl - 1) / ncl : 0;
+    const float inv_cols = 1.0f / (float)cols;
+    const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gamma + col));
+    const float2 g2[4] = {bf16x2_f2(gv.x), bf16x2_f2(gv.y), bf16x2_f2(gv.z), bf16x2_f2(gv.w)};
+    auto issue = [&](int64_t j, int buf) {
+        if (j < nb) {
+            const int64_t r0 = (cid + j * ncl) * BLK;
+            uint8_t *b = lsm + buf * BUF;
+            for (int i = 0; i < RPT; i++) {
+                const int64_t row = r0 + RPT * g + i;
+                const bool valid = row < rows;
+                const int64_t off = valid ? row * cols + col : 0;
+                const int soff = ((RPT * g + i) * LC_COLS + 8 * c) * 2;
+                cp_async16(smem_u32(b + soff), dy + off, valid);
+                cp_async16(smem_u32(b + BLK * LC_COLS * 2 + soff), x + off, valid);
+            }
+            if (t < 2 * BLK) {
+                const int64_t row = r0 + (t % BLK);
+                const bool valid = row < rows;
+                cp_async4(smem_u32(&mrs[buf][t / BLK][t % BLK]), (t < BLK ? mu : rs) + (valid ? row : 0), valid);
+            }
+        }
+        cp_async_commit();
+    };
+    auto drow = [&](int buf) { return reinterpret_cast<const uint4 *>(lsm + buf * BUF + RPT * g * LC_COLS * 2) + c; };
+    auto xrow = [&](int buf) {
+        return reinterpret_cast<const uint4 *>(lsm + buf * BUF + (BLK + RPT * g) * LC_COLS * 2) + c;
+    };
+    float2 pg[4], pb[4];  // column partials of dgamma, dbeta (columns 2k, 2k+1 in pg[k])
+#pragma unroll
+    for (int k = 0; k < 4; k++) pg[k] = pb[k] = make_float2(0.0f, 0.0f);
+    // Per-warp row partials of the staged block in `buf` into wsum; column partials into pg/pb.
+    auto partials = [&](int buf) {
+        const uint4 *dr = drow(buf), *xr = xrow(buf);
+        float2 s[RPT];
+#pragma unroll
+        for (int i = 0; i < RPT; i++) {
+            const float m = mrs[buf][0][RPT * g + i], sg = mrs[buf][1][RPT * g + i];
+            const float2 nm = make_float2(-m, -m), sg2 = make_float2(sg, sg);
+            const uint4 dq = dr[i * (LC_COLS / 8)], xq = xr[i * (LC_COLS / 8)];
+            const uint32_t dv[4] = {dq.x, dq.y, dq.z, dq.w}, xv[4] = {xq.x, xq.y, xq.z, xq.w};
+            float2 s1 = make_float2(0.0f, 0.0f), s2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const float2 d = bf16x2_f2(dv[q]);
+                const float2 h = __fmul2_rn(__fadd2_rn(bf16x2_f2(xv[q]), nm), sg2);  // xhat
+                const float2 gg = __fmul2_rn(d, g2[q]);                              // dy * gamma
+                s1 = __fadd2_rn(s1, gg);
+                s2 = __ffma2_rn(gg, h, s2);
+                pg[q] = __ffma2_rn(d, h, pg[q]);
+                pb[q] = __fadd2_rn(pb[q], d);
+            }
+            s[i] = make_float2(s1.x + s1.y, s2.x + s2.y);
+        }
+        const float2 r = warp_sum_rows<RPT>(s, lane);
+        if ((lane & (32 / RPT - 1)) == 0) wsum[w][lane / (32 / RPT)] = r;
+    };
+    // After a barrier: the CTA's row partials from the two warps of each row group, into xch[slot].
+    auto merge = [&](int slot) {
+        if (t < BLK) {
+            const float2 a = wsum[2 * (t / RPT)][t % RPT], b = wsum[2 * (t / RPT) + 1][t % RPT];
+            xch[slot][t] = make_float2(a.x + b.x, a.y + b.y);
+        }
+    };
+    if (nb > 0) {  // always, as no more clusters than blocks are launched
+        issue(0, 0);
+        issue(1, 1);
+        cp_async_wait<1>();
+        __syncthreads();  // mu and rs of block 0 were copied by other threads
+        partials(0);
+        __syncthreads();
+        merge(0);
+        cluster_arrive();
+    }
+    int buf = 0, slot = 0;
+    for (int64_t j = 0; j < nb; j++) {
+        const int64_t r0 = (cid + j * ncl) * BLK;
+        const int nslot = (slot + 1) & (LC_SLOTS - 1);
+        cp_async_wait<0>();  // block j+1 has landed (the only group in flight)
+        __syncthreads();     // ... including mu and rs; every thread is past block j-1
+        issue(j + 2, next_buf(next_buf(buf)));
+        if (j + 1 < nb) {
+            partials(next_buf(buf));
+            __syncthreads();
+            merge(nslot);
+        }
+        cluster_wait();                   // every CTA's partials of block j are published
+        if (j + 1 < nb) cluster_arrive();  // block j+1's partials are published
+        if (t < BLK) {
+            const uint32_t a = smem_u32(&xch[slot][t]);
+            float2 tot = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int k0 = 0; k0 < LC_MAX_CLUSTER; k0 += 8) {  // two rounds of 8 loads in flight
+                float2 p[8];
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (k0 + k < (int)ncta) p[k] = ld_dsmem_f32x2(mapa_shared(a, (uint32_t)(k0 + k)));
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (k0 + k < (int)ncta) {
+                        tot.x += p[k].x;
+                        tot.y += p[k].y;
+                    }
+            }
+            cst[t] = make_float2(tot.x * inv_cols, tot.y * inv_cols);
+        }
+        __syncthreads();
+        if (r0 + RPT * g < rows) {  // rows are a multiple of 16: always
+            const uint4 *dr = drow(buf), *xr = xrow(buf);
+#pragma unroll
+            for (int i = 0; i < RPT; i++) {
+                const float2 cc = cst[RPT * g + i];
+                const float m = mrs[buf][0][RPT * g + i], sg = mrs[buf][1][RPT * g + i];
+                const float2 nm = make_float2(-m, -m), sg2 = make_float2(sg, sg);
+                const float2 nc1 = make_float2(-cc.x, -cc.x), nc2 = make_float2(-cc.y, -cc.y);
+                const uint4 dq = dr[i * (LC_COLS / 8)], xq = xr[i * (LC_COLS / 8)];
+                const uint32_t dv[4] = {dq.x, dq.y, dq.z, dq.w}, xv[4] = {xq.x, xq.y, xq.z, xq.w};
+                uint32_t ow[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    // dx = rs * (dy * gamma - c1 - xhat * c2), two at a time
+                    const float2 h = __fmul2_rn(__fadd2_rn(bf16x2_f2(xv[q]), nm), sg2);
+                    const float2 u = __fadd2_rn(__fmul2_rn(bf16x2_f2(dv[q]), g2[q]), nc1);
+                    ow[q] = f2_bf16x2(__fmul2_rn(sg2, __ffma2_rn(h, nc2, u)));
+                }
+                *reinterpret_cast<uint4 *>(dx + (r0 + RPT * g + i) * cols + col) =
+                    make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+        }
+        buf = next_buf(buf);
+        slot = nslot;
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every thread is done with the staged blocks: reuse them for the column partials
+    float *red = reinterpret_cast<float *>(lsm);  // [dgamma, dbeta][row group][LC_COLS]
+    {
+        float4 *dg4 = reinterpret_cast<float4 *>(red + (0 * 4 + g) * LC_COLS + 8 * c);
+        float4 *db4 = reinterpret_cast<float4 *>(red + (1 * 4 + g) * LC_COLS + 8 * c);
+        dg4[0] = make_float4(pg[0].x, pg[0].y, pg[1].x, pg[1].y);
+        dg4[1] = make_float4(pg[2].x, pg[2].y, pg[3].x, pg[3].y);
+        db4[0] = make_float4(pb[0].x, pb[0].y, pb[1].x, pb[1].y);
+        db4[1] = make_float4(pb[2].x, pb[2].y, pb[3].x, pb[3].y);
+    }
+    __syncthreads();
+    for (int k = t; k < LC_COLS; k += LC_THREADS) {
+        float a = red[k], b = red[4 * LC_COLS + k];
+#pragma unroll
+        for (int q = 1; q < 4; q++) {
+            a += red[q * LC_COLS + k];
+            b += red[(4 + q) * LC_COLS + k];
+        }
+        part[cid * cols + col0 + k] = a;
+        part[(ncl + cid) * cols + col0 + k] = b;
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its exchange slots
+}
+
+// ---------------------------------------------------------------------------
+// Host side of the cluster path.
+// ---------------------------------------------------------------------------
+// Cluster size for `cols`, or 0 when the cluster path does not apply.
+static int ln_cluster_size(int64_t cols) {
+    return (cols % LC_COLS == 0 && cols / LC_COLS <= LC_MAX_CLUSTER) ? (int)(cols / LC_COLS) : 0;
+}
+
+static void cluster_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *at, int64_t clusters, int cl, int smem,
+                           cudaStream_t st) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3((unsigned)(clusters * cl), 1, 1);
+    cfg.blockDim = dim3(LC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)cl;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+}
+
+// How many clusters of `cl` CTAs of `kernel` can be resident at once (0: none).
+static int ln_max_clusters(const void *kernel, int smem, int cl) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess && cl > 8) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute at[1];
+    cluster_config(cfg, at, 1, cl, smem, nullptr);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    return n;
+}
+
+// Resident-cluster counts per device, kernel (0 fwd E4M3, 1 fwd E5M2, 2 bwd) and cluster size; -1 = not queried.
+static int g_ln_clusters[64][3][LC_MAX_CLUSTER + 1];
+static bool g_ln_init[64];
+
+// Number of clusters to launch over `nblk` row blocks, or 0 to take the tile path.
+// FP8DL_LN_VARIANT=tiles forces the tile path and FP8DL_LN_CLUSTERS=n caps the
+// cluster count (both for testing).
+static int64_t ln_cluster_count(int dev, int which, const void *kernel, int smem, int64_t nblk, int64_t cols,
+                                int64_t cap) {
+    const char *v = getenv("FP8DL_LN_VARIANT");
+    if (v && v[0] == 't') return 0;
+    const int cl = ln_cluster_size(cols);
+    if (cl == 0) return 0;
+    if (!g_ln_init[dev]) {
+        for (auto &k : g_ln_clusters[dev])
+            for (int &r : k) r = -1;
+        g_ln_init[dev] = true;
+    }
+    int &resident = g_ln_clusters[dev][which][cl];
+    if (resident < 0) resident = ln_max_clusters(kernel, smem, cl);
+    if (resident <= 0) return 0;
+    int64_t n = nblk < resident ? nblk : resident;
+    if (n > cap) n = cap;
+    const char *lim = getenv("FP8DL_LN_CLUSTERS");
+    if (lim && atoll(lim) > 0 && n > atoll(lim)) n = atoll(lim);
+    return n;
+}
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_clustered(void (*kernel)(KArgs...), int64_t clusters, int cl, int smem, cudaStream_t st,
+                                    Args... args) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute at[1];
+    cluster_config(cfg, at, clusters, cl, smem, st);
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace fp8dl
 
 using namespace fp8dl;
@@ -250,11 +847,28 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
     int dev = 0, sms = 0;
     FP8DL_TRY(current_device(&dev, &sms));
     cudaStream_t st = (cudaStream_t)stream;
-    // pass 1: per-row statistics (one read of x); pass 2: normalise + cast in 128x128 tiles
+    auto X = static_cast<const uint16_t *>(x);
+    {
+        const bool e4 = out_dtype == FP8DL_E4M3;
+        auto kern = e4 ? ln_fwd_cluster_kernel<FP8DL_E4M3> : ln_fwd_cluster_kernel<FP8DL_E5M2>;
+        const int64_t ncl = ln_cluster_count(dev, e4 ? 0 : 1, (const void *)kern, LF_SMEM,
+                                              (rows + LF_ROWS - 1) / LF_ROWS, cols, INT64_MAX);
+        if (ncl > 0) {
+            const cudaError_t e = launch_clustered(kern, ncl, ln_cluster_size(cols), LF_SMEM, st, X,
+                                                   static_cast<const uint16_t *>(gamma),
+                                                   static_cast<const uint16_t *>(beta), rows, cols, eps, scale, out,
+                                                   out_t, amax, mu, rsigma, static_cast<uint16_t *>(y));
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(FP8DL_ERR_CUDA, "fp8_layernorm_cast(cluster): %s", cudaGetErrorString(e));
+            }
+            return check_launch("fp8_layernorm_cast(cluster)");
+        }
+    }
+    // tile path. pass 1: per-row statistics (one read of x); pass 2: normalise + cast in 128x128 tiles
     const int64_t chunks_per_lane = (cols / 8 + 31) / 32;
     const int64_t row_ctas = (rows + 7) / 8;
     const unsigned g1 = (unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8);
-    auto X = static_cast<const uint16_t *>(x);
     if (chunks_per_lane <= 4)
         ln_stats_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
     else if (chunks_per_lane <= 8)
@@ -289,19 +903,35 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
     if (!workspace || workspace_bytes < fp8_layernorm_bwd_workspace_size(rows, cols))
         return fail(FP8DL_ERR_WORKSPACE, "fp8_layernorm_bwd needs a workspace of %zu bytes",
                     fp8_layernorm_bwd_workspace_size(rows, cols));
-    int sms = 0;
-    FP8DL_TRY(current_device(nullptr, &sms));
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
     cudaStream_t st = (cudaStream_t)stream;
     float *c12 = static_cast<float *>(workspace);
     float *part = c12 + 2 * rows;
     auto DY = static_cast<const uint16_t *>(dy);
     auto X = static_cast<const uint16_t *>(x);
     auto G = static_cast<const uint16_t *>(gamma);
+    const int64_t n_rt = (rows + LB_ROWS - 1) / LB_ROWS;
+    {
+        // the workspace holds n_rt partial rows per output: at most n_rt clusters
+        const int64_t ncl = ln_cluster_count(dev, 2, (const void *)ln_bwd_cluster_kernel<LB_BLK>, LB_SMEM,
+                                              (rows + LB_BLK - 1) / LB_BLK, cols, n_rt);
+        if (ncl > 0) {
+            const cudaError_t e = launch_clustered(ln_bwd_cluster_kernel<LB_BLK>, ncl, ln_cluster_size(cols), LB_SMEM, st, DY, X, G,
+                                                   mu, rsigma, rows, cols, static_cast<uint16_t *>(dx), part);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                return fail(FP8DL_ERR_CUDA, "fp8_layernorm_bwd(cluster): %s", cudaGetErrorString(e));
+            }
+            FP8DL_TRY(check_launch("fp8_layernorm_bwd(cluster)"));
+            ln_bwd_reduce_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(part, ncl, cols, dgamma, dbeta);
+            return check_launch("fp8_layernorm_bwd(reduce)");
+        }
+    }
     const int64_t row_ctas = (rows + 7) / 8;
     ln_bwd_rowsum_kernel<<<(unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8), 256, 0, st>>>(
         DY, X, G, mu, rsigma, rows, cols, c12);
     FP8DL_TRY(check_launch("fp8_layernorm_bwd(row sums)"));
-    const int64_t n_rt = (rows + LB_ROWS - 1) / LB_ROWS;
     const int64_t tiles = n_rt * ((cols + LB_COLS - 1) / LB_COLS);
     ln_bwd_tile_kernel<<<(unsigned)(tiles < (int64_t)sms * 4 ? tiles : (int64_t)sms * 4), 256, 0, st>>>(
         DY, X, G, mu, rsigma, c12, rows, cols, static_cast<uint16_t *>(dx), part);

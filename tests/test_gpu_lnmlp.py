@@ -20,8 +20,32 @@ def _fd():
     return fd
 
 
+# FP8DL_LN_VARIANT / FP8DL_LN_CLUSTERS select the implementation: widths that are a
+# multiple of 512 (up to 8192) take the cluster path, the rest the tile path.
+VARIANTS = {"default": {}, "tiles": {"FP8DL_LN_VARIANT": "tiles"}, "two-clusters": {"FP8DL_LN_CLUSTERS": "2"}}
+
+
+def _variant(monkeypatch, name):
+    for k in ("FP8DL_LN_VARIANT", "FP8DL_LN_CLUSTERS"):
+        monkeypatch.delenv(k, raising=False)
+    for k, v in VARIANTS[name].items():
+        monkeypatch.setenv(k, v)
+
+
 @pytest.mark.parametrize("shape", [(16, 64), (48, 768), (256, 4096), (32, 8192), (160, 1040), (64, 2000 // 16 * 16)])
 def test_layernorm_cast_parity(shape):
+    _layernorm_cast_check(shape, 0)
+
+
+# cluster sizes 1, 3, 8, 16; a 16-row tail block; two clusters walking many blocks
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("shape,fmt", [((16, 512), 0), ((208, 1536), 1), ((1040, 4096), 0), ((48, 8192), 1)])
+def test_layernorm_cast_variants(shape, fmt, variant, monkeypatch):
+    _variant(monkeypatch, variant)
+    _layernorm_cast_check(shape, fmt)
+
+
+def _layernorm_cast_check(shape, fmt):
     fd = _fd()
     dev = gpu()
     R, C = shape
@@ -38,7 +62,7 @@ def test_layernorm_cast_parity(shape):
     rs = torch.empty(R, dtype=torch.float32, device=dev)
     y = torch.empty((R, C), dtype=torch.bfloat16, device=dev)
     sc = torch.tensor([scale], dtype=torch.float32, device=dev)
-    fd.fp8_layernorm_cast(xd, gd, bd, 1e-5, fd.E4M3, sc, mu, rs, out=q, out_t=qt, amax=amax, y=y)
+    fd.fp8_layernorm_cast(xd, gd, bd, 1e-5, fmt, sc, mu, rs, out=q, out_t=qt, amax=amax, y=y)
     torch.cuda.synchronize()
     yr, mur, rsr = oracle.layernorm_fwd(host(x), host(gamma), host(beta), 1e-5)
     yg = as_f64(y)
@@ -46,7 +70,7 @@ def test_layernorm_cast_parity(shape):
     assert np.all(np.abs(mu.cpu().numpy() - mur) <= 2.0 ** -20 * np.abs(host_f(x)).max())
     assert np.all(np.abs(rs.cpu().numpy() - rsr) <= 2.0 ** -18 * rsr)
     yb = host(y)
-    qo = oracle.quantize(fd.E4M3, yb, scale)
+    qo = oracle.quantize(fmt, yb, scale)
     assert np.array_equal(q.cpu().numpy(), qo)
     assert np.array_equal(qt.cpu().numpy(), qo.T)
     assert amax.item() == oracle.amax(yb)
@@ -129,6 +153,17 @@ def test_dgelu_cast_parity(shape):
 
 @pytest.mark.parametrize("shape", [(16, 64), (48, 768), (256, 4096), (144, 1040)])
 def test_layernorm_bwd_parity(shape):
+    _layernorm_bwd_check(shape)
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("shape", [(16, 512), (208, 1536), (1040, 4096), (48, 8192)])
+def test_layernorm_bwd_variants(shape, variant, monkeypatch):
+    _variant(monkeypatch, variant)
+    _layernorm_bwd_check(shape)
+
+
+def _layernorm_bwd_check(shape):
     fd = _fd()
     dev = gpu()
     R, C = shape
