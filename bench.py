@@ -73,6 +73,10 @@ WORKLOADS = {
     "llama_proj_mb4_nocache": dict(desc="llama_proj_mb4 without the weight cache: every micro-batch casts the weights",
                                    tokens=8192, layers=llama_layers(), hist=1024, fmt="hybrid",
                                    x_dtype=torch.bfloat16, training=True, micro_batches=4, weight_cache=False),
+    "llama_proj_current": dict(desc="llama_proj with just-in-time (current) scaling: every cast is an amax pass, the "
+                                    "scale from that amax, then the cast (no history)",
+                               tokens=8192, layers=llama_layers(), hist=1, fmt="hybrid", x_dtype=torch.bfloat16,
+                               training=True, scaling="current"),
     "linear_hybrid": dict(desc="te.Linear 2048 tokens 768->3072 fwd+bwd, HYBRID, history 16",
                           tokens=2048, layers=[("linear", 768, 3072)], hist=16, fmt="hybrid",
                           x_dtype=torch.float32, training=True),
@@ -132,13 +136,14 @@ def hbm_bytes(cfg, fused=False):
         return {"cast": cast, "norm_act": norm_act}
     esz_x = 2 if cfg["x_dtype"] == torch.bfloat16 else 4
     w_casts = 1 if cfg.get("weight_cache") else cfg.get("micro_batches", 1)  # weight casts per step
+    reads = 2 if cfg.get("scaling") == "current" else 1  # just-in-time: an amax pass before each cast
     tot = 0
     for _, k, n in cfg["layers"]:
         t = 2 if cfg["training"] else 1
-        tot += M * k * esz_x + M * k * t          # X -> qX (+ qX^T)
-        tot += (n * k * esz_x + n * k * t) * w_casts  # W -> qW (+ qW^T)
+        tot += M * k * esz_x * reads + M * k * t          # X -> qX (+ qX^T)
+        tot += (n * k * esz_x * reads + n * k * t) * w_casts  # W -> qW (+ qW^T)
         if cfg["training"]:
-            tot += M * n * 2 + 2 * M * n + 4 * n  # dY bf16 -> qdY + qdY^T + dbias
+            tot += M * n * 2 * reads + 2 * M * n + 4 * n  # dY bf16 -> qdY + qdY^T + dbias
     return {"cast": tot}
 
 
@@ -256,18 +261,6 @@ class LnMlpModel:
             close_step(self.state, self.step_no)
         self.step_no += 1
 
-    def launches_per_step(self):
-        if self.blk.fused and not self.current:
-            # LN stats+cast, W1 cast, fc1+GELU+cast, W2 cast, fc2 | dY cast+reduce, fc2 wgrad,
-            # fc2 dgrad+dGELU+cast and its dbias reduce, 2 GEMMs, LN bwd (3 kernels) | update
-            return 2 + 1 + 1 + 1 + 1 + 2 + 1 + 2 + 2 + 3 + 1
-        if self.current:
-            # per cast: producer (+amax) pass, scale, cast; LN stats; GEMMs; reduces; LN bwd
-            return (2 + 1 + 1) + 3 + 1 + (3 + 1) + 3 + 1 + 3 + 1 + 2 + (1 + 3 + 2) + (1 + 3 + 2) + 2 + 3
-        # LN+cast, W1 cast, fc1, GELU+cast, W2 cast, fc2 | dY cast+reduce, 2 GEMMs, dGELU cast+reduce,
-        # 2 GEMMs, LN bwd (3 kernels) | update
-        return 6 + 2 + 2 + 2 + 2 + 3 + 1
-
     def step(self):
         self.blk.forward(self.x[0])
         self.blk.backward(self.x[0], self.dy[0])
@@ -301,9 +294,6 @@ class MxModel:
                 pass
         self.state = _NoState()
 
-    def launches_per_step(self):
-        return 2 * (2 + 1) + 2 * (1 + 2)  # per layer: quantise X, W, GEMM; quantise dY, 2 GEMMs
-
     def step(self):
         h = self.up.forward(self.x[0])
         self.down.forward(h)
@@ -331,7 +321,8 @@ class Model:
         for i, (name, k, n) in enumerate(cfg["layers"]):
             w = wl.normal((n, k), 0.02, wl.generator(seed, "W/" + name), cfg["x_dtype"]).to(dev)
             b = torch.zeros(n, dtype=cfg["x_dtype"], device=dev)
-            self.layers.append(Fp8Linear(self.state, i, w, b, self.Mmb, training=cfg["training"]))
+            self.layers.append(Fp8Linear(self.state, i, w, b, self.Mmb, training=cfg["training"],
+                                         scaling=cfg.get("scaling", "delayed")))
             if cfg["x_dtype"] == torch.bfloat16:
                 x = wl.student_t3((M, k), 0.5, wl.generator(seed, "X/" + name))
             else:
@@ -340,19 +331,12 @@ class Model:
             if cfg["training"]:
                 self.dy.append(wl.normal((M, n), 1e-3, wl.generator(seed, "dY/" + name), torch.bfloat16).to(dev))
         self.step_no = 0
-        for lin, x in zip(self.layers, self.x):
-            lin.seed_forward(x[:self.Mmb])
-        for lin, dy in zip(self.layers, self.dy):
-            lin.seed_backward(dy[:self.Mmb])
-
-    def launches_per_step(self):
-        per = 3 if not self.cfg["training"] else 3 + 1 + 1 + 2  # casts X, W, gemm; cast dY (+reduce), 2 gemms
-        if self.mb == 1:
-            return per * len(self.layers) + 1
-        # with the cache: the first micro-batch also writes the decode factor, the others skip the W cast
-        first = per + 1 if self.cache else per
-        rest = per - 1 if self.cache else per
-        return (first + rest * (self.mb - 1)) * len(self.layers) + self.mb
+        self.current = cfg.get("scaling") == "current"
+        if not self.current:  # delayed scaling: the first step's amaxes seed the histories
+            for lin, x in zip(self.layers, self.x):
+                lin.seed_forward(x[:self.Mmb])
+            for lin, dy in zip(self.layers, self.dy):
+                lin.seed_backward(dy[:self.Mmb])
 
     def outputs(self):
         out = []
@@ -371,7 +355,8 @@ class Model:
                 lin.forward(x[j * m:(j + 1) * m], is_first_microbatch=first)
             for lin, dy in zip(self.layers, self.dy):
                 lin.backward(dy[j * m:(j + 1) * m])
-            close_step(self.state, self.step_no)
+            if not self.current:  # current scaling keeps no history to update
+                close_step(self.state, self.step_no)
             self.step_no += 1
 
 
@@ -466,11 +451,14 @@ def profile_kernels(model, flush, stream, reps=5):
     for mod, name, fn in saved:
         setattr(mod, name, timed(kind_of[name], fn, name))
     model.state.update = timed("update", orig_update, "fp8_update_scale")
+    fd = sys.modules["fp8_delayed_scaling_gb300"]
+    n0 = fd.fp8dl_kernel_launches()
     try:
         for _ in range(reps):
             flush.fill_(1)
             model.step()
         torch.cuda.synchronize()
+        n1 = fd.fp8dl_kernel_launches()
     finally:
         for mod, name, fn in saved:
             setattr(mod, name, fn)
@@ -491,6 +479,9 @@ def profile_kernels(model, flush, stream, reps=5):
         out[k]["bytes_per_step"] = v
     if not times["norm_act"]:
         del out["norm_act"]
+    # the library's own kernel launches per step, counted by the library (a replayed graph
+    # of the step launches the same kernels)
+    out["launches_per_step"] = (n1 - n0) // reps
     return out
 
 
@@ -833,8 +824,8 @@ def main():
                      "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},
         "cast": hbm_class(kt["cast"]),
         "kernels": {k: ({kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
-                        if isinstance(v, dict) else v) for k, v in kt.items()},
-        "gpu_launches": model.launches_per_step() * args.steps,
+                        if isinstance(v, dict) else v) for k, v in kt.items() if k != "launches_per_step"},
+        "gpu_launches": kt["launches_per_step"] * args.steps,
         "e2e": {"value": round(flops * world / e2e_s / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
     }

@@ -68,6 +68,7 @@ _SIGS = {
     "fp8dl_device_supported": (_i32, [_i32]),
     "fp8dl_last_error": (ctypes.c_char_p, []),
     "fp8dl_version": (_i32, []),
+    "fp8dl_kernel_launches": (ctypes.c_uint64, []),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -119,6 +120,11 @@ def fp8dl_last_error() -> str:
 
 def fp8dl_version() -> int:
     return _lib.fp8dl_version()
+
+
+def fp8dl_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process (graph replays not included)."""
+    return _lib.fp8dl_kernel_launches()
 
 
 def fp8dl_device_supported(device: int = 0) -> bool:

@@ -1,5 +1,6 @@
 // abi.cu — library state of the C ABI: error messages, device checks, version.
 #include <stdarg.h>
+#include <atomic>
 #include <stdlib.h>
 #include <string.h>
 
@@ -34,6 +35,10 @@ fp8dl_status fail(fp8dl_status st, const char *fmt, ...) {
     if (debug_enabled()) fprintf(stderr, "[fp8dl] error %d: %s\n", (int)st, g_last_error);
     return st;
 }
+
+std::atomic<uint64_t> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 fp8dl_status check_launch(const char *what) {
     cudaError_t e = cudaGetLastError();
@@ -78,6 +83,8 @@ extern "C" {
 const char *fp8dl_last_error(void) { return fp8dl::g_last_error; }
 
 int32_t fp8dl_version(void) { return 100; }
+
+uint64_t fp8dl_kernel_launches(void) { return fp8dl::g_launches.load(std::memory_order_relaxed); }
 
 int32_t fp8dl_device_supported(int32_t device) {
     int n = 0;

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(RED_COLS *RED_WARPS) colsum_reduce_kernel(cons
 static void launch_colsum_reduce(const float *ws, int64_t n_tiles, int64_t cols, float *dbias, cudaStream_t st) {
     colsum_reduce_kernel<<<(unsigned)((cols + RED_COLS - 1) / RED_COLS), RED_COLS * RED_WARPS, 0, st>>>(ws, n_tiles,
                                                                                                        cols, dbias);
+    note_launch();
 }
 
 void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, cudaStream_t st) {
@@ -272,6 +273,7 @@ static void launch_cast(dim3 grid, cudaStream_t st, const void *x, int64_t rows,
                         uint8_t *out, uint8_t *out_t, float *amax, float *ws) {
     cast_kernel<XKIND, FMT, OP_NONE>
         <<<grid, CT_THREADS, 0, st>>>(x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, nullptr);
+    note_launch();
 }
 
 template <int OP>
@@ -284,6 +286,7 @@ static void launch_op_cast(dim3 grid, cudaStream_t st, int fmt, const void *x, c
     else
         cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP>
             <<<grid, CT_THREADS, 0, st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+    note_launch();
 }
 
 // LayerNorm + cast over 128 x 128 tiles, given the per-row statistics (used by
@@ -366,6 +369,7 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
     }
     if (scale_inv_out) {
         scale_inv_snapshot_kernel<<<1, 32, 0, st>>>(scale, scale_inv_out);
+        note_launch();
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(scale_inv)"));
     }
     return FP8DL_OK;

@@ -18,6 +18,9 @@ void set_error(const char *fmt, ...);
 fp8dl_status fail(fp8dl_status st, const char *fmt, ...);
 fp8dl_status check_launch(const char *what);
 
+// Counts one kernel launch of this library (read through fp8dl_kernel_launches).
+void note_launch();
+
 // Validates the current device (sm_103) once per device and caches the SM count.
 fp8dl_status current_device(int *dev, int *num_sms);
 

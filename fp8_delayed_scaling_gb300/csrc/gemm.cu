@@ -782,6 +782,7 @@ extern "C" fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arriv
     FP8DL_TRY(current_device(nullptr, nullptr));
     wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)budget_cycles, arrive_first ? 1 : 0,
                                                              dev_status);
+    note_launch();
     return check_launch("fp8dl_wait_selftest");
 }
 
@@ -868,6 +869,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
             fp8_gemm_pair_kernel<1, FP8DL_E5M2><<<grid, g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
         else
             fp8_gemm_pair_kernel<0, 0><<<grid, g2::threads(0), g2::smem_bytes(0), stream>>>(ta, tb, tq, args);
+        note_launch();
         return check_launch(epi == 2 ? "fp8_gemm_dgelu_cast(pair)"
                                      : epi == 1 ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");
     }
@@ -878,6 +880,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
     const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
     fp8_gemm_kernel<<<grid, g1::THREADS, g1::SMEM_BYTES, stream>>>(ta, tb, args);
+    note_launch();
     return check_launch("fp8_gemm");
 }
 

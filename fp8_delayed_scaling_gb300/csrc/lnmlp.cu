@@ -821,7 +821,9 @@ static cudaError_t launch_clustered(void (*kernel)(KArgs...), int64_t clusters, 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute at[1];
     cluster_config(cfg, at, clusters, cl, smem, st);
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) note_launch();
+    return e;
 }
 
 }  // namespace fp8dl
@@ -877,6 +879,7 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
         ln_stats_kernel<16><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
     else
         ln_stats_kernel<32><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+    note_launch();
     FP8DL_TRY(check_launch("fp8_layernorm_cast(statistics)"));
     if (!(out || out_t || amax || y)) return FP8DL_OK;
     return launch_layernorm_tile_cast(x, mu, rsigma, gamma, beta, rows, cols, out_dtype, scale, out, out_t, amax, y,
@@ -925,18 +928,22 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
             }
             FP8DL_TRY(check_launch("fp8_layernorm_bwd(cluster)"));
             ln_bwd_reduce_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(part, ncl, cols, dgamma, dbeta);
+            note_launch();
             return check_launch("fp8_layernorm_bwd(reduce)");
         }
     }
     const int64_t row_ctas = (rows + 7) / 8;
     ln_bwd_rowsum_kernel<<<(unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8), 256, 0, st>>>(
         DY, X, G, mu, rsigma, rows, cols, c12);
+    note_launch();
     FP8DL_TRY(check_launch("fp8_layernorm_bwd(row sums)"));
     const int64_t tiles = n_rt * ((cols + LB_COLS - 1) / LB_COLS);
     ln_bwd_tile_kernel<<<(unsigned)(tiles < (int64_t)sms * 4 ? tiles : (int64_t)sms * 4), 256, 0, st>>>(
         DY, X, G, mu, rsigma, c12, rows, cols, static_cast<uint16_t *>(dx), part);
+    note_launch();
     FP8DL_TRY(check_launch("fp8_layernorm_bwd(dx)"));
     ln_bwd_reduce_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(part, n_rt, cols, dgamma, dbeta);
+    note_launch();
     return check_launch("fp8_layernorm_bwd(reduce)");
 }
 

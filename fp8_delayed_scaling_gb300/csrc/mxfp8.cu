@@ -262,7 +262,10 @@ __global__ void sf_pad_kernel(uint8_t *__restrict__ s, int64_t R, int64_t NB, in
 static void launch_sf_pad(uint8_t *s, int64_t R, int64_t NB, cudaStream_t st) {
     const int64_t Rp = (R + 127) / 128 * 128, NBp = (NB + 3) / 4 * 4;
     const int64_t n = (Rp - R) * NBp + R * (NBp - NB);
-    if (n > 0) sf_pad_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(s, R, NB, Rp, NBp);
+    if (n > 0) {
+        sf_pad_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(s, R, NB, Rp, NBp);
+        note_launch();
+    }
 }
 
 
@@ -583,6 +586,7 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
     else
         mxfp8_quantize_kernel<FP8DL_F32><<<grid, MQ_THREADS, smem, (cudaStream_t)stream>>>(x, rows, cols, row_q,
                                                                                             row_s, col_q, col_s);
+    note_launch();
     FP8DL_TRY(check_launch("mxfp8_quantize"));
     if (row_s) launch_sf_pad(row_s, rows, cols / 32, (cudaStream_t)stream);
     if (col_s) launch_sf_pad(col_s, cols, rows / 32, (cudaStream_t)stream);
@@ -637,6 +641,7 @@ fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, 
     const int64_t tiles = ((M + mx::BM - 1) / mx::BM) * ((N + mx::BN - 1) / mx::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
     mxfp8_gemm_kernel<<<grid, mx::THREADS, mx::SMEM_BYTES, (cudaStream_t)stream>>>(ta, tb, args);
+    note_launch();
     return check_launch("mxfp8_gemm");
 }
 

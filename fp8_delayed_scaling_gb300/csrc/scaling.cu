@@ -111,6 +111,7 @@ static fp8dl_status launch_update(const fp8dl_recipe *recipe, int32_t n_slots, v
     const int blocks = (n_slots + slots_per_block - 1) / slots_per_block;
     update_scale_kernel<<<blocks, threads, 0, stream>>>(state, stride, n_slots, recipe->amax_history_len,
                                                         recipe->margin, do_recompute, seed);
+    note_launch();
     return check_launch(seed ? "fp8_seed_amax_history" : "fp8_update_scale");
 }
 
@@ -147,6 +148,7 @@ fp8dl_status fp8_scaling_state_init(const fp8dl_recipe *recipe, int32_t n_slots,
         for (int s = 0; s < count; s++)
             if (slot_fp8_dtype[first + s] == FP8DL_E5M2) m.e5m2[s >> 5] |= 1u << (s & 31);
         init_state_kernel<<<count, 256, 0, (cudaStream_t)stream>>>(state, stride, first, count, Lp, m);
+        note_launch();
         FP8DL_TRY(check_launch("fp8_scaling_state_init"));
     }
     return FP8DL_OK;

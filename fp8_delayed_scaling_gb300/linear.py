@@ -25,6 +25,12 @@ codes together with the decode factor they were cast at; later micro-batches
 factor must travel with the codes: the scale update after each forward may
 already have moved the slot's scale_inv on (a new weight amax entered the
 history).  A skipped cast records no weight amax for that step.
+
+scaling="current" runs the just-in-time alternative that §三.1 contrasts with
+delayed scaling: each tensor's scale comes from its own amax of this step.  A
+cast is then an amax-only pass over the tensor, the amax turned into the
+slot's scale (fp8_seed_amax_history over one slot), and the cast: the tensor
+is read twice, and no history is kept or updated.
 """
 from __future__ import annotations
 
@@ -79,7 +85,9 @@ class Fp8Linear:
     """One linear layer's FP8 buffers and step sequencing (no autograd)."""
 
     def __init__(self, state: ScalingState, layer_index: int, weight: torch.Tensor, bias: torch.Tensor | None,
-                 tokens: int, out_dtype=torch.bfloat16, training: bool = True):
+                 tokens: int, out_dtype=torch.bfloat16, training: bool = True, scaling: str = "delayed"):
+        assert scaling in ("delayed", "current")
+        self.scaling = scaling
         self.state = state
         self.base = layer_index * SLOTS_PER_LAYER
         self.recipe = state.recipe
@@ -125,9 +133,26 @@ class Fp8Linear:
         fp8_cast_amax_transpose(dy, self.bwd_dtype, None, amax=st.amax(self.slot(GRAD)), stream=stream)
         fp8_seed_amax_history(self.recipe, 1, self._state_at(GRAD), stream=stream)
 
+    def _current_cast(self, t: torch.Tensor, fmt: int, k: int, out, out_t, stream, dbias=None) -> None:
+        """Just-in-time cast of t into slot k: amax-only pass, this step's scale, cast."""
+        st = self.state
+        fp8_cast_amax_transpose(t, fmt, None, amax=st.amax(self.slot(k)), stream=stream)
+        fp8_seed_amax_history(self.recipe, 1, self._state_at(k), stream=stream)
+        fp8_cast_amax_transpose(t, fmt, st.scale(self.slot(k)), out=out, out_t=out_t, dbias=dbias,
+                                workspace=self.ws if dbias is not None else None, stream=stream)
+
     def forward(self, x: torch.Tensor, stream=None, is_first_microbatch=None) -> torch.Tensor:
         st = self.state
         tr = self.training
+        if self.scaling == "current":
+            if is_first_microbatch is not None:
+                raise RuntimeError("the weight cache keeps codes at a delayed scale; current scaling recasts")
+            self._current_cast(x, E4M3, IN, self.qx, self.qxT if tr else None, stream)
+            self._current_cast(self.w, E4M3, WEIGHT, self.qw, self.qwT if tr else None, stream)
+            self.w_sinv = st.scale_inv(self.slot(WEIGHT))
+            fp8_gemm(self.qx, E4M3, self.qw, E4M3, st.scale_inv(self.slot(IN)), self.w_sinv, self.y, bias=self.b,
+                     stream=stream)
+            return self.y
         self.wcache.check(is_first_microbatch)
         fp8_cast_amax_transpose(x, E4M3, st.scale(self.slot(IN)), out=self.qx, out_t=self.qxT if tr else None,
                                 amax=st.amax(self.slot(IN)), stream=stream)
@@ -139,8 +164,12 @@ class Fp8Linear:
     def backward(self, dy: torch.Tensor, stream=None):
         st = self.state
         g = self.slot(GRAD)
-        fp8_cast_amax_transpose(dy, self.bwd_dtype, st.scale(g), out=self.qdy, out_t=self.qdyT, amax=st.amax(g),
-                                dbias=self.db, workspace=self.ws if self.db is not None else None, stream=stream)
+        if self.scaling == "current":
+            self._current_cast(dy, self.bwd_dtype, GRAD, self.qdy, self.qdyT, stream, dbias=self.db)
+        else:
+            fp8_cast_amax_transpose(dy, self.bwd_dtype, st.scale(g), out=self.qdy, out_t=self.qdyT,
+                                    amax=st.amax(g), dbias=self.db, workspace=self.ws if self.db is not None else None,
+                                    stream=stream)
         fp8_gemm(self.qdy, self.bwd_dtype, self.qwT, E4M3, st.scale_inv(g), self.w_sinv, self.dx, stream=stream)
         fp8_gemm(self.qdyT, self.bwd_dtype, self.qxT, E4M3, st.scale_inv(g), st.scale_inv(self.slot(IN)),
                  self.dw, stream=stream)

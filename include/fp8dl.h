@@ -349,6 +349,11 @@ fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arrive_first, in
                                  fp8dl_stream_t stream);
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t fp8dl_version(void);
+/* Number of kernels this library has enqueued in this process, over all threads
+ * and devices (launches that failed are not counted).  A CUDA graph replay
+ * launches its captured kernels without calling the library, so it does not
+ * count: count one eager step to know what a replayed step launches. */
+uint64_t fp8dl_kernel_launches(void);
 
 #ifdef __cplusplus
 }

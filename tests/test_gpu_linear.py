@@ -119,3 +119,57 @@ def test_linear_hybrid_ten_steps():
         torch.cuda.synchronize()
         got = state.read()
         assert np.array_equal(got["scale"], ost.scale) and np.array_equal(got["hist"], ost.hist), step
+
+
+def test_linear_current_scaling_two_steps():
+    """Just-in-time (current) scaling, the alternative TE-brief §三.1 contrasts with
+    delayed scaling: every cast of a step uses FP8_MAX/amax of that step's own tensor.
+    The second step's tensors are 4x the first's, so a scale carried over from the
+    previous step would give different codes."""
+    import fp8_delayed_scaling_gb300 as fd
+    from fp8_delayed_scaling_gb300.linear import Fp8Linear, make_state
+    dev = gpu()
+    M2, K2, N2 = 384, 512, 640
+    g = wl.generator(91, "current-linear")
+    w = wl.normal((N2, K2), 0.02, g, torch.bfloat16)
+    b = torch.zeros(N2, dtype=torch.bfloat16)
+    recipe = fd.Recipe(margin=0, interval=1, fp8_format=fd.FORMAT_HYBRID, amax_history_len=1)
+    state = make_state(recipe, 1, device=dev)
+    lin = Fp8Linear(state, 0, w.to(dev), b.to(dev), M2, scaling="current")
+    ws = host(w)
+    for step, f in enumerate((1.0, 4.0)):
+        x = (wl.normal((M2, K2), 1.0, g) * f).to(torch.bfloat16)
+        dy = (wl.normal((M2, N2), 1e-3, g) * f).to(torch.bfloat16)
+        lin.forward(x.to(dev))
+        lin.backward(dy.to(dev))
+        torch.cuda.synchronize()
+        xs, dys = host(x), host(dy)
+        ost = oracle.ScalingState([0, 0, 1], hist_len=1)
+        for i, t in enumerate((xs, ws, dys)):
+            ost.record_amax(i, oracle.amax(t))
+        ost.seed()  # this step's own amaxes give this step's scales
+        got = state.read()
+        assert np.array_equal(got["scale"], ost.scale), step
+        assert np.array_equal(got["scale_inv"], ost.scale_inv), step
+        qx, qw, qdy = (oracle.quantize(0, xs, ost.scale[0]), oracle.quantize(0, ws, ost.scale[1]),
+                       oracle.quantize(1, dys, ost.scale[2]))
+        assert np.array_equal(lin.qx.cpu().numpy(), qx), step
+        assert np.array_equal(lin.qxT.cpu().numpy(), qx.T), step
+        assert np.array_equal(lin.qw.cpu().numpy(), qw), step
+        assert np.array_equal(lin.qdy.cpu().numpy(), qdy), step
+        assert np.array_equal(lin.qdyT.cpu().numpy(), qdy.T), step
+        si = ost.scale_inv
+        ms, ns = _all(M2, N2)
+        ref, absr = oracle.gemm_elems(qx, 0, qw, 0, si[0], si[1], host(b), ms, ns)
+        check_gemm(lin.y, ref, absr, what="forward step %d" % step)
+        ms, ks = _all(M2, K2)
+        ref, absr = oracle.gemm_elems(qdy, 1, np.ascontiguousarray(qw.T), 0, si[2], si[1], None, ms, ks)
+        check_gemm(lin.dx, ref, absr, what="dgrad step %d" % step)
+        ns, ks = _all(N2, K2)
+        ref, absr = oracle.gemm_elems(np.ascontiguousarray(qdy.T), 1, np.ascontiguousarray(qx.T), 0, si[2], si[0],
+                                      None, ns, ks)
+        check_gemm(lin.dw, ref, absr, what="wgrad step %d" % step)
+        s, sabs = oracle.colsum(dys)
+        assert np.all(np.abs(lin.db.cpu().numpy().astype(np.float64) - s) <= M2 * 2.0 ** -24 * sabs + 1e-30)
+    with pytest.raises(RuntimeError):
+        lin.forward(x.to(dev), is_first_microbatch=True)
