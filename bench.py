@@ -806,6 +806,9 @@ def main():
     gemm_ms = g["ms_per_step"]
     achieved = g["flops_per_step"] / (gemm_ms * 1e-3) / 1e12
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP8_PER_BF16
+    # The GEMMs are timed inside a long run of steps (the timing pass follows the timed steps,
+    # under the power cap): the sustained figure is their denominator; the burst one is kept beside.
+    sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP8_PER_BF16
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
 
     def hbm_class(c):  # achieved GB/s of algorithmic bytes against the HBM peak
@@ -819,9 +822,11 @@ def main():
         "dtype": "fp8(e4m3/e5m2)->fp32acc->bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": config,
         "roofline": {"bound": "tensor", "kernel": "mxfp8_gemm" if cfg.get("kind") == "mx" else "fp8_gemm", "achieved": round(achieved, 1),
-                     "peak": round(burst, 1), "unit": "TFLOP/s", "frac": round(achieved / burst, 4),
+                     "peak": round(sustained, 1), "unit": "TFLOP/s", "frac": round(achieved / sustained, 4),
                      "traffic": GEMM_TRAFFIC.get(args.workload),
-                     "peak_src": "%s bf16 burst x %.0f (nominal FP8:BF16)" % (peak_src, FP8_PER_BF16)},
+                     "peak_src": "%s bf16 sustained x %.0f (nominal FP8:BF16); timed inside a long run of steps"
+                                 % (peak_src, FP8_PER_BF16),
+                     "burst_peak": round(burst, 1), "frac_of_burst": round(achieved / burst, 4)},
         "cast": hbm_class(kt["cast"]),
         "kernels": {k: ({kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
                         if isinstance(v, dict) else v) for k, v in kt.items() if k != "launches_per_step"},
