@@ -369,9 +369,6 @@ def run_ours(args, cfg, dev, rank, world):
         model.step()
     torch.cuda.synchronize()
 
-    # per-kernel timing pass (events around each launch class) to find the dominant kernel
-    kt = profile_kernels(model, flush, stream)
-
     # Single-GPU runs replay the step from a CUDA graph (StepGraph): the same launches, without
     # the host cost of issuing them one by one, which decides the small layers' step time.
     # Every recipe here has interval 1, so one graph serves every step.
@@ -409,6 +406,9 @@ def run_ours(args, cfg, dev, rank, world):
     clk = clocks.stop()
     if clk is not None and extra:
         clk["note"] = "sampled during the timed steps and %d untimed steps of the same workload after them" % extra
+    # per-kernel timing pass (events around each launch class) to find the dominant kernel, right
+    # after the timed steps: the kernels run in the same sustained (power-capped) state as the step
+    kt = profile_kernels(model, flush, stream)
     ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -806,8 +806,9 @@ def main():
     gemm_ms = g["ms_per_step"]
     achieved = g["flops_per_step"] / (gemm_ms * 1e-3) / 1e12
     burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * FP8_PER_BF16
-    # The GEMMs are timed inside a long run of steps (the timing pass follows the timed steps,
-    # under the power cap): the sustained figure is their denominator; the burst one is kept beside.
+    # The GEMMs are timed inside a long run of steps (the timing pass directly follows the timed
+    # steps, in the same power-capped state): the sustained figure is their denominator; the burst
+    # one is kept beside.
     sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * FP8_PER_BF16
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
 
