@@ -393,6 +393,10 @@ def run_ours(args, cfg, dev, rank, world):
         b.record(stream)
         evs.append((a, b))
     torch.cuda.synchronize()
+    # per-kernel timing pass (events around each launch class) to find the dominant kernel,
+    # directly after the timed steps with no host pause between: the kernels run in the same
+    # sustained (power-capped) state as the timed steps
+    kt = profile_kernels(model, flush, stream)
     # A timed region shorter than nvidia-smi's first samples (the small layers) is followed by
     # untimed steps of the same workload until a few samples exist (at most 3 s).
     extra, t_extra = 0, time.perf_counter()
@@ -406,9 +410,6 @@ def run_ours(args, cfg, dev, rank, world):
     clk = clocks.stop()
     if clk is not None and extra:
         clk["note"] = "sampled during the timed steps and %d untimed steps of the same workload after them" % extra
-    # per-kernel timing pass (events around each launch class) to find the dominant kernel, right
-    # after the timed steps: the kernels run in the same sustained (power-capped) state as the step
-    kt = profile_kernels(model, flush, stream)
     ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
