@@ -47,8 +47,13 @@ fp8dl_status check_launch(const char *what) {
     return FP8DL_OK;
 }
 
-// Per-device cache: 0 = unknown, 1 = supported, -1 = unsupported.
-static int g_dev_state[64];
+std::mutex &init_mutex() {
+    static std::mutex m;
+    return m;
+}
+
+// Per-device cache: 0 = unknown, 1 = supported, -1 = unsupported (g_dev_sms is written first).
+static std::atomic<int> g_dev_state[64];
 static int g_dev_sms[64];
 
 static int probe_device(int dev) {
@@ -68,9 +73,16 @@ fp8dl_status current_device(int *dev, int *num_sms) {
     cudaError_t e = cudaGetDevice(&d);
     if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (d < 0 || d >= 64) return fail(FP8DL_ERR_UNSUPPORTED_DEVICE, "device index %d out of range", d);
-    if (g_dev_state[d] == 0) g_dev_state[d] = probe_device(d);
-    if (g_dev_state[d] != 1)
-        return fail(FP8DL_ERR_UNSUPPORTED_DEVICE, "device %d is not an sm_103 (GB300) GPU", d);
+    int st = g_dev_state[d].load(std::memory_order_acquire);
+    if (st == 0) {
+        std::lock_guard<std::mutex> lock(init_mutex());
+        st = g_dev_state[d].load(std::memory_order_relaxed);
+        if (st == 0) {
+            st = probe_device(d);
+            g_dev_state[d].store(st, std::memory_order_release);
+        }
+    }
+    if (st != 1) return fail(FP8DL_ERR_UNSUPPORTED_DEVICE, "device %d is not an sm_103 (GB300) GPU", d);
     if (dev) *dev = d;
     if (num_sms) *num_sms = g_dev_sms[d];
     return FP8DL_OK;

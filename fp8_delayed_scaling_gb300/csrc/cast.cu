@@ -458,19 +458,25 @@ namespace fp8dl {
 
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB, held on every device that loads the library
 static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
-static float *g_static_scratch_addr[64];  // device address of g_static_scratch, per device index
+static std::atomic<float *> g_static_scratch_addr[64];  // device address of g_static_scratch, per device index
 
 // The array's name in host code is a host-side stand-in, not a device address:
 // look the address up once per device, with that device current.
 static fp8dl_status static_scratch_address(int dev, float **out) {
-    if (g_static_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess || p == nullptr)
-            return fail(FP8DL_ERR_CUDA, "cudaGetSymbolAddress(static scratch) failed: %s", cudaGetErrorString(e));
-        g_static_scratch_addr[dev] = static_cast<float *>(p);
+    float *a = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+    if (a == nullptr) {
+        std::lock_guard<std::mutex> lock(init_mutex());
+        a = g_static_scratch_addr[dev].load(std::memory_order_relaxed);
+        if (a == nullptr) {
+            void *p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+            if (e != cudaSuccess || p == nullptr)
+                return fail(FP8DL_ERR_CUDA, "cudaGetSymbolAddress(static scratch) failed: %s", cudaGetErrorString(e));
+            a = static_cast<float *>(p);
+            g_static_scratch_addr[dev].store(a, std::memory_order_release);
+        }
     }
-    *out = g_static_scratch_addr[dev];
+    *out = a;
     return FP8DL_OK;
 }
 
@@ -505,6 +511,12 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
     const int64_t max_ctas = (int64_t)sms * 8;
     dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
+    // The cast's partials and their reduction are enqueued back to back with no other call's
+    // launches between them: calls from several host threads on one stream then run one
+    // after another on the GPU, each reading its own partials from the shared array.
+    static std::mutex scratch_order;
+    std::unique_lock<std::mutex> order(scratch_order, std::defer_lock);
+    if (dbias) order.lock();
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
             launch_cast<FP8DL_BF16, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);

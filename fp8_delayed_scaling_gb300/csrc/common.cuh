@@ -6,6 +6,9 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "fp8dl.h"
 #include <nvtx3/nvToolsExt.h>
 
@@ -20,6 +23,11 @@ fp8dl_status check_launch(const char *what);
 
 // Counts one kernel launch of this library (read through fp8dl_kernel_launches).
 void note_launch();
+
+// Serialises the library's one-time, per-device set-up (function attributes, occupancy
+// queries, symbol addresses) across host threads.  The caches it fills are atomics read
+// with acquire ordering, so a thread that sees a cache entry also sees what it stands for.
+std::mutex &init_mutex();
 
 // Validates the current device (sm_103) once per device and caches the SM count.
 fp8dl_status current_device(int *dev, int *num_sms);

@@ -788,12 +788,15 @@ extern "C" fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arriv
 
 namespace fp8dl {
 
-// Per-device launch state of the GEMM kernels.
-static bool g_attr_set[64];
+// Per-device launch state of the GEMM kernels.  g_pair_clusters is written before the
+// release store of g_attr_set; callers read it after gemm_device_setup returned.
+static std::atomic<bool> g_attr_set[64];
 static int g_pair_clusters[64];
 
 static fp8dl_status gemm_device_setup(int dev, int sms) {
-    if (g_attr_set[dev]) return FP8DL_OK;
+    if (g_attr_set[dev].load(std::memory_order_acquire)) return FP8DL_OK;
+    std::lock_guard<std::mutex> lock(init_mutex());
+    if (g_attr_set[dev].load(std::memory_order_relaxed)) return FP8DL_OK;
     cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g1::SMEM_BYTES);
     const void *pair_kernels[] = {(const void *)fp8_gemm_pair_kernel<0, 0>,
                                   (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3>,
@@ -817,7 +820,7 @@ static fp8dl_status gemm_device_setup(int dev, int sms) {
         clusters = 0;  // the pair kernels are not used on this device
     }
     g_pair_clusters[dev] = clusters;
-    g_attr_set[dev] = true;
+    g_attr_set[dev].store(true, std::memory_order_release);
     return FP8DL_OK;
 }
 

@@ -787,9 +787,9 @@ static int ln_max_clusters(const void *kernel, int smem, int cl) {
     return n;
 }
 
-// Resident-cluster counts per device, kernel (0 fwd E4M3, 1 fwd E5M2, 2 bwd) and cluster size; -1 = not queried.
-static int g_ln_clusters[64][3][LC_MAX_CLUSTER + 1];
-static bool g_ln_init[64];
+// Resident-cluster counts + 1 per device, kernel (0 fwd E4M3, 1 fwd E5M2, 2 bwd) and cluster
+// size; 0 = not queried yet.
+static std::atomic<int> g_ln_clusters[64][3][LC_MAX_CLUSTER + 1];
 
 // Number of clusters to launch over `nblk` row blocks, or 0 to take the tile path.
 // FP8DL_LN_VARIANT=tiles forces the tile path and FP8DL_LN_CLUSTERS=n caps the
@@ -800,13 +800,17 @@ static int64_t ln_cluster_count(int dev, int which, const void *kernel, int smem
     if (v && v[0] == 't') return 0;
     const int cl = ln_cluster_size(cols);
     if (cl == 0) return 0;
-    if (!g_ln_init[dev]) {
-        for (auto &k : g_ln_clusters[dev])
-            for (int &r : k) r = -1;
-        g_ln_init[dev] = true;
+    std::atomic<int> &slot = g_ln_clusters[dev][which][cl];
+    int known = slot.load(std::memory_order_acquire);
+    if (known == 0) {
+        std::lock_guard<std::mutex> lock(init_mutex());
+        known = slot.load(std::memory_order_relaxed);
+        if (known == 0) {
+            known = ln_max_clusters(kernel, smem, cl) + 1;  // sets the kernel's attributes first
+            slot.store(known, std::memory_order_release);
+        }
     }
-    int &resident = g_ln_clusters[dev][which][cl];
-    if (resident < 0) resident = ln_max_clusters(kernel, smem, cl);
+    const int64_t resident = known - 1;
     if (resident <= 0) return 0;
     int64_t n = nblk < resident ? nblk : resident;
     if (n > cap) n = cap;

@@ -564,21 +564,24 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
                     (long long)rows, (long long)cols);
     if (!aligned16(x) || !aligned16(row_q) || !aligned16(col_q))
         return fail(FP8DL_ERR_ALIGN, "x, row_q and col_q must be 16-byte aligned");
-    int sms = 0;
-    FP8DL_TRY(current_device(nullptr, &sms));
+    int dev = 0, sms = 0;
+    FP8DL_TRY(current_device(&dev, &sms));
     const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
     const int64_t max_ctas = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(tiles < max_ctas ? tiles : max_ctas);
     const size_t smem = (size_t)MQ_STAGES * 128 * 128 * (x_dtype == FP8DL_BF16 ? 2 : 4);
-    static bool attr[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr[dev]) {
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             MQ_STAGES * 128 * 128 * 2);
-        cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             MQ_STAGES * 128 * 128 * 4);
-        attr[dev] = true;
+    static std::atomic<bool> attr[64];
+    if (!attr[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(init_mutex());
+        if (!attr[dev].load(std::memory_order_relaxed)) {
+            cudaError_t e = cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_BF16>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MQ_STAGES * 128 * 128 * 2);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         MQ_STAGES * 128 * 128 * 4);
+            if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            attr[dev].store(true, std::memory_order_release);
+        }
     }
     if (x_dtype == FP8DL_BF16)
         mxfp8_quantize_kernel<FP8DL_BF16><<<grid, MQ_THREADS, smem, (cudaStream_t)stream>>>(x, rows, cols, row_q,
@@ -631,12 +634,15 @@ fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, 
     args.d_dtype = d_dtype;
     args.status = dev_status;
     pick_raster(M, N, K, mx::BM, mx::BN, args.raster_n, args.group);
-    static bool attr_set[64] = {};
-    if (!attr_set[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(mxfp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx::SMEM_BYTES);
-        if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        attr_set[dev] = true;
+    static std::atomic<bool> attr_set[64];
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(init_mutex());
+        if (!attr_set[dev].load(std::memory_order_relaxed)) {
+            cudaError_t e =
+                cudaFuncSetAttribute(mxfp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mx::SMEM_BYTES);
+            if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            attr_set[dev].store(true, std::memory_order_release);
+        }
     }
     const int64_t tiles = ((M + mx::BM - 1) / mx::BM) * ((N + mx::BN - 1) / mx::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);

@@ -182,9 +182,11 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
  *   call before any stream capture.
  *   Sharing: all calls on a device share the one array, which keeps the last
  *   call's contents; each call writes every scratch entry it reads, so no
- *   clearing is needed.  Calls that overlap on the GPU (different streams, or
- *   host threads without ordering) race on the array and give wrong dbias:
- *   order them on one stream. */
+ *   clearing is needed.  A call enqueues its two launches (partials, then
+ *   their reduction) under a library lock, so calls from several host
+ *   threads on one stream run one after another on the GPU.  Calls whose
+ *   work overlaps on the GPU (different streams not ordered by events) race
+ *   on the array and give wrong dbias: put them on one stream. */
 fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
                                              int32_t out_dtype, const float *scale, uint8_t *out,
                                              uint8_t *out_t, float *amax, float *dbias,
