@@ -398,9 +398,17 @@ def run_ours(args, cfg, dev, rank, world):
     # sustained (power-capped) state as the timed steps
     kt = profile_kernels(model, flush, stream)
     # A timed region shorter than nvidia-smi's first samples (the small layers) is followed by
-    # untimed steps of the same workload until a few samples exist (at most 3 s).
+    # untimed steps of the same workload until a few samples exist (at most 3 s).  With several
+    # ranks every step ends in a collective, so the ranks agree on each round (MAX of their needs).
     extra, t_extra = 0, time.perf_counter()
-    while clocks.proc is not None and clocks.count() < 3 and time.perf_counter() - t_extra < 3.0:
+    while True:
+        need = clocks.proc is not None and clocks.count() < 3 and time.perf_counter() - t_extra < 3.0
+        if world > 1:
+            flag = torch.tensor([1.0 if need else 0.0], device=dev)
+            torch.distributed.all_reduce(flag, op=torch.distributed.ReduceOp.MAX)
+            need = flag.item() > 0
+        if not need:
+            break
         for _ in range(20):
             run_step()
         extra += 20
