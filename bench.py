@@ -369,11 +369,16 @@ def run_ours(args, cfg, dev, rank, world):
         model.step()
     torch.cuda.synchronize()
 
-    # Single-GPU runs replay the step from a CUDA graph (StepGraph): the same launches, without
-    # the host cost of issuing them one by one, which decides the small layers' step time.
-    # Every recipe here has interval 1, so one graph serves every step.
+    # Single-GPU runs replay the step from a CUDA graph (StepGraph: the same launches without
+    # the per-launch host cost, which decides the small layers' step time).  Their per-kernel
+    # times come from eager steps directly after the timed ones (events recorded inside the
+    # graph would add a dependency node between every two kernels and slow the steps they
+    # time).  Several ranks (or --no-graph) step eagerly and time the kernels of the timed
+    # steps themselves.  Every recipe here has interval 1, so one graph serves every step.
+    use_graph = world == 1 and not args.no_graph
+    timer = KernelTimer(model)
     run_step = model.step
-    if world == 1 and not args.no_graph:
+    if use_graph:
         from fp8_delayed_scaling_gb300.graph import StepGraph
         graph = StepGraph(lambda n: model.step(), interval=1, warmup=1)
         run_step = graph.replay
@@ -384,6 +389,8 @@ def run_ours(args, cfg, dev, rank, world):
     torch.cuda.synchronize()
     clocks.start()
     evs = []
+    if not use_graph:
+        timer.__enter__()
     for _ in range(args.steps):
         flush.fill_(1)
         a = torch.cuda.Event(enable_timing=True)
@@ -392,11 +399,27 @@ def run_ours(args, cfg, dev, rank, world):
         run_step()
         b.record(stream)
         evs.append((a, b))
-    torch.cuda.synchronize()
-    # per-kernel timing pass (events around each launch class) to find the dominant kernel,
-    # directly after the timed steps with no host pause between: the kernels run in the same
-    # sustained (power-capped) state as the timed steps
-    kt = profile_kernels(model, flush, stream)
+        if not use_graph:
+            torch.cuda.synchronize()  # between steps, outside the step's events
+            timer.harvest()
+    if use_graph:
+        torch.cuda.synchronize()
+        # per-kernel timing pass: 5 eager steps directly after the timed steps, with no host
+        # pause between, so the kernels run in the same (power-capped) state
+        with timer:
+            for _ in range(5):
+                flush.fill_(1)
+                model.step()
+                torch.cuda.synchronize()
+                timer.harvest()
+        kt = timer.summary(timer.launches // 5)
+        kt["timing"] = "events around every call of 5 eager steps right after the timed (graph-replayed) steps"
+        kt["launch"] = "cuda graph per step"
+    else:
+        timer.__exit__(None, None, None)
+        kt = timer.summary(timer.launches // args.steps)
+        kt["timing"] = "events around every call of the timed steps"
+        kt["launch"] = "eager, one launch at a time"
     # A timed region shorter than nvidia-smi's first samples (the small layers) is followed by
     # untimed steps of the same workload until a few samples exist (at most 3 s).  With several
     # ranks every step ends in a collective, so the ranks agree on each round (MAX of their needs).
@@ -428,70 +451,89 @@ def run_ours(args, cfg, dev, rank, world):
     return model, ms, kt, clk, e2e
 
 
-def profile_kernels(model, flush, stream, reps=5):
-    """Average device time per launch class (cast / gemm / update) over `reps` steps."""
-    import fp8_delayed_scaling_gb300.linear as L
-    import fp8_delayed_scaling_gb300.lnmlp as LM
-    import fp8_delayed_scaling_gb300.mxlinear as MX
-    times = {"gemm": [], "cast": [], "norm_act": [], "update": []}
-    by_entry = {}  # entry point -> [(start, end) events]
-    seq = []        # (entry point, start, end) in call order, all reps
-    flops_per_gemm_step = step_flops(model.cfg)
+class KernelTimer:
+    """CUDA events around every ABI entry point a step calls (and the scale update), by launch
+    class, recorded on the stream each call is enqueued on.  After each step run inside the
+    `with` block has completed, harvest() adds that step's per-call times; summary() averages
+    over the harvested steps.  The library's own launch counter, read around the `with`
+    block, gives the kernels enqueued in it."""
     classes = {"gemm": ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast", "fp8_gemm_dgelu_cast"],
                "cast": ["fp8_cast_amax_transpose", "mxfp8_quantize"],
                "norm_act": ["fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast", "fp8_layernorm_bwd"],
                "update": ["fp8_seed_amax_history"]}  # the just-in-time scale computation
-    kind_of = {name: k for k, names in classes.items() for name in names}
-    saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in kind_of if hasattr(mod, name)]
-    orig_update = model.state.update
 
-    def timed(kind, fn, name):
+    def __init__(self, model):
+        self.model = model
+        self.calls = []  # (class, entry point, start, end) of the step(s) recorded since the last harvest
+        self.tot = {k: 0.0 for k in ("gemm", "cast", "norm_act", "update")}
+        self.ncalls = {k: 0 for k in self.tot}
+        self.by_entry = {}  # entry point -> [total ms, calls]
+        self.by_call = None  # [entry point, total ms] in call order
+        self.steps = 0
+        self.launches = 0
+
+    def _timed(self, kind, fn, name):
         def w(*a, **k):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
+            e0.record()
             fn(*a, **k)
-            e1.record(stream)
-            times[kind].append((e0, e1))
-            by_entry.setdefault(name, []).append((e0, e1))
-            seq.append((name, e0, e1))
+            e1.record()
+            self.calls.append((kind, name, e0, e1))
         return w
 
-    for mod, name, fn in saved:
-        setattr(mod, name, timed(kind_of[name], fn, name))
-    model.state.update = timed("update", orig_update, "fp8_update_scale")
-    fd = sys.modules["fp8_delayed_scaling_gb300"]
-    n0 = fd.fp8dl_kernel_launches()
-    try:
-        for _ in range(reps):
-            flush.fill_(1)
-            model.step()
-        torch.cuda.synchronize()
-        n1 = fd.fp8dl_kernel_launches()
-    finally:
-        for mod, name, fn in saved:
+    def __enter__(self):
+        import fp8_delayed_scaling_gb300.linear as L
+        import fp8_delayed_scaling_gb300.lnmlp as LM
+        import fp8_delayed_scaling_gb300.mxlinear as MX
+        kind_of = {name: k for k, names in self.classes.items() for name in names}
+        self.saved = [(mod, name, getattr(mod, name)) for mod in (L, LM, MX) for name in kind_of if hasattr(mod, name)]
+        for mod, name, fn in self.saved:
+            setattr(mod, name, self._timed(kind_of[name], fn, name))
+        self.orig_update = self.model.state.update
+        self.model.state.update = self._timed("update", self.orig_update, "fp8_update_scale")
+        self.n0 = sys.modules["fp8_delayed_scaling_gb300"].fp8dl_kernel_launches()
+        return self
+
+    def __exit__(self, *exc):
+        self.launches += sys.modules["fp8_delayed_scaling_gb300"].fp8dl_kernel_launches() - self.n0
+        for mod, name, fn in self.saved:
             setattr(mod, name, fn)
-        model.state.update = orig_update
-    out = {}
-    for k, v in times.items():
-        tot = sum(a.elapsed_time(b) for a, b in v)
-        out[k] = {"ms_per_step": tot / reps, "launches_per_step": len(v) // reps,
-                  "avg_launch_ms": tot / max(1, len(v))}
-    out["by_entry"] = {k: {"ms_per_step": round(sum(a.elapsed_time(b) for a, b in v) / reps, 5),
-                           "calls_per_step": len(v) // reps} for k, v in by_entry.items()}
-    per = len(seq) // reps  # the calls of one step, in order, averaged over the reps
-    out["by_call"] = [[seq[i][0], round(sum(seq[r * per + i][1].elapsed_time(seq[r * per + i][2])
-                                            for r in range(reps)) / reps, 5)] for i in range(per)]
-    out["gemm"]["flops_per_step"] = flops_per_gemm_step
-    fused = getattr(getattr(model, "blk", None), "fused", False) and not getattr(model, "current", False)
-    for k, v in hbm_bytes(model.cfg, fused=fused).items():
-        out[k]["bytes_per_step"] = v
-    if not times["norm_act"]:
-        del out["norm_act"]
-    # the library's own kernel launches per step, counted by the library (a replayed graph
-    # of the step launches the same kernels)
-    out["launches_per_step"] = (n1 - n0) // reps
-    return out
+        self.model.state.update = self.orig_update
+        return False
+
+    def harvest(self):
+        """Add the per-call times of the step that just completed (the caller synchronised)."""
+        if self.by_call is None:
+            self.by_call = [[name, 0.0] for _, name, _, _ in self.calls]
+        assert len(self.by_call) == len(self.calls), "every step must make the same calls"
+        for i, (kind, name, e0, e1) in enumerate(self.calls):
+            t = e0.elapsed_time(e1)
+            self.tot[kind] += t
+            self.ncalls[kind] += 1
+            ent = self.by_entry.setdefault(name, [0.0, 0])
+            ent[0] += t
+            ent[1] += 1
+            self.by_call[i][1] += t
+        self.steps += 1
+        self.calls = []
+
+    def summary(self, launches_per_step):
+        n = max(1, self.steps)
+        out = {k: {"ms_per_step": self.tot[k] / n, "launches_per_step": self.ncalls[k] // n,
+                   "avg_launch_ms": self.tot[k] / max(1, self.ncalls[k])} for k in self.tot}
+        out["by_entry"] = {k: {"ms_per_step": round(v[0] / n, 5), "calls_per_step": v[1] // n}
+                           for k, v in self.by_entry.items()}
+        out["by_call"] = [[name, round(t / n, 5)] for name, t in (self.by_call or [])]
+        model = self.model
+        out["gemm"]["flops_per_step"] = step_flops(model.cfg)
+        fused = getattr(getattr(model, "blk", None), "fused", False) and not getattr(model, "current", False)
+        for k, v in hbm_bytes(model.cfg, fused=fused).items():
+            out[k]["bytes_per_step"] = v
+        if not self.ncalls["norm_act"]:
+            del out["norm_act"]
+        out["launches_per_step"] = launches_per_step  # the library's own kernels, counted by the library
+        return out
 
 
 def run_e2e(args, model, dev, stream, world):
@@ -768,11 +810,12 @@ def main():
     peaks, peak_src = load_peaks()
     config = {"workload": args.workload, "desc": cfg["desc"], "tokens": cfg["tokens"],
               "l2": "flushed between timed steps (512 MB write)", "parallelism": "replicas" if world > 1 else "single",
-              "launch": "cuda graph per step" if world == 1 and not args.no_graph else "eager"}
+              "launch": None}  # set from the run
 
     if args.impl == "reference":
         if rank != 0:
             return
+        del config["launch"]  # the oracle runs on the host
         # the oracle as it stands on the host cores: W untimed and K timed steps, each a bounded
         # sample of the step scaled to the whole step.  The sample is the cpu_baseline one
         # (64-row slabs, 8 output rows per GEMM) unless W + K of those would take more than
@@ -809,6 +852,7 @@ def main():
             run_only(args, dev)
         return
     model, ms, kt, clk, (e2e_s, h2d, d2h) = run_ours(args, cfg, dev, rank, world)
+    config["launch"] = kt.pop("launch")
     flops = step_flops(cfg)
     value = flops * world / (ms * 1e-3) / 1e12
     g = kt["gemm"]
