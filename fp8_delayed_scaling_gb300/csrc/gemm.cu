@@ -488,6 +488,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
         constexpr int NEPI = 32 * epi_warps(EPI);            // epilogue threads
         const float sc = __fmul_rn(__ldg(args.a_scale_inv), __ldg(args.b_scale_inv));
         const float qscale = EPI ? __ldg(args.q_scale) : 0.0f;
+        // 32-byte row stores where every row segment is 32-byte aligned: D's 32-column chunks of
+        // bf16 (N a multiple of 16) and q's 32-byte chunks (N a multiple of 32)
+        const bool d_v8 = (reinterpret_cast<uintptr_t>(args.D) & 31) == 0;
+        const bool q_v8 = EPI && (reinterpret_cast<uintptr_t>(args.q) & 31) == 0 && (args.N & 31) == 0;
         // Transposed staging of the fused epilogue: qt_stage holds the CTA's q^T block as 256
         // rows of 128 bytes (one per output column) in the TMA 128-byte swizzle (16-byte chunk
         // k of row R at chunk k ^ (R & 7)).  A 4x4 byte transpose across each lane quad leaves
@@ -540,11 +544,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                 if (row_ok && n0 < args.N && args.D) {
                     if (EPI || args.d_dtype == FP8DL_BF16) {
                         __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.D) + row * args.N + n0;
+                        if (d_v8 && n0 + 32 <= args.N) {  // two full 32-byte sectors
+                            st_global_v8(drow, hw[0], hw[1], hw[2], hw[3], hw[4], hw[5], hw[6], hw[7]);
+                            st_global_v8(drow + 16, hw[8], hw[9], hw[10], hw[11], hw[12], hw[13], hw[14], hw[15]);
+                        } else {
 #pragma unroll
-                        for (int g = 0; g < 4; g++)
-                            if (n0 + 8 * g < args.N)
-                                *reinterpret_cast<uint4 *>(drow + 8 * g) =
-                                    make_uint4(hw[4 * g], hw[4 * g + 1], hw[4 * g + 2], hw[4 * g + 3]);
+                            for (int g = 0; g < 4; g++)
+                                if (n0 + 8 * g < args.N)
+                                    *reinterpret_cast<uint4 *>(drow + 8 * g) =
+                                        make_uint4(hw[4 * g], hw[4 * g + 1], hw[4 * g + 2], hw[4 * g + 3]);
+                        }
                     } else {
                         float *drow = static_cast<float *>(args.D) + row * args.N + n0;
 #pragma unroll
@@ -636,9 +645,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     if (row_ok) gmax = fmaxf(gmax, cmax);
                     if (row_store) {
                         uint8_t *qrow = args.q + row * args.N + n0;
-                        if (n0 + 16 <= args.N) *reinterpret_cast<uint4 *>(qrow) = make_uint4(code[0], code[1], code[2], code[3]);
-                        if (n0 + 32 <= args.N)
-                            *reinterpret_cast<uint4 *>(qrow + 16) = make_uint4(code[4], code[5], code[6], code[7]);
+                        if (q_v8 && n0 + 32 <= args.N) {  // one full 32-byte sector
+                            st_global_v8(qrow, code[0], code[1], code[2], code[3], code[4], code[5], code[6], code[7]);
+                        } else {
+                            if (n0 + 16 <= args.N)
+                                *reinterpret_cast<uint4 *>(qrow) = make_uint4(code[0], code[1], code[2], code[3]);
+                            if (n0 + 32 <= args.N)
+                                *reinterpret_cast<uint4 *>(qrow + 16) = make_uint4(code[4], code[5], code[6], code[7]);
+                        }
                     }
                     if (EPI == 2 && args.ws) {
                         // the rest of the reduce-scatter: lane l ends with column n0 + l summed
