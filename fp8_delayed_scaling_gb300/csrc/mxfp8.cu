@@ -56,7 +56,7 @@ __host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t b, int6
 // an in-register 8 x 8 byte transpose as 8-byte pieces of the transposed rows
 // (four lanes fill each 32-byte sector).
 // ---------------------------------------------------------------------------
-constexpr int MQ_THREADS = 256, MQ_WARPS = MQ_THREADS / 32, MQ_STAGES = 3;
+constexpr int MQ_THREADS = 256, MQ_STAGES = 3;
 
 // Transpose a 4x4 byte block held as 4 row words: word c of the result holds
 // column c, rows in byte order.
