@@ -36,7 +36,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose,
+from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose,
                fp8_cast_workspace_size, fp8_gemm, fp8_seed_amax_history)
 
 SLOTS_PER_LAYER = 3

@@ -1,7 +1,6 @@
 """Failure detection without a GPU fault: bounded waits report a timeout
 through a device status word and leave the context usable; bad arguments fail
 on the host before any launch; checkpoint/resume of the scaling state."""
-import numpy as np
 import pytest
 import torch
 

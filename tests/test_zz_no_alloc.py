@@ -12,8 +12,6 @@ beyond the static array are refused before any launch.
 Kept in a file that pytest collects last, so that a run stopping at the first
 failure has already run every other test.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
