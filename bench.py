@@ -268,9 +268,13 @@ class LnMlpModel:
             close_step(self.state, self.step_no)
         self.step_no += 1
 
-    def outputs(self):
+    def output_slots(self):
+        """(object, attribute) of every tensor a step produces for the host, in order."""
         b = self.blk
-        return [b.dw1, b.dw2, b.db1, b.db2, b.dgamma, b.dbeta, b.dx]
+        return [(b, "dw1"), (b, "dw2"), (b, "db1"), (b, "db2"), (b, "dgamma"), (b, "dbeta"), (b, "dx")]
+
+    def outputs(self):
+        return [getattr(o, a) for o, a in self.output_slots()]
 
 
 class MxModel:
@@ -300,8 +304,11 @@ class MxModel:
         dh, _, _ = self.down.backward(self.dy[0])
         self.up.backward(dh)
 
+    def output_slots(self):
+        return [(self.up, "dw"), (self.down, "dw"), (self.up, "dx")]
+
     def outputs(self):
-        return [self.up.dw, self.down.dw, self.up.dx]
+        return [getattr(o, a) for o, a in self.output_slots()]
 
 
 class Model:
@@ -338,14 +345,17 @@ class Model:
             for lin, dy in zip(self.layers, self.dy):
                 lin.seed_backward(dy[:self.Mmb])
 
-    def outputs(self):
+    def output_slots(self):
         out = []
         for lin in self.layers:
             if self.cfg["training"]:
-                out += [lin.dw] + ([lin.db] if lin.db is not None else [])
+                out += [(lin, "dw")] + ([(lin, "db")] if lin.db is not None else [])
             else:
-                out.append(lin.y)
+                out.append((lin, "y"))
         return out
+
+    def outputs(self):
+        return [getattr(o, a) for o, a in self.output_slots()]
 
     def step(self, timers=None):
         m = self.Mmb
@@ -540,31 +550,36 @@ def run_e2e(args, model, dev, stream, world):
     """Same step through the C ABI with HOST inputs and outputs: every step copies every
     layer's X and dY from pinned memory to the device and the step's products (weight and
     bias gradients, dx, ...) back to pinned memory.  The copies run through
-    HostStepPipeline: on two copy streams, overlapped with the neighbouring steps' compute.
-    On one GPU the step itself is replayed from a CUDA graph captured for each input set."""
+    HostStepPipeline: on two copy streams, overlapped with the neighbouring steps' compute,
+    with two input and two output sets (each step writes its products straight into the
+    output set whose host copy finished, so nothing is copied on the device).  On one GPU
+    the step itself is replayed from a CUDA graph captured for each pair of sets."""
     from fp8_delayed_scaling_gb300.pipeline import HostStepPipeline
     nx = len(model.x)
     host_in = [x.cpu().pin_memory() for x in model.x] + [d.cpu().pin_memory() for d in model.dy]
+    slots = model.output_slots()
     dev_out = model.outputs()
     host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in dev_out]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(h.numel() * h.element_size() for h in host_out)
-    pipe = HostStepPipeline(model.x + model.dy, dev_out)
+    pipe = HostStepPipeline(model.x + model.dy, dev_out, out_sets=True)
 
-    def eager(ins):
+    def eager(ins, outs):
         model.x[:] = ins[:nx]
         model.dy[:] = ins[nx:]
+        for (obj, attr), t in zip(slots, outs):
+            setattr(obj, attr, t)
         model.step()
 
     step = eager
-    if world == 1 and not args.no_graph:  # one captured step per input buffer set
+    if world == 1 and not args.no_graph:  # one captured step per input/output set pair
         from fp8_delayed_scaling_gb300.graph import StepGraph
         graphs = []
         for k in range(2):
-            ins = pipe.sets[k]
-            graphs.append(StepGraph(lambda n, ins=ins: eager(ins), interval=1, warmup=1))
+            ins, outs = pipe.sets[k], pipe.out_sets[k]
+            graphs.append(StepGraph(lambda n, ins=ins, outs=outs: eager(ins, outs), interval=1, warmup=1))
 
-        def step(ins):
+        def step(ins, outs):
             graphs[0 if ins is pipe.sets[0] else 1].replay()
 
     steps = max(1, min(args.steps, 20))

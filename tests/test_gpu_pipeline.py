@@ -64,3 +64,45 @@ def test_pipelined_steps_match_in_order_steps():
     for i in range(steps):
         for a, b in zip(outs[i], ref[i]):
             assert torch.equal(a, b), "step %d" % i
+
+
+def test_pipelined_steps_with_two_output_sets_match_in_order_steps():
+    """out_sets=True: each step writes its products straight into output set i%2 (no
+    snapshot copy); step i+2 waits for the host copy of step i's set."""
+    from fp8_delayed_scaling_gb300.pipeline import HostStepPipeline
+    dev = gpu()
+    steps = 5
+    hx = [wl.normal((M, K), 1.0 + 3 * i, wl.generator(92, "X", i), torch.bfloat16).pin_memory() for i in range(steps)]
+    hdy = [wl.normal((M, N), 1e-3 * (1 + i), wl.generator(92, "dY", i), torch.bfloat16).pin_memory()
+           for i in range(steps)]
+    names = ("dx", "dw", "db", "y")
+
+    state, lin, x, dy = _layer(dev)
+    ref = []
+    for i in range(steps):
+        x.copy_(hx[i])
+        dy.copy_(hdy[i])
+        lin.forward(x)
+        lin.backward(dy)
+        state.update(i)
+        ref.append([getattr(lin, n).cpu() for n in names])
+
+    state, lin, x, dy = _layer(dev)
+    outs = [[torch.empty_like(getattr(lin, n), device="cpu").pin_memory() for n in names] for _ in range(steps)]
+    pipe = HostStepPipeline([x, dy], [getattr(lin, n) for n in names], out_sets=True)
+    assert pipe.out_sets[0][0] is not pipe.out_sets[1][0]
+    count = [0]
+
+    def step(ins, outs_dev):
+        for n, t in zip(names, outs_dev):
+            setattr(lin, n, t)
+        lin.forward(ins[0])
+        lin.backward(ins[1])
+        state.update(count[0])
+        count[0] += 1
+
+    pipe.run(steps, step, lambda i: [hx[i], hdy[i]], lambda i: outs[i])
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for n, a, b in zip(names, outs[i], ref[i]):
+            assert torch.equal(a, b), "step %d %s" % (i, n)
