@@ -11,10 +11,10 @@
 //
 // Two implementations of each direction:
 //  - cluster path (cols a multiple of 512, at most 16 x 512): a thread-block
-//    cluster owns blocks of 32 rows; CTA k of the cluster keeps columns
-//    [512k, 512k + 512) of the block in registers, the CTAs exchange per-row
-//    partial sums through distributed shared memory, and x (and dy) are read
-//    from HBM once;
+//    cluster owns blocks of rows (32 forward, 16 backward); CTA k of the cluster
+//    stages columns [512k, 512k + 512) of the block in shared memory, the CTAs
+//    push their per-row partial sums into each other's shared memory, and x
+//    (and dy) are read from HBM once;
 //  - tile path (any other width): a warp-per-row statistics pass, then 128 x 128
 //    tiles (the cast kernel with a LayerNorm element operation, in cast.cu).
 #include <cuda_bf16.h>
@@ -92,16 +92,17 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
 //
 // Software pipeline, per CTA, in iteration j:
 //   - block j+2 is copied into shared memory;
-//   - the row partials of block j+1 are reduced over the CTA and published in
-//     this CTA's exchange slot;
-//   - the CTA waits on the cluster barrier for block j (arrived one iteration
-//     earlier), arrives for block j+1, and warp 0 gathers block j's partials
-//     from every CTA of the cluster, in rank order; block j is normalised and
-//     written.
-// The barrier's latency is thus hidden behind a whole block's work.  Exchange
-// slots rotate over four blocks: a CTA writes the slot of block j+4 only after
-// its wait for block j+2, which needs every peer's arrival for block j+2, which
-// each peer makes after gathering block j.
+//   - the row partials of block j+1 are reduced over the CTA and pushed with
+//     st.async into exchange slot (j+1) mod 4 of every CTA of the cluster
+//     (this CTA's entry of each), completing on that CTA's slot barrier;
+//   - warp 0 waits on its own slot barrier for block j (pushed one iteration
+//     earlier), merges the CTAs' partials in rank order, re-arms the barrier
+//     for block j+4, and block j is normalised and written.
+// The exchange's latency is thus hidden behind a whole block's work, and no
+// cluster-wide barrier or release fence (which would also wait for the
+// previous block's global stores) sits in the loop.  Slots rotate over four
+// blocks: a CTA pushes block j+4 only after it has received block j+2 from
+// every CTA, and each CTA pushes block j+2 after it has read block j.
 // A barrier at the top of every iteration separates the refill of a buffer
 // from the previous block's reads of it.
 // ---------------------------------------------------------------------------
@@ -111,7 +112,10 @@ constexpr int LF_ROWS = 32;  // forward block: two halves of 16 rows, 32-byte co
 constexpr int LB_BLK = 16;   // backward block: 4 rows per thread
 constexpr int LB_CTAS = 2;   // backward CTAs per SM (registers and shared memory sized for it)
 constexpr int LF_BUF = LF_ROWS * LC_COLS * 2;      // one staged x block
-constexpr int LF_SMEM = LC_NBUF * LF_BUF;
+constexpr int LF_SMEM = LC_NBUF * LF_BUF;  // then LC_SLOTS x cluster size x LF_ROWS pushed float2
+// dynamic shared memory of a launch: staged blocks plus `slot_rows` rows of pushed partials per
+// slot and CTA of the cluster
+constexpr int ln_smem(int base, int slot_rows, int cl) { return base + LC_SLOTS * cl * slot_rows * 8; }
 constexpr int LB_SMEM = LC_NBUF * 2 * LB_BLK * LC_COLS * 2;  // three staged (dy, x) blocks
 
 __device__ __forceinline__ int next_buf(int b) { return b == LC_NBUF - 1 ? 0 : b + 1; }
@@ -204,9 +208,9 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     int64_t rows, int64_t cols, float eps, const float *__restrict__ scale_p, uint8_t *__restrict__ out,
     uint8_t *__restrict__ out_t, float *__restrict__ amax_p, float *__restrict__ mu_out, float *__restrict__ rs_out,
     uint16_t *__restrict__ y) {
-    extern __shared__ __align__(128) uint8_t lsm[];      // [LC_NBUF][LF_ROWS][LC_COLS] bf16
+    extern __shared__ __align__(128) uint8_t lsm[];      // [LC_NBUF][LF_ROWS][LC_COLS] bf16, then the slots
     __shared__ float2 wst[LC_WARPS][2][16];              // per-warp (mean, M2) of 64 values of a row
-    __shared__ float2 xch[LC_SLOTS][LF_ROWS];            // slab (mean, M2) of a block, read by the cluster
+    __shared__ __align__(8) uint64_t xbar[LC_SLOTS];     // slot s complete: every CTA's slabs of its block arrived
     __shared__ float2 stat[LF_ROWS];                     // mean, rsigma
     __shared__ float wmax[LC_WARPS];
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -216,6 +220,8 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     const int64_t nblk = (rows + LF_ROWS - 1) / LF_ROWS;
     const int64_t cid = blockIdx.x / ncta, ncl = gridDim.x / ncta;
     const int64_t nb = cid < nblk ? (nblk - cid + ncl - 1) / ncl : 0;  // this cluster's blocks
+    float2 *gath = reinterpret_cast<float2 *>(lsm + LF_SMEM);  // [LC_SLOTS][ncta][LF_ROWS], pushed by the CTAs
+    const uint32_t push_bytes = ncta * LF_ROWS * (uint32_t)sizeof(float2);  // per slot and block
     const float scale = (out || out_t) ? __ldg(scale_p) : 1.0f;
     const float2 sc2 = make_float2(scale, scale);
     const uint2 gv = __ldg(reinterpret_cast<const uint2 *>(gamma + col));
@@ -255,16 +261,26 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
         }
         wst[w][h][lane >> 1] = warp_chan_rows16(st, lane);  // row 8*b4 + 4*b3 + 2*b2 + b1 of half h
     };
-    // After a barrier: the slab (mean, M2) of each row from the eight warps, into xch[slot].
-    auto merge = [&](int slot) {
+    // After a barrier: the slab (mean, M2) of each row from the eight warps, pushed into slot
+    // `slot` of every CTA of the cluster (this CTA's entry), completing on that CTA's barrier.
+    auto push = [&](int slot) {
         if (t < LF_ROWS) {
             const int hh = t >> 4, ri = t & 15;  // the row's half, row within it
             float2 q[4];
 #pragma unroll
             for (int k = 0; k < 4; k++) q[k] = chan_equal(wst[2 * k][hh][ri], wst[2 * k + 1][hh][ri], 32.0f);
-            xch[slot][t] = chan_equal(chan_equal(q[0], q[1], 64.0f), chan_equal(q[2], q[3], 64.0f), 128.0f);
+            const float2 v = chan_equal(chan_equal(q[0], q[1], 64.0f), chan_equal(q[2], q[3], 64.0f), 128.0f);
+            const uint32_t la = smem_u32(&gath[(slot * ncta + rank) * LF_ROWS + t]), lb = smem_u32(&xbar[slot]);
+            for (uint32_t k = 0; k < ncta; k++) st_async_f2(mapa_shared(la, k), v, mapa_shared(lb, k));
         }
     };
+    if (t == 0) {
+        for (int k = 0; k < LC_SLOTS; k++) mbar_init(smem_u32(&xbar[k]), 1);
+        mbar_fence_init();
+    }
+    cluster_sync();  // every CTA's barriers are initialised before anything is pushed to them
+    if (t == 0)
+        for (int k = 0; k < LC_SLOTS && k < nb; k++) mbar_expect_tx(smem_u32(&xbar[k]), push_bytes);
     float amax = 0.0f;
     if (nb > 0) {  // always, as no more clusters than blocks are launched
         issue(0, 0);
@@ -273,8 +289,7 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
         __syncthreads();  // block 0 was copied by every thread
         partials(0);
         __syncthreads();
-        merge(0);
-        cluster_arrive();
+        push(0);
     }
     int buf = 0, slot = 0;
     for (int64_t j = 0; j < nb; j++) {
@@ -286,17 +301,16 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
         if (j + 1 < nb) {
             partials(next_buf(buf));
             __syncthreads();
-            merge(nslot);
+            push(nslot);
         }
-        cluster_wait();                   // every slab of block j is published
-        if (j + 1 < nb) cluster_arrive();  // block j+1's slab is published
         if (t < LF_ROWS) {
-            const uint32_t a = smem_u32(&xch[slot][t]);
+            // every CTA's slab of block j has arrived (a wait that runs out leaves NaN statistics)
+            const bool arrived = mbar_wait_bounded(smem_u32(&xbar[slot]), (uint32_t)((j / LC_SLOTS) & 1));
             float2 p[LC_MAX_CLUSTER];
 #pragma unroll
             for (int k = 0; k < LC_MAX_CLUSTER; k++)
-                if (k < (int)ncta) p[k] = ld_dsmem_f32x2(mapa_shared(a, (uint32_t)k));
-            float sm = 0.0f;
+                if (k < (int)ncta) p[k] = gath[(slot * ncta + k) * LF_ROWS + t];
+            float sm = arrived ? 0.0f : __int_as_float(0x7fc00000);
 #pragma unroll
             for (int k = 0; k < LC_MAX_CLUSTER; k++)
                 if (k < (int)ncta) sm += p[k].x;
@@ -314,6 +328,8 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
                 mu_out[r0 + t] = mean;
                 rs_out[r0 + t] = rsig;
             }
+            // the slot's next block: its barrier counts the pushes of block j + LC_SLOTS
+            if (t == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
         }
         __syncthreads();
         if (r0 + 16 * h < rows) {  // rows are a multiple of 16: a half is all in or all out
@@ -364,7 +380,7 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
             atomic_max_nonneg(amax_p, mm);
         }
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its exchange slots
+    cluster_sync();  // every push to this CTA has arrived (it waited for them); none leaves before the rest
 }
 
 // ---------------------------------------------------------------------------
@@ -577,9 +593,9 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
     uint16_t *__restrict__ dx, float *__restrict__ part) {
     constexpr int RPT = BLK / 4;                     // rows per thread
     constexpr int BUF = 2 * BLK * LC_COLS * 2;       // one staged (dy, x) block
-    extern __shared__ __align__(128) uint8_t lsm[];  // [LC_NBUF][dy, x][BLK][LC_COLS] bf16
+    extern __shared__ __align__(128) uint8_t lsm[];  // [LC_NBUF][dy, x][BLK][LC_COLS] bf16, then the slots
     __shared__ float2 wsum[LC_WARPS][RPT];
-    __shared__ float2 xch[LC_SLOTS][BLK];
+    __shared__ __align__(8) uint64_t xbar[LC_SLOTS];  // slot s complete: every CTA's partials of its block arrived
     __shared__ float2 cst[BLK];                      // mean(g), mean(g * xhat)
     __shared__ float mrs[LC_NBUF][2][BLK];           // [buffer][mu, rs][row]
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
@@ -589,6 +605,8 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
     const int64_t nblk = (rows + BLK - 1) / BLK;
     const int64_t cid = blockIdx.x / ncta, ncl = gridDim.x / ncta;
     const int64_t nb = cid < nblk ? (nblk - cid + ncl - 1) / ncl : 0;
+    float2 *gath = reinterpret_cast<float2 *>(lsm + LC_NBUF * BUF);  // [LC_SLOTS][ncta][BLK], pushed by the CTAs
+    const uint32_t push_bytes = ncta * BLK * (uint32_t)sizeof(float2);  // per slot and block
     const float inv_cols = 1.0f / (float)cols;
     const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gamma + col));
     const float2 g2[4] = {bf16x2_f2(gv.x), bf16x2_f2(gv.y), bf16x2_f2(gv.z), bf16x2_f2(gv.w)};
@@ -645,13 +663,23 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
         const float2 r = warp_sum_rows<RPT>(s, lane);
         if ((lane & (32 / RPT - 1)) == 0) wsum[w][lane / (32 / RPT)] = r;
     };
-    // After a barrier: the CTA's row partials from the two warps of each row group, into xch[slot].
-    auto merge = [&](int slot) {
+    // After a barrier: the CTA's row partials from the two warps of each row group, pushed into
+    // slot `slot` of every CTA of the cluster (this CTA's entry), completing on that CTA's barrier.
+    auto push = [&](int slot) {
         if (t < BLK) {
             const float2 a = wsum[2 * (t / RPT)][t % RPT], b = wsum[2 * (t / RPT) + 1][t % RPT];
-            xch[slot][t] = make_float2(a.x + b.x, a.y + b.y);
+            const float2 v = make_float2(a.x + b.x, a.y + b.y);
+            const uint32_t la = smem_u32(&gath[(slot * ncta + rank) * BLK + t]), lb = smem_u32(&xbar[slot]);
+            for (uint32_t k = 0; k < ncta; k++) st_async_f2(mapa_shared(la, k), v, mapa_shared(lb, k));
         }
     };
+    if (t == 0) {
+        for (int k = 0; k < LC_SLOTS; k++) mbar_init(smem_u32(&xbar[k]), 1);
+        mbar_fence_init();
+    }
+    cluster_sync();  // every CTA's barriers are initialised before anything is pushed to them
+    if (t == 0)
+        for (int k = 0; k < LC_SLOTS && k < nb; k++) mbar_expect_tx(smem_u32(&xbar[k]), push_bytes);
     if (nb > 0) {  // always, as no more clusters than blocks are launched
         issue(0, 0);
         issue(1, 1);
@@ -659,8 +687,7 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
         __syncthreads();  // mu and rs of block 0 were copied by other threads
         partials(0);
         __syncthreads();
-        merge(0);
-        cluster_arrive();
+        push(0);
     }
     int buf = 0, slot = 0;
     for (int64_t j = 0; j < nb; j++) {
@@ -672,27 +699,21 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
         if (j + 1 < nb) {
             partials(next_buf(buf));
             __syncthreads();
-            merge(nslot);
+            push(nslot);
         }
-        cluster_wait();                   // every CTA's partials of block j are published
-        if (j + 1 < nb) cluster_arrive();  // block j+1's partials are published
         if (t < BLK) {
-            const uint32_t a = smem_u32(&xch[slot][t]);
-            float2 tot = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int k0 = 0; k0 < LC_MAX_CLUSTER; k0 += 8) {  // two rounds of 8 loads in flight
-                float2 p[8];
-#pragma unroll
-                for (int k = 0; k < 8; k++)
-                    if (k0 + k < (int)ncta) p[k] = ld_dsmem_f32x2(mapa_shared(a, (uint32_t)(k0 + k)));
-#pragma unroll
-                for (int k = 0; k < 8; k++)
-                    if (k0 + k < (int)ncta) {
-                        tot.x += p[k].x;
-                        tot.y += p[k].y;
-                    }
+            // every CTA's partials of block j have arrived (a wait that runs out leaves NaN)
+            const bool arrived = mbar_wait_bounded(smem_u32(&xbar[slot]), (uint32_t)((j / LC_SLOTS) & 1));
+            const float nan = __int_as_float(0x7fc00000);
+            float2 tot = arrived ? make_float2(0.0f, 0.0f) : make_float2(nan, nan);
+            for (uint32_t k = 0; k < ncta; k++) {  // rank order
+                const float2 p = gath[(slot * ncta + k) * BLK + t];
+                tot.x += p.x;
+                tot.y += p.y;
             }
             cst[t] = make_float2(tot.x * inv_cols, tot.y * inv_cols);
+            // the slot's next block: its barrier counts the pushes of block j + LC_SLOTS
+            if (t == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
         }
         __syncthreads();
         if (r0 + RPT * g < rows) {  // rows are a multiple of 16: always
@@ -742,7 +763,7 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
         part[cid * cols + col0 + k] = a;
         part[(ncl + cid) * cols + col0 + k] = b;
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its exchange slots
+    cluster_sync();  // every push to this CTA has arrived (it waited for them); none leaves before the rest
 }
 
 // ---------------------------------------------------------------------------
@@ -769,8 +790,8 @@ static void cluster_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *at, int
 }
 
 // How many clusters of `cl` CTAs of `kernel` can be resident at once (0: none).
-static int ln_max_clusters(const void *kernel, int smem, int cl) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+static int ln_max_clusters(const void *kernel, int smem, int smem_max, int cl) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
     if (e == cudaSuccess && cl > 8) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -794,8 +815,8 @@ static std::atomic<int> g_ln_clusters[64][3][LC_MAX_CLUSTER + 1];
 // Number of clusters to launch over `nblk` row blocks, or 0 to take the tile path.
 // FP8DL_LN_VARIANT=tiles forces the tile path and FP8DL_LN_CLUSTERS=n caps the
 // cluster count (both for testing).
-static int64_t ln_cluster_count(int dev, int which, const void *kernel, int smem, int64_t nblk, int64_t cols,
-                                int64_t cap) {
+static int64_t ln_cluster_count(int dev, int which, const void *kernel, int smem_base, int slot_rows, int64_t nblk,
+                                int64_t cols, int64_t cap) {
     const char *v = getenv("FP8DL_LN_VARIANT");
     if (v && v[0] == 't') return 0;
     const int cl = ln_cluster_size(cols);
@@ -806,7 +827,9 @@ static int64_t ln_cluster_count(int dev, int which, const void *kernel, int smem
         std::lock_guard<std::mutex> lock(init_mutex());
         known = slot.load(std::memory_order_relaxed);
         if (known == 0) {
-            known = ln_max_clusters(kernel, smem, cl) + 1;  // sets the kernel's attributes first
+            // sets the kernel's attributes first (shared memory for the largest cluster)
+            known = ln_max_clusters(kernel, ln_smem(smem_base, slot_rows, cl),
+                                    ln_smem(smem_base, slot_rows, LC_MAX_CLUSTER), cl) + 1;
             slot.store(known, std::memory_order_release);
         }
     }
@@ -857,10 +880,11 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
     {
         const bool e4 = out_dtype == FP8DL_E4M3;
         auto kern = e4 ? ln_fwd_cluster_kernel<FP8DL_E4M3> : ln_fwd_cluster_kernel<FP8DL_E5M2>;
-        const int64_t ncl = ln_cluster_count(dev, e4 ? 0 : 1, (const void *)kern, LF_SMEM,
+        const int64_t ncl = ln_cluster_count(dev, e4 ? 0 : 1, (const void *)kern, LF_SMEM, LF_ROWS,
                                               (rows + LF_ROWS - 1) / LF_ROWS, cols, INT64_MAX);
         if (ncl > 0) {
-            const cudaError_t e = launch_clustered(kern, ncl, ln_cluster_size(cols), LF_SMEM, st, X,
+            const int cl = ln_cluster_size(cols);
+            const cudaError_t e = launch_clustered(kern, ncl, cl, ln_smem(LF_SMEM, LF_ROWS, cl), st, X,
                                                    static_cast<const uint16_t *>(gamma),
                                                    static_cast<const uint16_t *>(beta), rows, cols, eps, scale, out,
                                                    out_t, amax, mu, rsigma, static_cast<uint16_t *>(y));
@@ -921,11 +945,12 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
     const int64_t n_rt = (rows + LB_ROWS - 1) / LB_ROWS;
     {
         // the workspace holds n_rt partial rows per output: at most n_rt clusters
-        const int64_t ncl = ln_cluster_count(dev, 2, (const void *)ln_bwd_cluster_kernel<LB_BLK>, LB_SMEM,
+        const int64_t ncl = ln_cluster_count(dev, 2, (const void *)ln_bwd_cluster_kernel<LB_BLK>, LB_SMEM, LB_BLK,
                                               (rows + LB_BLK - 1) / LB_BLK, cols, n_rt);
         if (ncl > 0) {
-            const cudaError_t e = launch_clustered(ln_bwd_cluster_kernel<LB_BLK>, ncl, ln_cluster_size(cols), LB_SMEM, st, DY, X, G,
-                                                   mu, rsigma, rows, cols, static_cast<uint16_t *>(dx), part);
+            const int cl = ln_cluster_size(cols);
+            const cudaError_t e = launch_clustered(ln_bwd_cluster_kernel<LB_BLK>, ncl, cl, ln_smem(LB_SMEM, LB_BLK, cl), st,
+                                                   DY, X, G, mu, rsigma, rows, cols, static_cast<uint16_t *>(dx), part);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 return fail(FP8DL_ERR_CUDA, "fp8_layernorm_bwd(cluster): %s", cudaGetErrorString(e));

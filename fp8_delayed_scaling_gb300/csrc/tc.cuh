@@ -83,6 +83,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Wait for the phase with parity `parity` of a barrier of this CTA; false when the
+// budget (several seconds) runs out.  Never traps.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  long long budget = kWaitBudgetCycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > budget) return false;
+    return true;
+}
+
+// Asynchronous store of a float2 into shared memory of a CTA of the cluster (shared::cluster
+// addresses from mapa_shared); its 8 bytes complete on that CTA's barrier `remote_bar`.
+__device__ __forceinline__ void st_async_f2(uint32_t remote, float2 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(remote),
+                 "f"(v.x), "f"(v.y), "r"(remote_bar)
+                 : "memory");
+}
+
 // Bounded wait used only while draining after an abort (about a millisecond).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
     const long long t0 = clock64();
@@ -223,23 +242,7 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// The two halves of cluster_sync, for overlapping work with the barrier; a thread
-// alternates arrive and wait.
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-// Loads from distributed shared memory (a shared::cluster address, see mapa_shared).
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
-}
+
 // Address of the same shared-memory object in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     uint32_t r;
