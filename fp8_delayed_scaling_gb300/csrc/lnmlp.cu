@@ -98,6 +98,9 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
 //   - warp 0 waits on its own slot barrier for block j (pushed one iteration
 //     earlier), merges the CTAs' partials in rank order, re-arms the barrier
 //     for block j+4, and block j is normalised and written.
+// The forward gathers block j while the other warps reduce block j+1 (one
+// barrier publishes both); the backward, with shorter blocks, pushes block
+// j+1 first so that block j's pushes have longer to arrive.
 // The exchange's latency is thus hidden behind a whole block's work, and no
 // cluster-wide barrier or release fence (which would also wait for the
 // previous block's global stores) sits in the loop.  Slots rotate over four
@@ -298,11 +301,8 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
         cp_async_wait<0>();  // this thread's copies of block j+1 have landed (the only group in flight)
         __syncthreads();     // ... everyone's; and every thread is past block j-1, whose buffer is refilled now
         issue(j + 2, next_buf(next_buf(buf)));
-        if (j + 1 < nb) {
-            partials(next_buf(buf));
-            __syncthreads();
-            push(nslot);
-        }
+        // warp 0 gathers block j (pushed during the previous iteration) while every warp
+        // reduces block j+1; one barrier publishes both, then warp 0 pushes block j+1
         if (t < LF_ROWS) {
             // every CTA's slab of block j has arrived (a wait that runs out leaves NaN statistics)
             const bool arrived = mbar_wait_bounded(smem_u32(&xbar[slot]), (uint32_t)((j / LC_SLOTS) & 1));
@@ -331,7 +331,9 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
             // the slot's next block: its barrier counts the pushes of block j + LC_SLOTS
             if (t == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
         }
+        if (j + 1 < nb) partials(next_buf(buf));
         __syncthreads();
+        if (j + 1 < nb) push(nslot);
         if (r0 + 16 * h < rows) {  // rows are a multiple of 16: a half is all in or all out
             uint32_t codes[16];
 #pragma unroll
@@ -696,6 +698,8 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
         cp_async_wait<0>();  // block j+1 has landed (the only group in flight)
         __syncthreads();     // ... including mu and rs; every thread is past block j-1
         issue(j + 2, next_buf(next_buf(buf)));
+        // block j+1's partials are pushed before block j is gathered: with short blocks the
+        // pushes of block j then have a whole reduction to arrive in
         if (j + 1 < nb) {
             partials(next_buf(buf));
             __syncthreads();
