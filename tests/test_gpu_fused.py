@@ -126,3 +126,41 @@ def test_fused_dgelu_epilogue_matches_unfused_and_oracle(M, N, K, monkeypatch):
     qo = oracle.quantize(1, dhb, 1024.0)
     assert np.array_equal(q1.cpu().numpy(), qo) and np.array_equal(t1.cpu().numpy(), qo.T)
     assert a1.item() == oracle.amax(dhb)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 128), (384, 1024, 256)])
+def test_epilogue_16_byte_aligned_outputs(M, N, K, monkeypatch):
+    """Outputs whose base is 16- but not 32-byte aligned take the 16-byte store path of the
+    pair epilogue; their contents equal those written through 32-byte aligned outputs."""
+    import fp8_delayed_scaling_gb300 as fd
+    monkeypatch.setenv("FP8DL_GEMM_VARIANT", "2sm")
+    dev = gpu()
+    rng = np.random.default_rng(7 * M + N + K)
+    A = torch.from_numpy(_codes(rng, (M, K))).to(dev)
+    B = torch.from_numpy(_codes(rng, (N, K))).to(dev)
+    sa = torch.tensor([0.05], device=dev)
+    sb = torch.tensor([0.03], device=dev)
+    bias = wl.normal((N,), 0.5, wl.generator(72, "abias/%d" % N), torch.bfloat16).to(dev)
+    qs = torch.tensor([37.0], device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+
+    def outputs(offset):
+        hb = torch.full((M * N + 16,), float("nan"), dtype=torch.bfloat16, device=dev)
+        qb = torch.full((M * N + 32,), 0xAA, **u8)
+        H = hb[offset // 2: offset // 2 + M * N].view(M, N)
+        q = qb[offset: offset + M * N].view(M, N)
+        assert H.data_ptr() % 32 == offset and q.data_ptr() % 32 == offset
+        return H, q, torch.full((N, M), 0xAA, **u8), torch.zeros(1, device=dev)
+
+    res = []
+    for offset in (0, 16):
+        H, q, t, a = outputs(offset)
+        fd.fp8_gemm_gelu_cast(A, fd.E4M3, B, fd.E4M3, sa, sb, H, fd.E4M3, qs, q, t, a, bias=bias)
+        D = outputs(offset)[0]
+        fd.fp8_gemm(A, fd.E4M3, B, fd.E4M3, sa, sb, D, bias=bias)
+        res.append((H, q, t, a, D))
+    torch.cuda.synchronize()
+    (H0, q0, t0, a0, D0), (H1, q1, t1, a1, D1) = res
+    assert not torch.isnan(H0.float()).any() and not torch.isnan(D0.float()).any()
+    assert torch.equal(H0, H1) and torch.equal(q0, q1) and torch.equal(t0, t1) and a0.item() == a1.item()
+    assert torch.equal(D0, D1)
