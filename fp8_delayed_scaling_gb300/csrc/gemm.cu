@@ -305,9 +305,9 @@ constexpr int TMEM_COLS = 512;
 __host__ __device__ constexpr int epi_warps(int epi) { return epi ? 16 : 4; }
 __host__ __device__ constexpr int threads(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int QT_BYTES = BN * BM;  // transposed FP8 codes of one CTA's 128 x 256 output (fused epilogue)
-// The fused epilogues double-buffer their transposed-code tile, paid for with one operand stage.
-__host__ __device__ constexpr int stages(int epi) { return epi ? STAGES - 1 : STAGES; }
-__host__ __device__ constexpr int qt_bufs(int epi) { return epi ? 2 : 0; }
+// The fused epilogues stage their transposed codes in one tile beside the full operand ring.
+__host__ __device__ constexpr int stages(int) { return STAGES; }
+__host__ __device__ constexpr int qt_bufs(int epi) { return epi ? 1 : 0; }
 constexpr int smem_bytes(int epi) { return stages(epi) * STAGE_BYTES + 1024 + qt_bufs(epi) * QT_BYTES + 1024; }
 }  // namespace g2
 
@@ -369,7 +369,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     uint64_t *tempty = tfull + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint8_t *qt_stage = bar_area + 1024;  // EPI >= 1: two [256 columns][128 rows] code tiles
+    uint8_t *qt_stage = bar_area + 1024;  // EPI >= 1: one [256 columns][128 rows] code tile
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -514,7 +514,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                 prefetch_l2(hrow + tn * BN + part * CHUNKS * 32);
             if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
             tc_fence_after();
-            uint8_t *qt_buf = qt_stage + (jt & 1) * QT_BYTES;  // free: see the barrier at the tile's end
+            uint8_t *qt_buf = qt_stage;
+            if (EPI && jt > 0) {
+                // The previous tile's store has finished reading the staging tile before anyone
+                // writes it again.  Every epilogue warp got past the wait above (an abort stops
+                // them all at the same tile's wait), so all of them reach this barrier.
+                if (threadIdx.x == 64) bulk_wait_read();
+                named_barrier(2, NEPI);
+            }
 #pragma unroll 1
             for (int cc = 0; cc < CHUNKS; cc++) {
                 const int c = part * CHUNKS + cc;  // chunk of 32 columns within the tile
@@ -527,11 +534,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     load_bias32(args.bias, args.bias_dtype, n0, args.N, b);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __fmul_rn(__uint_as_float(r[j]), sc) + b[j];  // two roundings
+                    for (int j = 0; j < 32; j += 2) {  // two roundings, two columns per instruction
+                        const float2 a = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                        const float2 y = __fadd2_rn(__fmul2_rn(a, f2(sc)), make_float2(b[j], b[j + 1]));
+                        v[j] = y.x;
+                        v[j + 1] = y.y;
+                    }
                 } else {
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]) * sc;
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 y = __fmul2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), f2(sc));
+                        v[j] = y.x;
+                        v[j + 1] = y.y;
+                    }
                 }
                 uint32_t hw[16];  // the bf16 output as packed pairs (also the activation's input)
                 if (EPI || args.d_dtype == FP8DL_BF16) {
@@ -590,15 +606,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
 #pragma unroll
                         for (int p = 0; p < 4; p++) {
                             const uint32_t w = hw[4 * g + p];
-                            float lo, hi;
-                            if (EPI == 1) {
-                                lo = gelu_f32(bf16_lo(w));
-                                hi = gelu_f32(bf16_hi(w));
-                            } else {
-                                lo = dgelu_f32(bf16_lo(w), bf16_lo(hv[p]));
-                                hi = dgelu_f32(bf16_hi(w), bf16_hi(hv[p]));
-                            }
-                            __nv_bfloat162 y2 = __floats2bfloat162_rn(lo, hi);
+                            const float2 x = make_float2(bf16_lo(w), bf16_hi(w));
+                            const float2 y = EPI == 1 ? gelu2_f32(x)
+                                                      : dgelu2_f32(x, make_float2(bf16_lo(hv[p]), bf16_hi(hv[p])));
+                            __nv_bfloat162 y2 = __floats2bfloat162_rn(y.x, y.y);
                             gw[p] = *reinterpret_cast<uint32_t *>(&y2);
                             y8[2 * p] = bf16_lo(gw[p]);
                             y8[2 * p + 1] = bf16_hi(gw[p]);
@@ -608,8 +619,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
 #pragma unroll
                         for (int h2 = 0; h2 < 2; h2++) {
                             const float *y4 = y8 + 4 * h2;
-                            code[2 * g + h2] = pack4<QF>(__fmul_rn(y4[0], qscale), __fmul_rn(y4[1], qscale),
-                                                         __fmul_rn(y4[2], qscale), __fmul_rn(y4[3], qscale));
+                            const float2 s01 = __fmul2_rn(make_float2(y4[0], y4[1]), f2(qscale));
+                            const float2 s23 = __fmul2_rn(make_float2(y4[2], y4[3]), f2(qscale));
+                            code[2 * g + h2] = pack4<QF>(s01.x, s01.y, s23.x, s23.y);
                         }
                         if (args.g_out && row_store && n0 + 8 * g < args.N)
                             *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.g_out) + row * args.N + n0 +
@@ -676,9 +688,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
             }
             if (EPI) {  // the CTA's transposed codes: one TMA store of [256 columns x 128 rows]
                 fence_proxy_async_smem();
-                // The previous tile's store (the other buffer, issued a tile ago) has finished reading
-                // before anyone passes this barrier, so the next tile may overwrite that buffer.
-                if (threadIdx.x == 64) bulk_wait_read();
                 named_barrier(1, NEPI);
                 if (threadIdx.x == 64 && tm * 2 * BM + rank * BM < args.M) {  // no store when all rows lie beyond M
                     tma_store_2d(&tmap_qt, smem_u32(qt_buf), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * BN));
