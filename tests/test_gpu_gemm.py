@@ -35,7 +35,7 @@ def _gemm(A, afmt, B, bfmt, sa, sb, bias, d_dtype, dev):
 
 
 SHAPES = [(128, 256, 128), (16, 16, 16), (48, 80, 32), (144, 272, 400), (256, 512, 384), (384, 768, 1040),
-          (2048, 3072, 768), (1000 // 16 * 16, 2000 // 16 * 16, 1024)]
+          (2048, 3072, 768), (1000 // 16 * 16, 2000 // 16 * 16, 1024), (784, 272, 1040)]
 
 
 @pytest.fixture(params=["1sm", "2sm"])
@@ -104,3 +104,4 @@ def test_gemm_large_sampled(variant):
     ms, ns = sample_elems(M, N, rng)
     ref, absr = oracle.gemm_elems(A, 1, B, 0, 1e-3, 3e-2, None, ms, ns)
     check_gemm(D, ref, absr, ms, ns)
+
