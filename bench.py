@@ -907,6 +907,20 @@ def main():
         line["norm_act"] = hbm_class(kt["norm_act"])
     if clk:
         line["clocks"] = clk
+    if world == 1 and args.workload == "ln_mlp":
+        # The te.Linear layer of the pages' fwd+bwd HYBRID recipe (2048 tokens, 768 -> 3072),
+        # measured the same way right after the main workload, so one line carries both.
+        small = argparse.Namespace(**vars(args))
+        small.workload = "linear_hybrid"
+        scfg = WORKLOADS[small.workload]
+        _, s_ms, s_kt, _, (s_e2e, s_h2d, s_d2h) = run_ours(small, scfg, dev, rank, world)
+        s_flops = step_flops(scfg)
+        line["te_linear"] = {
+            "workload": small.workload, "desc": scfg["desc"], "value": round(s_flops / (s_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "ms_per_step": round(s_ms, 4), "steps": small.steps, "launch": s_kt["launch"],
+            "gpu_launches": s_kt["launches_per_step"] * small.steps,
+            "e2e": {"value": round(s_flops / s_e2e / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": s_h2d,
+                    "d2h_bytes_per_step": s_d2h}}
     if rank == 0 and world == 1:
         val, cores, sample, _ = run_oracle_sample(cfg, 2)
         line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
