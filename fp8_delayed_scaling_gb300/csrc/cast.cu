@@ -246,8 +246,18 @@ __global__ void __launch_bounds__(RED_COLS *RED_WARPS) colsum_reduce_kernel(cons
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t c = blockIdx.x * (int64_t)RED_COLS + lane;
     float s = 0.0f;
-    if (c < cols)
-        for (int64_t k = w; k < n_tiles; k += RED_WARPS) s += ws[k * cols + c];
+    if (c < cols) {
+        // 16 loads in flight, then their sums in the same order as one at a time
+        int64_t k = w;
+        for (; k + 15 * RED_WARPS < n_tiles; k += 16 * RED_WARPS) {
+            float v[16];
+#pragma unroll
+            for (int u = 0; u < 16; u++) v[u] = ws[(k + u * RED_WARPS) * cols + c];
+#pragma unroll
+            for (int u = 0; u < 16; u++) s += v[u];
+        }
+        for (; k < n_tiles; k += RED_WARPS) s += ws[k * cols + c];
+    }
     part[w][lane] = s;
     __syncthreads();
     if (w == 0 && c < cols) {
