@@ -41,7 +41,7 @@ FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 # DRAM bytes (read + write) per GEMM launch, the mean over one step's launches,
 # from one ncu capture of this workload with the kernels as they are now
 # (profiles/fp8_gemm_traffic_ln_mlp.md).  Workloads without a capture report null.
-GEMM_TRAFFIC = {"ln_mlp": 1.321e9}
+GEMM_TRAFFIC = {"ln_mlp": 1.219e9}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -767,18 +767,20 @@ fp8dl_status encode_tmap_2d_u8(CUtensorMap *map, const void *base, uint64_t inne
 // grows with the number of distinct A and B panels it spans; a square-ish block of
 // concurrent tiles (group ~ sqrt of the tiles in flight, counted in elements) keeps that
 // smallest.  Each group reads the other dimension's operand once more.  With square tiles
-// (the pair kernel's 256 x 256) a group of 8 is square-ish either way, and the groups run
-// along the dimension with fewer tiles: fewer groups, fewer re-reads.  Measured at
-// 16384 x 4096 x 16384: row groups 0.564 ms, column groups 0.554 ms; the reverse at
-// 4096 x 16384 x 16384.  The 128 x 256 tiles keep row groups of 16.  An order that keeps a
+// (the pair kernel's 256 x 256) the groups run along the dimension with fewer tiles: fewer
+// groups, fewer re-reads.  Measured at 16384 x 4096 x 16384: row groups 0.564 ms, column
+// groups 0.554 ms; the reverse at 4096 x 16384 x 16384.  Their group size follows the panel
+// size (256 x K bytes): with K <= 8192 groups of 16 re-read less and still fit the wave's
+// panels in L2 (16384 x 16384 x 4096: 0.560 ms with 8, 0.546 with 16, 0.591 with 64; the
+// fused GELU/dGELU epilogues 1-1.4 % faster with 16); with K = 16384 groups of 8 are
+// fastest (6: +1.3 %, 12: +0.9 %).  The 128 x 256 tiles keep row groups of 16.  An order that keeps a
 // whole operand "resident" instead streamed the other operand's panels through L2 and
 // raised DRAM reads (16384x16384x4096: 601 MB -> 927 MB).  FP8DL_GEMM_RASTER=m|n and
 // FP8DL_GEMM_GROUP=g override the order (testing).
 void pick_raster(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n, int &raster_n, int64_t &group) {
-    (void)K;
     const int64_t tiles_m = (M + tile_m - 1) / tile_m, tiles_n = (N + tile_n - 1) / tile_n;
     raster_n = tile_m == tile_n && tiles_n < tiles_m ? 1 : 0;
-    group = tile_m >= tile_n ? 8 : 16;  // 256x256 pair tiles: 8; 128x256 single-CTA tiles: 16
+    group = tile_m >= tile_n ? (K <= 8192 ? 16 : 8) : 16;  // pair tiles: 16 / 8 by K; 128x256 tiles: 16
     const char *r = getenv("FP8DL_GEMM_RASTER");
     const char *g = getenv("FP8DL_GEMM_GROUP");
     if (r && r[0] == 'n') raster_n = 1;
