@@ -357,6 +357,20 @@ int32_t fp8dl_version(void);
  * count: count one eager step to know what a replayed step launches. */
 uint64_t fp8dl_kernel_launches(void);
 
+/* ----------------------------------------------------------------------------
+ * Environment switches (testing and diagnosis).  They choose which kernel, tile
+ * order or grid runs.  The GEMM switches leave every output bit unchanged; the
+ * LayerNorm ones can change the rounding of the row statistics and of dgamma /
+ * dbeta, within the tolerances the tests state.
+ *   FP8DL_DEBUG=1               print every launch and error message to stderr
+ *                               (read once per process)
+ *   FP8DL_GEMM_VARIANT=1sm|2sm  force the one-CTA or the CTA-pair FP8 GEMM
+ *   FP8DL_GEMM_RASTER=m|n       group the GEMM tiles along rows (m) or columns (n)
+ *   FP8DL_GEMM_GROUP=g          tiles per group (g > 0)
+ *   FP8DL_LN_VARIANT=tiles      LayerNorm by the two-pass tile kernels
+ *   FP8DL_LN_CLUSTERS=n         cap on the clusters of the LayerNorm cluster kernels
+ * All but FP8DL_DEBUG are read at each call. */
+
 #ifdef __cplusplus
 }
 #endif
