@@ -164,3 +164,38 @@ def test_epilogue_16_byte_aligned_outputs(M, N, K, monkeypatch):
     assert not torch.isnan(H0.float()).any() and not torch.isnan(D0.float()).any()
     assert torch.equal(H0, H1) and torch.equal(q0, q1) and torch.equal(t0, t1) and a0.item() == a1.item()
     assert torch.equal(D0, D1)
+
+
+def test_fused_epilogues_independent_of_tile_order(monkeypatch):
+    """The fused GELU and dGELU GEMMs write the same bits under any tile order and group
+    size: every output element, code, bias-gradient partial and the amax (a max) depend
+    only on their own tile."""
+    import fp8_delayed_scaling_gb300 as fd
+    dev = gpu()
+    M, N, K = 1040, 784, 512
+    rng = np.random.default_rng(11)
+    A = torch.from_numpy(_codes(rng, (M, K))).to(dev)
+    B = torch.from_numpy(_codes(rng, (N, K))).to(dev)
+    sa = torch.tensor([0.05], device=dev)
+    sb = torch.tensor([0.03], device=dev)
+    qs = torch.tensor([37.0], device=dev)
+    h = wl.normal((M, N), 2.0, wl.generator(73, "oh"), torch.bfloat16).to(dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    ws = torch.empty(fd.fp8_gemm_dgelu_workspace_size(M, N), **u8)
+    res = []
+    for order, group in (("", ""), ("n", "3"), ("m", "1")):
+        monkeypatch.setenv("FP8DL_GEMM_RASTER", order)
+        monkeypatch.setenv("FP8DL_GEMM_GROUP", group)
+        H = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        q, qt = torch.empty((M, N), **u8), torch.empty((N, M), **u8)
+        a = torch.zeros(1, device=dev)
+        fd.fp8_gemm_gelu_cast(A, fd.E4M3, B, fd.E4M3, sa, sb, H, fd.E4M3, qs, q, qt, a)
+        q2, qt2 = torch.empty((M, N), **u8), torch.empty((N, M), **u8)
+        a2 = torch.zeros(1, device=dev)
+        db = torch.empty(N, device=dev)
+        fd.fp8_gemm_dgelu_cast(A, fd.E4M3, B, fd.E4M3, sa, sb, h, fd.E5M2, qs, q2, qt2, a2, dbias=db, workspace=ws)
+        torch.cuda.synchronize()
+        res.append((H, q, qt, a, q2, qt2, a2, db))
+    for other in res[1:]:
+        for x, y in zip(res[0], other):
+            assert torch.equal(x, y)
