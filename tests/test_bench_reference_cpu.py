@@ -23,3 +23,7 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and "oracle" in cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # each timed step is a sample scaled to a whole step, and the line says so
+    assert d["extrapolated"] is True and d["timed_wall_s"] > 0 and d["sampled_ms_per_step"] > 0
+    # the config is the GPU arm's, key for key (how that arm launches is a top-level key)
+    assert set(d["config"]) == {"workload", "desc", "tokens", "l2", "parallelism"}

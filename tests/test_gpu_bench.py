@@ -1,6 +1,7 @@
 """bench.py's default run on the GPU prints one JSON line with the contract's keys:
 the metric, whole-job value, roofline of the dominant kernel, cpu_baseline, e2e,
-clocks, the library's launch count, and the te.Linear layer measured beside."""
+clocks, the library's launch count, and the te.Linear layer and the MXFP8 MLP
+measured beside."""
 import json
 import os
 import subprocess
@@ -32,6 +33,10 @@ def test_default_bench_line_carries_the_contract():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] > 0 and r["achieved"] > 0
     assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
     assert r["traffic"] is None or r["traffic"] > 0
+    # the FP8 denominator is the larger burst figure: 2 x the measured bf16 burst, or cuBLASLt's FP8
+    p = d["fp8_peak"]
+    assert r["peak"] == p["used"] == max([p["bf16_burst_x2"]] + list(p["scaled_mm"].values()))
+    assert set(d["config"]) == {"workload", "desc", "tokens", "l2", "parallelism"} and d["launch"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
     e = d["e2e"]
@@ -40,3 +45,10 @@ def test_default_bench_line_carries_the_contract():
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     t = d["te_linear"]
     assert t["workload"] == "linear_hybrid" and t["value"] > 0 and t["gpu_launches"] > 0 and t["e2e"]["value"] > 0
+    mx = d["mx_mlp"]
+    assert mx["workload"] == "mx_mlp" and mx["value"] > 0 and mx["e2e"]["value"] > 0
+    assert abs(mx["value"] - bench.step_flops(bench.WORKLOADS["mx_mlp"]) / (mx["ms_per_step"] * 1e-3) / 1e12) \
+        <= 1e-3 * mx["value"] + 0.01
+    assert mx["roofline"]["kernel"] == "mxfp8_gemm" and mx["roofline"]["peak"] == r["peak"]
+    assert mx["roofline"]["gemm_launches_per_step"] == 6
+    assert 0 < mx["quantize"]["frac"] < 1.2 and mx["quantize"]["launches_per_step"] > 0

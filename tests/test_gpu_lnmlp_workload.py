@@ -1,11 +1,16 @@
 """The LayerNormMLP workload at full size (16384 tokens, 4096 -> 16384 -> 4096,
 HYBRID, history 16) through the step sequencing of lnmlp.py, vs the oracle.
 
-Two steps (the seeded first step and one delayed step).  Checked every step:
-every slot's amax and, after the update, scale/scale_inv/history bit-exact;
-the FP8 codes of every cast bit-exact on sampled rows of both orientations
-(from the GPU's own bf16 pre-cast tensors); every GEMM and the activations on
-sampled elements within their bounds; dbias/dgamma/dbeta in full."""
+All 20 steps of the workload: the seeded first step, then 19 delayed steps,
+so the 16-entry amax history ring wraps (step 16 overwrites the seeded entry
+0, and the window max over the last 16 amaxes decides the scale from then
+on; "FP8 低精度训练：Transformer Engine 简析" §三.1).  Checked after every step:
+every slot's recorded amax (the oracle's amax of the GPU's own pre-cast
+tensors), then after the update every slot's scale, scale_inv, history and
+position, all bit-exact.  On steps 0, 1, 16 and 19 also: the FP8 codes of
+every cast bit-exact on sampled rows of both orientations, every GEMM and the
+activations on sampled elements within their bounds, dbias/dgamma/dbeta in
+full."""
 import numpy as np
 import pytest
 import torch
@@ -34,7 +39,7 @@ def _check_codes(fmt, pre_bits, scale, q, qT, rng, what):
     assert np.array_equal(qth, oracle.quantize(fmt, np.ascontiguousarray(pre_bits[:, cols].T), scale)), what + "^T"
 
 
-def test_ln_mlp_two_steps():
+def test_ln_mlp_twenty_steps():
     import fp8_delayed_scaling_gb300 as fd
     from fp8_delayed_scaling_gb300.lnmlp import Fp8LayerNormMLP, make_state
     dev = gpu()
@@ -52,7 +57,9 @@ def test_ln_mlp_two_steps():
     ost = oracle.ScalingState([0, 0, 1, 0, 0, 1], hist_len=16)
     rng = np.random.default_rng(0)
     gb, bb, w1b, w2b = host(gamma), host(beta), host(w1), host(w2)
-    for step in range(2):
+    w_amax = (oracle.amax(w1b), oracle.amax(w2b))
+    for step in range(20):
+        full = step in (0, 1, 16, 19)
         x = wl.normal((M, H), 1.0, wl.generator(seed, "x", step), torch.bfloat16)
         dy = wl.normal((M, H), 1e-3, wl.generator(seed, "dY", step), torch.bfloat16)
         xd, dyd = x.to(dev), dy.to(dev)
@@ -63,8 +70,7 @@ def test_ln_mlp_two_steps():
         xb, dyb = host(x), host(dy)
         y_ln, g_act, dh = host(blk.y_ln), host(blk.g), host(blk.dh)
         # --- amaxes recorded by this step's casts (from the GPU's own pre-cast tensors)
-        amaxes = [oracle.amax(y_ln), oracle.amax(w1b), oracle.amax(dh), oracle.amax(g_act), oracle.amax(w2b),
-                  oracle.amax(dyb)]
+        amaxes = [oracle.amax(y_ln), w_amax[0], oracle.amax(dh), oracle.amax(g_act), w_amax[1], oracle.amax(dyb)]
         if first:  # seeding used the same tensors
             for i, a in enumerate(amaxes):
                 ost.record_amax(i, a)
@@ -75,61 +81,68 @@ def test_ln_mlp_two_steps():
             ost.record_amax(i, a)
         assert np.array_equal(got["amax"], ost.amax_cur), (step, got["amax"], ost.amax_cur)
         sc, si = ost.scale, ost.scale_inv
-        # --- LayerNorm forward values on sampled rows, then the casts
-        rows = _rows(rng, M)
-        yr, _, _ = oracle.layernorm_fwd(xb[rows], gb, bb, 1e-5)
-        yg = as_f64(blk.y_ln)[rows]
-        assert np.all(np.abs(yg - yr) <= 2.0 ** -7 * np.abs(yr) + 2.0 ** -14)
-        _check_codes(0, y_ln, sc[0], blk.q_ln, blk.q_lnT, rng, "q_ln")
-        _check_codes(0, w1b, sc[1], blk.qw1, blk.qw1T, rng, "qW1")
-        _check_codes(0, g_act, sc[3], blk.q_g, blk.q_gT, rng, "q_g")
-        _check_codes(0, w2b, sc[4], blk.qw2, blk.qw2T, rng, "qW2")
-        _check_codes(1, dyb, sc[5], blk.qdy, blk.qdyT, rng, "qdY")
-        _check_codes(1, dh, sc[2], blk.qdh, blk.qdhT, rng, "qdh")
-        # --- activations on sampled rows
-        h = host(blk.h)
-        gr = oracle.gelu(np.ascontiguousarray(h[rows]))
-        ga = as_f64(blk.g)[rows]
-        assert np.all(np.abs(ga - gr) <= 2.0 ** -7 * np.abs(gr) + 2.0 ** -21 * np.abs(as_f64(blk.h)[rows]))
-        dgb = host(blk.dg)
-        dhr = oracle.dgelu(np.ascontiguousarray(dgb[rows]), np.ascontiguousarray(h[rows]))
-        dha = as_f64(blk.dh)[rows]
-        assert np.all(np.abs(dha - dhr) <= 2.0 ** -7 * np.abs(dhr) + 2.0 ** -21 * np.abs(as_f64(blk.dg)[rows]))
-        # --- GEMMs on sampled elements (operands: the GPU's bit-exact codes)
-        qln, qw1, qg, qw2 = (blk.q_ln.cpu().numpy(), blk.qw1.cpu().numpy(), blk.q_g.cpu().numpy(),
-                             blk.qw2.cpu().numpy())
-        qdy, qdh = blk.qdy.cpu().numpy(), blk.qdh.cpu().numpy()
-        gemms = [
-            ("fc1", blk.h, qln, 0, qw1, 0, si[0], si[1], host(b1)),
-            ("fc2", blk.y, qg, 0, qw2, 0, si[3], si[4], host(b2)),
-            ("fc2 dgrad", blk.dg, qdy, 1, np.ascontiguousarray(qw2.T), 0, si[5], si[4], None),
-            ("fc2 wgrad", blk.dw2, np.ascontiguousarray(qdy.T), 1, np.ascontiguousarray(qg.T), 0, si[5], si[3], None),
-            ("fc1 dgrad", blk.dln, qdh, 1, np.ascontiguousarray(qw1.T), 0, si[2], si[1], None),
-            ("fc1 wgrad", blk.dw1, np.ascontiguousarray(qdh.T), 1, np.ascontiguousarray(qln.T), 0, si[2], si[0], None),
-        ]
-        for name, D, A, af, B, bf, sa, sb, bias in gemms:
-            ms, ns = sample_elems(D.shape[0], D.shape[1], rng, n=1024)
-            ref, absr = oracle.gemm_elems(A, af, B, bf, sa, sb, bias, ms, ns)
-            check_gemm(D, ref, absr, ms, ns, what="%s step %d" % (name, step))
-        # --- bias gradients in full
-        for db, src, n in ((blk.db2, dyb, M), (blk.db1, dh, M)):
-            s, sabs = oracle.colsum(src)
-            assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= n * 2.0 ** -24 * sabs + 1e-30)
-        # --- LayerNorm backward: dx on sampled rows, dgamma/dbeta in full, from the GPU's saved statistics
-        mu, rs = blk.mu.cpu().numpy().astype(np.float64), blk.rs.cpu().numpy().astype(np.float64)
-        dlnb = host(blk.dln)
-        rdx, rdg, rdb, adx, adg, adb = oracle.layernorm_bwd(dlnb, xb, gb, mu, rs)
-        dxg = as_f64(blk.dx)
-        assert np.all(np.abs(dxg[rows] - rdx[rows]) <= 2.0 ** -7 * np.abs(rdx[rows]) + 2.0 ** -16 * adx[rows])
-        assert np.all(np.abs(blk.dgamma.cpu().numpy() - rdg) <= (M + 8) * 2.0 ** -22 * adg + 1e-30)
-        assert np.all(np.abs(blk.dbeta.cpu().numpy() - rdb) <= M * 2.0 ** -24 * adb + 1e-30)
+        if full:
+            _full_checks(blk, step, xb, dyb, y_ln, g_act, dh, w1b, w2b, gb, bb, b1, b2, sc, si, rng)
         # --- the delayed update
         state.update(step)
         ost.update(step)
         torch.cuda.synchronize()
         got = state.read()
-        assert np.array_equal(got["scale"], ost.scale) and np.array_equal(got["scale_inv"], ost.scale_inv)
-        assert np.array_equal(got["hist"], ost.hist) and np.array_equal(got["pos"], ost.pos)
+        assert np.array_equal(got["scale"], ost.scale) and np.array_equal(got["scale_inv"], ost.scale_inv), step
+        assert np.array_equal(got["hist"], ost.hist) and np.array_equal(got["pos"], ost.pos), step
+    assert np.all(ost.pos == 20 % 16)  # the ring wrapped
+
+
+def _full_checks(blk, step, xb, dyb, y_ln, g_act, dh, w1b, w2b, gb, bb, b1, b2, sc, si, rng):
+    """Codes, activations, GEMMs, bias gradients and the LayerNorm of one step."""
+    # --- LayerNorm forward values on sampled rows, then the casts
+    rows = _rows(rng, M)
+    yr, _, _ = oracle.layernorm_fwd(xb[rows], gb, bb, 1e-5)
+    yg = as_f64(blk.y_ln)[rows]
+    assert np.all(np.abs(yg - yr) <= 2.0 ** -7 * np.abs(yr) + 2.0 ** -14)
+    _check_codes(0, y_ln, sc[0], blk.q_ln, blk.q_lnT, rng, "q_ln")
+    _check_codes(0, w1b, sc[1], blk.qw1, blk.qw1T, rng, "qW1")
+    _check_codes(0, g_act, sc[3], blk.q_g, blk.q_gT, rng, "q_g")
+    _check_codes(0, w2b, sc[4], blk.qw2, blk.qw2T, rng, "qW2")
+    _check_codes(1, dyb, sc[5], blk.qdy, blk.qdyT, rng, "qdY")
+    _check_codes(1, dh, sc[2], blk.qdh, blk.qdhT, rng, "qdh")
+    # --- activations on sampled rows
+    h = host(blk.h)
+    gr = oracle.gelu(np.ascontiguousarray(h[rows]))
+    ga = as_f64(blk.g)[rows]
+    assert np.all(np.abs(ga - gr) <= 2.0 ** -7 * np.abs(gr) + 2.0 ** -21 * np.abs(as_f64(blk.h)[rows]))
+    dgb = host(blk.dg)
+    dhr = oracle.dgelu(np.ascontiguousarray(dgb[rows]), np.ascontiguousarray(h[rows]))
+    dha = as_f64(blk.dh)[rows]
+    assert np.all(np.abs(dha - dhr) <= 2.0 ** -7 * np.abs(dhr) + 2.0 ** -21 * np.abs(as_f64(blk.dg)[rows]))
+    # --- GEMMs on sampled elements (operands: the GPU's bit-exact codes)
+    qln, qw1, qg, qw2 = (blk.q_ln.cpu().numpy(), blk.qw1.cpu().numpy(), blk.q_g.cpu().numpy(),
+                         blk.qw2.cpu().numpy())
+    qdy, qdh = blk.qdy.cpu().numpy(), blk.qdh.cpu().numpy()
+    gemms = [
+        ("fc1", blk.h, qln, 0, qw1, 0, si[0], si[1], host(b1)),
+        ("fc2", blk.y, qg, 0, qw2, 0, si[3], si[4], host(b2)),
+        ("fc2 dgrad", blk.dg, qdy, 1, np.ascontiguousarray(qw2.T), 0, si[5], si[4], None),
+        ("fc2 wgrad", blk.dw2, np.ascontiguousarray(qdy.T), 1, np.ascontiguousarray(qg.T), 0, si[5], si[3], None),
+        ("fc1 dgrad", blk.dln, qdh, 1, np.ascontiguousarray(qw1.T), 0, si[2], si[1], None),
+        ("fc1 wgrad", blk.dw1, np.ascontiguousarray(qdh.T), 1, np.ascontiguousarray(qln.T), 0, si[2], si[0], None),
+    ]
+    for name, D, A, af, B, bf, sa, sb, bias in gemms:
+        ms, ns = sample_elems(D.shape[0], D.shape[1], rng, n=1024)
+        ref, absr = oracle.gemm_elems(A, af, B, bf, sa, sb, bias, ms, ns)
+        check_gemm(D, ref, absr, ms, ns, what="%s step %d" % (name, step))
+    # --- bias gradients in full
+    for db, src, n in ((blk.db2, dyb, M), (blk.db1, dh, M)):
+        s, sabs = oracle.colsum(src)
+        assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= n * 2.0 ** -24 * sabs + 1e-30)
+    # --- LayerNorm backward: dx on sampled rows, dgamma/dbeta in full, from the GPU's saved statistics
+    mu, rs = blk.mu.cpu().numpy().astype(np.float64), blk.rs.cpu().numpy().astype(np.float64)
+    dlnb = host(blk.dln)
+    rdx, rdg, rdb, adx, adg, adb = oracle.layernorm_bwd(dlnb, xb, gb, mu, rs)
+    dxg = as_f64(blk.dx)
+    assert np.all(np.abs(dxg[rows] - rdx[rows]) <= 2.0 ** -7 * np.abs(rdx[rows]) + 2.0 ** -16 * adx[rows])
+    assert np.all(np.abs(blk.dgamma.cpu().numpy() - rdg) <= (M + 8) * 2.0 ** -22 * adg + 1e-30)
+    assert np.all(np.abs(blk.dbeta.cpu().numpy() - rdb) <= M * 2.0 ** -24 * adb + 1e-30)
 
 
 def test_ln_mlp_current_scaling_step():

@@ -72,3 +72,43 @@ def test_noalloc_refuses_sizes_beyond_the_static_array():
     assert "static" in fd.fp8dl_last_error()
     # the largest size that fits: ceil(8192/128) * 16384 * 4 = 4 MiB exactly is accepted by the check
     assert fd.fp8_cast_workspace_size(8192, 16384) == 4 << 20
+
+
+def test_noalloc_at_the_full_static_array():
+    """A bias gradient whose scratch fills the 4 MiB array exactly (8192 x 16384 bf16:
+    64 row tiles x 16384 columns x 4 bytes) matches the workspace entry point, twice in a
+    row; one size step larger in either dimension is refused before any launch."""
+    import fp8_delayed_scaling_gb300 as fd
+    dev = gpu()
+    rows, cols = 8192, 16384
+    assert fd.fp8_cast_workspace_size(rows, cols) == 4 << 20
+    g = wl.generator(78, "noalloc-full")
+    x = wl.normal((rows, cols), 1e-2, g, torch.bfloat16).to(dev)
+    scale = torch.tensor([2048.0], dtype=torch.float32, device=dev)
+    ws = torch.empty(fd.fp8_cast_workspace_size(rows, cols), dtype=torch.uint8, device=dev)
+    ref = [torch.empty((rows, cols), dtype=torch.uint8, device=dev), torch.empty((cols, rows), dtype=torch.uint8,
+           device=dev), torch.zeros(1, dtype=torch.float32, device=dev), torch.empty(cols, dtype=torch.float32,
+                                                                                       device=dev)]
+    fd.fp8_cast_amax_transpose(x, fd.E4M3, scale, out=ref[0], out_t=ref[1], amax=ref[2], dbias=ref[3], workspace=ws)
+    xs = x.float().cpu().numpy().astype(np.float64)
+    bound = rows * 2.0 ** -24 * np.abs(xs).sum(0) + 1e-30
+    for _ in range(2):
+        out = torch.full((rows, cols), 0xAA, dtype=torch.uint8, device=dev)
+        out_t = torch.full((cols, rows), 0xAA, dtype=torch.uint8, device=dev)
+        amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        db = torch.full((cols,), float("nan"), dtype=torch.float32, device=dev)
+        fd.fp8_cast_amax_transpose_noalloc(x, fd.E4M3, scale, out=out, out_t=out_t, amax=amax, dbias=db)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref[0]) and torch.equal(out_t, ref[1]) and torch.equal(amax, ref[2])
+        d1, d2 = ref[3].cpu().numpy().astype(np.float64), db.cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(d2 - d1) <= bound) and np.all(np.abs(d2 - xs.sum(0)) <= bound)
+    # one step of 16 beyond the array in rows (65 row tiles) or in columns: refused, outputs untouched
+    for r, c in ((rows + 16, cols), (rows, cols + 16)):
+        assert fd.fp8_cast_workspace_size(r, c) > 4 << 20
+        xb = torch.zeros((r, c), dtype=torch.bfloat16, device=dev)
+        db = torch.full((c,), 7.0, dtype=torch.float32, device=dev)
+        with pytest.raises(fd.FP8DLError) as e:
+            fd.fp8_cast_amax_transpose_noalloc(xb, fd.E4M3, scale, dbias=db)
+        assert e.value.status == fd.ERR_WORKSPACE
+        torch.cuda.synchronize()
+        assert torch.all(db == 7.0)
