@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
             uint32_t aph = 0;
             bool ok = true, any = false;
             uint32_t last_bar = 0, last_par = 0;
+            const SDesc desc0 = sdesc_k_sw128_split(smem_u32(smem));  // stage 0's A tile
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
                 if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1, abort_flag, args.status)) {
                     ok = false;
@@ -185,13 +186,12 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t lo_a = desc0.lo + (uint32_t)s * (STAGE_BYTES >> 4);
+                    const uint32_t lo_b = lo_a + (A_BYTES >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 32; kk++) {
-                        umma_f8f6f4(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), args.idesc,
-                                    (kb | kk) != 0);
-                    }
+                    for (int kk = 0; kk < BK / 32; kk++)  // K = 32 bytes per MMA: 2 descriptor units
+                        umma_f8f6f4(d_tmem, sdesc_join(lo_a + 2 * kk, desc0.hi), sdesc_join(lo_b + 2 * kk, desc0.hi),
+                                    args.idesc, (kb | kk) != 0);
                     umma_commit(smem_u32(&empty[s]));
                     any = true;
                     last_bar = smem_u32(&empty[s]);
@@ -298,11 +298,13 @@ constexpr int BM = 128, BN = 256, BNH = 128, BK = 128;  // per-CTA rows of A and
 constexpr int STAGES = 6;
 constexpr int A_BYTES = BM * BK, B_BYTES = BNH * BK, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
-// epilogue warps: 4 (one per TMEM lane quarter) for the plain epilogue; 16 for the
-// fused GELU + cast one, whose per-element work needs four warps per SM
-// sub-partition to hide its arithmetic latency (each warp drains 2 of the 8
-// 32-column chunks of its lane quarter)
-__host__ __device__ constexpr int epi_warps(int epi) { return epi ? 16 : 4; }
+// epilogue warps: 4 (one per TMEM lane quarter) for the plain epilogue; 8 for the
+// fused activation + cast ones, two per SM sub-partition, each draining 4 of the 8
+// 32-column chunks of its lane quarter.  The MMA-issuing thread shares a sub-partition
+// with them, and every epilogue instruction issued there delays it: with 16 warps
+// (enough to hide all of the epilogue's latency) the tensor pipe lost more cycles than
+// the shorter epilogue saved (measured: 8 warps take 3-4 % fewer cycles per launch).
+__host__ __device__ constexpr int epi_warps(int epi) { return epi ? 8 : 4; }
 __host__ __device__ constexpr int threads(int epi) { return 64 + 32 * epi_warps(epi); }
 constexpr int QT_BYTES = BN * BM;  // transposed FP8 codes of one CTA's 128 x 256 output (fused epilogue)
 // The fused epilogues stage their transposed codes in one tile beside the full operand ring.
@@ -444,6 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
             uint32_t aph = 0;
             bool ok = true, any = false;
             uint32_t last_bar = 0, last_par = 0;
+            const SDesc desc0 = sdesc_k_sw128_split(smem_u32(smem));  // stage 0's A tile
             for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
                 if (!mbar_wait(smem_u32(&tempty[acc]), aph ^ 1, abort_flag, args.status)) {
                     ok = false;
@@ -457,12 +460,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t lo_a = desc0.lo + (uint32_t)s * (STAGE_BYTES >> 4);
+                    const uint32_t lo_b = lo_a + (A_BYTES >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 32; kk++)
-                        umma_f8f6f4_pair(d_tmem, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32),
-                                         args.idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < BK / 32; kk++)  // K = 32 bytes per MMA: 2 descriptor units
+                        umma_f8f6f4_pair(d_tmem, sdesc_join(lo_a + 2 * kk, desc0.hi),
+                                         sdesc_join(lo_b + 2 * kk, desc0.hi), args.idesc, (kb | kk) != 0);
                     umma_commit_pair(smem_u32(&empty[s]), 0x3);
                     any = true;
                     last_bar = smem_u32(&empty[s]);

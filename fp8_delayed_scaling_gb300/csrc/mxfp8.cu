@@ -416,6 +416,7 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
             uint32_t ph = 0, aph = 0;
             bool ok = true, any = false;
             uint32_t last_bar = 0, last_par = 0;
+            const SDesc desc0 = sdesc_k_sw128_split(smem_u32(smem));  // stage 0's A tile
             for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
                 if (!mbar_wait(smem_u32(tempty), aph ^ 1, abort_flag, args.status)) {
                     ok = false;
@@ -428,7 +429,8 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * AB_BYTES), sb = sa + A_BYTES;
+                    const uint32_t lo_a = desc0.lo + (uint32_t)s * (AB_BYTES >> 4);
+                    const uint32_t lo_b = lo_a + (A_BYTES >> 4);
                     const uint32_t sf = smem_u32(sf_area + s * SF_BYTES);
                     const uint32_t t_sfa = tmem_base + (uint32_t)(SF_COL0 + s * SF_COLS_PER_STAGE);
                     const uint32_t t_sfb = t_sfa + 4;
@@ -439,8 +441,8 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
                     for (int kk = 0; kk < BK / 32; kk++) {
                         // scale-factor ids: byte kk of each scale word, for A (bits 29-30) and B (bits 4-5)
                         const uint32_t idesc = args.idesc | ((uint32_t)kk << 29) | ((uint32_t)kk << 4);
-                        umma_mxf8f6f4(tmem_base, sdesc_k_sw128(sa + kk * 32), sdesc_k_sw128(sb + kk * 32), idesc,
-                                      t_sfa, t_sfb, (kb | kk) != 0);
+                        umma_mxf8f6f4(tmem_base, sdesc_join(lo_a + 2 * kk, desc0.hi), sdesc_join(lo_b + 2 * kk, desc0.hi),
+                                      idesc, t_sfa, t_sfb, (kb | kk) != 0);
                     }
                     umma_commit(smem_u32(&empty[s]));
                     any = true;

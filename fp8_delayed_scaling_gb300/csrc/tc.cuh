@@ -171,6 +171,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// The same wait, tied to the registers of one tcgen05.ld: the compiler cannot move any
+// use of r above it.
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row (1024-byte) swizzle atoms.
@@ -181,6 +193,19 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+
+// The same descriptor as two 32-bit words, for the MMA issue loops.  Shared memory
+// addresses stay below 2^18, so the address field (bits 0-13 of the low word) of the
+// tile `bytes` further on is the low word + bytes / 16 with no carry out of the field:
+// one integer add per operand per MMA instead of rebuilding the descriptor.
+struct SDesc {
+    uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc_k_sw128_split(uint32_t saddr) {
+    const uint64_t d = sdesc_k_sw128(saddr);
+    return {(uint32_t)d, (uint32_t)(d >> 32)};
+}
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo, uint32_t hi) { return ((uint64_t)hi << 32) | lo; }
 
 // Block-scaled MMA, kind::mxf8f6f4 with one E8M0 scale per 32 K (scale_vec::1X);
 // the scales of A and B are read from tensor memory.
