@@ -153,8 +153,8 @@ WORKLOADS = {
                                 "each activation is written in bf16 with its amax, then cast in a second pass",
                            tokens=16384, layers=[("fc1", 4096, 16384), ("fc2", 16384, 4096)], hist=16, fmt="hybrid",
                            x_dtype=torch.bfloat16, training=True, kind="lnmlp", scaling="current"),
-    "mx_mlp": dict(desc="MXFP8 (1x32 E8M0 blocks) MLP fwd+bwd: 16384 tokens, 8192 -> 28672 -> 8192, X with per-channel "
-                        "factors log-uniform in [1e-3, 1e2]", tokens=16384, layers=[("up", 8192, 28672),
+    "mx_mlp": dict(desc="MXFP8 (1x32 E8M0 blocks) MLP fwd+bwd: 16384 tokens, 8192 -> 28672 -> 8192 with zero biases, "
+                        "X with per-channel factors log-uniform in [1e-3, 1e2]", tokens=16384, layers=[("up", 8192, 28672),
                                                                                 ("down", 28672, 8192)],
                    hist=0, fmt="mxfp8", x_dtype=torch.bfloat16, training=True, kind="mx"),
     "linear_fwd": dict(desc="te.Linear 2048 tokens 768->3072 forward, E4M3, history 16",
@@ -177,8 +177,9 @@ def hbm_bytes(cfg, fused=False):
     With the activations fused into the GEMM epilogues (fused: GELU + cast in fc1, dGELU + cast
     + db1 in the fc2 dgrad), those passes belong to the GEMMs."""
     M = cfg["tokens"]
-    if cfg.get("kind") == "mx":  # quantise X, W, dY of each layer: read 2 B, write 2 B + 2/32 B of scales
-        return {"cast": sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) for _, k, n in cfg["layers"])}
+    if cfg.get("kind") == "mx":  # quantise X, W, dY of each layer: read 2 B, write 2 B + 2/32 B of scales;
+        # dY's quantisation also writes the bias gradient (4 B per column)
+        return {"cast": sum((M * k + n * k + M * n) * (2 + 2 + 2 / 32.0) + 4 * n for _, k, n in cfg["layers"])}
     if cfg.get("kind") == "lnmlp":
         H, F = cfg["layers"][0][1], cfg["layers"][0][2]
         if cfg.get("scaling") == "current":  # amax passes first, casts of the bf16 tensors after
@@ -348,8 +349,12 @@ class MxModel:
         self.cfg = cfg
         M = cfg["tokens"]
         (_, H, F), _ = cfg["layers"]
-        self.up = MxLinear(wl.normal((F, H), 0.02, wl.generator(seed, "W1"), torch.bfloat16).to(dev), None, M)
-        self.down = MxLinear(wl.normal((H, F), 0.02, wl.generator(seed, "W2"), torch.bfloat16).to(dev), None, M)
+        # zero biases, as in the te.Linear example (bias=True); their gradients come from the
+        # column sums fused into the quantisation of dY and dh
+        self.up = MxLinear(wl.normal((F, H), 0.02, wl.generator(seed, "W1"), torch.bfloat16).to(dev),
+                           torch.zeros(F, dtype=torch.bfloat16, device=dev), M)
+        self.down = MxLinear(wl.normal((H, F), 0.02, wl.generator(seed, "W2"), torch.bfloat16).to(dev),
+                             torch.zeros(H, dtype=torch.bfloat16, device=dev), M)
         self.layers = [self.up, self.down]
         self.x = [wl.channel_scaled_normal(M, H, wl.generator(seed, "X")).to(dev)]
         self.dy = [wl.normal((M, H), 1.0, wl.generator(seed, "dY"), torch.bfloat16).to(dev)]
@@ -366,7 +371,7 @@ class MxModel:
         self.up.backward(dh)
 
     def output_slots(self):
-        return [(self.up, "dw"), (self.down, "dw"), (self.up, "dx")]
+        return [(self.up, "dw"), (self.down, "dw"), (self.up, "db"), (self.down, "db"), (self.up, "dx")]
 
     def outputs(self):
         return [getattr(o, a) for o, a in self.output_slots()]

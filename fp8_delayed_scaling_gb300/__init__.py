@@ -56,7 +56,7 @@ _SIGS = {
     "fp8_gemm_dgelu_cast": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _sz, _vp, _vp, _vp]),
     "mxfp8_scale_bytes": (_sz, [_i64, _i64]),
-    "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "mxfp8_quantize": (_i32, [_vp, _i32, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "mxfp8_gemm": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp]),
     "fp8_layernorm_cast": (_i32, [_vp, _i64, _i64, _vp, _vp, ctypes.c_float, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
                                   _vp, _vp]),
@@ -311,11 +311,15 @@ def mxfp8_scale_bytes(rows: int, cols: int) -> int:
     return _lib.mxfp8_scale_bytes(rows, cols)
 
 
-def mxfp8_quantize(x: torch.Tensor, row_q=None, row_s=None, col_q=None, col_s=None, stream=None) -> None:
+def mxfp8_quantize(x: torch.Tensor, row_q=None, row_s=None, col_q=None, col_s=None, dbias=None, workspace=None,
+                   stream=None) -> None:
+    """Row- and/or column-wise MXFP8 codes and tiled E8M0 scales of x; dbias (fp32 [cols])
+    receives the column sums of x in the same pass (workspace: fp8_cast_workspace_size bytes)."""
     assert x.dim() == 2 and x.is_contiguous()
     rows, cols = x.shape
-    _check(_lib.mxfp8_quantize(_p(x), _hp(x), rows, cols, _p(row_q), _p(row_s), _p(col_q), _p(col_s),
-                               _stream(stream)), "mxfp8_quantize")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_lib.mxfp8_quantize(_p(x), _hp(x), rows, cols, _p(row_q), _p(row_s), _p(col_q), _p(col_s), _p(dbias),
+                               _p(workspace), ws_bytes, _stream(stream)), "mxfp8_quantize")
 
 
 def mxfp8_gemm(A, A_s, B, B_s, D: torch.Tensor, bias: torch.Tensor | None = None, dev_status=None,

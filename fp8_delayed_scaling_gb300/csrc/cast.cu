@@ -278,24 +278,51 @@ void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, 
     launch_colsum_reduce(ws, n_rows, cols, dbias, st);
 }
 
+// Grid of a tiled cast launch: no more CTAs than fit on the GPU at once.  Every CTA is then
+// resident from the start and walks tiles blockIdx.x, + gridDim.x, ..., so the CTAs' tile
+// counts differ by at most one.  (With more CTAs than slots, CTAs of 3 and 4 tiles queue
+// behind each other and the last slots finish up to two tiles after the average.)
+template <int XKIND, int FMT, int OP>
+static dim3 cast_grid(int64_t tiles, int sms) {
+    static std::atomic<int> per_sm{0};  // resident CTAs per SM; the same on every sm_103 device
+    int occ = per_sm.load(std::memory_order_acquire);
+    if (occ == 0) {
+        std::lock_guard<std::mutex> lock(init_mutex());
+        occ = per_sm.load(std::memory_order_relaxed);
+        if (occ == 0) {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_kernel<XKIND, FMT, OP>, CT_THREADS, 0) !=
+                    cudaSuccess ||
+                n < 1) {
+                cudaGetLastError();
+                n = 1;
+            }
+            occ = n;
+            per_sm.store(occ, std::memory_order_release);
+        }
+    }
+    const int64_t slots = (int64_t)sms * occ;
+    return dim3((unsigned)(tiles < slots ? tiles : slots));
+}
+
 template <int XKIND, int FMT>
-static void launch_cast(dim3 grid, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
+static void launch_cast(int64_t tiles, int sms, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
                         uint8_t *out, uint8_t *out_t, float *amax, float *ws) {
-    cast_kernel<XKIND, FMT, OP_NONE>
-        <<<grid, CT_THREADS, 0, st>>>(x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, nullptr);
+    cast_kernel<XKIND, FMT, OP_NONE><<<cast_grid<XKIND, FMT, OP_NONE>(tiles, sms), CT_THREADS, 0, st>>>(
+        x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, nullptr);
     note_launch();
 }
 
 template <int OP>
-static void launch_op_cast(dim3 grid, cudaStream_t st, int fmt, const void *x, const OpArgs &op, int64_t rows,
-                           int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *ws,
-                           uint16_t *pre_out) {
+static void launch_op_cast(int64_t tiles, int sms, cudaStream_t st, int fmt, const void *x, const OpArgs &op,
+                           int64_t rows, int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
+                           float *ws, uint16_t *pre_out) {
     if (fmt == FP8DL_E4M3)
-        cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP>
-            <<<grid, CT_THREADS, 0, st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+        cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP><<<cast_grid<FP8DL_BF16, FP8DL_E4M3, OP>(tiles, sms), CT_THREADS, 0,
+                                                   st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
     else
-        cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP>
-            <<<grid, CT_THREADS, 0, st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+        cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP><<<cast_grid<FP8DL_BF16, FP8DL_E5M2, OP>(tiles, sms), CT_THREADS, 0,
+                                                   st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
     note_launch();
 }
 
@@ -306,10 +333,8 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
                                         uint8_t *out, uint8_t *out_t, float *amax, void *y, int sms,
                                         cudaStream_t st) {
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
-    const int64_t max_ctas = (int64_t)sms * 8;
-    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
     OpArgs op{nullptr, mu, rs, static_cast<const uint16_t *>(gamma), static_cast<const uint16_t *>(beta)};
-    launch_op_cast<OP_LAYERNORM>(grid, st, fmt, x, op, rows, cols, scale, out, out_t, amax, nullptr,
+    launch_op_cast<OP_LAYERNORM>(tiles, sms, st, fmt, x, op, rows, cols, scale, out, out_t, amax, nullptr,
                                  static_cast<uint16_t *>(y));
     return check_launch("fp8_layernorm_cast(tiles)");
 }
@@ -357,19 +382,17 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
     FP8DL_TRY(current_device(nullptr, &sms));
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
-    const int64_t max_ctas = (int64_t)sms * 8;
-    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_BF16, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
         else
-            launch_cast<FP8DL_BF16, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
     } else {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_F32, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
         else
-            launch_cast<FP8DL_F32, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
     }
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose"));
     if (dbias) {
@@ -417,14 +440,12 @@ static fp8dl_status op_cast_common(int op, const void *x, const void *aux, int64
     FP8DL_TRY(current_device(nullptr, &sms));
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
-    const int64_t max_ctas = (int64_t)sms * 8;
-    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     uint16_t *pre = static_cast<uint16_t *>(pre_out);
     if (op == OP_GELU)
-        launch_op_cast<OP_GELU>(grid, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre);
+        launch_op_cast<OP_GELU>(tiles, sms, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre);
     else
-        launch_op_cast<OP_DGELU>(grid, st, out_dtype, x, OpArgs{aux, nullptr, nullptr, nullptr, nullptr}, rows, cols,
+        launch_op_cast<OP_DGELU>(tiles, sms, st, out_dtype, x, OpArgs{aux, nullptr, nullptr, nullptr, nullptr}, rows, cols,
                                  scale, out, out_t, amax, ws, pre);
     FP8DL_TRY(check_launch(name));
     if (dbias) {
@@ -519,8 +540,6 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     if (dbias) FP8DL_TRY(static_scratch_address(dev, &ws));
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
-    const int64_t max_ctas = (int64_t)sms * 8;
-    dim3 grid((unsigned)(tiles < max_ctas ? tiles : max_ctas));
     // The cast's partials and their reduction are enqueued back to back with no other call's
     // launches between them: calls from several host threads on one stream then run one
     // after another on the GPU, each reading its own partials from the shared array.
@@ -529,14 +548,14 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     if (dbias) order.lock();
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_BF16, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
         else
-            launch_cast<FP8DL_BF16, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
     } else {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_F32, FP8DL_E4M3>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
         else
-            launch_cast<FP8DL_F32, FP8DL_E5M2>(grid, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
     }
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc"));
     if (dbias) {

@@ -94,18 +94,24 @@ __device__ __forceinline__ void mq_stage(uint8_t *buf, const void *x, int64_t ro
     }
 }
 
-template <int XKIND>
+// ws (optional): column sums of x per 128-row tile, ws[tile row][column] (the bias
+// gradient before its final reduction over tile rows).  Per tile: each lane sums its 8
+// rows, the four lanes of a 32-row band add theirs (two shuffles), and the four bands of
+// the tile are added in band order, so the sums are the same on every run.
+template <int XKIND, bool DBIAS>
 __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *__restrict__ x, int64_t rows,
                                                                     int64_t cols, uint8_t *__restrict__ row_q,
                                                                     uint8_t *__restrict__ row_s,
                                                                     uint8_t *__restrict__ col_q,
-                                                                    uint8_t *__restrict__ col_s) {
+                                                                    uint8_t *__restrict__ col_s,
+                                                                    float *__restrict__ ws) {
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
     constexpr int ROW_BYTES = 128 * ESZ, STAGE = 128 * ROW_BYTES;
     extern __shared__ __align__(16) uint8_t mq_smem[];
     // Scales of one CTA tile: exactly one 512-byte tile of the tiled scale layout per
     // orientation (128 rows x 4 blocks).  Double-buffered; written out one iteration later.
     __shared__ __align__(16) uint8_t sf_tile[2][2][512];  // [buffer][row-wise, column-wise]
+    __shared__ __align__(16) float band_sum[DBIAS ? 2 : 1][4][128];  // [buffer][32-row band][column] (DBIAS)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int cc = lane & 3, rr = (lane >> 2) & 3, sub = lane >> 4;
     const int wr = warp >> 1, wc = warp & 1;  // this warp's 32-row band and 64-column half of the tile
@@ -139,6 +145,14 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
             if ((which == 0 ? row_q : col_q) != nullptr) *(reinterpret_cast<uint4 *>(dst) + o) = *src;
             *src = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);  // padding default for reuse
         }
+        if constexpr (DBIAS) {
+            if (prev_tile >= 0 && threadIdx.x >= 128) {  // the previous tile's column sums, bands in order
+                const int c = threadIdx.x - 128;
+                const int64_t ptr = prev_tile / tiles_c, pc = (prev_tile % tiles_c) * 128 + c;
+                const float(*bs)[128] = band_sum[sfb ^ 1];
+                if (pc < cols) ws[ptr * cols + pc] = ((bs[0][c] + bs[1][c]) + bs[2][c]) + bs[3][c];
+            }
+        }
         const int64_t tr0 = (tile / tiles_c) * 128, tc0 = (tile % tiles_c) * 128;
         const bool ok = tr0 + 32 * wr < rows && tc0 + 64 * wc + 32 * sub < cols;  // whole 32 x 32 block present
         const uint8_t *sb = mq_smem + stage * STAGE + prow * ROW_BYTES + pcol * ESZ;
@@ -163,6 +177,25 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
             }
         }
         __syncthreads();  // the stage may be refilled once every thread has read it
+        if constexpr (DBIAS) {
+            // bands of the tile beyond the matrix (rows are a multiple of 32) add zeros
+            const bool band_ok = tr0 + 32 * wr < rows;
+            float cs[8];
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                float a = v[0][j];
+#pragma unroll
+                for (int i = 1; i < 8; i++) a += v[i][j];
+                cs[j] = band_ok ? a : 0.0f;
+                cs[j] += __shfl_xor_sync(0xffffffffu, cs[j], 4);
+                cs[j] += __shfl_xor_sync(0xffffffffu, cs[j], 8);
+            }
+            if (rr == 0) {
+                float4 *dst = reinterpret_cast<float4 *>(&band_sum[sfb][wr][pcol]);
+                dst[0] = make_float4(cs[0], cs[1], cs[2], cs[3]);
+                dst[1] = make_float4(cs[4], cs[5], cs[6], cs[7]);
+            }
+        }
         float rmax[8], cmax[8];
 #pragma unroll
         for (int i = 0; i < 8; i++) {
@@ -230,6 +263,14 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
     }
     cp_async_wait<0>();
     __syncthreads();
+    if constexpr (DBIAS) {
+        if (prev_tile >= 0 && threadIdx.x >= 128) {  // the last tile's column sums
+            const int c = threadIdx.x - 128;
+            const int64_t ptr = prev_tile / tiles_c, pc = (prev_tile % tiles_c) * 128 + c;
+            const float(*bs)[128] = band_sum[sfb ^ 1];
+            if (pc < cols) ws[ptr * cols + pc] = ((bs[0][c] + bs[1][c]) + bs[2][c]) + bs[3][c];
+        }
+    }
     if (prev_tile >= 0 && threadIdx.x < 64) {  // the last tile's scales
         const int o = threadIdx.x & 31, which = threadIdx.x >> 5;
         const int64_t ptr = prev_tile / tiles_c, ptc = prev_tile % tiles_c;
@@ -554,7 +595,8 @@ size_t mxfp8_scale_bytes(int64_t rows, int64_t cols) {
 }
 
 fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols, uint8_t *row_q,
-                            uint8_t *row_s, uint8_t *col_q, uint8_t *col_s, fp8dl_stream_t stream) {
+                            uint8_t *row_s, uint8_t *col_q, uint8_t *col_s, float *dbias, void *workspace,
+                            size_t workspace_bytes, fp8dl_stream_t stream) {
     FP8DL_NVTX("mxfp8_quantize");
     FP8DL_CHECK_ARG(x != nullptr, "x is NULL");
     FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
@@ -564,11 +606,20 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
     if (!dim_ok(rows, 32) || !dim_ok(cols, 32))
         return fail(FP8DL_ERR_SHAPE, "rows (%lld) and cols (%lld) must be positive multiples of 32",
                     (long long)rows, (long long)cols);
-    if (!aligned16(x) || !aligned16(row_q) || !aligned16(col_q))
-        return fail(FP8DL_ERR_ALIGN, "x, row_q and col_q must be 16-byte aligned");
+    if (!aligned16(x) || !aligned16(row_q) || !aligned16(col_q) || !aligned16(dbias))
+        return fail(FP8DL_ERR_ALIGN, "x, row_q, col_q and dbias must be 16-byte aligned");
+    const int64_t row_tiles = (rows + 127) / 128;
+    if (dbias) {
+        const size_t need = (size_t)row_tiles * (size_t)cols * sizeof(float);
+        if (!workspace || workspace_bytes < need)
+            return fail(FP8DL_ERR_WORKSPACE, "mxfp8_quantize: dbias needs a workspace of %zu bytes (got %zu)", need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if (!aligned16(workspace)) return fail(FP8DL_ERR_ALIGN, "workspace must be 16-byte aligned");
+    }
+    float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     int dev = 0, sms = 0;
     FP8DL_TRY(current_device(&dev, &sms));
-    const int64_t tiles = ((rows + 127) / 128) * ((cols + 127) / 128);
+    const int64_t tiles = row_tiles * ((cols + 127) / 128);
     const int64_t max_ctas = (int64_t)sms * 2;
     const unsigned grid = (unsigned)(tiles < max_ctas ? tiles : max_ctas);
     const size_t smem = (size_t)MQ_STAGES * 128 * 128 * (x_dtype == FP8DL_BF16 ? 2 : 4);
@@ -576,23 +627,41 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
     if (!attr[dev].load(std::memory_order_acquire)) {
         std::lock_guard<std::mutex> lock(init_mutex());
         if (!attr[dev].load(std::memory_order_relaxed)) {
-            cudaError_t e = cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_BF16>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, MQ_STAGES * 128 * 128 * 2);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(mxfp8_quantize_kernel<FP8DL_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         MQ_STAGES * 128 * 128 * 4);
+            cudaError_t e = cudaSuccess;
+            for (const void *k : {(const void *)mxfp8_quantize_kernel<FP8DL_BF16, false>,
+                                  (const void *)mxfp8_quantize_kernel<FP8DL_BF16, true>})
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MQ_STAGES * 128 * 128 * 2);
+            for (const void *k : {(const void *)mxfp8_quantize_kernel<FP8DL_F32, false>,
+                                  (const void *)mxfp8_quantize_kernel<FP8DL_F32, true>})
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, MQ_STAGES * 128 * 128 * 4);
             if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
             attr[dev].store(true, std::memory_order_release);
         }
     }
-    if (x_dtype == FP8DL_BF16)
-        mxfp8_quantize_kernel<FP8DL_BF16><<<grid, MQ_THREADS, smem, (cudaStream_t)stream>>>(x, rows, cols, row_q,
-                                                                                             row_s, col_q, col_s);
-    else
-        mxfp8_quantize_kernel<FP8DL_F32><<<grid, MQ_THREADS, smem, (cudaStream_t)stream>>>(x, rows, cols, row_q,
-                                                                                            row_s, col_q, col_s);
+    const cudaStream_t st = (cudaStream_t)stream;
+    if (x_dtype == FP8DL_BF16) {
+        if (ws)
+            mxfp8_quantize_kernel<FP8DL_BF16, true><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+                                                                                  col_s, ws);
+        else
+            mxfp8_quantize_kernel<FP8DL_BF16, false><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+                                                                                   col_s, nullptr);
+    } else {
+        if (ws)
+            mxfp8_quantize_kernel<FP8DL_F32, true><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+                                                                                 col_s, ws);
+        else
+            mxfp8_quantize_kernel<FP8DL_F32, false><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+                                                                                  col_s, nullptr);
+    }
     note_launch();
     FP8DL_TRY(check_launch("mxfp8_quantize"));
+    if (dbias) {
+        colsum_reduce(ws, row_tiles, cols, dbias, (cudaStream_t)stream);
+        FP8DL_TRY(check_launch("mxfp8_quantize(dbias reduce)"));
+    }
     if (row_s) launch_sf_pad(row_s, rows, cols / 32, (cudaStream_t)stream);
     if (col_s) launch_sf_pad(col_s, cols, rows / 32, (cudaStream_t)stream);
     return check_launch("mxfp8_quantize(scale padding)");

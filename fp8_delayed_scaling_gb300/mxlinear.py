@@ -10,14 +10,13 @@ axis with its own E8M0 scale, so there is no amax history and no delay:
   backward  dY -> row-wise (blocks along N) + column-wise (blocks along M)
             dX[M,K] = mx_gemm(dY_row, W_col)     (reduction over N)
             dW[N,K] = mx_gemm(dY_col, X_col)     (reduction over M)
-            db      = column sums of dY
+            db      = column sums of dY, in the same pass as dY's quantisation
 """
 from __future__ import annotations
 
 import torch
 
-from . import (E4M3, fp8_cast_amax_transpose, fp8_cast_workspace_size, mxfp8_gemm, mxfp8_quantize,
-               mxfp8_scale_bytes)
+from . import fp8_cast_workspace_size, mxfp8_gemm, mxfp8_quantize, mxfp8_scale_bytes
 
 
 class MXTensor:
@@ -30,9 +29,10 @@ class MXTensor:
         self.col_q = torch.empty((cols, rows), **u8)
         self.col_s = torch.empty(mxfp8_scale_bytes(cols, rows), **u8)
 
-    def quantize(self, x: torch.Tensor, rowwise=True, colwise=True, stream=None) -> None:
+    def quantize(self, x: torch.Tensor, rowwise=True, colwise=True, dbias=None, workspace=None, stream=None) -> None:
         mxfp8_quantize(x, self.row_q if rowwise else None, self.row_s if rowwise else None,
-                       self.col_q if colwise else None, self.col_s if colwise else None, stream=stream)
+                       self.col_q if colwise else None, self.col_s if colwise else None, dbias=dbias,
+                       workspace=workspace, stream=stream)
 
 
 class MxLinear:
@@ -49,7 +49,7 @@ class MxLinear:
         self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
         self.db = torch.empty(N, dtype=torch.float32, device=dev) if bias is not None else None
-        self.ws = torch.empty(fp8_cast_workspace_size(M, N), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(fp8_cast_workspace_size(M, N), dtype=torch.uint8, device=dev) if bias is not None else None
 
     def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
         self.mx_x.quantize(x, stream=stream)
@@ -59,9 +59,7 @@ class MxLinear:
         return self.y
 
     def backward(self, dy: torch.Tensor, stream=None):
-        self.mx_dy.quantize(dy, stream=stream)
-        if self.db is not None:
-            fp8_cast_amax_transpose(dy, E4M3, None, dbias=self.db, workspace=self.ws, stream=stream)
+        self.mx_dy.quantize(dy, dbias=self.db, workspace=self.ws, stream=stream)
         mxfp8_gemm(self.mx_dy.row_q, self.mx_dy.row_s, self.mx_w.col_q, self.mx_w.col_s, self.dx, stream=stream)
         mxfp8_gemm(self.mx_dy.col_q, self.mx_dy.col_s, self.mx_x.col_q, self.mx_x.col_s, self.dw, stream=stream)
         return self.dx, self.dw, self.db

@@ -267,11 +267,19 @@ fp8dl_status fp8_gemm_dgelu_cast(const uint8_t *A, int32_t a_dtype, const uint8_
  * (g * ceil(NB/4) + h) * 512, and inside the tile
  *     byte (r % 32) * 16 + ((r % 128) / 32) * 4 + (b % 4)  holds  S[r][b].
  * Total size: mxfp8_scale_bytes(R, 32*NB).  Entries for rows >= R or blocks
- * >= NB (padding) are written as 127 (2^0). */
+ * >= NB (padding) are written as 127 (2^0).
+ *
+ * dbias [cols] fp32 receives the column sums of x (the bias gradient when x
+ * is grad_output; the te.Linear example has bias=True), in the same pass over
+ * x, or NULL; overwritten, not accumulated.  The sum runs in a fixed order,
+ * so repeated calls give the same bits.  workspace/workspace_bytes: scratch
+ * of fp8_cast_workspace_size(rows, cols) bytes (16-byte aligned), needed
+ * only when dbias != NULL (FP8DL_ERR_WORKSPACE otherwise). */
 size_t mxfp8_scale_bytes(int64_t rows, int64_t cols);
 
 fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_t cols,
                             uint8_t *row_q, uint8_t *row_s, uint8_t *col_q, uint8_t *col_s,
+                            float *dbias, void *workspace, size_t workspace_bytes,
                             fp8dl_stream_t stream);
 
 /* MXFP8 GEMM: D[m,n] = round_d( sum_b 2^(ea[m,b]+eb[n,b]) * sum_{k in b} A[m,k]*B[n,k]

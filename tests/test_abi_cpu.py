@@ -66,7 +66,7 @@ def test_host_validation_without_gpu(lib):
     assert L.fp8_cast_amax_transpose(a16, 1, 32, 0, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_SHAPE
     assert L.fp8_gemm(a16, 0, a16, 0, 0, 16, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
     assert L.fp8_gemm(a16, 0, a16, 0, 16, 16, 0, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
-    assert L.mxfp8_quantize(a16, 1, 0, 32, a16, a16, None, None, None) == lib.ERR_SHAPE
+    assert L.mxfp8_quantize(a16, 1, 0, 32, a16, a16, None, None, None, None, 0, None) == lib.ERR_SHAPE
     assert L.mxfp8_gemm(a16, a16, a16, a16, 32, 0, 32, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
     # dimension not a multiple of 16
     assert L.fp8_cast_amax_transpose(a16, 1, 33, 32, 0, a16, a16, None, None, None, None, None, 0, None) == lib.ERR_SHAPE
@@ -79,7 +79,9 @@ def test_host_validation_without_gpu(lib):
     assert L.fp8_cast_amax_transpose(a16, 1, 32, 32, 0, None, None, None, a16, a16, None, None, 0, None) == lib.ERR_INVALID_ARG
     # bad dtype enums
     assert L.fp8_gemm(a16, 2, a16, 0, 16, 16, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_INVALID_ARG
-    assert L.mxfp8_quantize(a16, 1, 48, 32, a16, a16, None, None, None) == lib.ERR_SHAPE
+    assert L.mxfp8_quantize(a16, 1, 48, 32, a16, a16, None, None, None, None, 0, None) == lib.ERR_SHAPE
+    # MX bias gradient without workspace
+    assert L.mxfp8_quantize(a16, 1, 64, 32, a16, a16, None, None, a16, None, 0, None) == lib.ERR_WORKSPACE
     assert L.mxfp8_gemm(a16, a16, a16, a16, 32, 32, 48, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
     r = lib.fp8dl_recipe(0, 0, 1, 16, 0)  # interval 0 is invalid
     assert L.fp8_update_scale(ctypes.byref(r), 3, a16, 0, None) == lib.ERR_INVALID_ARG

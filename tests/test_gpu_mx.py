@@ -65,6 +65,40 @@ def test_mx_quantize_parity(shape, dtype):
         assert np.all(b[mask] == 127)
 
 
+@pytest.mark.parametrize("shape", [(32, 32), (160, 288), (512, 1024), (96, 800), (384, 128)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_mx_quantize_dbias(shape, dtype):
+    """Column sums fused into the quantisation: within rows * 2^-24 * sum|x| of the oracle's
+    fp64 sums (partial 128-row tiles included), the same bits on a second call, and the codes
+    and scales unchanged by the extra output."""
+    import fp8_delayed_scaling_gb300 as fd
+    dev = gpu()
+    R, C = shape
+    g = wl.generator(42, "mxq-dbias/%s/%s" % (shape, dtype))
+    x = (wl.channel_scaled_normal(R, C, g) * 1e-2).to(dtype)
+    xd = x.to(dev)
+    rq0, rs0, cq0, cs0 = _quantize(x, dev)
+    ws = torch.full((fd.fp8_cast_workspace_size(R, C),), 0xFF, dtype=torch.uint8, device=dev)  # NaN-filled scratch
+    res = []
+    for outs in (("row", "col"), ("row",), ("col",), ("row", "col")):
+        rq = torch.empty((R, C), dtype=torch.uint8, device=dev) if "row" in outs else None
+        rs = torch.empty((fd._lib.mxfp8_scale_bytes(R, C),), dtype=torch.uint8, device=dev) if "row" in outs else None
+        cq = torch.empty((C, R), dtype=torch.uint8, device=dev) if "col" in outs else None
+        cs = torch.empty((fd._lib.mxfp8_scale_bytes(C, R),), dtype=torch.uint8, device=dev) if "col" in outs else None
+        db = torch.full((C,), float("nan"), dtype=torch.float32, device=dev)
+        fd.mxfp8_quantize(xd, rq, rs, cq, cs, dbias=db, workspace=ws)
+        torch.cuda.synchronize()
+        if rq is not None:
+            assert torch.equal(rq, rq0) and torch.equal(rs, rs0)
+        if cq is not None:
+            assert torch.equal(cq, cq0) and torch.equal(cs, cs0)
+        res.append(db.cpu().numpy())
+    s, sabs = oracle.colsum(host(x))
+    for d in res:
+        assert np.array_equal(d, res[0])  # a fixed summation order
+    assert np.all(np.abs(res[0].astype(np.float64) - s) <= R * 2.0 ** -24 * sabs + 1e-30)
+
+
 def test_mx_quantize_special_blocks():
     """Blocks of zeros, powers of two, 448*2^k and values just above it, subnormals."""
     dev = gpu()

@@ -109,14 +109,19 @@ def test_mx_mlp_step():
     w1 = wl.normal((F, H), 0.02, wl.generator(seed, "W1"), torch.bfloat16)
     w2 = wl.normal((H, F), 0.02, wl.generator(seed, "W2"), torch.bfloat16)
     dy = wl.normal((M, H), 1.0, wl.generator(seed, "dY"), torch.bfloat16)
-    up = MxLinear(w1.to(dev), None, M)
-    down = MxLinear(w2.to(dev), None, M)
+    # zero biases, as in the te.Linear example (bias=True): their gradients come from the
+    # column sums fused into the quantisation of dY and of dh
+    up = MxLinear(w1.to(dev), torch.zeros(F, dtype=torch.bfloat16, device=dev), M)
+    down = MxLinear(w2.to(dev), torch.zeros(H, dtype=torch.bfloat16, device=dev), M)
     hid = up.forward(x.to(dev))
     down.forward(hid)
     dh, _, _ = down.backward(dy.to(dev))
     up.backward(dh)
     torch.cuda.synchronize()
     rng = np.random.default_rng(2)
+    for lin, src in ((down, dy), (up, dh)):  # bias gradients in full
+        s, sabs = oracle.colsum(host(src))
+        assert np.all(np.abs(lin.db.cpu().numpy().astype(np.float64) - s) <= M * 2.0 ** -24 * sabs + 1e-30)
     # quantisation of every operand: sampled rows of both orientations, bit-exact
     for mxt, src in ((up.mx_x, x), (up.mx_w, w1), (down.mx_x, hid), (down.mx_w, w2), (down.mx_dy, dy),
                      (up.mx_dy, dh)):
