@@ -7,9 +7,12 @@ The default workload is the LayerNormMLP block (16384 tokens, 4096 -> 16384 ->
 4096, HYBRID delayed scaling, history 16): LayerNorm+cast, the weight casts,
 fc1, GELU+cast, fc2, the grad_output cast with bias gradient, dgrad and wgrad
 of both GEMMs, dGELU+cast with bias gradient, the LayerNorm backward, and one
-delayed scale update of all six slots.  `--workload llama_proj | mx_mlp |
-linear_hybrid | linear_fwd` selects the other workloads.  Inputs are resident in HBM before timing; the L2
-is flushed (a 512 MB write) between timed steps, outside the step events.
+delayed scale update of all six slots.  The default run then measures the te.Linear layer
+(2048 tokens, 768 -> 3072) and the MXFP8 MLP (16384 tokens, 8192 -> 28672 -> 8192) the same
+way, as the `te_linear` and `mx_mlp` entries of the same line.  `--workload NAME` runs one
+workload alone (ln_mlp, llama_proj, mx_mlp, linear_hybrid, linear_fwd, ...).  Inputs are
+resident in HBM before timing; the L2 is flushed (a 512 MB write) between timed steps, outside
+the step events.
 
 Prints one JSON line (rank 0).  `value` is TFLOP/s of algorithmic GEMM work
 (2*M*N*K per GEMM) over the step time; `roofline` is the dominant kernel (the
@@ -38,23 +41,27 @@ import workloads as wl  # noqa: E402
 
 METRIC = "FP8 linear fwd+bwd TFLOP/s & cast/amax GB/s, % of GB300 FP8/HBM peak"
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
-# DRAM bytes (read + write) per GEMM launch, the mean over one step's launches, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of every fp8_gemm_pair_kernel
-# launch of the workload's steps).  Each figure carries the SHA-256 of the GEMM kernel
-# sources it was taken with; once those sources differ, the line reports null instead.
-GEMM_TRAFFIC = {"ln_mlp": {"bytes": 1.219e9,
-                           "src_sha256": "ff33f37eca048513505364fe22a02b6ae075ae7f3dd921964fa058210fa71a6a",
-                           "capture": "fp8_gemm_pair_kernel<0,0>/<1,0>/<2,1> of commit ee20ef7, mean of the "
-                                      "6 launches of a step"}}
-GEMM_SOURCES = ("fp8_delayed_scaling_gb300/csrc/gemm.cu", "fp8_delayed_scaling_gb300/csrc/tc.cuh",
-                "fp8_delayed_scaling_gb300/csrc/common.cuh")
+# DRAM bytes (read + write) per GEMM launch, the mean over one step's GEMM launches, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of every GEMM launch of the
+# workload's steps).  Each figure carries the SHA-256 of the kernel sources it was taken with;
+# once those sources differ, the line reports null instead.
+_COMMON_SRC = ("fp8_delayed_scaling_gb300/csrc/tc.cuh", "fp8_delayed_scaling_gb300/csrc/common.cuh")
+GEMM_TRAFFIC = {
+    "ln_mlp": {"bytes": 1.218e9, "sources": ("fp8_delayed_scaling_gb300/csrc/gemm.cu",) + _COMMON_SRC,
+               "src_sha256": "92b1b36ce380c8689ed42515151c041a56dcc53d092dd006cbfe3c838a11bfc4",
+               "capture": "fp8_gemm_pair_kernel<0,0>/<1,0>/<2,1> of commit 3238a2c, mean of the 6 launches of a "
+                          "step over 17 steps"},
+    "mx_mlp": {"bytes": 3.710e9, "sources": ("fp8_delayed_scaling_gb300/csrc/mxfp8.cu",) + _COMMON_SRC,
+               "src_sha256": "fad80103f5cb02b10b8573d6ee5aaca7ad5417b17cbaadfba1678e1993a60853",
+               "capture": "mxfp8_gemm_kernel of commit 0e29eba, mean of the 6 launches of a step over 17 steps"},
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def gemm_source_sha():
+def source_sha(paths):
     import hashlib
     h = hashlib.sha256()
-    for rel in GEMM_SOURCES:
+    for rel in paths:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -65,7 +72,7 @@ def gemm_traffic(workload):
     t = GEMM_TRAFFIC.get(workload)
     if t is None:
         return None, "no capture for this workload"
-    if t["src_sha256"] != gemm_source_sha():
+    if t["src_sha256"] != source_sha(t["sources"]):
         return None, "the GEMM kernels changed since the capture"
     return t["bytes"], "ncu capture: " + t["capture"]
 
@@ -875,7 +882,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="ln_mlp", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
+                    help="one workload alone; without it: ln_mlp, then te.Linear and the MXFP8 MLP beside it")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--only", default=None, choices=["gemm", "gemm_gelu", "gemm_dgelu", "cast", "mxq", "mxgemm", "gelu", "dgelu",
                                                           "ln", "lnbwd"])
@@ -883,6 +891,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="issue the timed steps one launch at a time")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    default_run = args.workload is None
+    if default_run:
+        args.workload = "ln_mlp"
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -1001,7 +1012,7 @@ def main():
         line["norm_act"] = hbm_class(kt["norm_act"])
     if clk:
         line["clocks"] = clk
-    if world == 1 and args.workload == "ln_mlp":
+    if world == 1 and default_run:
         # Two more workloads measured the same way right after the main one, so one line carries
         # them: the te.Linear layer of the pages' fwd+bwd HYBRID recipe (2048 tokens, 768 -> 3072)
         # and the MXFP8 MLP (16384 tokens, 8192 -> 28672 -> 8192), the largest configuration.

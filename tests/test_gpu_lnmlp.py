@@ -80,6 +80,29 @@ def host_f(t):
     return t.float().numpy()
 
 
+@pytest.mark.parametrize("variant", ["default", "tiles"])
+def test_layernorm_cast_offset_rows(variant, monkeypatch):
+    """Rows whose mean is far from zero (64 +- 0.5): the statistics are merged from two-pass
+    partials, so no cancellation of sum(x^2) - n mean^2 spoils rsigma."""
+    _variant(monkeypatch, variant)
+    fd = _fd()
+    dev = gpu()
+    R, C = 256, 4096
+    g = wl.generator(55, "ln-offset")
+    x = (wl.normal((R, C), 0.5, g) + 64.0).to(torch.bfloat16)
+    gamma = torch.ones(C, dtype=torch.bfloat16)
+    beta = torch.zeros(C, dtype=torch.bfloat16)
+    mu = torch.empty(R, dtype=torch.float32, device=dev)
+    rs = torch.empty(R, dtype=torch.float32, device=dev)
+    q = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    sc = torch.tensor([16.0], dtype=torch.float32, device=dev)
+    fd.fp8_layernorm_cast(x.to(dev), gamma.to(dev), beta.to(dev), 1e-5, 0, sc, mu, rs, out=q)
+    torch.cuda.synchronize()
+    _, mur, rsr = oracle.layernorm_fwd(host(x), host(gamma), host(beta), 1e-5)
+    assert np.all(np.abs(mu.cpu().numpy() - mur) <= 2.0 ** -20 * np.abs(host_f(x)).max())
+    assert np.all(np.abs(rs.cpu().numpy() - rsr) <= 2.0 ** -18 * rsr)
+
+
 def test_layernorm_cast_without_outputs_records_amax_and_stats():
     fd = _fd()
     dev = gpu()
