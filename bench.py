@@ -541,7 +541,7 @@ class KernelTimer:
     over the harvested steps.  The library's own launch counter, read around the `with`
     block, gives the kernels enqueued in it."""
     classes = {"gemm": ["fp8_gemm", "mxfp8_gemm", "fp8_gemm_gelu_cast", "fp8_gemm_dgelu_cast"],
-               "cast": ["fp8_cast_amax_transpose", "mxfp8_quantize"],
+               "cast": ["fp8_cast_amax_transpose", "fp8_cast_amax_transpose_multi", "mxfp8_quantize"],
                "norm_act": ["fp8_layernorm_cast", "fp8_gelu_cast", "fp8_dgelu_cast", "fp8_layernorm_bwd"],
                "update": ["fp8_seed_amax_history"]}  # the just-in-time scale computation
 

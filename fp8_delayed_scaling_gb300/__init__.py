@@ -40,6 +40,13 @@ class fp8dl_recipe(ctypes.Structure):
                 ("amax_compute_algo", _i32)]
 
 
+class fp8dl_cast_item(ctypes.Structure):
+    """One tensor of fp8_cast_amax_transpose_multi (include/fp8dl.h)."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("scale", ctypes.c_void_p), ("out", ctypes.c_void_p), ("out_t", ctypes.c_void_p),
+                ("amax", ctypes.c_void_p), ("scale_inv_out", ctypes.c_void_p)]
+
+
 _SIGS = {
     "fp8dl_slot_stride": (_sz, [_i32]),
     "fp8dl_scaling_state_bytes": (_sz, [_i32, _i32]),
@@ -49,6 +56,7 @@ _SIGS = {
     "fp8_cast_workspace_size": (_sz, [_i64, _i64]),
     "fp8_cast_amax_transpose": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fp8_cast_amax_transpose_noalloc": (_i32, [_vp, _i32, _i64, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "fp8_cast_amax_transpose_multi": (_i32, [_i32, ctypes.POINTER(fp8dl_cast_item), _i32, _i32, _vp]),
     "fp8_gemm": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp]),
     "fp8_gemm_gelu_cast": (_i32, [_vp, _i32, _vp, _i32, _i64, _i64, _i64, _vp, _vp, _vp, _i32, _vp, _i32, _vp, _vp,
                                   _vp, _vp, _vp, _vp, _vp]),
@@ -249,6 +257,24 @@ def fp8_cast_amax_transpose(x: torch.Tensor, out_dtype: int, scale, out=None, ou
                                         _p(amax), _p(scale_inv_out), _p(dbias), _p(workspace), ws_bytes,
                                         _stream(stream)),
            "fp8_cast_amax_transpose")
+
+
+def fp8_cast_amax_transpose_multi(items, out_dtype: int, stream=None) -> None:
+    """Grouped cast: items is a list of dicts with keys x, scale, and any of out, out_t, amax,
+    scale_inv_out (as for fp8_cast_amax_transpose, without dbias); one launch for all."""
+    n = len(items)
+    arr = (fp8dl_cast_item * n)()
+    x_dtype = None
+    for k, it in enumerate(items):
+        x = it["x"]
+        assert x.dim() == 2 and x.is_contiguous()
+        if x_dtype is None:
+            x_dtype = _hp(x)
+        assert _hp(x) == x_dtype, "all items share one input dtype"
+        arr[k] = fp8dl_cast_item(_p(x), x.shape[0], x.shape[1], _p(it.get("scale")), _p(it.get("out")),
+                                 _p(it.get("out_t")), _p(it.get("amax")), _p(it.get("scale_inv_out")))
+    _check(_lib.fp8_cast_amax_transpose_multi(n, arr, x_dtype if x_dtype is not None else BF16, out_dtype,
+                                              _stream(stream)), "fp8_cast_amax_transpose_multi")
 
 
 def fp8_cast_amax_transpose_noalloc(x: torch.Tensor, out_dtype: int, scale, out=None, out_t=None, amax=None,

@@ -72,166 +72,223 @@ struct OpArgs {
     const uint16_t *gamma, *beta;
 };
 
+// One 128 x 128 tile of the cast; every thread of the CTA calls it with the same tile.
+// amax: the calling thread's running max of |x|.
 template <int XKIND, int FMT, int OP>
-__global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_NONE ? 3 : (XKIND == FP8DL_BF16 ? 4 : 2)) cast_kernel(const void *__restrict__ x, const OpArgs op,
-                                                          int64_t rows, int64_t cols,
-                                                          const float *__restrict__ scale_p,
-                                                          uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
-                                                          float *__restrict__ amax_p, float *__restrict__ ws,
-                                                          uint16_t *__restrict__ pre_out) {
+__device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpArgs &op, int64_t rows, int64_t cols,
+                                          int64_t tile, float scale, uint8_t *__restrict__ out,
+                                          uint8_t *__restrict__ out_t, float *__restrict__ ws,
+                                          uint16_t *__restrict__ pre_out, uint8_t *stage, float (*red)[CT_COLS],
+                                          float &amax) {
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
-    __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
-    __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // per-warp column partials (dbias)
-
     const int t = threadIdx.x;
     const int cb = t & 7, rb = t >> 3;                               // phase 1
     const int lane = t & 31, wi = t >> 5;                            // phase 2
     const int p2_h = lane & 1, p2_w = (wi & 1) * 16 + (lane >> 1), p2_rg = wi >> 1;
-    const float scale = out || out_t ? __ldg(scale_p) : 1.0f;
     const int64_t tiles_c = (cols + CT_COLS - 1) / CT_COLS;
-    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * tiles_c;
-    float amax = 0.0f;
-
-    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-        const int64_t r0 = (tile / tiles_c) * CT_ROWS, c0 = (tile % tiles_c) * CT_COLS;
-        const bool p1_ok = (r0 + 4 * rb < rows) && (c0 + 16 * cb < cols);
-        float csum[16];
+    const int64_t r0 = (tile / tiles_c) * CT_ROWS, c0 = (tile % tiles_c) * CT_COLS;
+    const bool p1_ok = (r0 + 4 * rb < rows) && (c0 + 16 * cb < cols);
+    float csum[16];
 #pragma unroll
-        for (int j = 0; j < 16; j++) csum[j] = 0.0f;
-        if (p1_ok) {
-            RowSeg16<XKIND> seg[4];
-            RowSeg16<XKIND> hseg[OP == OP_DGELU ? 4 : 1];
-            const int64_t eoff = (r0 + 4 * rb) * cols + c0 + 16 * cb;
-            const char *base = static_cast<const char *>(x) + eoff * ESZ;
+    for (int j = 0; j < 16; j++) csum[j] = 0.0f;
+    if (p1_ok) {
+        RowSeg16<XKIND> seg[4];
+        RowSeg16<XKIND> hseg[OP == OP_DGELU ? 4 : 1];
+        const int64_t eoff = (r0 + 4 * rb) * cols + c0 + 16 * cb;
+        const char *base = static_cast<const char *>(x) + eoff * ESZ;
 #pragma unroll
-            for (int i = 0; i < 4; i++) seg[i].load(base + i * cols * ESZ);
-            float ln_mu[4], ln_rs[4];
-            uint32_t ln_g[8], ln_b[8];
-            if (OP == OP_LAYERNORM) {
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    ln_mu[i] = __ldg(op.mu + r0 + 4 * rb + i);
-                    ln_rs[i] = __ldg(op.rs + r0 + 4 * rb + i);
-                }
-                const uint4 g0 = __ldg(reinterpret_cast<const uint4 *>(op.gamma + c0 + 16 * cb));
-                const uint4 g1 = __ldg(reinterpret_cast<const uint4 *>(op.gamma + c0 + 16 * cb + 8));
-                const uint4 b0 = __ldg(reinterpret_cast<const uint4 *>(op.beta + c0 + 16 * cb));
-                const uint4 b1 = __ldg(reinterpret_cast<const uint4 *>(op.beta + c0 + 16 * cb + 8));
-                ln_g[0] = g0.x; ln_g[1] = g0.y; ln_g[2] = g0.z; ln_g[3] = g0.w;
-                ln_g[4] = g1.x; ln_g[5] = g1.y; ln_g[6] = g1.z; ln_g[7] = g1.w;
-                ln_b[0] = b0.x; ln_b[1] = b0.y; ln_b[2] = b0.z; ln_b[3] = b0.w;
-                ln_b[4] = b1.x; ln_b[5] = b1.y; ln_b[6] = b1.z; ln_b[7] = b1.w;
-            }
-            if (OP == OP_DGELU) {
-                const char *hbase = static_cast<const char *>(op.aux) + eoff * ESZ;
-#pragma unroll
-                for (int i = 0; i < 4; i++) hseg[OP == OP_DGELU ? i : 0].load(hbase + i * cols * ESZ);
-            }
+        for (int i = 0; i < 4; i++) seg[i].load(base + i * cols * ESZ);
+        float ln_mu[4], ln_rs[4];
+        uint32_t ln_g[8], ln_b[8];
+        if (OP == OP_LAYERNORM) {
 #pragma unroll
             for (int i = 0; i < 4; i++) {
-                uint32_t w[4];
-                const int r = 4 * rb + i;
+                ln_mu[i] = __ldg(op.mu + r0 + 4 * rb + i);
+                ln_rs[i] = __ldg(op.rs + r0 + 4 * rb + i);
+            }
+            const uint4 g0 = __ldg(reinterpret_cast<const uint4 *>(op.gamma + c0 + 16 * cb));
+            const uint4 g1 = __ldg(reinterpret_cast<const uint4 *>(op.gamma + c0 + 16 * cb + 8));
+            const uint4 b0 = __ldg(reinterpret_cast<const uint4 *>(op.beta + c0 + 16 * cb));
+            const uint4 b1 = __ldg(reinterpret_cast<const uint4 *>(op.beta + c0 + 16 * cb + 8));
+            ln_g[0] = g0.x; ln_g[1] = g0.y; ln_g[2] = g0.z; ln_g[3] = g0.w;
+            ln_g[4] = g1.x; ln_g[5] = g1.y; ln_g[6] = g1.z; ln_g[7] = g1.w;
+            ln_b[0] = b0.x; ln_b[1] = b0.y; ln_b[2] = b0.z; ln_b[3] = b0.w;
+            ln_b[4] = b1.x; ln_b[5] = b1.y; ln_b[6] = b1.z; ln_b[7] = b1.w;
+        }
+        if (OP == OP_DGELU) {
+            const char *hbase = static_cast<const char *>(op.aux) + eoff * ESZ;
 #pragma unroll
-                for (int hh = 0; hh < 2; hh++) {  // two halves of 8 elements
-                    float v[8];
+            for (int i = 0; i < 4; i++) hseg[OP == OP_DGELU ? i : 0].load(hbase + i * cols * ESZ);
+        }
 #pragma unroll
-                    for (int j = 0; j < 8; j++) {
-                        float xv = seg[i].get(8 * hh + j);
-                        if (OP == OP_GELU) xv = gelu_bf16(xv);
-                        if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(8 * hh + j));
-                        if (OP == OP_LAYERNORM) {
-                            const int k = 8 * hh + j;  // y = bf16((x - mu) * rs * gamma + beta)
-                            const float gk = (k & 1) ? bf16_hi(ln_g[k >> 1]) : bf16_lo(ln_g[k >> 1]);
-                            const float bk = (k & 1) ? bf16_hi(ln_b[k >> 1]) : bf16_lo(ln_b[k >> 1]);
-                            xv = bf16_round(fmaf((xv - ln_mu[i]) * ln_rs[i], gk, bk));
-                        }
-                        v[j] = xv;
-                        amax = fmaxf(amax, fabsf(xv));
-                        if (OP == OP_NONE || OP == OP_DGELU) csum[8 * hh + j] += xv;  // dbias only there
+        for (int i = 0; i < 4; i++) {
+            uint32_t w[4];
+            const int r = 4 * rb + i;
+#pragma unroll
+            for (int hh = 0; hh < 2; hh++) {  // two halves of 8 elements
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; j++) {
+                    float xv = seg[i].get(8 * hh + j);
+                    if (OP == OP_GELU) xv = gelu_bf16(xv);
+                    if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(8 * hh + j));
+                    if (OP == OP_LAYERNORM) {
+                        const int k = 8 * hh + j;  // y = bf16((x - mu) * rs * gamma + beta)
+                        const float gk = (k & 1) ? bf16_hi(ln_g[k >> 1]) : bf16_lo(ln_g[k >> 1]);
+                        const float bk = (k & 1) ? bf16_hi(ln_b[k >> 1]) : bf16_lo(ln_b[k >> 1]);
+                        xv = bf16_round(fmaf((xv - ln_mu[i]) * ln_rs[i], gk, bk));
                     }
-                    w[2 * hh] = pack4<FMT>(__fmul_rn(v[0], scale), __fmul_rn(v[1], scale), __fmul_rn(v[2], scale),
-                                           __fmul_rn(v[3], scale));
-                    w[2 * hh + 1] = pack4<FMT>(__fmul_rn(v[4], scale), __fmul_rn(v[5], scale),
-                                               __fmul_rn(v[6], scale), __fmul_rn(v[7], scale));
-                    if (OP != OP_NONE && pre_out) {
-                        uint32_t pw[4];
-#pragma unroll
-                        for (int p = 0; p < 4; p++) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * p], v[2 * p + 1]);
-                            pw[p] = *reinterpret_cast<uint32_t *>(&b2);
-                        }
-                        *reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb + 8 * hh) =
-                            make_uint4(pw[0], pw[1], pw[2], pw[3]);
-                    }
+                    v[j] = xv;
+                    amax = fmaxf(amax, fabsf(xv));
+                    if (OP == OP_NONE || OP == OP_DGELU) csum[8 * hh + j] += xv;  // dbias only there
                 }
-                const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
-                if (out) *reinterpret_cast<uint4 *>(out + (r0 + r) * cols + c0 + 16 * cb) = codes;
-                if (out_t) *reinterpret_cast<uint4 *>(stage + stage_off(r, cb)) = codes;
-            }
-        }
-        if (ws) {
-            // lanes l, l+8, l+16, l+24 share a column block: reduce over them, then lanes 0-7
-            // hold the warp's 16-row partial of columns 16*cb .. 16*cb+15
+                w[2 * hh] = pack4<FMT>(__fmul_rn(v[0], scale), __fmul_rn(v[1], scale), __fmul_rn(v[2], scale),
+                                       __fmul_rn(v[3], scale));
+                w[2 * hh + 1] = pack4<FMT>(__fmul_rn(v[4], scale), __fmul_rn(v[5], scale),
+                                           __fmul_rn(v[6], scale), __fmul_rn(v[7], scale));
+                if (OP != OP_NONE && pre_out) {
+                    uint32_t pw[4];
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 8);
-                csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 16);
-            }
-            if (lane < 8) {
-                float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
-#pragma unroll
-                for (int j = 0; j < 4; j++)
-                    dst[j] = make_float4(csum[4 * j], csum[4 * j + 1], csum[4 * j + 2], csum[4 * j + 3]);
-            }
-        }
-        if (out_t || ws) __syncthreads();
-        if (out_t) {
-            const int rl = 32 * p2_rg + 16 * p2_h;  // first of this thread's 16 rows within the tile
-            if (r0 + rl < rows && c0 + 4 * p2_w < cols) {
-                uint32_t col[4][4];  // col[j][g]: rows rl+4g..rl+4g+3 of column 4*p2_w+j
-#pragma unroll
-                for (int g = 0; g < 4; g++) {
-                    uint32_t W[4];
-#pragma unroll
-                    for (int k = 0; k < 4; k++) {
-                        const int r = rl + 4 * g + k;
-                        W[k] = *reinterpret_cast<const uint32_t *>(stage + stage_off(r, p2_w >> 2) + 4 * (p2_w & 3));
+                    for (int p = 0; p < 4; p++) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * p], v[2 * p + 1]);
+                        pw[p] = *reinterpret_cast<uint32_t *>(&b2);
                     }
-                    const uint32_t t0 = __byte_perm(W[0], W[1], 0x5140), t1 = __byte_perm(W[2], W[3], 0x5140);
-                    const uint32_t t2 = __byte_perm(W[0], W[1], 0x7362), t3 = __byte_perm(W[2], W[3], 0x7362);
-                    col[0][g] = __byte_perm(t0, t1, 0x5410);
-                    col[1][g] = __byte_perm(t0, t1, 0x7632);
-                    col[2][g] = __byte_perm(t2, t3, 0x5410);
-                    col[3][g] = __byte_perm(t2, t3, 0x7632);
+                    *reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb + 8 * hh) =
+                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
                 }
-#pragma unroll
-                for (int j = 0; j < 4; j++)
-                    *reinterpret_cast<uint4 *>(out_t + (c0 + 4 * p2_w + j) * rows + r0 + rl) =
-                        make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
             }
-        }
-        if (ws) {
-            const int64_t tr = r0 / CT_ROWS;
-            if (t < CT_COLS && c0 + t < cols) {
-                float s = 0.0f;
-#pragma unroll
-                for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
-                ws[tr * cols + c0 + t] = s;
-            }
-        }
-        if (out_t || ws) __syncthreads();
-    }
-    if (amax_p) {
-        __shared__ float wmax[CT_THREADS / 32];
-        const float m = warp_max(amax);
-        if (lane == 0) wmax[wi] = m;
-        __syncthreads();
-        if (t == 0) {
-            float mm = wmax[0];
-            for (int k = 1; k < CT_THREADS / 32; k++) mm = fmaxf(mm, wmax[k]);
-            atomic_max_nonneg(amax_p, mm);
+            const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
+            if (out) *reinterpret_cast<uint4 *>(out + (r0 + r) * cols + c0 + 16 * cb) = codes;
+            if (out_t) *reinterpret_cast<uint4 *>(stage + stage_off(r, cb)) = codes;
         }
     }
+    if (ws) {
+        // lanes l, l+8, l+16, l+24 share a column block: reduce over them, then lanes 0-7
+        // hold the warp's 16-row partial of columns 16*cb .. 16*cb+15
+#pragma unroll
+        for (int j = 0; j < 16; j++) {
+            csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 8);
+            csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 16);
+        }
+        if (lane < 8) {
+            float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                dst[j] = make_float4(csum[4 * j], csum[4 * j + 1], csum[4 * j + 2], csum[4 * j + 3]);
+        }
+    }
+    if (out_t || ws) __syncthreads();
+    if (out_t) {
+        const int rl = 32 * p2_rg + 16 * p2_h;  // first of this thread's 16 rows within the tile
+        if (r0 + rl < rows && c0 + 4 * p2_w < cols) {
+            uint32_t col[4][4];  // col[j][g]: rows rl+4g..rl+4g+3 of column 4*p2_w+j
+#pragma unroll
+            for (int g = 0; g < 4; g++) {
+                uint32_t W[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const int r = rl + 4 * g + k;
+                    W[k] = *reinterpret_cast<const uint32_t *>(stage + stage_off(r, p2_w >> 2) + 4 * (p2_w & 3));
+                }
+                const uint32_t t0 = __byte_perm(W[0], W[1], 0x5140), t1 = __byte_perm(W[2], W[3], 0x5140);
+                const uint32_t t2 = __byte_perm(W[0], W[1], 0x7362), t3 = __byte_perm(W[2], W[3], 0x7362);
+                col[0][g] = __byte_perm(t0, t1, 0x5410);
+                col[1][g] = __byte_perm(t0, t1, 0x7632);
+                col[2][g] = __byte_perm(t2, t3, 0x5410);
+                col[3][g] = __byte_perm(t2, t3, 0x7632);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                *reinterpret_cast<uint4 *>(out_t + (c0 + 4 * p2_w + j) * rows + r0 + rl) =
+                    make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
+        }
+    }
+    if (ws) {
+        const int64_t tr = r0 / CT_ROWS;
+        if (t < CT_COLS && c0 + t < cols) {
+            float s = 0.0f;
+#pragma unroll
+            for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
+            ws[tr * cols + c0 + t] = s;
+        }
+    }
+    if (out_t || ws) __syncthreads();
+}
+
+// The CTA's largest |x| max-ed into *amax_p; every thread calls it (wmax: CT_THREADS / 32 floats).
+__device__ __forceinline__ void cta_amax_flush(float amax, float *amax_p, float *wmax) {
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+    const float m = warp_max(amax);
+    if (lane == 0) wmax[wi] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float mm = wmax[0];
+        for (int k = 1; k < CT_THREADS / 32; k++) mm = fmaxf(mm, wmax[k]);
+        atomic_max_nonneg(amax_p, mm);
+    }
+    __syncthreads();  // wmax is free again
+}
+
+template <int XKIND, int FMT, int OP>
+__global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_NONE ? 3 : (XKIND == FP8DL_BF16 ? 4 : 2))
+    cast_kernel(const void *__restrict__ x, const OpArgs op, int64_t rows, int64_t cols,
+                const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
+                float *__restrict__ amax_p, float *__restrict__ ws, uint16_t *__restrict__ pre_out) {
+    __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
+    __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // per-warp column partials (dbias)
+    __shared__ float wmax[CT_THREADS / 32];
+    const float scale = out || out_t ? __ldg(scale_p) : 1.0f;
+    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    float amax = 0.0f;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x)
+        cast_tile<XKIND, FMT, OP>(x, op, rows, cols, tile, scale, out, out_t, ws, pre_out, stage, red, amax);
+    if (amax_p) cta_amax_flush(amax, amax_p, wmax);
+}
+
+// Several tensors cast in one launch: their tiles are numbered one tensor after the
+// other, and each CTA walks tiles blockIdx.x, + gridDim.x, ... of the whole set.  A
+// CTA's tiles reach the tensors in order, so it flushes its amax once per tensor.
+constexpr int CAST_MULTI_MAX = 8;
+struct CastMultiArgs {
+    int n;
+    const void *x[CAST_MULTI_MAX];
+    int64_t rows[CAST_MULTI_MAX], cols[CAST_MULTI_MAX];
+    const float *scale[CAST_MULTI_MAX];
+    uint8_t *out[CAST_MULTI_MAX], *out_t[CAST_MULTI_MAX];
+    float *amax[CAST_MULTI_MAX];
+    float *scale_inv_out[CAST_MULTI_MAX];
+    int64_t tile_end[CAST_MULTI_MAX];  // tiles of tensors 0 .. k together
+};
+
+template <int XKIND, int FMT>
+__global__ void __launch_bounds__(CT_THREADS, XKIND == FP8DL_BF16 ? 4 : 2)
+    cast_multi_kernel(const __grid_constant__ CastMultiArgs a) {
+    __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
+    __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // unused: no bias gradients here
+    __shared__ float wmax[CT_THREADS / 32];
+    const int64_t tiles = a.tile_end[a.n - 1];
+    int item = 0;
+    float amax = 0.0f;
+    for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        int k = item;
+        while (tile >= a.tile_end[k]) k++;
+        if (k != item) {  // the same for every thread of the CTA
+            if (a.amax[item]) cta_amax_flush(amax, a.amax[item], wmax);
+            amax = 0.0f;
+            item = k;
+        }
+        const int64_t first = item ? a.tile_end[item - 1] : 0;
+        const float scale = (a.out[item] || a.out_t[item]) ? __ldg(a.scale[item]) : 1.0f;
+        cast_tile<XKIND, FMT, OP_NONE>(a.x[item], OpArgs{}, a.rows[item], a.cols[item], tile - first, scale,
+                                       a.out[item], a.out_t[item], nullptr, nullptr, stage, red, amax);
+    }
+    if (a.amax[item]) cta_amax_flush(amax, a.amax[item], wmax);
+}
+
+// The decode factors fl32(1 / scale) of the tensors of a grouped cast that ask for one.
+__global__ void scale_inv_multi_kernel(const __grid_constant__ CastMultiArgs a) {
+    const int k = threadIdx.x;
+    if (k < a.n && a.scale_inv_out[k]) *a.scale_inv_out[k] = __frcp_rn(*a.scale[k]);
 }
 
 // dbias[c] = sum over row tiles of ws[tile][c], in a fixed order: CTA = 32
@@ -282,18 +339,15 @@ void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, 
 // resident from the start and walks tiles blockIdx.x, + gridDim.x, ..., so the CTAs' tile
 // counts differ by at most one.  (With more CTAs than slots, CTAs of 3 and 4 tiles queue
 // behind each other and the last slots finish up to two tiles after the average.)
-template <int XKIND, int FMT, int OP>
-static dim3 cast_grid(int64_t tiles, int sms) {
-    static std::atomic<int> per_sm{0};  // resident CTAs per SM; the same on every sm_103 device
+// per_sm caches the kernel's resident CTAs per SM (the same on every sm_103 device).
+static dim3 resident_grid(const void *kernel, std::atomic<int> &per_sm, int64_t tiles, int sms) {
     int occ = per_sm.load(std::memory_order_acquire);
     if (occ == 0) {
         std::lock_guard<std::mutex> lock(init_mutex());
         occ = per_sm.load(std::memory_order_relaxed);
         if (occ == 0) {
             int n = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, cast_kernel<XKIND, FMT, OP>, CT_THREADS, 0) !=
-                    cudaSuccess ||
-                n < 1) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, CT_THREADS, 0) != cudaSuccess || n < 1) {
                 cudaGetLastError();
                 n = 1;
             }
@@ -303,6 +357,12 @@ static dim3 cast_grid(int64_t tiles, int sms) {
     }
     const int64_t slots = (int64_t)sms * occ;
     return dim3((unsigned)(tiles < slots ? tiles : slots));
+}
+
+template <int XKIND, int FMT, int OP>
+static dim3 cast_grid(int64_t tiles, int sms) {
+    static std::atomic<int> per_sm{0};
+    return resident_grid((const void *)cast_kernel<XKIND, FMT, OP>, per_sm, tiles, sms);
 }
 
 template <int XKIND, int FMT>
@@ -404,6 +464,71 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
         scale_inv_snapshot_kernel<<<1, 32, 0, st>>>(scale, scale_inv_out);
         note_launch();
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(scale_inv)"));
+    }
+    return FP8DL_OK;
+}
+
+fp8dl_status fp8_cast_amax_transpose_multi(int32_t n, const fp8dl_cast_item *items, int32_t x_dtype,
+                                           int32_t out_dtype, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8_cast_amax_transpose_multi");
+    FP8DL_CHECK_ARG(n >= 1 && n <= CAST_MULTI_MAX, "n (%d) must be in 1..%d", (int)n, CAST_MULTI_MAX);
+    FP8DL_CHECK_ARG(items != nullptr, "items is NULL");
+    FP8DL_CHECK_ARG(x_dtype == FP8DL_F32 || x_dtype == FP8DL_BF16, "x_dtype must be FP8DL_F32 or FP8DL_BF16");
+    FP8DL_CHECK_ARG(out_dtype == FP8DL_E4M3 || out_dtype == FP8DL_E5M2, "out_dtype must be E4M3 or E5M2");
+    CastMultiArgs a{};
+    a.n = n;
+    bool any_inv = false;
+    int64_t tiles = 0;
+    for (int k = 0; k < n; k++) {
+        const fp8dl_cast_item &it = items[k];
+        FP8DL_CHECK_ARG(it.x != nullptr, "item %d: x is NULL", k);
+        FP8DL_CHECK_ARG(!(it.out || it.out_t || it.scale_inv_out) || it.scale != nullptr,
+                        "item %d: scale is NULL but an output needs it", k);
+        FP8DL_CHECK_ARG(it.out || it.out_t || it.amax, "item %d: nothing to compute", k);
+        if (!dim_ok(it.rows, 16) || !dim_ok(it.cols, 16))
+            return fail(FP8DL_ERR_SHAPE, "item %d: rows (%lld) and cols (%lld) must be positive multiples of 16", k,
+                        (long long)it.rows, (long long)it.cols);
+        if (!aligned16(it.x) || !aligned16(it.out) || !aligned16(it.out_t))
+            return fail(FP8DL_ERR_ALIGN, "item %d: x, out and out_t must be 16-byte aligned", k);
+        a.x[k] = it.x;
+        a.rows[k] = it.rows;
+        a.cols[k] = it.cols;
+        a.scale[k] = it.scale;
+        a.out[k] = it.out;
+        a.out_t[k] = it.out_t;
+        a.amax[k] = it.amax;
+        a.scale_inv_out[k] = it.scale_inv_out;
+        any_inv = any_inv || it.scale_inv_out != nullptr;
+        tiles += ((it.rows + CT_ROWS - 1) / CT_ROWS) * ((it.cols + CT_COLS - 1) / CT_COLS);
+        a.tile_end[k] = tiles;
+    }
+    int sms = 0;
+    FP8DL_TRY(current_device(nullptr, &sms));
+    cudaStream_t st = (cudaStream_t)stream;
+    static std::atomic<int> occ[2][2];
+    const int xi = x_dtype == FP8DL_BF16, fi = out_dtype == FP8DL_E5M2;
+    const void *kern = xi ? (fi ? (const void *)cast_multi_kernel<FP8DL_BF16, FP8DL_E5M2>
+                                : (const void *)cast_multi_kernel<FP8DL_BF16, FP8DL_E4M3>)
+                          : (fi ? (const void *)cast_multi_kernel<FP8DL_F32, FP8DL_E5M2>
+                                : (const void *)cast_multi_kernel<FP8DL_F32, FP8DL_E4M3>);
+    const dim3 grid = resident_grid(kern, occ[xi][fi], tiles, sms);
+    if (xi) {
+        if (fi)
+            cast_multi_kernel<FP8DL_BF16, FP8DL_E5M2><<<grid, CT_THREADS, 0, st>>>(a);
+        else
+            cast_multi_kernel<FP8DL_BF16, FP8DL_E4M3><<<grid, CT_THREADS, 0, st>>>(a);
+    } else {
+        if (fi)
+            cast_multi_kernel<FP8DL_F32, FP8DL_E5M2><<<grid, CT_THREADS, 0, st>>>(a);
+        else
+            cast_multi_kernel<FP8DL_F32, FP8DL_E4M3><<<grid, CT_THREADS, 0, st>>>(a);
+    }
+    note_launch();
+    FP8DL_TRY(check_launch("fp8_cast_amax_transpose_multi"));
+    if (any_inv) {
+        scale_inv_multi_kernel<<<1, 32, 0, st>>>(a);
+        note_launch();
+        FP8DL_TRY(check_launch("fp8_cast_amax_transpose_multi(scale_inv)"));
     }
     return FP8DL_OK;
 }

@@ -37,7 +37,7 @@ from __future__ import annotations
 import torch
 
 from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_transpose,
-               fp8_cast_workspace_size, fp8_gemm, fp8_seed_amax_history)
+               fp8_cast_amax_transpose_multi, fp8_cast_workspace_size, fp8_gemm, fp8_seed_amax_history)
 
 SLOTS_PER_LAYER = 3
 IN, WEIGHT, GRAD = 0, 1, 2
@@ -71,6 +71,22 @@ class WeightCache:
                                 scale_inv_out=self.scale_inv if keep else None, stream=stream)
         self.valid = keep
         return self.scale_inv if keep else state.scale_inv(slot)
+
+
+def cast_weights(caches, weights, state: ScalingState, slots, is_first_microbatch, stream=None):
+    """WeightCache.cast of several weights with one grouped launch (the same codes, amaxes and
+    decode factors as one cast each); returns their decode factors."""
+    for c in caches:
+        c.check(is_first_microbatch)
+    if is_first_microbatch is False:
+        return [c.scale_inv for c in caches]
+    keep = bool(is_first_microbatch)
+    fp8_cast_amax_transpose_multi([dict(x=w, scale=state.scale(s), out=c.q, out_t=c.q_t, amax=state.amax(s),
+                                        scale_inv_out=c.scale_inv if keep else None)
+                                   for c, w, s in zip(caches, weights, slots)], E4M3, stream=stream)
+    for c in caches:
+        c.valid = keep
+    return [c.scale_inv if keep else state.scale_inv(s) for c, s in zip(caches, slots)]
 
 
 def layer_slot_dtypes(recipe: Recipe):

@@ -6,7 +6,8 @@ Engine 简析" §三.1, §三.3) every GEMM operand is an FP8 cast with a stored
 scale, so each activation is fused with the cast of its output:
 
   forward   LN+cast(x)        -> q_ln, q_ln^T      (slot fc1.in)
-            cast W1           -> qW1, qW1^T        (slot fc1.w)
+            cast W1           -> qW1, qW1^T        (slot fc1.w; one grouped launch with
+                                                    W2's cast after step 0)
             h  = fc1(q_ln, qW1) + b1               (bf16)
             GELU+cast(h)      -> q_g, q_g^T        (slot fc2.in; fused into
                                                     the fc1 epilogue after step 0)
@@ -43,7 +44,7 @@ from . import (E4M3, E5M2, FORMAT_HYBRID, Recipe, ScalingState, fp8_cast_amax_tr
                fp8_dgelu_cast, fp8_gelu_cast, fp8_gemm, fp8_gemm_dgelu_cast, fp8_gemm_dgelu_workspace_size,
                fp8_gemm_gelu_cast, fp8_layernorm_bwd,
                fp8_layernorm_bwd_workspace_size, fp8_layernorm_cast, fp8_seed_amax_history)
-from .linear import WeightCache
+from .linear import WeightCache, cast_weights
 
 FC1_IN, FC1_W, FC1_GRAD, FC2_IN, FC2_W, FC2_GRAD = range(6)
 SLOTS = 6
@@ -144,15 +145,17 @@ class Fp8LayerNormMLP:
             self._seed(FC1_IN, 2, stream)
         fp8_layernorm_cast(x, self.gamma, self.beta, self.eps, E4M3, st.scale(s(FC1_IN)), self.mu, self.rs,
                            out=self.q_ln, out_t=self.q_lnT, amax=st.amax(s(FC1_IN)), y=self.y_ln, stream=stream)
-        self.w1_sinv = self.w1cache.cast(self.w1, st, s(FC1_W), is_first_microbatch, stream)
         if self.fused and not seed:
+            # both weights in one grouped cast (their scales are this step's delayed ones)
+            self.w1_sinv, self.w2_sinv = cast_weights([self.w1cache, self.w2cache], [self.w1, self.w2], st,
+                                                      [s(FC1_W), s(FC2_W)], is_first_microbatch, stream)
             fp8_gemm_gelu_cast(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), self.w1_sinv, self.h,
                                E4M3, st.scale(s(FC2_IN)), self.q_g, self.q_gT, q_amax=st.amax(s(FC2_IN)),
                                bias=self.b1, g=self.g, stream=stream)
-            self.w2_sinv = self.w2cache.cast(self.w2, st, s(FC2_W), is_first_microbatch, stream)
             fp8_gemm(self.q_g, E4M3, self.qw2, E4M3, st.scale_inv(s(FC2_IN)), self.w2_sinv, self.y,
                      bias=self.b2, stream=stream)
             return self.y
+        self.w1_sinv = self.w1cache.cast(self.w1, st, s(FC1_W), is_first_microbatch, stream)
         fp8_gemm(self.q_ln, E4M3, self.qw1, E4M3, st.scale_inv(s(FC1_IN)), self.w1_sinv, self.h,
                  bias=self.b1, stream=stream)
         if seed:

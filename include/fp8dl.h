@@ -162,6 +162,29 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
                                      uint8_t *out_t, float *amax, float *scale_inv_out, float *dbias,
                                      void *workspace, size_t workspace_bytes, fp8dl_stream_t stream);
 
+/* Grouped cast: the casts of up to 8 tensors (say the two weights of a
+ * LayerNormMLP, or the weights of several layers) in one launch, so that the
+ * small tensors share one grid instead of each paying a launch, a ramp-up
+ * and a tail.  Per tensor the results are exactly those of
+ * fp8_cast_amax_transpose without dbias (§三.1 / §三.3: the cast with the
+ * stored scale records the tensor's amax).
+ *   items  HOST array of n items (1 <= n <= 8), each with its own x
+ *          [rows x cols], scale, outputs and amax, as in
+ *          fp8_cast_amax_transpose; all share x_dtype and out_dtype.
+ *   Argument errors of any item are reported before any launch. */
+typedef struct {
+    const void *x;          /* [rows x cols] of the call's x_dtype */
+    int64_t rows, cols;     /* positive multiples of 16 */
+    const float *scale;     /* device float */
+    uint8_t *out;           /* [rows x cols] codes, or NULL */
+    uint8_t *out_t;         /* [cols x rows] codes, or NULL */
+    float *amax;            /* device float, max-ed with max |x|, or NULL */
+    float *scale_inv_out;   /* device float receiving fl32(1 / *scale), or NULL */
+} fp8dl_cast_item;
+
+fp8dl_status fp8_cast_amax_transpose_multi(int32_t n, const fp8dl_cast_item *items, int32_t x_dtype,
+                                           int32_t out_dtype, fp8dl_stream_t stream);
+
 /* The same cast for callers that cannot allocate device memory.  The paper
  * has no counterpart to this call: it exists for callers that only hand the
  * library their input and output buffers (a plugin or custom-op interface

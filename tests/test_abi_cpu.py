@@ -80,6 +80,12 @@ def test_host_validation_without_gpu(lib):
     # bad dtype enums
     assert L.fp8_gemm(a16, 2, a16, 0, 16, 16, 16, a16, a16, None, 1, a16, 1, None, None) == lib.ERR_INVALID_ARG
     assert L.mxfp8_quantize(a16, 1, 48, 32, a16, a16, None, None, None, None, 0, None) == lib.ERR_SHAPE
+    # grouped cast: item count out of range, a ragged item (checked before any launch)
+    items = (lib.fp8dl_cast_item * 2)(lib.fp8dl_cast_item(a16, 32, 32, a16, a16, None, None, None),
+                                      lib.fp8dl_cast_item(a16, 40, 32, a16, a16, None, None, None))
+    assert L.fp8_cast_amax_transpose_multi(0, items, 1, 0, None) == lib.ERR_INVALID_ARG
+    assert L.fp8_cast_amax_transpose_multi(9, items, 1, 0, None) == lib.ERR_INVALID_ARG
+    assert L.fp8_cast_amax_transpose_multi(2, items, 1, 0, None) == lib.ERR_SHAPE
     # MX bias gradient without workspace
     assert L.mxfp8_quantize(a16, 1, 64, 32, a16, a16, None, None, a16, None, 0, None) == lib.ERR_WORKSPACE
     assert L.mxfp8_gemm(a16, a16, a16, a16, 32, 32, 48, None, 1, a16, 1, None, None) == lib.ERR_SHAPE

@@ -57,6 +57,66 @@ def test_cast_parity(shape, kind, fmt):
     assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= bound)
 
 
+@pytest.mark.parametrize("kind,fmt", [(torch.bfloat16, 0), (torch.float32, 1)])
+def test_grouped_cast_parity(kind, fmt):
+    """fp8_cast_amax_transpose_multi: several tensors of different (ragged) shapes and scales in
+    one launch; each tensor's codes, transposed codes, amax and decode factor bit-exact against
+    the oracle, and the outputs one item leaves out untouched."""
+    fd = _fd()
+    dev = gpu()
+    shapes = [(2048, 768), (16, 16), (400, 1040), (144, 272), (4096, 4096), (48, 80)]
+    items, ref = [], []
+    for k, shape in enumerate(shapes):
+        g = wl.generator(35, "multi/%d/%s/%d" % (k, kind, fmt))
+        x = wl.normal(shape, 10.0 ** (k - 3), g, kind)
+        xs = host(x)
+        scale_val = float(np.float32(oracle.fp8_max(fmt)) / oracle.amax(xs) / np.float32(1 + k))
+        rows, cols = shape
+        it = dict(x=x.to(dev), scale=torch.tensor([scale_val], dtype=torch.float32, device=dev),
+                  out=torch.full((rows, cols), 0xAA, dtype=torch.uint8, device=dev),
+                  out_t=torch.full((cols, rows), 0xAA, dtype=torch.uint8, device=dev) if k != 1 else None,
+                  amax=torch.zeros(1, dtype=torch.float32, device=dev) if k != 3 else None,
+                  scale_inv_out=torch.full((1,), float("nan"), dtype=torch.float32, device=dev) if k % 2 else None)
+        items.append(it)
+        ref.append((xs, scale_val))
+    fd.fp8_cast_amax_transpose_multi(items, fmt)
+    torch.cuda.synchronize()
+    for it, (xs, scale_val) in zip(items, ref):
+        q = oracle.quantize(fmt, xs, scale_val)
+        assert np.array_equal(it["out"].cpu().numpy(), q)
+        if it["out_t"] is not None:
+            assert np.array_equal(it["out_t"].cpu().numpy(), q.T)
+        if it["amax"] is not None:
+            assert it["amax"].item() == oracle.amax(xs)
+        if it["scale_inv_out"] is not None:
+            assert it["scale_inv_out"].item() == float(np.float32(1.0) / np.float32(scale_val))
+
+
+def test_grouped_cast_matches_single_casts():
+    """The grouped cast of two weights gives the bits of two separate casts (the LayerNormMLP
+    forward uses it for W1 and W2)."""
+    fd = _fd()
+    dev = gpu()
+    g = wl.generator(36, "multi-vs-single")
+    ws = [wl.normal((1024, 512), 0.02, g, torch.bfloat16).to(dev), wl.normal((512, 1024), 0.02, g, torch.bfloat16).to(dev)]
+    sc = [torch.tensor([4096.0], device=dev), torch.tensor([8192.0], device=dev)]
+    res = []
+    for grouped in (False, True):
+        outs = [(torch.empty_like(w, dtype=torch.uint8), torch.empty(w.shape[::-1], dtype=torch.uint8, device=dev),
+                 torch.zeros(1, device=dev), torch.empty(1, device=dev)) for w in ws]
+        if grouped:
+            fd.fp8_cast_amax_transpose_multi([dict(x=w, scale=s, out=o[0], out_t=o[1], amax=o[2], scale_inv_out=o[3])
+                                              for w, s, o in zip(ws, sc, outs)], fd.E4M3)
+        else:
+            for w, s, o in zip(ws, sc, outs):
+                fd.fp8_cast_amax_transpose(w, fd.E4M3, s, out=o[0], out_t=o[1], amax=o[2], scale_inv_out=o[3])
+        torch.cuda.synchronize()
+        res.append(outs)
+    for a, b in zip(*res):
+        for ta, tb in zip(a, b):
+            assert torch.equal(ta, tb)
+
+
 def test_cast_special_values():
     """NaN, infinities, overflow, fp32 subnormals and signed zeros through the hardware cvt."""
     dev = gpu()

@@ -33,6 +33,12 @@ def test_launch_counts_per_entry_point(monkeypatch):
     assert _count(fd, lambda: fd.fp8_cast_amax_transpose(x, fd.E4M3, sc, out=q, out_t=qt, amax=am)) == 1
     assert _count(fd, lambda: fd.fp8_cast_amax_transpose(x, fd.E4M3, sc, out=q, amax=am, dbias=db, workspace=ws,
                                                          scale_inv_out=sinv)) == 3  # cast, column sums, 1/scale
+    w2 = torch.empty((C, R), dtype=torch.bfloat16, device=dev).fill_(0.5)
+    q2 = torch.empty((C, R), dtype=torch.uint8, device=dev)
+    grouped = [dict(x=x, scale=sc, out=q, out_t=qt, amax=am), dict(x=w2, scale=sc, out=q2, amax=am)]
+    assert _count(fd, lambda: fd.fp8_cast_amax_transpose_multi(grouped, fd.E4M3)) == 1  # one grid for both
+    grouped[1]["scale_inv_out"] = sinv
+    assert _count(fd, lambda: fd.fp8_cast_amax_transpose_multi(grouped, fd.E4M3)) == 2  # + the decode factors
     gam = torch.ones(C, dtype=torch.bfloat16, device=dev)
     bet = torch.zeros(C, dtype=torch.bfloat16, device=dev)
     mu = torch.empty(R, device=dev)
