@@ -231,12 +231,14 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
                 const int64_t n0 = tn * BN + c * 32;
                 if (row_ok && n0 < args.N) {
                     float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; j++) v[j] = __fmul_rn(__uint_as_float(r[j]), s);  // not fused with + bias
-                    if (args.bias_dtype >= 0) {
+                    if (args.bias_dtype >= 0) {  // acc * s + bias with one rounding, as in the pair kernel
 #pragma unroll
                         for (int j = 0; j < 32; j++)
-                            if (n0 + j < args.N) v[j] += load_bias(args.bias, args.bias_dtype, n0 + j);
+                            v[j] = __fmaf_rn(__uint_as_float(r[j]), s,
+                                             n0 + j < args.N ? load_bias(args.bias, args.bias_dtype, n0 + j) : 0.0f);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j++) v[j] = __fmul_rn(__uint_as_float(r[j]), s);
                     }
                     if (args.d_dtype == FP8DL_BF16) {
                         __nv_bfloat16 *drow = static_cast<__nv_bfloat16 *>(args.D) + row * args.N + n0;
@@ -537,9 +539,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     load_bias32(args.bias, args.bias_dtype, n0, args.N, b);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {  // two roundings, two columns per instruction
+                    for (int j = 0; j < 32; j += 2) {  // acc * s + bias, one rounding, two columns per instruction
                         const float2 a = make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
-                        const float2 y = __fadd2_rn(__fmul2_rn(a, f2(sc)), make_float2(b[j], b[j + 1]));
+                        const float2 y = __ffma2_rn(a, f2(sc), make_float2(b[j], b[j + 1]));
                         v[j] = y.x;
                         v[j + 1] = y.y;
                     }

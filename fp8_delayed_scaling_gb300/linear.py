@@ -12,6 +12,7 @@ base+1 weight (E4M3), base+2 grad_output (E5M2 in HYBRID, else E4M3).
 
 Per step, for D = X W^T + b with X [M x K], W [N x K]:
   forward   cast X -> qX (+ qX^T for wgrad), cast W -> qW (+ qW^T for dgrad)
+            (one grouped launch for both)
             Y[M,N]  = fp8_gemm(qX, qW)            * sx_inv * sw_inv + b
   backward  cast dY -> qdY, qdY^T (+ db = column sums of dY)
             dX[M,K] = fp8_gemm(qdY, qW^T)        * sdy_inv * sw_inv
@@ -170,9 +171,22 @@ class Fp8Linear:
                      stream=stream)
             return self.y
         self.wcache.check(is_first_microbatch)
-        fp8_cast_amax_transpose(x, E4M3, st.scale(self.slot(IN)), out=self.qx, out_t=self.qxT if tr else None,
-                                amax=st.amax(self.slot(IN)), stream=stream)
-        self.w_sinv = self.wcache.cast(self.w, st, self.slot(WEIGHT), is_first_microbatch, stream)
+        x_item = dict(x=x, scale=st.scale(self.slot(IN)), out=self.qx, out_t=self.qxT if tr else None,
+                      amax=st.amax(self.slot(IN)))
+        if is_first_microbatch is not False and x.dtype == self.w.dtype:
+            # input and weight in one grouped cast
+            keep = bool(is_first_microbatch)
+            c = self.wcache
+            fp8_cast_amax_transpose_multi([x_item, dict(x=self.w, scale=st.scale(self.slot(WEIGHT)), out=c.q,
+                                                        out_t=c.q_t, amax=st.amax(self.slot(WEIGHT)),
+                                                        scale_inv_out=c.scale_inv if keep else None)],
+                                          E4M3, stream=stream)
+            c.valid = keep
+            self.w_sinv = c.scale_inv if keep else st.scale_inv(self.slot(WEIGHT))
+        else:
+            fp8_cast_amax_transpose(x, E4M3, x_item["scale"], out=self.qx, out_t=x_item["out_t"],
+                                    amax=x_item["amax"], stream=stream)
+            self.w_sinv = self.wcache.cast(self.w, st, self.slot(WEIGHT), is_first_microbatch, stream)
         fp8_gemm(self.qx, E4M3, self.qw, E4M3, st.scale_inv(self.slot(IN)), self.w_sinv, self.y, bias=self.b,
                  stream=stream)
         return self.y

@@ -219,6 +219,7 @@ fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x_dtype, int
  * FP8 GEMM with dequantising epilogue (§三.3 fp8_gemm; §三.4 high-precision
  * output, dims multiple of 16):
  *   D[m,n] = round_d( acc[m,n] * fl32(a_scale_inv * b_scale_inv) + bias[n] )
+ *   (the product and the bias add are one fp32 fused multiply-add)
  *   acc[m,n] = sum_k A[m,k] * B[n,k] on the tcgen05 tensor cores, fp32 accumulate.
  *   A [M x K] codes of a_dtype, B [N x K] codes of b_dtype (E4M3/E5M2 mixed ok)
  *   a_scale_inv, b_scale_inv   device floats (the operands' slots' scale_inv)
