@@ -95,12 +95,13 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
 //   - the row partials of block j+1 are reduced over the CTA and pushed with
 //     st.async into exchange slot (j+1) mod 4 of every CTA of the cluster
 //     (this CTA's entry of each), completing on that CTA's slot barrier;
-//   - warp 0 waits on its own slot barrier for block j (pushed one iteration
-//     earlier), merges the CTAs' partials in rank order, re-arms the barrier
-//     for block j+4, and block j is normalised and written.
-// The forward gathers block j while the other warps reduce block j+1 (one
-// barrier publishes both); the backward, with shorter blocks, pushes block
-// j+1 first so that block j's pushes have longer to arrive.
+//   - the CTA waits on its own slot barrier for block j (pushed one iteration
+//     earlier), merges the CTAs' partials, re-arms the barrier for block j+4,
+//     and block j is normalised and written.
+// The forward reduces block j+1 and then gathers block j, spreading the merge
+// over all threads (one barrier publishes both); the backward, with shorter
+// blocks, pushes block j+1 first so that block j's pushes have longer to
+// arrive, and warp 0 merges.
 // The exchange's latency is thus hidden behind a whole block's work, and no
 // cluster-wide barrier or release fence (which would also wait for the
 // previous block's global stores) sits in the loop.  Slots rotate over four
@@ -169,42 +170,29 @@ __device__ __forceinline__ float2 chan_equal(float2 a, float2 b, float half_n) {
     return make_float2((a.x + b.x) * 0.5f, (a.y + b.y) + d * d * half_n);
 }
 
-// Reduce-scatter of the (mean, M2) of 16 rows over the 16 lanes of a warp with
-// the same parity, each lane starting from its own 4 values per row: lane l
-// returns row 8*b4 + 4*b3 + 2*b2 + b1 (b = bits of l) merged over those 16
-// lanes (64 values).  Halving exchanges: each level sends the half of the rows
-// the partner keeps.
-__device__ __forceinline__ float2 warp_chan_rows16(const float2 (&s)[16], int lane) {
-    const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4, u1 = lane & 2;
-    float2 k8[8], k4[4], k2[2];
-#pragma unroll
-    for (int i = 0; i < 8; i++) {
-        const float2 send = u4 ? s[i] : s[i + 8], keep = u4 ? s[i + 8] : s[i];
-        k8[i] = chan_equal(keep, shfl_xor2(send, 16), 2.0f);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const float2 send = u3 ? k8[i] : k8[i + 4], keep = u3 ? k8[i + 4] : k8[i];
-        k4[i] = chan_equal(keep, shfl_xor2(send, 8), 4.0f);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; i++) {
-        const float2 send = u2 ? k4[i] : k4[i + 2], keep = u2 ? k4[i + 2] : k4[i];
-        k2[i] = chan_equal(keep, shfl_xor2(send, 4), 8.0f);
-    }
-    const float2 send = u1 ? k2[0] : k2[1], keep = u1 ? k2[1] : k2[0];
-    return chan_equal(keep, shfl_xor2(send, 2), 16.0f);
+// |a| and |b| maxima of two bf16x2 words, lane by lane (the sign bits of the
+// result are the XOR of the inputs' and carry no meaning; a NaN input is
+// ignored, as fmaxf ignores it).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// LayerNorm forward + cast.  Thread t holds columns 4*(t >> 1) .. +3 of the
-// CTA's slab for rows 16*(t & 1) .. +15 of the block, so the transposed codes of
-// a column leave a lane pair as one full 32-byte segment (two 16-byte stores).
-// Statistics: each thread takes the mean and M2 of its 4 values of a row; the
-// lanes of equal parity, the eight warps and the cluster's slabs (in rank order, general equal-count form
+// LayerNorm forward + cast.  Warp w covers columns 64w .. 64w+63 of the CTA's
+// slab; lane (rg = lane >> 2, cg = lane & 3) holds columns 64w + 16cg .. +15 of
+// rows 4rg .. 4rg+3 of the 32-row block.  In shared memory the 16-byte chunk
+// ch of row r sits at chunk ch ^ ((r >> 2) & 7) of its row, so the two chunk
+// loads of a lane's row hit every bank group four times per warp.
+// Statistics: each lane takes the mean and M2 of its 16 values of a row (two
+// passes over registers); the four lanes of a row group, the eight warps and
+// the cluster's slabs (in rank order, general equal-count form
 // M2 = sum_k M2_k + n sum_k (m_k - mean)^2) are merged; var = M2 / cols,
 // rs = 1/sqrt(var + eps).  Every CTA then normalises its slab:
 // y = bf16((x - mu) * rs * gamma + beta), codes = cvt(y * scale), written
-// row-major (out) and transposed (out_t).
+// row-major (out: 16 bytes per lane and row) and transposed (out_t: the four
+// rows of a column are one 4-byte word, and the eight row groups of a warp
+// fill one 32-byte segment).
 template <int FMT>
 __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma, const uint16_t *__restrict__ beta,
@@ -212,14 +200,15 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     uint8_t *__restrict__ out_t, float *__restrict__ amax_p, float *__restrict__ mu_out, float *__restrict__ rs_out,
     uint16_t *__restrict__ y) {
     extern __shared__ __align__(128) uint8_t lsm[];      // [LC_NBUF][LF_ROWS][LC_COLS] bf16, then the slots
-    __shared__ float2 wst[LC_WARPS][2][16];              // per-warp (mean, M2) of 64 values of a row
+    __shared__ float2 wst[LC_WARPS][LF_ROWS + 1];        // per-warp (mean, M2) of 64 values of a row
     __shared__ __align__(8) uint64_t xbar[LC_SLOTS];     // slot s complete: every CTA's slabs of its block arrived
     __shared__ float2 stat[LF_ROWS];                     // mean, rsigma
     __shared__ float wmax[LC_WARPS];
     const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-    const int cq = t >> 1, h = t & 1;
+    const int rg = lane >> 2, cg = lane & 3;
+    const int c0 = 8 * w + 2 * cg;  // the lane's first 16-byte chunk of a row (of 64)
     const uint32_t rank = cluster_ctarank(), ncta = cluster_nctarank();
-    const int64_t col0 = (int64_t)rank * LC_COLS, col = col0 + 4 * cq;
+    const int64_t col0 = (int64_t)rank * LC_COLS, col = col0 + 8 * c0;
     const int64_t nblk = (rows + LF_ROWS - 1) / LF_ROWS;
     const int64_t cid = blockIdx.x / ncta, ncl = gridDim.x / ncta;
     const int64_t nb = cid < nblk ? (nblk - cid + ncl - 1) / ncl : 0;  // this cluster's blocks
@@ -227,55 +216,124 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     const uint32_t push_bytes = ncta * LF_ROWS * (uint32_t)sizeof(float2);  // per slot and block
     const float scale = (out || out_t) ? __ldg(scale_p) : 1.0f;
     const float2 sc2 = make_float2(scale, scale);
-    const uint2 gv = __ldg(reinterpret_cast<const uint2 *>(gamma + col));
-    const uint2 bv = __ldg(reinterpret_cast<const uint2 *>(beta + col));
-    const float2 g2[2] = {bf16x2_f2(gv.x), bf16x2_f2(gv.y)}, b2[2] = {bf16x2_f2(bv.x), bf16x2_f2(bv.y)};
-    // Copy block j into buffer `buf`: 32 rows x 64 chunks of 16 bytes, 8 per thread, a warp per row segment.
+    uint8_t *const out_tb = out_t ? out_t + col * rows + 4 * rg : nullptr;  // plus r0: the lane's first out_t word
+    float2 g2[8], b2[8];
+    {
+        const uint4 ga = __ldg(reinterpret_cast<const uint4 *>(gamma + col));
+        const uint4 gb = __ldg(reinterpret_cast<const uint4 *>(gamma + col + 8));
+        const uint4 ba = __ldg(reinterpret_cast<const uint4 *>(beta + col));
+        const uint4 bb = __ldg(reinterpret_cast<const uint4 *>(beta + col + 8));
+        const uint32_t gw[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+        const uint32_t bw[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            g2[q] = bf16x2_f2(gw[q]);
+            b2[q] = bf16x2_f2(bw[q]);
+        }
+    }
+    // Copy block j into buffer `buf`: 32 rows x 64 chunks of 16 bytes, 8 per thread (rows
+    // t/64 + 4i, chunk t % 64), a warp per half row; chunk ch of row r goes to chunk
+    // ch ^ ((r >> 2) & 7), which is ch ^ i here.
+    const int crow = t >> 6, cch = t & 63;
+    const uint16_t *xsrc = x + (int64_t)crow * cols + col0 + 8 * cch;
+    const uint32_t sdst = smem_u32(lsm) + (crow * LC_COLS) * 2;
     auto issue = [&](int64_t j, int buf) {
         if (j < nb) {
             const int64_t r0 = (cid + j * ncl) * LF_ROWS;
+            const uint16_t *src = xsrc + r0 * cols;
+            const int64_t lim = rows - r0 - crow;  // copy i is valid while 4i < lim
+            const uint32_t dst = sdst + buf * LF_BUF;
+#pragma unroll
             for (int i = 0; i < 8; i++) {
-                const int k = t + LC_THREADS * i, r = k >> 6, ch = k & 63;
-                const int64_t row = r0 + r;
-                const bool valid = row < rows;
-                cp_async16(smem_u32(lsm + buf * LF_BUF + (r * LC_COLS + 8 * ch) * 2),
-                           valid ? x + row * cols + col0 + 8 * ch : x, valid);
+                const bool valid = 4 * i < lim;
+                cp_async16(dst + i * 4 * LC_COLS * 2 + 16 * (cch ^ i), valid ? src + 4 * i * cols : x, valid);
             }
         }
         cp_async_commit();  // possibly empty: one group per block keeps the wait counts uniform
     };
-    // this thread's 4 values of row i of its half, as two bf16x2 words
-    auto xrow = [&](int buf, int i) {
-        return *reinterpret_cast<const uint2 *>(lsm + buf * LF_BUF + ((16 * h + i) * LC_COLS + 4 * cq) * 2);
+    // the lane's 16 values of row 4rg + i, as eight bf16x2 words
+    const uint8_t *xl0 = lsm + 4 * rg * LC_COLS * 2 + 16 * (c0 ^ rg), *xl1 = lsm + 4 * rg * LC_COLS * 2 + 16 * ((c0 + 1) ^ rg);
+    auto xrow = [&](int buf, int i, uint32_t (&v)[8]) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(xl0 + buf * LF_BUF + i * LC_COLS * 2);
+        const uint4 b = *reinterpret_cast<const uint4 *>(xl1 + buf * LF_BUF + i * LC_COLS * 2);
+        v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
     };
     // Per-warp (mean, M2) of the staged block in `buf`, into wst.
     auto partials = [&](int buf) {
-        float2 st[16];
+        float2 s[4];
 #pragma unroll
-        for (int i = 0; i < 16; i++) {
-            const uint2 q = xrow(buf, i);
-            const float2 v0 = bf16x2_f2(q.x), v1 = bf16x2_f2(q.y);
-            const float2 s = __fadd2_rn(v0, v1);
-            const float m = (s.x + s.y) * 0.25f;
+        for (int i = 0; i < 4; i++) {
+            uint32_t q[8];
+            xrow(buf, i, q);
+            float2 v[8];
+#pragma unroll
+            for (int k = 0; k < 8; k++) v[k] = bf16x2_f2(q[k]);
+            const float2 s01 = __fadd2_rn(__fadd2_rn(v[0], v[1]), __fadd2_rn(v[2], v[3]));
+            const float2 s23 = __fadd2_rn(__fadd2_rn(v[4], v[5]), __fadd2_rn(v[6], v[7]));
+            const float2 sum = __fadd2_rn(s01, s23);
+            const float m = (sum.x + sum.y) * 0.0625f;
             const float2 nm = make_float2(-m, -m);
-            const float2 d0 = __fadd2_rn(v0, nm), d1 = __fadd2_rn(v1, nm);
-            const float2 m2 = __ffma2_rn(d1, d1, __fmul2_rn(d0, d0));
-            st[i] = make_float2(m, m2.x + m2.y);
-        }
-        wst[w][h][lane >> 1] = warp_chan_rows16(st, lane);  // row 8*b4 + 4*b3 + 2*b2 + b1 of half h
-    };
-    // After a barrier: the slab (mean, M2) of each row from the eight warps, pushed into slot
-    // `slot` of every CTA of the cluster (this CTA's entry), completing on that CTA's barrier.
-    auto push = [&](int slot) {
-        if (t < LF_ROWS) {
-            const int hh = t >> 4, ri = t & 15;  // the row's half, row within it
-            float2 q[4];
+            float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int k = 0; k < 4; k++) q[k] = chan_equal(wst[2 * k][hh][ri], wst[2 * k + 1][hh][ri], 32.0f);
-            const float2 v = chan_equal(chan_equal(q[0], q[1], 64.0f), chan_equal(q[2], q[3], 64.0f), 128.0f);
-            const uint32_t la = smem_u32(&gath[(slot * ncta + rank) * LF_ROWS + t]), lb = smem_u32(&xbar[slot]);
-            for (uint32_t k = 0; k < ncta; k++) st_async_f2(mapa_shared(la, k), v, mapa_shared(lb, k));
+            for (int k = 0; k < 8; k++) {
+                const float2 d = __fadd2_rn(v[k], nm);
+                acc = __ffma2_rn(d, d, acc);
+            }
+            s[i] = make_float2(m, acc.x + acc.y);
         }
+        // reduce-scatter over the four lanes of the row group: lane bit 0, then bit 1
+        const bool u1 = lane & 1, u2 = lane & 2;
+        float2 k2[2];
+#pragma unroll
+        for (int i = 0; i < 2; i++) {
+            const float2 send = u1 ? s[i] : s[i + 2], keep = u1 ? s[i + 2] : s[i];
+            k2[i] = chan_equal(keep, shfl_xor2(send, 1), 8.0f);
+        }
+        const float2 send = u2 ? k2[0] : k2[1], keep = u2 ? k2[1] : k2[0];
+        wst[w][4 * rg + 2 * u1 + u2] = chan_equal(keep, shfl_xor2(send, 2), 16.0f);
+    };
+    // The exchange is spread over all threads: thread t serves row gr = t / 8 of the block and
+    // the slabs (warps, then cluster ranks) gk = t % 8 and gk + 8; the eight threads of a row
+    // merge by butterfly, which leaves the same bits in each of them.
+    const int gr = t >> 3, gk = t & 7;
+    // After a barrier: the CTA's (mean, M2) of row gr, merged over the eight warps, pushed into
+    // slot `slot` of every CTA of the cluster (this CTA's entry), completing on that CTA's barrier.
+    auto push = [&](int slot) {
+        float2 v = wst[gk][gr];
+        v = chan_equal(v, shfl_xor2(v, 1), 32.0f);
+        v = chan_equal(v, shfl_xor2(v, 2), 64.0f);
+        v = chan_equal(v, shfl_xor2(v, 4), 128.0f);
+        const uint32_t la = smem_u32(&gath[(slot * ncta + rank) * LF_ROWS + gr]), lb = smem_u32(&xbar[slot]);
+        for (uint32_t k = gk; k < ncta; k += 8) st_async_f2(mapa_shared(la, k), v, mapa_shared(lb, k));
+    };
+    // Statistics of block j (row gr) from every CTA's slab in slot `slot`: mean = sum_k m_k / ncta,
+    // M2 = sum_k (M2_k + LC_COLS (m_k - mean)^2).  A wait that runs out leaves NaN statistics.
+    auto gather = [&](int64_t j, int slot) {
+        const bool arrived = mbar_wait_bounded(smem_u32(&xbar[slot]), (uint32_t)((j / LC_SLOTS) & 1));
+        const bool ha = gk < (int)ncta, hb = gk + 8 < (int)ncta;
+        const float2 pa = ha ? gath[(slot * ncta + gk) * LF_ROWS + gr] : make_float2(0.0f, 0.0f);
+        const float2 pb = hb ? gath[(slot * ncta + gk + 8) * LF_ROWS + gr] : make_float2(0.0f, 0.0f);
+        float sm = arrived ? pa.x + pb.x : __int_as_float(0x7fc00000);
+        sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+        sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+        sm += __shfl_xor_sync(0xffffffffu, sm, 4);
+        const float mean = sm / (float)ncta;
+        const float da = pa.x - mean, db = pb.x - mean;
+        float m2 = (ha ? pa.y + da * da * (float)LC_COLS : 0.0f) + (hb ? pb.y + db * db * (float)LC_COLS : 0.0f);
+        m2 += __shfl_xor_sync(0xffffffffu, m2, 1);
+        m2 += __shfl_xor_sync(0xffffffffu, m2, 2);
+        m2 += __shfl_xor_sync(0xffffffffu, m2, 4);
+        if (gk == 0) {
+            const int64_t r0 = (cid + j * ncl) * LF_ROWS;
+            const float rsig = 1.0f / sqrtf(m2 / (float)cols + eps);
+            stat[gr] = make_float2(mean, rsig);
+            if (rank == 0 && r0 + gr < rows) {
+                mu_out[r0 + gr] = mean;
+                rs_out[r0 + gr] = rsig;
+            }
+        }
+        // the slot's next block: its barrier counts the pushes of block j + LC_SLOTS
+        if (t == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
     };
     if (t == 0) {
         for (int k = 0; k < LC_SLOTS; k++) mbar_init(smem_u32(&xbar[k]), 1);
@@ -284,7 +342,7 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     cluster_sync();  // every CTA's barriers are initialised before anything is pushed to them
     if (t == 0)
         for (int k = 0; k < LC_SLOTS && k < nb; k++) mbar_expect_tx(smem_u32(&xbar[k]), push_bytes);
-    float amax = 0.0f;
+    uint32_t amax2 = 0;  // bf16x2 running |y| maxima
     if (nb > 0) {  // always, as no more clusters than blocks are launched
         issue(0, 0);
         issue(1, 1);
@@ -301,71 +359,54 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
         cp_async_wait<0>();  // this thread's copies of block j+1 have landed (the only group in flight)
         __syncthreads();     // ... everyone's; and every thread is past block j-1, whose buffer is refilled now
         issue(j + 2, next_buf(next_buf(buf)));
-        // warp 0 gathers block j (pushed during the previous iteration) while every warp
-        // reduces block j+1; one barrier publishes both, then warp 0 pushes block j+1
-        if (t < LF_ROWS) {
-            // every CTA's slab of block j has arrived (a wait that runs out leaves NaN statistics)
-            const bool arrived = mbar_wait_bounded(smem_u32(&xbar[slot]), (uint32_t)((j / LC_SLOTS) & 1));
-            float2 p[LC_MAX_CLUSTER];
-#pragma unroll
-            for (int k = 0; k < LC_MAX_CLUSTER; k++)
-                if (k < (int)ncta) p[k] = gath[(slot * ncta + k) * LF_ROWS + t];
-            float sm = arrived ? 0.0f : __int_as_float(0x7fc00000);
-#pragma unroll
-            for (int k = 0; k < LC_MAX_CLUSTER; k++)
-                if (k < (int)ncta) sm += p[k].x;
-            const float mean = sm / (float)ncta;
-            float m2 = 0.0f;
-#pragma unroll
-            for (int k = 0; k < LC_MAX_CLUSTER; k++)
-                if (k < (int)ncta) {
-                    const float d = p[k].x - mean;
-                    m2 += p[k].y + d * d * (float)LC_COLS;
-                }
-            const float rsig = 1.0f / sqrtf(m2 / (float)cols + eps);
-            stat[t] = make_float2(mean, rsig);
-            if (rank == 0 && r0 + t < rows) {
-                mu_out[r0 + t] = mean;
-                rs_out[r0 + t] = rsig;
-            }
-            // the slot's next block: its barrier counts the pushes of block j + LC_SLOTS
-            if (t == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
-        }
+        // every warp reduces block j+1, then gathers block j (pushed during the previous
+        // iteration); one barrier publishes both, then block j+1 is pushed
         if (j + 1 < nb) partials(next_buf(buf));
+        gather(j, slot);
         __syncthreads();
         if (j + 1 < nb) push(nslot);
-        if (r0 + 16 * h < rows) {  // rows are a multiple of 16: a half is all in or all out
-            uint32_t codes[16];
+        if (r0 + 4 * rg < rows) {  // rows are a multiple of 16: a row group is all in or all out
+            const int64_t rowoff = (r0 + 4 * rg) * cols + col;  // of this lane's first element
+            uint32_t codes[4][4];  // [row][column quad]
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const float2 sr = stat[16 * h + i];
+            for (int i = 0; i < 4; i++) {
+                const float2 sr = stat[4 * rg + i];
                 const float2 nmu = make_float2(-sr.x, -sr.x), rs2 = make_float2(sr.y, sr.y);
-                const uint2 q = xrow(buf, i);
-                const int64_t row = r0 + 16 * h + i;
-                // y = bf16((x - mu) * rs * gamma + beta), two at a time
-                const uint32_t y0 = f2_bf16x2(__ffma2_rn(__fmul2_rn(__fadd2_rn(bf16x2_f2(q.x), nmu), rs2), g2[0], b2[0]));
-                const uint32_t y1 = f2_bf16x2(__ffma2_rn(__fmul2_rn(__fadd2_rn(bf16x2_f2(q.y), nmu), rs2), g2[1], b2[1]));
-                const float2 yr0 = bf16x2_f2(y0), yr1 = bf16x2_f2(y1);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(yr0.x), fabsf(yr0.y)), fmaxf(fabsf(yr1.x), fabsf(yr1.y))));
-                if (y) *reinterpret_cast<uint2 *>(y + row * cols + col) = make_uint2(y0, y1);
-                const float2 ys0 = __fmul2_rn(yr0, sc2), ys1 = __fmul2_rn(yr1, sc2);
-                codes[i] = pack4<FMT>(ys0.x, ys0.y, ys1.x, ys1.y);
-                if (out) *reinterpret_cast<uint32_t *>(out + row * cols + col) = codes[i];
-            }
-            if (out_t) {
-                uint32_t colw[4][4];  // colw[jj][k]: rows 4k..4k+3 of column 4*cq + jj
+                uint32_t q[8], yw[8];
+                xrow(buf, i, q);
 #pragma unroll
-                for (int k = 0; k < 4; k++) {
-                    const uint32_t wr[4] = {codes[4 * k], codes[4 * k + 1], codes[4 * k + 2], codes[4 * k + 3]};
-                    uint32_t cw[4];
-                    transpose4x4_bytes(wr, cw);
-#pragma unroll
-                    for (int jj = 0; jj < 4; jj++) colw[jj][k] = cw[jj];
+                for (int k = 0; k < 8; k++) {
+                    // y = bf16((x - mu) * rs * gamma + beta), two at a time
+                    yw[k] = f2_bf16x2(__ffma2_rn(__fmul2_rn(__fadd2_rn(bf16x2_f2(q[k]), nmu), rs2), g2[k], b2[k]));
+                    amax2 = bf16x2_absmax(amax2, yw[k]);
+                }
+                if (y) {
+                    uint4 *yp = reinterpret_cast<uint4 *>(y + rowoff + i * cols);
+                    yp[0] = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+                    yp[1] = make_uint4(yw[4], yw[5], yw[6], yw[7]);
                 }
 #pragma unroll
-                for (int jj = 0; jj < 4; jj++)
-                    *reinterpret_cast<uint4 *>(out_t + (col + jj) * rows + r0 + 16 * h) =
-                        make_uint4(colw[jj][0], colw[jj][1], colw[jj][2], colw[jj][3]);
+                for (int k = 0; k < 4; k++) {
+                    const float2 ya = __fmul2_rn(bf16x2_f2(yw[2 * k]), sc2), yb = __fmul2_rn(bf16x2_f2(yw[2 * k + 1]), sc2);
+                    codes[i][k] = pack4<FMT>(ya.x, ya.y, yb.x, yb.y);
+                }
+                if (out)
+                    *reinterpret_cast<uint4 *>(out + rowoff + i * cols) =
+                        make_uint4(codes[i][0], codes[i][1], codes[i][2], codes[i][3]);
+            }
+            if (out_t) {
+                uint8_t *ot = out_tb + r0;  // column `col`, row r0 + 4rg
+#pragma unroll
+                for (int k = 0; k < 4; k++) {
+                    const uint32_t wr[4] = {codes[0][k], codes[1][k], codes[2][k], codes[3][k]};
+                    uint32_t cw[4];  // cw[jj]: rows 4rg .. 4rg+3 of column 4k + jj
+                    transpose4x4_bytes(wr, cw);
+#pragma unroll
+                    for (int jj = 0; jj < 4; jj++) {
+                        *reinterpret_cast<uint32_t *>(ot) = cw[jj];
+                        ot += rows;
+                    }
+                }
             }
         }
         buf = next_buf(buf);
@@ -373,7 +414,7 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     }
     cp_async_wait<0>();
     if (amax_p) {
-        const float m = warp_max(amax);
+        const float m = warp_max(fmaxf(fabsf(bf16_lo(amax2)), fabsf(bf16_hi(amax2))));
         if (lane == 0) wmax[w] = m;
         __syncthreads();
         if (t == 0) {
