@@ -88,9 +88,10 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
     const int64_t tiles_c = (cols + CT_COLS - 1) / CT_COLS;
     const int64_t r0 = (tile / tiles_c) * CT_ROWS, c0 = (tile % tiles_c) * CT_COLS;
     const bool p1_ok = (r0 + 4 * rb < rows) && (c0 + 16 * cb < cols);
-    float csum[16];
+    float2 csum[8];  // column sums for dbias: columns 16cb + 2k, +1 in csum[k]
 #pragma unroll
-    for (int j = 0; j < 16; j++) csum[j] = 0.0f;
+    for (int k = 0; k < 8; k++) csum[k] = make_float2(0.0f, 0.0f);
+    uint32_t amax2 = 0;  // bf16x2 running |x| maxima (plain bf16 casts)
     if (p1_ok) {
         RowSeg16<XKIND> seg[4];
         RowSeg16<XKIND> hseg[OP == OP_DGELU ? 4 : 1];
@@ -126,35 +127,58 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
             const int r = 4 * rb + i;
 #pragma unroll
             for (int hh = 0; hh < 2; hh++) {  // two halves of 8 elements
-                float v[8];
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    float xv = seg[i].get(8 * hh + j);
-                    if (OP == OP_GELU) xv = gelu_bf16(xv);
-                    if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(8 * hh + j));
-                    if (OP == OP_LAYERNORM) {
-                        const int k = 8 * hh + j;  // y = bf16((x - mu) * rs * gamma + beta)
-                        const float gk = (k & 1) ? bf16_hi(ln_g[k >> 1]) : bf16_lo(ln_g[k >> 1]);
-                        const float bk = (k & 1) ? bf16_hi(ln_b[k >> 1]) : bf16_lo(ln_b[k >> 1]);
-                        xv = bf16_round(fmaf((xv - ln_mu[i]) * ln_rs[i], gk, bk));
-                    }
-                    v[j] = xv;
-                    amax = fmaxf(amax, fabsf(xv));
-                    if (OP == OP_NONE || OP == OP_DGELU) csum[8 * hh + j] += xv;  // dbias only there
-                }
-                w[2 * hh] = pack4<FMT>(__fmul_rn(v[0], scale), __fmul_rn(v[1], scale), __fmul_rn(v[2], scale),
-                                       __fmul_rn(v[3], scale));
-                w[2 * hh + 1] = pack4<FMT>(__fmul_rn(v[4], scale), __fmul_rn(v[5], scale),
-                                           __fmul_rn(v[6], scale), __fmul_rn(v[7], scale));
-                if (OP != OP_NONE && pre_out) {
-                    uint32_t pw[4];
+                if constexpr (XKIND == FP8DL_BF16 && OP == OP_NONE) {
+                    // plain bf16 cast, two elements per instruction: |x| maxima on the bf16x2
+                    // words, fp32 products x * scale, column sums
+                    const uint4 q = seg[i].v[hh];
+                    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+                    const float2 sc2 = make_float2(scale, scale);
+                    float2 f[4];
 #pragma unroll
                     for (int p = 0; p < 4; p++) {
-                        __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * p], v[2 * p + 1]);
-                        pw[p] = *reinterpret_cast<uint32_t *>(&b2);
+                        amax2 = bf16x2_absmax(amax2, qw[p]);
+                        f[p] = make_float2(bf16_lo(qw[p]), bf16_hi(qw[p]));
+                        if (ws) csum[4 * hh + p] = __fadd2_rn(csum[4 * hh + p], f[p]);
+                        f[p] = __fmul2_rn(f[p], sc2);
                     }
-                    *reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb + 8 * hh) =
-                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    w[2 * hh] = pack4<FMT>(f[0].x, f[0].y, f[1].x, f[1].y);
+                    w[2 * hh + 1] = pack4<FMT>(f[2].x, f[2].y, f[3].x, f[3].y);
+                } else {
+                    float v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        float xv = seg[i].get(8 * hh + j);
+                        if (OP == OP_GELU) xv = gelu_bf16(xv);
+                        if (OP == OP_DGELU) xv = dgelu_bf16(xv, hseg[OP == OP_DGELU ? i : 0].get(8 * hh + j));
+                        if (OP == OP_LAYERNORM) {
+                            const int k = 8 * hh + j;  // y = bf16((x - mu) * rs * gamma + beta)
+                            const float gk = (k & 1) ? bf16_hi(ln_g[k >> 1]) : bf16_lo(ln_g[k >> 1]);
+                            const float bk = (k & 1) ? bf16_hi(ln_b[k >> 1]) : bf16_lo(ln_b[k >> 1]);
+                            xv = bf16_round(fmaf((xv - ln_mu[i]) * ln_rs[i], gk, bk));
+                        }
+                        v[j] = xv;
+                        amax = fmaxf(amax, fabsf(xv));
+                        if (OP == OP_NONE || OP == OP_DGELU) {  // dbias only there
+                            if (j & 1)
+                                csum[4 * hh + (j >> 1)].y += xv;
+                            else
+                                csum[4 * hh + (j >> 1)].x += xv;
+                        }
+                    }
+                    w[2 * hh] = pack4<FMT>(__fmul_rn(v[0], scale), __fmul_rn(v[1], scale), __fmul_rn(v[2], scale),
+                                           __fmul_rn(v[3], scale));
+                    w[2 * hh + 1] = pack4<FMT>(__fmul_rn(v[4], scale), __fmul_rn(v[5], scale),
+                                               __fmul_rn(v[6], scale), __fmul_rn(v[7], scale));
+                    if (OP != OP_NONE && pre_out) {
+                        uint32_t pw[4];
+#pragma unroll
+                        for (int p = 0; p < 4; p++) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * p], v[2 * p + 1]);
+                            pw[p] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(pre_out + (r0 + r) * cols + c0 + 16 * cb + 8 * hh) =
+                            make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    }
                 }
             }
             const uint4 codes = make_uint4(w[0], w[1], w[2], w[3]);
@@ -162,19 +186,25 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
             if (out_t) *reinterpret_cast<uint4 *>(stage + stage_off(r, cb)) = codes;
         }
     }
+    if constexpr (XKIND == FP8DL_BF16 && OP == OP_NONE)
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(amax2)), fabsf(bf16_hi(amax2))));
     if (ws) {
         // lanes l, l+8, l+16, l+24 share a column block: reduce over them, then lanes 0-7
         // hold the warp's 16-row partial of columns 16*cb .. 16*cb+15
 #pragma unroll
-        for (int j = 0; j < 16; j++) {
-            csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 8);
-            csum[j] += __shfl_xor_sync(0xffffffffu, csum[j], 16);
+        for (int k = 0; k < 8; k++) {
+#pragma unroll
+            for (int o = 8; o <= 16; o <<= 1) {
+                const float2 p = make_float2(__shfl_xor_sync(0xffffffffu, csum[k].x, o),
+                                             __shfl_xor_sync(0xffffffffu, csum[k].y, o));
+                csum[k] = __fadd2_rn(csum[k], p);
+            }
         }
         if (lane < 8) {
             float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
 #pragma unroll
             for (int j = 0; j < 4; j++)
-                dst[j] = make_float4(csum[4 * j], csum[4 * j + 1], csum[4 * j + 2], csum[4 * j + 3]);
+                dst[j] = make_float4(csum[2 * j].x, csum[2 * j].y, csum[2 * j + 1].x, csum[2 * j + 1].y);
         }
     }
     if (out_t || ws) __syncthreads();

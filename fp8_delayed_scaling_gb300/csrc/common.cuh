@@ -89,6 +89,15 @@ __device__ __forceinline__ uint32_t pack4(float v0, float v1, float v2, float v3
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// |a| and |b| maxima of two bf16x2 words, lane by lane (the sign bits of the
+// result are the XOR of the inputs' and carry no meaning; a NaN input is
+// ignored, as fmaxf ignores it).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Non-negative floats order like their bit patterns: atomicMax on the bits.
 __device__ __forceinline__ void atomic_max_nonneg(float *addr, float v) {
     atomicMax(reinterpret_cast<unsigned int *>(addr), __float_as_uint(v));

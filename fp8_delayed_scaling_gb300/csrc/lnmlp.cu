@@ -170,15 +170,6 @@ __device__ __forceinline__ float2 chan_equal(float2 a, float2 b, float half_n) {
     return make_float2((a.x + b.x) * 0.5f, (a.y + b.y) + d * d * half_n);
 }
 
-// |a| and |b| maxima of two bf16x2 words, lane by lane (the sign bits of the
-// result are the XOR of the inputs' and carry no meaning; a NaN input is
-// ignored, as fmaxf ignores it).
-__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
 // LayerNorm forward + cast.  Warp w covers columns 64w .. 64w+63 of the CTA's
 // slab; lane (rg = lane >> 2, cg = lane & 3) holds columns 64w + 16cg .. +15 of
 // rows 4rg .. 4rg+3 of the 32-row block.  In shared memory the 16-byte chunk
@@ -623,8 +614,9 @@ __device__ __forceinline__ float2 warp_sum_rows(const float2 (&s)[R], int lane) 
 // g = dy * gamma and xhat = (x - mu) * rs for its slab; the row partials of
 // sum(g) and sum(g * xhat) are published for the cluster (one block ahead),
 // summed over the CTAs in rank order, and
-// dx = rs * (g - mean(g) - xhat * mean(g * xhat)) is written from the staged
-// block.  Each thread keeps the column partials of dgamma (dy * xhat) and dbeta
+//   dx = rs * (g - c1 - xhat * c2) = (x - mu) * k2 + (rs * g + k1),
+//   c1 = mean(g), c2 = mean(g * xhat), k1 = -rs * c1, k2 = -rs^2 * c2,
+// is written from the staged block.  Each thread keeps the column partials of dgamma (dy * xhat) and dbeta
 // (dy) of its 8 columns across all of the cluster's blocks; at the end the CTA
 // writes one partial row per cluster, part[cluster][col] (dgamma) and
 // part[n_clusters + cluster][col] (dbeta), which ln_bwd_reduce_kernel sums in
@@ -653,14 +645,16 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
     const float inv_cols = 1.0f / (float)cols;
     const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gamma + col));
     const float2 g2[4] = {bf16x2_f2(gv.x), bf16x2_f2(gv.y), bf16x2_f2(gv.z), bf16x2_f2(gv.w)};
+    const int64_t goff0 = (int64_t)(RPT * g) * cols + col;  // element offset of the thread's first row, less r0
     auto issue = [&](int64_t j, int buf) {
         if (j < nb) {
             const int64_t r0 = (cid + j * ncl) * BLK;
+            const int64_t goff = goff0 + r0 * cols, lim = rows - r0 - RPT * g;  // row i is valid while i < lim
             uint8_t *b = lsm + buf * BUF;
+#pragma unroll
             for (int i = 0; i < RPT; i++) {
-                const int64_t row = r0 + RPT * g + i;
-                const bool valid = row < rows;
-                const int64_t off = valid ? row * cols + col : 0;
+                const bool valid = i < lim;
+                const int64_t off = valid ? goff + i * cols : 0;
                 const int soff = ((RPT * g + i) * LC_COLS + 8 * c) * 2;
                 cp_async16(smem_u32(b + soff), dy + off, valid);
                 cp_async16(smem_u32(b + BLK * LC_COLS * 2 + soff), x + off, valid);
@@ -768,19 +762,17 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
                 const float2 cc = cst[RPT * g + i];
                 const float m = mrs[buf][0][RPT * g + i], sg = mrs[buf][1][RPT * g + i];
                 const float2 nm = make_float2(-m, -m), sg2 = make_float2(sg, sg);
-                const float2 nc1 = make_float2(-cc.x, -cc.x), nc2 = make_float2(-cc.y, -cc.y);
+                const float k1 = -sg * cc.x, k2 = -(sg * sg) * cc.y;
                 const uint4 dq = dr[i * (LC_COLS / 8)], xq = xr[i * (LC_COLS / 8)];
                 const uint32_t dv[4] = {dq.x, dq.y, dq.z, dq.w}, xv[4] = {xq.x, xq.y, xq.z, xq.w};
                 uint32_t ow[4];
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    // dx = rs * (dy * gamma - c1 - xhat * c2), two at a time
-                    const float2 h = __fmul2_rn(__fadd2_rn(bf16x2_f2(xv[q]), nm), sg2);
-                    const float2 u = __fadd2_rn(__fmul2_rn(bf16x2_f2(dv[q]), g2[q]), nc1);
-                    ow[q] = f2_bf16x2(__fmul2_rn(sg2, __ffma2_rn(h, nc2, u)));
+                    // dx = (x - mu) * k2 + (rs * (dy * gamma) + k1), two at a time
+                    const float2 u = __ffma2_rn(__fmul2_rn(bf16x2_f2(dv[q]), g2[q]), sg2, f2(k1));
+                    ow[q] = f2_bf16x2(__ffma2_rn(__fadd2_rn(bf16x2_f2(xv[q]), nm), f2(k2), u));
                 }
-                *reinterpret_cast<uint4 *>(dx + (r0 + RPT * g + i) * cols + col) =
-                    make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                *reinterpret_cast<uint4 *>(dx + goff0 + (r0 + i) * cols) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             }
         }
         buf = next_buf(buf);
