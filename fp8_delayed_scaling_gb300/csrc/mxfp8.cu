@@ -156,24 +156,22 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
         const int64_t tr0 = (tile / tiles_c) * 128, tc0 = (tile % tiles_c) * 128;
         const bool ok = tr0 + 32 * wr < rows && tc0 + 64 * wc + 32 * sub < cols;  // whole 32 x 32 block present
         const uint8_t *sb = mq_smem + stage * STAGE + prow * ROW_BYTES + pcol * ESZ;
-        float v[8][8];
+        float2 v[8][4];     // v[i][q]: columns 2q, 2q+1 of row i of the lane's piece
+        uint32_t wq[8][4];  // bf16 input: the same pairs as bf16x2 words
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             const uint8_t *p = sb + i * ROW_BYTES;
             if (ESZ == 2) {
                 const uint4 u = *reinterpret_cast<const uint4 *>(p);
-                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                wq[i][0] = u.x, wq[i][1] = u.y, wq[i][2] = u.z, wq[i][3] = u.w;
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    v[i][2 * q] = bf16_lo(w4[q]);
-                    v[i][2 * q + 1] = bf16_hi(w4[q]);
-                }
+                for (int q = 0; q < 4; q++) v[i][q] = make_float2(bf16_lo(wq[i][q]), bf16_hi(wq[i][q]));
             } else {
                 const uint4 u0 = *reinterpret_cast<const uint4 *>(p), u1 = *reinterpret_cast<const uint4 *>(p + 16);
-                v[i][0] = __uint_as_float(u0.x); v[i][1] = __uint_as_float(u0.y);
-                v[i][2] = __uint_as_float(u0.z); v[i][3] = __uint_as_float(u0.w);
-                v[i][4] = __uint_as_float(u1.x); v[i][5] = __uint_as_float(u1.y);
-                v[i][6] = __uint_as_float(u1.z); v[i][7] = __uint_as_float(u1.w);
+                v[i][0] = make_float2(__uint_as_float(u0.x), __uint_as_float(u0.y));
+                v[i][1] = make_float2(__uint_as_float(u0.z), __uint_as_float(u0.w));
+                v[i][2] = make_float2(__uint_as_float(u1.x), __uint_as_float(u1.y));
+                v[i][3] = make_float2(__uint_as_float(u1.z), __uint_as_float(u1.w));
             }
         }
         __syncthreads();  // the stage may be refilled once every thread has read it
@@ -182,11 +180,15 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
             const bool band_ok = tr0 + 32 * wr < rows;
             float cs[8];
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                float a = v[0][j];
+            for (int q = 0; q < 4; q++) {
+                float2 a = v[0][q];
 #pragma unroll
-                for (int i = 1; i < 8; i++) a += v[i][j];
-                cs[j] = band_ok ? a : 0.0f;
+                for (int i = 1; i < 8; i++) a = __fadd2_rn(a, v[i][q]);
+                cs[2 * q] = band_ok ? a.x : 0.0f;
+                cs[2 * q + 1] = band_ok ? a.y : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
                 cs[j] += __shfl_xor_sync(0xffffffffu, cs[j], 4);
                 cs[j] += __shfl_xor_sync(0xffffffffu, cs[j], 8);
             }
@@ -197,19 +199,36 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
             }
         }
         float rmax[8], cmax[8];
+        if constexpr (ESZ == 2) {  // |x| maxima on the bf16x2 words, two columns per instruction
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            rmax[i] = 0.0f;
-            cmax[i] = 0.0f;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; i++)
-#pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const float a = fabsf(v[i][j]);
-                rmax[i] = fmaxf(rmax[i], a);
-                cmax[j] = fmaxf(cmax[j], a);
+            for (int i = 0; i < 8; i++) {
+                const uint32_t r2 = bf16x2_absmax(bf16x2_absmax(wq[i][0], wq[i][1]), bf16x2_absmax(wq[i][2], wq[i][3]));
+                rmax[i] = fmaxf(fabsf(bf16_lo(r2)), fabsf(bf16_hi(r2)));
             }
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                uint32_t c2 = wq[0][q];
+#pragma unroll
+                for (int i = 1; i < 8; i++) c2 = bf16x2_absmax(c2, wq[i][q]);
+                cmax[2 * q] = fabsf(bf16_lo(c2));
+                cmax[2 * q + 1] = fabsf(bf16_hi(c2));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                rmax[i] = 0.0f;
+                cmax[i] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++)
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const float a = fabsf(v[i][q].x), b = fabsf(v[i][q].y);
+                    rmax[i] = fmaxf(rmax[i], fmaxf(a, b));
+                    cmax[2 * q] = fmaxf(cmax[2 * q], a);
+                    cmax[2 * q + 1] = fmaxf(cmax[2 * q + 1], b);
+                }
+        }
 #pragma unroll
         for (int i = 0; i < 8; i++) {
             rmax[i] = fmaxf(rmax[i], __shfl_xor_sync(0xffffffffu, rmax[i], 1));
@@ -222,11 +241,11 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const int e = e8m0_exponent(rmax[i]);
-                const float m = pow2_neg(e);
-                const uint32_t lo = pack4<FP8DL_E4M3>(__fmul_rn(v[i][0], m), __fmul_rn(v[i][1], m),
-                                                      __fmul_rn(v[i][2], m), __fmul_rn(v[i][3], m));
-                const uint32_t hi = pack4<FP8DL_E4M3>(__fmul_rn(v[i][4], m), __fmul_rn(v[i][5], m),
-                                                      __fmul_rn(v[i][6], m), __fmul_rn(v[i][7], m));
+                const float2 m = f2(pow2_neg(e));
+                const float2 a = __fmul2_rn(v[i][0], m), b = __fmul2_rn(v[i][1], m);
+                const float2 c = __fmul2_rn(v[i][2], m), d = __fmul2_rn(v[i][3], m);
+                const uint32_t lo = pack4<FP8DL_E4M3>(a.x, a.y, b.x, b.y);
+                const uint32_t hi = pack4<FP8DL_E4M3>(c.x, c.y, d.x, d.y);
                 *reinterpret_cast<uint2 *>(qrow + i * cols) = make_uint2(lo, hi);
                 if (cc == 0) sf_tile[sfb][0][sf_byte(prow + i, pcol >> 5)] = (uint8_t)(e + 127);
             }
@@ -244,11 +263,11 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
             for (int half = 0; half < 2; half++) {  // columns 4*half .. 4*half+3
                 uint32_t wcode[8];
 #pragma unroll
-                for (int i = 0; i < 8; i++)
-                    wcode[i] = pack4<FP8DL_E4M3>(__fmul_rn(v[i][4 * half], m[4 * half]),
-                                                 __fmul_rn(v[i][4 * half + 1], m[4 * half + 1]),
-                                                 __fmul_rn(v[i][4 * half + 2], m[4 * half + 2]),
-                                                 __fmul_rn(v[i][4 * half + 3], m[4 * half + 3]));
+                for (int i = 0; i < 8; i++) {
+                    const float2 a = __fmul2_rn(v[i][2 * half], make_float2(m[4 * half], m[4 * half + 1]));
+                    const float2 b = __fmul2_rn(v[i][2 * half + 1], make_float2(m[4 * half + 2], m[4 * half + 3]));
+                    wcode[i] = pack4<FP8DL_E4M3>(a.x, a.y, b.x, b.y);
+                }
                 uint32_t lo[4], hi[4];
                 transpose4x4(wcode[0], wcode[1], wcode[2], wcode[3], lo);
                 transpose4x4(wcode[4], wcode[5], wcode[6], wcode[7], hi);
