@@ -219,6 +219,32 @@ def hbm_bytes(cfg, fused=False):
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
+class CycleClock:
+    """Mean SM clock between two probes on a stream (fp8dl_clock_probe): each SM's cycle-counter
+    delta over the global timer's, median over the SMs seen in both probes.  Unlike nvidia-smi's
+    200 ms samples it covers exactly the work enqueued between the probes."""
+
+    def __init__(self, dev, stream):
+        import fp8_delayed_scaling_gb300 as fd
+        self.fd = fd
+        self.n = 2 * torch.cuda.get_device_properties(dev).multi_processor_count
+        self.buf = [torch.zeros(3 * self.n, dtype=torch.int64, device=dev) for _ in range(2)]
+        self.stream = stream
+
+    def mark(self, k):
+        self.fd.fp8dl_clock_probe(self.buf[k], self.n, self.stream)
+
+    def mhz(self):
+        """(median MHz, SMs measured); call after both marks have completed."""
+        first = [{}, {}]
+        for k in range(2):
+            for smid, cyc, ns in self.buf[k].view(-1, 3).cpu().tolist():
+                first[k].setdefault(smid, (cyc, ns))
+        v = sorted((first[1][sm][0] - first[0][sm][0]) / (first[1][sm][1] - first[0][sm][1]) * 1e3
+                   for sm in first[0] if sm in first[1] and first[1][sm][1] > first[0][sm][1])
+        return (round(v[len(v) // 2], 1) if v else None), len(v)
+
+
 class ClockSampler:
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -467,10 +493,12 @@ def run_ours(args, cfg, dev, rank, world):
         run_step = graph.replay
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    cyc = CycleClock(dev, stream)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    cyc.mark(0)
     evs = []
     if not use_graph:
         timer.__enter__()
@@ -485,6 +513,7 @@ def run_ours(args, cfg, dev, rank, world):
         if not use_graph:
             torch.cuda.synchronize()  # between steps, outside the step's events
             timer.harvest()
+    cyc.mark(1)
     if use_graph:
         torch.cuda.synchronize()
         # per-kernel timing pass: 5 eager steps directly after the timed steps, with no host
@@ -524,6 +553,12 @@ def run_ours(args, cfg, dev, rank, world):
     clk = clocks.stop()
     if clk is not None and extra:
         clk["note"] = "sampled during the timed steps and %d untimed steps of the same workload after them" % extra
+    mhz, n_sm = cyc.mhz()
+    if mhz is not None:
+        clk = clk or {}
+        clk["sm_mhz_cycles"] = mhz
+        clk["sm_mhz_cycles_src"] = ("mean SM clock over the timed steps (and the L2 flushes between them): per-SM "
+                                    "cycle counter over the global timer, median of %d SMs" % n_sm)
     ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -974,18 +1009,26 @@ def main():
         return {"achieved_gbs": round(gbs, 1), "peak_gbs": hbm, "frac": round(gbs / hbm, 4),
                 "ms_per_step": round(c["ms_per_step"], 4), "launches_per_step": c["launches_per_step"]}
 
-    def roofline(wcfg, wname, kt):
+    def roofline(wcfg, wname, kt, clk):
         """The workload's dominant kernel class, its GEMMs: algorithmic FLOPs of a step's GEMM
-        launches over their summed CUDA-event durations, against the burst FP8 peak."""
+        launches over their summed CUDA-event durations, against the burst FP8 peak.  Side keys:
+        the fraction of the sustained peak, and of the burst peak scaled to the SM clock the
+        cycle counters measured over the timed steps (what the same GEMMs could do at that clock)."""
         g = kt["gemm"]
         achieved = g["flops_per_step"] / (g["ms_per_step"] * 1e-3) / 1e12
         traffic, tnote = gemm_traffic(wname)
-        return {"bound": "tensor", "kernel": "mxfp8_gemm" if wcfg.get("kind") == "mx" else "fp8_gemm",
-                "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                "frac": round(achieved / fp8_peak, 4), "traffic": traffic, "traffic_src": tnote,
-                "peak_src": peak_src, "gemm_ms_per_step": round(g["ms_per_step"], 4),
-                "gemm_launches_per_step": g["launches_per_step"],
-                "frac_of_sustained": round(achieved / sustained, 4)}
+        r = {"bound": "tensor", "kernel": "mxfp8_gemm" if wcfg.get("kind") == "mx" else "fp8_gemm",
+             "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+             "frac": round(achieved / fp8_peak, 4), "traffic": traffic, "traffic_src": tnote,
+             "peak_src": peak_src, "gemm_ms_per_step": round(g["ms_per_step"], 4),
+             "gemm_launches_per_step": g["launches_per_step"],
+             "frac_of_sustained": round(achieved / sustained, 4)}
+        if clk and clk.get("sm_mhz_cycles"):
+            top = clk.get("sm_max_mhz") or 2070.0
+            r["frac_at_clock"] = round(achieved / (fp8_peak * clk["sm_mhz_cycles"] / top), 4)
+            r["frac_at_clock_src"] = "burst peak x sm_mhz_cycles / sm_max_mhz (%.0f / %.0f MHz)" % (
+                clk["sm_mhz_cycles"], top)
+        return r
 
     model, ms, kt, clk, (e2e_s, h2d, d2h) = run_ours(args, cfg, dev, rank, world)
     launch = kt.pop("launch")
@@ -997,7 +1040,7 @@ def main():
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8(e4m3/e5m2)->fp32acc->bf16", "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": config, "launch": launch,
-        "roofline": roofline(cfg, args.workload, kt),
+        "roofline": roofline(cfg, args.workload, kt, clk),
         "fp8_peak": fp8_peak_info,
         "cast": hbm_class(kt["cast"]),
         "kernels": {k: ({kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
@@ -1032,7 +1075,7 @@ def main():
                 "e2e": {"value": round(s_flops / s_e2e / 1e12, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": s_h2d,
                         "d2h_bytes_per_step": s_d2h}}
             if key == "mx_mlp":
-                entry["roofline"] = roofline(scfg, wname, s_kt)
+                entry["roofline"] = roofline(scfg, wname, s_kt, s_clk)
                 entry["quantize"] = hbm_class(s_kt["cast"])
                 entry["by_entry"] = s_kt["by_entry"]
                 if s_clk:

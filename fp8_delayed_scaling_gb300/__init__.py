@@ -74,6 +74,7 @@ _SIGS = {
     "fp8_layernorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "fp8dl_wait_selftest": (_i32, [_i64, _i32, _vp, _vp]),
     "fp8dl_device_supported": (_i32, [_i32]),
+    "fp8dl_clock_probe": (_i32, [_vp, _i32, _vp]),
     "fp8dl_last_error": (ctypes.c_char_p, []),
     "fp8dl_version": (_i32, []),
     "fp8dl_kernel_launches": (ctypes.c_uint64, []),
@@ -137,6 +138,11 @@ def fp8dl_kernel_launches() -> int:
 
 def fp8dl_device_supported(device: int = 0) -> bool:
     return bool(_lib.fp8dl_device_supported(device))
+
+
+def fp8dl_clock_probe(out, n_ctas: int, stream=None) -> None:
+    """out: uint64 device tensor of 3 * n_ctas entries (SM id, cycle counter, ns timer per CTA)."""
+    _check(_lib.fp8dl_clock_probe(_p(out), int(n_ctas), _stream(stream)), "fp8dl_clock_probe")
 
 
 def fp8dl_wait_selftest(budget_cycles: int, arrive_first: bool, dev_status, stream=None) -> None:

@@ -38,6 +38,20 @@ fp8dl_status fail(fp8dl_status st, const char *fmt, ...) {
 
 std::atomic<uint64_t> g_launches{0};
 
+// One record per CTA: the SM it ran on, that SM's cycle counter and the global
+// nanosecond timer, read together by lane 0.
+__global__ void clock_probe_kernel(uint64_t *__restrict__ out) {
+    if (threadIdx.x != 0) return;
+    uint32_t smid;
+    uint64_t ns;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const long long c = clock64();
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ns));
+    out[3 * blockIdx.x] = smid;
+    out[3 * blockIdx.x + 1] = (uint64_t)c;
+    out[3 * blockIdx.x + 2] = ns;
+}
+
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 fp8dl_status check_launch(const char *what) {
@@ -97,6 +111,17 @@ const char *fp8dl_last_error(void) { return fp8dl::g_last_error; }
 int32_t fp8dl_version(void) { return 100; }
 
 uint64_t fp8dl_kernel_launches(void) { return fp8dl::g_launches.load(std::memory_order_relaxed); }
+
+fp8dl_status fp8dl_clock_probe(uint64_t *out, int32_t n_ctas, fp8dl_stream_t stream) {
+    FP8DL_NVTX("fp8dl_clock_probe");
+    FP8DL_CHECK_ARG(out != nullptr, "out is NULL");
+    FP8DL_CHECK_ARG(n_ctas >= 1 && n_ctas <= 65536, "n_ctas must be in [1, 65536]");
+    if (!fp8dl::aligned16(out)) return fp8dl::fail(FP8DL_ERR_ALIGN, "out must be 16-byte aligned");
+    FP8DL_TRY(fp8dl::current_device(nullptr, nullptr));
+    fp8dl::clock_probe_kernel<<<(unsigned)n_ctas, 32, 0, (cudaStream_t)stream>>>(out);
+    fp8dl::note_launch();
+    return fp8dl::check_launch("fp8dl_clock_probe");
+}
 
 int32_t fp8dl_device_supported(int32_t device) {
     int n = 0;

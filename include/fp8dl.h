@@ -381,6 +381,13 @@ const char *fp8dl_last_error(void);
  * The CUDA context stays usable either way. */
 fp8dl_status fp8dl_wait_selftest(int64_t budget_cycles, int32_t arrive_first, int32_t *dev_status,
                                  fp8dl_stream_t stream);
+/* Clock probe (measurement): n_ctas CTAs each write, to out[3 * i .. 3 * i + 2]
+ * (device memory, 16-byte aligned, 3 * n_ctas uint64), the id of the SM CTA i
+ * ran on, that SM's cycle counter (clock64) and the global nanosecond timer
+ * (%globaltimer), read back to back.  Two probes on a stream around some work
+ * give each SM's mean clock over it: (cycles_2 - cycles_1) / (ns_2 - ns_1) GHz
+ * for an SM seen in both.  One launch; no other effect. */
+fp8dl_status fp8dl_clock_probe(uint64_t *out, int32_t n_ctas, fp8dl_stream_t stream);
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t fp8dl_version(void);
 /* Number of kernels this library has enqueued in this process, over all threads

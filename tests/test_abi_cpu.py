@@ -89,6 +89,10 @@ def test_host_validation_without_gpu(lib):
     # MX bias gradient without workspace
     assert L.mxfp8_quantize(a16, 1, 64, 32, a16, a16, None, None, a16, None, 0, None) == lib.ERR_WORKSPACE
     assert L.mxfp8_gemm(a16, a16, a16, a16, 32, 32, 48, None, 1, a16, 1, None, None) == lib.ERR_SHAPE
+    # clock probe: NULL output, CTA count out of range, misaligned output
+    assert L.fp8dl_clock_probe(None, 4, None) == lib.ERR_INVALID_ARG
+    assert L.fp8dl_clock_probe(a16, 0, None) == lib.ERR_INVALID_ARG
+    assert L.fp8dl_clock_probe(a16 + 8, 4, None) == lib.ERR_ALIGN
     r = lib.fp8dl_recipe(0, 0, 1, 16, 0)  # interval 0 is invalid
     assert L.fp8_update_scale(ctypes.byref(r), 3, a16, 0, None) == lib.ERR_INVALID_ARG
     r = lib.fp8dl_recipe(-1, 1, 1, 16, 0)

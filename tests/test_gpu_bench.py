@@ -43,6 +43,9 @@ def test_default_bench_line_carries_the_contract():
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert d["gpu_launches"] == 14 * d["steps"]  # the library's kernels of one LayerNormMLP step
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    # the cycle counters' mean SM clock over the timed steps, and the GEMM fraction at that clock
+    assert 200 < d["clocks"]["sm_mhz_cycles"] <= 2300
+    assert abs(r["frac_at_clock"] - r["frac"] * d["clocks"]["sm_max_mhz"] / d["clocks"]["sm_mhz_cycles"]) < 2e-3
     t = d["te_linear"]
     assert t["workload"] == "linear_hybrid" and t["value"] > 0 and t["gpu_launches"] > 0 and t["e2e"]["value"] > 0
     mx = d["mx_mlp"]
