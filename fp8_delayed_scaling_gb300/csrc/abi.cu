@@ -38,6 +38,14 @@ fp8dl_status fail(fp8dl_status st, const char *fmt, ...) {
 
 std::atomic<uint64_t> g_launches{0};
 
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char *e = getenv("FP8DL_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 // One record per CTA: the SM it ran on, that SM's cycle counter and the global
 // nanosecond timer, read together by lane 0.
 __global__ void clock_probe_kernel(uint64_t *__restrict__ out) {

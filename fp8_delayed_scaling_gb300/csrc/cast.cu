@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_
     cast_kernel(const void *__restrict__ x, const OpArgs op, int64_t rows, int64_t cols,
                 const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
                 float *__restrict__ amax_p, float *__restrict__ ws, uint16_t *__restrict__ pre_out) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
     __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // per-warp column partials (dbias)
     __shared__ float wmax[CT_THREADS / 32];
@@ -293,6 +295,8 @@ struct CastMultiArgs {
 template <int XKIND, int FMT>
 __global__ void __launch_bounds__(CT_THREADS, XKIND == FP8DL_BF16 ? 4 : 2)
     cast_multi_kernel(const __grid_constant__ CastMultiArgs a) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
     __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // unused: no bias gradients here
     __shared__ float wmax[CT_THREADS / 32];
@@ -317,6 +321,8 @@ __global__ void __launch_bounds__(CT_THREADS, XKIND == FP8DL_BF16 ? 4 : 2)
 
 // The decode factors fl32(1 / scale) of the tensors of a grouped cast that ask for one.
 __global__ void scale_inv_multi_kernel(const __grid_constant__ CastMultiArgs a) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     const int k = threadIdx.x;
     if (k < a.n && a.scale_inv_out[k]) *a.scale_inv_out[k] = __frcp_rn(*a.scale[k]);
 }
@@ -329,6 +335,8 @@ constexpr int RED_COLS = 32, RED_WARPS = 8;
 __global__ void __launch_bounds__(RED_COLS *RED_WARPS) colsum_reduce_kernel(const float *__restrict__ ws,
                                                                             int64_t n_tiles, int64_t cols,
                                                                             float *__restrict__ dbias) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     __shared__ float part[RED_WARPS][RED_COLS];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t c = blockIdx.x * (int64_t)RED_COLS + lane;
@@ -355,14 +363,15 @@ __global__ void __launch_bounds__(RED_COLS *RED_WARPS) colsum_reduce_kernel(cons
     }
 }
 
-static void launch_colsum_reduce(const float *ws, int64_t n_tiles, int64_t cols, float *dbias, cudaStream_t st) {
-    colsum_reduce_kernel<<<(unsigned)((cols + RED_COLS - 1) / RED_COLS), RED_COLS * RED_WARPS, 0, st>>>(ws, n_tiles,
+static void launch_colsum_reduce(const float *ws, int64_t n_tiles, int64_t cols, float *dbias, cudaStream_t st,
+                                 bool pdl) {
+    (void)launch_kernel(colsum_reduce_kernel, (unsigned)((cols + RED_COLS - 1) / RED_COLS), RED_COLS * RED_WARPS, 0, st, 0, pdl, ws, n_tiles,
                                                                                                        cols, dbias);
     note_launch();
 }
 
-void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, cudaStream_t st) {
-    launch_colsum_reduce(ws, n_rows, cols, dbias, st);
+void colsum_reduce(const float *ws, int64_t n_rows, int64_t cols, float *dbias, cudaStream_t st, bool pdl) {
+    launch_colsum_reduce(ws, n_rows, cols, dbias, st, pdl);
 }
 
 // Grid of a tiled cast launch: no more CTAs than fit on the GPU at once.  Every CTA is then
@@ -397,8 +406,8 @@ static dim3 cast_grid(int64_t tiles, int sms) {
 
 template <int XKIND, int FMT>
 static void launch_cast(int64_t tiles, int sms, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
-                        uint8_t *out, uint8_t *out_t, float *amax, float *ws) {
-    cast_kernel<XKIND, FMT, OP_NONE><<<cast_grid<XKIND, FMT, OP_NONE>(tiles, sms), CT_THREADS, 0, st>>>(
+                        uint8_t *out, uint8_t *out_t, float *amax, float *ws, bool pdl) {
+    (void)launch_kernel(cast_kernel<XKIND, FMT, OP_NONE>, cast_grid<XKIND, FMT, OP_NONE>(tiles, sms), CT_THREADS, 0, st, 0, pdl, 
         x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, nullptr);
     note_launch();
 }
@@ -406,13 +415,13 @@ static void launch_cast(int64_t tiles, int sms, cudaStream_t st, const void *x, 
 template <int OP>
 static void launch_op_cast(int64_t tiles, int sms, cudaStream_t st, int fmt, const void *x, const OpArgs &op,
                            int64_t rows, int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
-                           float *ws, uint16_t *pre_out) {
+                           float *ws, uint16_t *pre_out, bool pdl) {
     if (fmt == FP8DL_E4M3)
-        cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP><<<cast_grid<FP8DL_BF16, FP8DL_E4M3, OP>(tiles, sms), CT_THREADS, 0,
-                                                   st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+        (void)launch_kernel(cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP>, cast_grid<FP8DL_BF16, FP8DL_E4M3, OP>(tiles, sms), CT_THREADS, 0,
+                                                   st, 0, pdl, x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
     else
-        cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP><<<cast_grid<FP8DL_BF16, FP8DL_E5M2, OP>(tiles, sms), CT_THREADS, 0,
-                                                   st>>>(x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+        (void)launch_kernel(cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP>, cast_grid<FP8DL_BF16, FP8DL_E5M2, OP>(tiles, sms), CT_THREADS, 0,
+                                                   st, 0, pdl, x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
     note_launch();
 }
 
@@ -421,17 +430,19 @@ static void launch_op_cast(int64_t tiles, int sms, cudaStream_t st, int fmt, con
 fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const float *rs, const void *gamma,
                                         const void *beta, int64_t rows, int64_t cols, int fmt, const float *scale,
                                         uint8_t *out, uint8_t *out_t, float *amax, void *y, int sms,
-                                        cudaStream_t st) {
+                                        cudaStream_t st, bool pdl) {
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
     OpArgs op{nullptr, mu, rs, static_cast<const uint16_t *>(gamma), static_cast<const uint16_t *>(beta)};
     launch_op_cast<OP_LAYERNORM>(tiles, sms, st, fmt, x, op, rows, cols, scale, out, out_t, amax, nullptr,
-                                 static_cast<uint16_t *>(y));
+                                 static_cast<uint16_t *>(y), pdl);
     return check_launch("fp8_layernorm_cast(tiles)");
 }
 
 // The decode factor of codes cast at *scale: fl32(1 / scale), the same
 // rounding as the scale_inv the scale update stores beside the scale.
 __global__ void scale_inv_snapshot_kernel(const float *scale, float *scale_inv) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     if (threadIdx.x == 0) *scale_inv = __frcp_rn(*scale);
 }
 
@@ -473,25 +484,26 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
+    const bool pdl = short_call_bytes((double)rows * cols * (x_dtype == FP8DL_BF16 ? 4 : 6));
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     } else {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     }
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose"));
     if (dbias) {
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
+        launch_colsum_reduce(ws, n_tiles, cols, dbias, st, pdl);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(dbias reduce)"));
     }
     if (scale_inv_out) {
-        scale_inv_snapshot_kernel<<<1, 32, 0, st>>>(scale, scale_inv_out);
+        (void)launch_kernel(scale_inv_snapshot_kernel, 1, 32, 0, st, 0, pdl, scale, scale_inv_out);
         note_launch();
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(scale_inv)"));
     }
@@ -509,6 +521,7 @@ fp8dl_status fp8_cast_amax_transpose_multi(int32_t n, const fp8dl_cast_item *ite
     a.n = n;
     bool any_inv = false;
     int64_t tiles = 0;
+    double bytes = 0.0;
     for (int k = 0; k < n; k++) {
         const fp8dl_cast_item &it = items[k];
         FP8DL_CHECK_ARG(it.x != nullptr, "item %d: x is NULL", k);
@@ -531,7 +544,9 @@ fp8dl_status fp8_cast_amax_transpose_multi(int32_t n, const fp8dl_cast_item *ite
         any_inv = any_inv || it.scale_inv_out != nullptr;
         tiles += ((it.rows + CT_ROWS - 1) / CT_ROWS) * ((it.cols + CT_COLS - 1) / CT_COLS);
         a.tile_end[k] = tiles;
+        bytes += (double)it.rows * it.cols * (x_dtype == FP8DL_BF16 ? 4 : 6);
     }
+    const bool pdl = short_call_bytes(bytes);
     int sms = 0;
     FP8DL_TRY(current_device(nullptr, &sms));
     cudaStream_t st = (cudaStream_t)stream;
@@ -544,19 +559,19 @@ fp8dl_status fp8_cast_amax_transpose_multi(int32_t n, const fp8dl_cast_item *ite
     const dim3 grid = resident_grid(kern, occ[xi][fi], tiles, sms);
     if (xi) {
         if (fi)
-            cast_multi_kernel<FP8DL_BF16, FP8DL_E5M2><<<grid, CT_THREADS, 0, st>>>(a);
+            (void)launch_kernel(cast_multi_kernel<FP8DL_BF16, FP8DL_E5M2>, grid, CT_THREADS, 0, st, 0, pdl, a);
         else
-            cast_multi_kernel<FP8DL_BF16, FP8DL_E4M3><<<grid, CT_THREADS, 0, st>>>(a);
+            (void)launch_kernel(cast_multi_kernel<FP8DL_BF16, FP8DL_E4M3>, grid, CT_THREADS, 0, st, 0, pdl, a);
     } else {
         if (fi)
-            cast_multi_kernel<FP8DL_F32, FP8DL_E5M2><<<grid, CT_THREADS, 0, st>>>(a);
+            (void)launch_kernel(cast_multi_kernel<FP8DL_F32, FP8DL_E5M2>, grid, CT_THREADS, 0, st, 0, pdl, a);
         else
-            cast_multi_kernel<FP8DL_F32, FP8DL_E4M3><<<grid, CT_THREADS, 0, st>>>(a);
+            (void)launch_kernel(cast_multi_kernel<FP8DL_F32, FP8DL_E4M3>, grid, CT_THREADS, 0, st, 0, pdl, a);
     }
     note_launch();
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose_multi"));
     if (any_inv) {
-        scale_inv_multi_kernel<<<1, 32, 0, st>>>(a);
+        (void)launch_kernel(scale_inv_multi_kernel, 1, 32, 0, st, 0, pdl, a);
         note_launch();
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose_multi(scale_inv)"));
     }
@@ -597,15 +612,17 @@ static fp8dl_status op_cast_common(int op, const void *x, const void *aux, int64
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     uint16_t *pre = static_cast<uint16_t *>(pre_out);
+    const bool pdl = short_call_bytes((double)rows * cols * (op == OP_DGELU ? 8 : 6));
     if (op == OP_GELU)
-        launch_op_cast<OP_GELU>(tiles, sms, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre);
+        launch_op_cast<OP_GELU>(tiles, sms, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre,
+                                pdl);
     else
         launch_op_cast<OP_DGELU>(tiles, sms, st, out_dtype, x, OpArgs{aux, nullptr, nullptr, nullptr, nullptr}, rows, cols,
-                                 scale, out, out_t, amax, ws, pre);
+                                 scale, out, out_t, amax, ws, pre, pdl);
     FP8DL_TRY(check_launch(name));
     if (dbias) {
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
+        launch_colsum_reduce(ws, n_tiles, cols, dbias, st, pdl);
         FP8DL_TRY(check_launch(name));
     }
     return FP8DL_OK;
@@ -695,6 +712,7 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     if (dbias) FP8DL_TRY(static_scratch_address(dev, &ws));
     cudaStream_t st = (cudaStream_t)stream;
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    const bool pdl = short_call_bytes((double)rows * cols * (x_dtype == FP8DL_BF16 ? 4 : 6));
     // The cast's partials and their reduction are enqueued back to back with no other call's
     // launches between them: calls from several host threads on one stream then run one
     // after another on the GPU, each reading its own partials from the shared array.
@@ -703,19 +721,19 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     if (dbias) order.lock();
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     } else {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws);
+            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     }
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc"));
     if (dbias) {
         const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        launch_colsum_reduce(ws, n_tiles, cols, dbias, st);
+        launch_colsum_reduce(ws, n_tiles, cols, dbias, st, pdl);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc(dbias reduce)"));
     }
     return FP8DL_OK;

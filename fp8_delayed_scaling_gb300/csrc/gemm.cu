@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(g1::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // set-up done; the previous kernel of the stream has completed
+    pdl_trigger();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -406,6 +408,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     cluster_sync();  // both CTAs' barriers initialised before any cross-CTA signal
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // set-up done; the previous kernel of the stream has completed
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------------ producer (both CTAs)
@@ -877,6 +881,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
                                 int64_t N, int64_t K, GemmArgs &args, int epi, int dev, int sms, bool use_pair,
                                 cudaStream_t stream) {
     CUtensorMap ta, tb, tq;
+    const bool pdl = short_call_flops(2.0 * (double)M * (double)N * (double)K);
     // Instruction descriptor, kind::f8f6f4: D fp32 (bit 4), A type bits 7-9, B type bits 10-12
     // (0 = E4M3, 1 = E5M2), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28
     // (M = 128 for one CTA, 256 for a CTA pair; N = 256 either way).
@@ -902,15 +907,15 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
         const unsigned grid = (unsigned)(2 * pairs);
         const bool e4 = args.q_fmt == FP8DL_E4M3;
         if (epi == 2 && e4)
-            fp8_gemm_pair_kernel<2, FP8DL_E4M3><<<grid, g2::threads(2), g2::smem_bytes(2), stream>>>(ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E4M3>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
         else if (epi == 2)
-            fp8_gemm_pair_kernel<2, FP8DL_E5M2><<<grid, g2::threads(2), g2::smem_bytes(2), stream>>>(ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E5M2>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
         else if (epi == 1 && e4)
-            fp8_gemm_pair_kernel<1, FP8DL_E4M3><<<grid, g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<1, FP8DL_E4M3>, grid, g2::threads(1), g2::smem_bytes(1), stream, 0, pdl, ta, tb, tq, args);
         else if (epi == 1)
-            fp8_gemm_pair_kernel<1, FP8DL_E5M2><<<grid, g2::threads(1), g2::smem_bytes(1), stream>>>(ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<1, FP8DL_E5M2>, grid, g2::threads(1), g2::smem_bytes(1), stream, 0, pdl, ta, tb, tq, args);
         else
-            fp8_gemm_pair_kernel<0, 0><<<grid, g2::threads(0), g2::smem_bytes(0), stream>>>(ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<0, 0>, grid, g2::threads(0), g2::smem_bytes(0), stream, 0, pdl, ta, tb, tq, args);
         note_launch();
         return check_launch(epi == 2 ? "fp8_gemm_dgelu_cast(pair)"
                                      : epi == 1 ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");
@@ -921,7 +926,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
     pick_raster(M, N, K, g1::BM, g1::BN, args.raster_n, args.group);
     const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-    fp8_gemm_kernel<<<grid, g1::THREADS, g1::SMEM_BYTES, stream>>>(ta, tb, args);
+    (void)launch_kernel(fp8_gemm_kernel, grid, g1::THREADS, g1::SMEM_BYTES, stream, 0, pdl, ta, tb, args);
     note_launch();
     return check_launch("fp8_gemm");
 }
@@ -1035,7 +1040,7 @@ extern "C" fp8dl_status fp8_gemm_dgelu_cast(const uint8_t *A, int32_t a_dtype, c
     cudaStream_t st = (cudaStream_t)stream;
     FP8DL_TRY(launch_gemm(A, a_dtype, B, b_dtype, M, N, K, args, 2, dev, sms, true, st));
     if (dbias) {
-        colsum_reduce(args.ws, (M + 31) / 32, N, dbias, st);
+        colsum_reduce(args.ws, (M + 31) / 32, N, dbias, st, short_call_flops(2.0 * (double)M * (double)N * (double)K));
         FP8DL_TRY(check_launch("fp8_gemm_dgelu_cast(dbias reduce)"));
     }
     return FP8DL_OK;

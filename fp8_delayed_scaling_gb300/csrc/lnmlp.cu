@@ -41,6 +41,8 @@ template <int CPL>
 __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
                                                        float eps, float *__restrict__ mu_out,
                                                        float *__restrict__ rs_out) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t nchunks = cols / 8;
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(256) ln_stats_kernel(const uint16_t *__restric
 fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const float *rs, const void *gamma,
                                         const void *beta, int64_t rows, int64_t cols, int fmt, const float *scale,
                                         uint8_t *out, uint8_t *out_t, float *amax, void *y, int sms,
-                                        cudaStream_t st);
+                                        cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------------------
 // Cluster path.  CTA `rank` of a cluster covers columns [LC_COLS*rank,
@@ -190,6 +192,8 @@ __global__ void __launch_bounds__(LC_THREADS, 2) ln_fwd_cluster_kernel(
     int64_t rows, int64_t cols, float eps, const float *__restrict__ scale_p, uint8_t *__restrict__ out,
     uint8_t *__restrict__ out_t, float *__restrict__ amax_p, float *__restrict__ mu_out, float *__restrict__ rs_out,
     uint16_t *__restrict__ y) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     extern __shared__ __align__(128) uint8_t lsm[];      // [LC_NBUF][LF_ROWS][LC_COLS] bf16, then the slots
     __shared__ float2 wst[LC_WARPS][LF_ROWS + 1];        // per-warp (mean, M2) of 64 values of a row
     __shared__ __align__(8) uint64_t xbar[LC_SLOTS];     // slot s complete: every CTA's slabs of its block arrived
@@ -431,6 +435,8 @@ __global__ void __launch_bounds__(256) ln_bwd_rowsum_kernel(const uint16_t *__re
                                                             const float *__restrict__ mu,
                                                             const float *__restrict__ rs, int64_t rows, int64_t cols,
                                                             float *__restrict__ c12) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const float inv_cols = 1.0f / (float)cols;
@@ -468,6 +474,8 @@ __global__ void __launch_bounds__(256) ln_bwd_tile_kernel(const uint16_t *__rest
                                                           const float *__restrict__ mu, const float *__restrict__ rs,
                                                           const float *__restrict__ c12, int64_t rows, int64_t cols,
                                                           uint16_t *__restrict__ dx, float *__restrict__ part) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     __shared__ __align__(16) float red_g[8][LB_COLS];
     __shared__ __align__(16) float red_b[8][LB_COLS];
     const int t = threadIdx.x, cb = t & 7, rb = t >> 3, lane = t & 31, wi = t >> 5;
@@ -546,6 +554,8 @@ __global__ void __launch_bounds__(256) ln_bwd_tile_kernel(const uint16_t *__rest
 // dgamma/dbeta[c] = sum over row tiles of the partials, fixed order (see colsum_reduce_kernel).
 __global__ void __launch_bounds__(256) ln_bwd_reduce_kernel(const float *__restrict__ part, int64_t n_rt, int64_t cols,
                                                             float *__restrict__ dgamma, float *__restrict__ dbeta) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     __shared__ float pg[8][32], pb[8][32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t c = blockIdx.x * (int64_t)32 + lane;
@@ -626,6 +636,8 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
     const uint16_t *__restrict__ dy, const uint16_t *__restrict__ x, const uint16_t *__restrict__ gamma,
     const float *__restrict__ mu, const float *__restrict__ rs, int64_t rows, int64_t cols,
     uint16_t *__restrict__ dx, float *__restrict__ part) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     constexpr int RPT = BLK / 4;                     // rows per thread
     constexpr int BUF = 2 * BLK * LC_COLS * 2;       // one staged (dy, x) block
     extern __shared__ __align__(128) uint8_t lsm[];  // [LC_NBUF][dy, x][BLK][LC_COLS] bf16, then the slots
@@ -880,12 +892,10 @@ static int64_t ln_cluster_count(int dev, int which, const void *kernel, int smem
 }
 
 template <typename... KArgs, typename... Args>
-static cudaError_t launch_clustered(void (*kernel)(KArgs...), int64_t clusters, int cl, int smem, cudaStream_t st,
+static cudaError_t launch_clustered(void (*kernel)(KArgs...), int64_t clusters, int cl, int smem, cudaStream_t st, bool pdl,
                                     Args... args) {
-    cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute at[1];
-    cluster_config(cfg, at, clusters, cl, smem, st);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    const cudaError_t e = launch_kernel(kernel, dim3((unsigned)(clusters * cl)), dim3(LC_THREADS), (size_t)smem, st,
+                                        cl, pdl, args...);
     if (e == cudaSuccess) note_launch();
     return e;
 }
@@ -913,6 +923,7 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
     int dev = 0, sms = 0;
     FP8DL_TRY(current_device(&dev, &sms));
     cudaStream_t st = (cudaStream_t)stream;
+    const bool pdl = short_call_bytes((double)rows * cols * 4);
     auto X = static_cast<const uint16_t *>(x);
     {
         const bool e4 = out_dtype == FP8DL_E4M3;
@@ -921,7 +932,7 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
                                               (rows + LF_ROWS - 1) / LF_ROWS, cols, INT64_MAX);
         if (ncl > 0) {
             const int cl = ln_cluster_size(cols);
-            const cudaError_t e = launch_clustered(kern, ncl, cl, ln_smem(LF_SMEM, LF_ROWS, cl), st, X,
+            const cudaError_t e = launch_clustered(kern, ncl, cl, ln_smem(LF_SMEM, LF_ROWS, cl), st, pdl, X,
                                                    static_cast<const uint16_t *>(gamma),
                                                    static_cast<const uint16_t *>(beta), rows, cols, eps, scale, out,
                                                    out_t, amax, mu, rsigma, static_cast<uint16_t *>(y));
@@ -937,18 +948,18 @@ fp8dl_status fp8_layernorm_cast(const void *x, int64_t rows, int64_t cols, const
     const int64_t row_ctas = (rows + 7) / 8;
     const unsigned g1 = (unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8);
     if (chunks_per_lane <= 4)
-        ln_stats_kernel<4><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+        (void)launch_kernel(ln_stats_kernel<4>, g1, 256, 0, st, 0, pdl, X, rows, cols, eps, mu, rsigma);
     else if (chunks_per_lane <= 8)
-        ln_stats_kernel<8><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+        (void)launch_kernel(ln_stats_kernel<8>, g1, 256, 0, st, 0, pdl, X, rows, cols, eps, mu, rsigma);
     else if (chunks_per_lane <= 16)
-        ln_stats_kernel<16><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+        (void)launch_kernel(ln_stats_kernel<16>, g1, 256, 0, st, 0, pdl, X, rows, cols, eps, mu, rsigma);
     else
-        ln_stats_kernel<32><<<g1, 256, 0, st>>>(X, rows, cols, eps, mu, rsigma);
+        (void)launch_kernel(ln_stats_kernel<32>, g1, 256, 0, st, 0, pdl, X, rows, cols, eps, mu, rsigma);
     note_launch();
     FP8DL_TRY(check_launch("fp8_layernorm_cast(statistics)"));
     if (!(out || out_t || amax || y)) return FP8DL_OK;
     return launch_layernorm_tile_cast(x, mu, rsigma, gamma, beta, rows, cols, out_dtype, scale, out, out_t, amax, y,
-                                      sms, st);
+                                      sms, st, pdl);
 }
 
 size_t fp8_layernorm_bwd_workspace_size(int64_t rows, int64_t cols) {
@@ -974,6 +985,7 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
     int dev = 0, sms = 0;
     FP8DL_TRY(current_device(&dev, &sms));
     cudaStream_t st = (cudaStream_t)stream;
+    const bool pdl = short_call_bytes((double)rows * cols * 6);
     float *c12 = static_cast<float *>(workspace);
     float *part = c12 + 2 * rows;
     auto DY = static_cast<const uint16_t *>(dy);
@@ -986,29 +998,29 @@ fp8dl_status fp8_layernorm_bwd(const void *dy, const void *x, const void *gamma,
                                               (rows + LB_BLK - 1) / LB_BLK, cols, n_rt);
         if (ncl > 0) {
             const int cl = ln_cluster_size(cols);
-            const cudaError_t e = launch_clustered(ln_bwd_cluster_kernel<LB_BLK>, ncl, cl, ln_smem(LB_SMEM, LB_BLK, cl), st,
+            const cudaError_t e = launch_clustered(ln_bwd_cluster_kernel<LB_BLK>, ncl, cl, ln_smem(LB_SMEM, LB_BLK, cl), st, pdl,
                                                    DY, X, G, mu, rsigma, rows, cols, static_cast<uint16_t *>(dx), part);
             if (e != cudaSuccess) {
                 cudaGetLastError();
                 return fail(FP8DL_ERR_CUDA, "fp8_layernorm_bwd(cluster): %s", cudaGetErrorString(e));
             }
             FP8DL_TRY(check_launch("fp8_layernorm_bwd(cluster)"));
-            ln_bwd_reduce_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(part, ncl, cols, dgamma, dbeta);
+            (void)launch_kernel(ln_bwd_reduce_kernel, (unsigned)((cols + 31) / 32), 256, 0, st, 0, pdl, part, ncl, cols, dgamma, dbeta);
             note_launch();
             return check_launch("fp8_layernorm_bwd(reduce)");
         }
     }
     const int64_t row_ctas = (rows + 7) / 8;
-    ln_bwd_rowsum_kernel<<<(unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8), 256, 0, st>>>(
+    (void)launch_kernel(ln_bwd_rowsum_kernel, (unsigned)(row_ctas < (int64_t)sms * 8 ? row_ctas : (int64_t)sms * 8), 256, 0, st, 0, pdl, 
         DY, X, G, mu, rsigma, rows, cols, c12);
     note_launch();
     FP8DL_TRY(check_launch("fp8_layernorm_bwd(row sums)"));
     const int64_t tiles = n_rt * ((cols + LB_COLS - 1) / LB_COLS);
-    ln_bwd_tile_kernel<<<(unsigned)(tiles < (int64_t)sms * 4 ? tiles : (int64_t)sms * 4), 256, 0, st>>>(
+    (void)launch_kernel(ln_bwd_tile_kernel, (unsigned)(tiles < (int64_t)sms * 4 ? tiles : (int64_t)sms * 4), 256, 0, st, 0, pdl, 
         DY, X, G, mu, rsigma, c12, rows, cols, static_cast<uint16_t *>(dx), part);
     note_launch();
     FP8DL_TRY(check_launch("fp8_layernorm_bwd(dx)"));
-    ln_bwd_reduce_kernel<<<(unsigned)((cols + 31) / 32), 256, 0, st>>>(part, n_rt, cols, dgamma, dbeta);
+    (void)launch_kernel(ln_bwd_reduce_kernel, (unsigned)((cols + 31) / 32), 256, 0, st, 0, pdl, part, n_rt, cols, dgamma, dbeta);
     note_launch();
     return check_launch("fp8_layernorm_bwd(reduce)");
 }

@@ -105,6 +105,8 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
                                                                     uint8_t *__restrict__ col_q,
                                                                     uint8_t *__restrict__ col_s,
                                                                     float *__restrict__ ws) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
     constexpr int ROW_BYTES = 128 * ESZ, STAGE = 128 * ROW_BYTES;
     extern __shared__ __align__(16) uint8_t mq_smem[];
@@ -303,6 +305,8 @@ __global__ void __launch_bounds__(MQ_THREADS) mxfp8_quantize_kernel(const void *
 // real row) are set to 127 (2^0): the GEMM then multiplies the zero-filled
 // padding data by 1.
 __global__ void sf_pad_kernel(uint8_t *__restrict__ s, int64_t R, int64_t NB, int64_t Rp, int64_t NBp) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     const int64_t n1 = (Rp - R) * NBp, n2 = R * (NBp - NB);
     int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
     int64_t r, b;
@@ -319,11 +323,11 @@ __global__ void sf_pad_kernel(uint8_t *__restrict__ s, int64_t R, int64_t NB, in
     s[sf_offset(r, b, NBp / 4)] = 127;
 }
 
-static void launch_sf_pad(uint8_t *s, int64_t R, int64_t NB, cudaStream_t st) {
+static void launch_sf_pad(uint8_t *s, int64_t R, int64_t NB, cudaStream_t st, bool pdl) {
     const int64_t Rp = (R + 127) / 128 * 128, NBp = (NB + 3) / 4 * 4;
     const int64_t n = (Rp - R) * NBp + R * (NBp - NB);
     if (n > 0) {
-        sf_pad_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(s, R, NB, Rp, NBp);
+        (void)launch_kernel(sf_pad_kernel, (unsigned)((n + 255) / 256), 256, 0, st, 0, pdl, s, R, NB, Rp, NBp);
         note_launch();
     }
 }
@@ -433,6 +437,8 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    pdl_wait();  // set-up done; the previous kernel of the stream has completed
+    pdl_trigger();
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------------ producer
@@ -660,29 +666,30 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
         }
     }
     const cudaStream_t st = (cudaStream_t)stream;
+    const bool pdl = short_call_bytes((double)rows * cols * (x_dtype == FP8DL_BF16 ? 4 : 6));
     if (x_dtype == FP8DL_BF16) {
         if (ws)
-            mxfp8_quantize_kernel<FP8DL_BF16, true><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+            (void)launch_kernel(mxfp8_quantize_kernel<FP8DL_BF16, true>, grid, MQ_THREADS, smem, st, 0, pdl, x, rows, cols, row_q, row_s, col_q,
                                                                                   col_s, ws);
         else
-            mxfp8_quantize_kernel<FP8DL_BF16, false><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+            (void)launch_kernel(mxfp8_quantize_kernel<FP8DL_BF16, false>, grid, MQ_THREADS, smem, st, 0, pdl, x, rows, cols, row_q, row_s, col_q,
                                                                                    col_s, nullptr);
     } else {
         if (ws)
-            mxfp8_quantize_kernel<FP8DL_F32, true><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+            (void)launch_kernel(mxfp8_quantize_kernel<FP8DL_F32, true>, grid, MQ_THREADS, smem, st, 0, pdl, x, rows, cols, row_q, row_s, col_q,
                                                                                  col_s, ws);
         else
-            mxfp8_quantize_kernel<FP8DL_F32, false><<<grid, MQ_THREADS, smem, st>>>(x, rows, cols, row_q, row_s, col_q,
+            (void)launch_kernel(mxfp8_quantize_kernel<FP8DL_F32, false>, grid, MQ_THREADS, smem, st, 0, pdl, x, rows, cols, row_q, row_s, col_q,
                                                                                   col_s, nullptr);
     }
     note_launch();
     FP8DL_TRY(check_launch("mxfp8_quantize"));
     if (dbias) {
-        colsum_reduce(ws, row_tiles, cols, dbias, (cudaStream_t)stream);
+        colsum_reduce(ws, row_tiles, cols, dbias, (cudaStream_t)stream, pdl);
         FP8DL_TRY(check_launch("mxfp8_quantize(dbias reduce)"));
     }
-    if (row_s) launch_sf_pad(row_s, rows, cols / 32, (cudaStream_t)stream);
-    if (col_s) launch_sf_pad(col_s, cols, rows / 32, (cudaStream_t)stream);
+    if (row_s) launch_sf_pad(row_s, rows, cols / 32, (cudaStream_t)stream, pdl);
+    if (col_s) launch_sf_pad(col_s, cols, rows / 32, (cudaStream_t)stream, pdl);
     return check_launch("mxfp8_quantize(scale padding)");
 }
 
@@ -736,7 +743,8 @@ fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, 
     }
     const int64_t tiles = ((M + mx::BM - 1) / mx::BM) * ((N + mx::BN - 1) / mx::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-    mxfp8_gemm_kernel<<<grid, mx::THREADS, mx::SMEM_BYTES, (cudaStream_t)stream>>>(ta, tb, args);
+    const bool pdl = short_call_flops(2.0 * (double)M * (double)N * (double)K);
+    (void)launch_kernel(mxfp8_gemm_kernel, grid, mx::THREADS, mx::SMEM_BYTES, (cudaStream_t)stream, 0, pdl, ta, tb, args);
     note_launch();
     return check_launch("mxfp8_gemm");
 }

@@ -42,6 +42,8 @@ __device__ __forceinline__ void recompute(SlotHeader *h, float a, int margin) {
 // One warp per slot.
 __global__ void update_scale_kernel(void *state, int64_t stride, int n_slots, int L, int margin,
                                     int do_recompute, int seed) {
+    pdl_wait();  // the previous kernel of the stream has completed
+    pdl_trigger();
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (warp >= n_slots) return;
@@ -109,7 +111,7 @@ static fp8dl_status launch_update(const fp8dl_recipe *recipe, int32_t n_slots, v
     const int do_recompute = seed ? 1 : (step % recipe->interval == 0);
     const int threads = 256, slots_per_block = threads / 32;
     const int blocks = (n_slots + slots_per_block - 1) / slots_per_block;
-    update_scale_kernel<<<blocks, threads, 0, stream>>>(state, stride, n_slots, recipe->amax_history_len,
+    (void)launch_kernel(update_scale_kernel, blocks, threads, 0, stream, 0, true, state, stride, n_slots, recipe->amax_history_len,
                                                         recipe->margin, do_recompute, seed);
     note_launch();
     return check_launch(seed ? "fp8_seed_amax_history" : "fp8_update_scale");

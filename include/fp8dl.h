@@ -408,7 +408,17 @@ uint64_t fp8dl_kernel_launches(void);
  *   FP8DL_GEMM_GROUP=g          tiles per group (g > 0)
  *   FP8DL_LN_VARIANT=tiles      LayerNorm by the two-pass tile kernels
  *   FP8DL_LN_CLUSTERS=n         cap on the clusters of the LayerNorm cluster kernels
- * All but FP8DL_DEBUG are read at each call. */
+ *   FP8DL_PDL=0                 launch without programmatic dependent launch: every
+ *                               kernel then starts only after the previous kernel of
+ *                               its stream has finished (read once per process)
+ * All but FP8DL_DEBUG and FP8DL_PDL are read at each call.
+ *
+ * Launch order.  Every compute kernel is launched with the programmatic stream
+ * serialization attribute: it may be scheduled while the previous kernel of the
+ * stream is still running, does only its own set-up (shared-memory barriers,
+ * tensor-memory allocation, descriptor prefetch), and waits for that kernel to
+ * complete before its first access to global memory.  Stream order and results
+ * are those of ordinary launches. */
 
 #ifdef __cplusplus
 }
