@@ -74,12 +74,12 @@ struct OpArgs {
 
 // One 128 x 128 tile of the cast; every thread of the CTA calls it with the same tile.
 // amax: the calling thread's running max of |x|.
-template <int XKIND, int FMT, int OP>
+template <int XKIND, int FMT, int OP, bool ACC>
 __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpArgs &op, int64_t rows, int64_t cols,
                                           int64_t tile, float scale, uint8_t *__restrict__ out,
                                           uint8_t *__restrict__ out_t, float *__restrict__ ws,
                                           uint16_t *__restrict__ pre_out, uint8_t *stage, float (*red)[CT_COLS],
-                                          float &amax) {
+                                          float &amax, float2 *accsm) {
     constexpr int ESZ = XKIND == FP8DL_BF16 ? 2 : 4;
     const int t = threadIdx.x;
     const int cb = t & 7, rb = t >> 3;                               // phase 1
@@ -188,7 +188,17 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
     }
     if constexpr (XKIND == FP8DL_BF16 && OP == OP_NONE)
         amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(amax2)), fabsf(bf16_hi(amax2))));
-    if (ws) {
+    // ACC: the CTA's running column sums in shared memory (accsm[k][thread]), flushed by the
+    // caller after its last tile; else this tile writes its own ws row
+    if constexpr (ACC) {
+        if (ws) {
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                accsm[k * CT_THREADS + t] = __fadd2_rn(accsm[k * CT_THREADS + t], csum[k]);
+        }
+    }
+    const bool wsf = !ACC && ws;
+    if (wsf) {
         // lanes l, l+8, l+16, l+24 share a column block: reduce over them, then lanes 0-7
         // hold the warp's 16-row partial of columns 16*cb .. 16*cb+15
 #pragma unroll
@@ -207,7 +217,7 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
                 dst[j] = make_float4(csum[2 * j].x, csum[2 * j].y, csum[2 * j + 1].x, csum[2 * j + 1].y);
         }
     }
-    if (out_t || ws) __syncthreads();
+    if (out_t || wsf) __syncthreads();
     if (out_t) {
         const int rl = 32 * p2_rg + 16 * p2_h;  // first of this thread's 16 rows within the tile
         if (r0 + rl < rows && c0 + 4 * p2_w < cols) {
@@ -233,7 +243,7 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
                     make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
         }
     }
-    if (ws) {
+    if (wsf) {
         const int64_t tr = r0 / CT_ROWS;
         if (t < CT_COLS && c0 + t < cols) {
             float s = 0.0f;
@@ -242,7 +252,38 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
             ws[tr * cols + c0 + t] = s;
         }
     }
-    if (out_t || ws) __syncthreads();
+    if (out_t || wsf) __syncthreads();
+}
+
+// The CTA's column sums (csum: this thread's 16 columns as pairs, phase-1 layout) added over
+// its threads in the fixed order of the per-tile flush above and written to ws_row[0 .. 128)
+// (columns c0 .. c0 + 127; none beyond cols).  Every thread calls it.
+__device__ __forceinline__ void colsum_flush(float2 (&csum)[8], float (*red)[CT_COLS], float *ws_row, int64_t c0,
+                                             int64_t cols) {
+    const int t = threadIdx.x, lane = t & 31, wi = t >> 5, cb = t & 7;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+#pragma unroll
+        for (int o = 8; o <= 16; o <<= 1) {
+            const float2 p = make_float2(__shfl_xor_sync(0xffffffffu, csum[k].x, o),
+                                         __shfl_xor_sync(0xffffffffu, csum[k].y, o));
+            csum[k] = __fadd2_rn(csum[k], p);
+        }
+    }
+    if (lane < 8) {
+        float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            dst[j] = make_float4(csum[2 * j].x, csum[2 * j].y, csum[2 * j + 1].x, csum[2 * j + 1].y);
+    }
+    __syncthreads();
+    if (t < CT_COLS && c0 + t < cols) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
+        ws_row[t] = s;
+    }
+    __syncthreads();
 }
 
 // The CTA's largest |x| max-ed into *amax_p; every thread calls it (wmax: CT_THREADS / 32 floats).
@@ -259,7 +300,7 @@ __device__ __forceinline__ void cta_amax_flush(float amax, float *amax_p, float 
     __syncthreads();  // wmax is free again
 }
 
-template <int XKIND, int FMT, int OP>
+template <int XKIND, int FMT, int OP, bool ACC>
 __global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_NONE ? 3 : (XKIND == FP8DL_BF16 ? 4 : 2))
     cast_kernel(const void *__restrict__ x, const OpArgs op, int64_t rows, int64_t cols,
                 const float *__restrict__ scale_p, uint8_t *__restrict__ out, uint8_t *__restrict__ out_t,
@@ -268,12 +309,29 @@ __global__ void __launch_bounds__(CT_THREADS, OP == OP_LAYERNORM ? 2 : OP != OP_
     pdl_trigger();
     __shared__ __align__(16) uint8_t stage[CT_ROWS * CT_COLS];
     __shared__ __align__(16) float red[CT_THREADS / 32][CT_COLS];  // per-warp column partials (dbias)
+    __shared__ __align__(16) float2 accsm[ACC ? 8 * CT_THREADS : 1];  // running column sums (ACC)
     __shared__ float wmax[CT_THREADS / 32];
     const float scale = out || out_t ? __ldg(scale_p) : 1.0f;
-    const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
+    const int64_t tiles_c = (cols + CT_COLS - 1) / CT_COLS, tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * tiles_c;
     float amax = 0.0f;
+    // ACC: the grid is a multiple of tiles_c, so every tile of this CTA lies in column block
+    // blockIdx.x % tiles_c; its column sums gather in accsm and go to ws row blockIdx.x / tiles_c
+    // once.  Otherwise every tile writes its own ws row.
+    const bool acc = ACC && ws;
+    if (acc) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) accsm[k * CT_THREADS + threadIdx.x] = make_float2(0.0f, 0.0f);
+    }
     for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x)
-        cast_tile<XKIND, FMT, OP>(x, op, rows, cols, tile, scale, out, out_t, ws, pre_out, stage, red, amax);
+        cast_tile<XKIND, FMT, OP, ACC>(x, op, rows, cols, tile, scale, out, out_t, ws, pre_out, stage, red, amax,
+                                       accsm);
+    if (acc) {
+        float2 csum[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++) csum[k] = accsm[k * CT_THREADS + threadIdx.x];
+        const int64_t c0 = (blockIdx.x % tiles_c) * CT_COLS;
+        colsum_flush(csum, red, ws + (blockIdx.x / tiles_c) * cols + c0, c0, cols);
+    }
     if (amax_p) cta_amax_flush(amax, amax_p, wmax);
 }
 
@@ -313,8 +371,8 @@ __global__ void __launch_bounds__(CT_THREADS, XKIND == FP8DL_BF16 ? 4 : 2)
         }
         const int64_t first = item ? a.tile_end[item - 1] : 0;
         const float scale = (a.out[item] || a.out_t[item]) ? __ldg(a.scale[item]) : 1.0f;
-        cast_tile<XKIND, FMT, OP_NONE>(a.x[item], OpArgs{}, a.rows[item], a.cols[item], tile - first, scale,
-                                       a.out[item], a.out_t[item], nullptr, nullptr, stage, red, amax);
+        cast_tile<XKIND, FMT, OP_NONE, false>(a.x[item], OpArgs{}, a.rows[item], a.cols[item], tile - first, scale,
+                                       a.out[item], a.out_t[item], nullptr, nullptr, stage, red, amax, nullptr);
     }
     if (a.amax[item]) cta_amax_flush(amax, a.amax[item], wmax);
 }
@@ -398,31 +456,52 @@ static dim3 resident_grid(const void *kernel, std::atomic<int> &per_sm, int64_t 
     return dim3((unsigned)(tiles < slots ? tiles : slots));
 }
 
-template <int XKIND, int FMT, int OP>
+template <int XKIND, int FMT, int OP, bool ACC = false>
 static dim3 cast_grid(int64_t tiles, int sms) {
     static std::atomic<int> per_sm{0};
-    return resident_grid((const void *)cast_kernel<XKIND, FMT, OP>, per_sm, tiles, sms);
+    return resident_grid((const void *)cast_kernel<XKIND, FMT, OP, ACC>, per_sm, tiles, sms);
+}
+
+// A cast with column sums (ws != NULL) runs the running-sum variant when its grid can be a
+// multiple of the column-tile count: every CTA then stays in one column block and writes one
+// ws row.  Returns the ws rows the column-sum reduction adds.
+template <int XKIND, int FMT, int OP>
+static int64_t launch_cast_op(int64_t tiles, int sms, cudaStream_t st, const void *x, const OpArgs &op, int64_t rows,
+                              int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *ws,
+                              uint16_t *pre_out, bool pdl) {
+    const int64_t tiles_c = (cols + CT_COLS - 1) / CT_COLS;
+    if (ws) {
+        dim3 grid = cast_grid<XKIND, FMT, OP, true>(tiles, sms);
+        if ((int64_t)grid.x >= tiles_c) {
+            grid.x -= (unsigned)((int64_t)grid.x % tiles_c);
+            (void)launch_kernel(cast_kernel<XKIND, FMT, OP, true>, grid, CT_THREADS, 0, st, 0, pdl, x, op, rows, cols,
+                                scale, out, out_t, amax, ws, pre_out);
+            note_launch();
+            return (int64_t)grid.x / tiles_c;
+        }
+    }
+    (void)launch_kernel(cast_kernel<XKIND, FMT, OP, false>, cast_grid<XKIND, FMT, OP, false>(tiles, sms), CT_THREADS, 0,
+                        st, 0, pdl, x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
+    note_launch();
+    return (rows + CT_ROWS - 1) / CT_ROWS;
 }
 
 template <int XKIND, int FMT>
-static void launch_cast(int64_t tiles, int sms, cudaStream_t st, const void *x, int64_t rows, int64_t cols, const float *scale,
-                        uint8_t *out, uint8_t *out_t, float *amax, float *ws, bool pdl) {
-    (void)launch_kernel(cast_kernel<XKIND, FMT, OP_NONE>, cast_grid<XKIND, FMT, OP_NONE>(tiles, sms), CT_THREADS, 0, st, 0, pdl, 
-        x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, nullptr);
-    note_launch();
+static int64_t launch_cast(int64_t tiles, int sms, cudaStream_t st, const void *x, int64_t rows, int64_t cols,
+                           const float *scale, uint8_t *out, uint8_t *out_t, float *amax, float *ws, bool pdl) {
+    return launch_cast_op<XKIND, FMT, OP_NONE>(tiles, sms, st, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws,
+                                               nullptr, pdl);
 }
 
 template <int OP>
-static void launch_op_cast(int64_t tiles, int sms, cudaStream_t st, int fmt, const void *x, const OpArgs &op,
-                           int64_t rows, int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t, float *amax,
-                           float *ws, uint16_t *pre_out, bool pdl) {
+static int64_t launch_op_cast(int64_t tiles, int sms, cudaStream_t st, int fmt, const void *x, const OpArgs &op,
+                              int64_t rows, int64_t cols, const float *scale, uint8_t *out, uint8_t *out_t,
+                              float *amax, float *ws, uint16_t *pre_out, bool pdl) {
     if (fmt == FP8DL_E4M3)
-        (void)launch_kernel(cast_kernel<FP8DL_BF16, FP8DL_E4M3, OP>, cast_grid<FP8DL_BF16, FP8DL_E4M3, OP>(tiles, sms), CT_THREADS, 0,
-                                                   st, 0, pdl, x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
-    else
-        (void)launch_kernel(cast_kernel<FP8DL_BF16, FP8DL_E5M2, OP>, cast_grid<FP8DL_BF16, FP8DL_E5M2, OP>(tiles, sms), CT_THREADS, 0,
-                                                   st, 0, pdl, x, op, rows, cols, scale, out, out_t, amax, ws, pre_out);
-    note_launch();
+        return launch_cast_op<FP8DL_BF16, FP8DL_E4M3, OP>(tiles, sms, st, x, op, rows, cols, scale, out, out_t, amax, ws,
+                                                          pre_out, pdl);
+    return launch_cast_op<FP8DL_BF16, FP8DL_E5M2, OP>(tiles, sms, st, x, op, rows, cols, scale, out, out_t, amax, ws,
+                                                      pre_out, pdl);
 }
 
 // LayerNorm + cast over 128 x 128 tiles, given the per-row statistics (used by
@@ -485,21 +564,21 @@ fp8dl_status fp8_cast_amax_transpose(const void *x, int32_t x_dtype, int64_t row
     const int64_t tiles = ((rows + CT_ROWS - 1) / CT_ROWS) * ((cols + CT_COLS - 1) / CT_COLS);
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     const bool pdl = short_call_bytes((double)rows * cols * (x_dtype == FP8DL_BF16 ? 4 : 6));
+    int64_t ws_rows = 0;  // ws rows the column-sum reduction adds
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     } else {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     }
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose"));
     if (dbias) {
-        const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        launch_colsum_reduce(ws, n_tiles, cols, dbias, st, pdl);
+        launch_colsum_reduce(ws, ws_rows, cols, dbias, st, pdl);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose(dbias reduce)"));
     }
     if (scale_inv_out) {
@@ -613,16 +692,16 @@ static fp8dl_status op_cast_common(int op, const void *x, const void *aux, int64
     float *ws = dbias ? static_cast<float *>(workspace) : nullptr;
     uint16_t *pre = static_cast<uint16_t *>(pre_out);
     const bool pdl = short_call_bytes((double)rows * cols * (op == OP_DGELU ? 8 : 6));
+    int64_t ws_rows = 0;  // ws rows the column-sum reduction adds
     if (op == OP_GELU)
-        launch_op_cast<OP_GELU>(tiles, sms, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre,
+        ws_rows = launch_op_cast<OP_GELU>(tiles, sms, st, out_dtype, x, OpArgs{}, rows, cols, scale, out, out_t, amax, ws, pre,
                                 pdl);
     else
-        launch_op_cast<OP_DGELU>(tiles, sms, st, out_dtype, x, OpArgs{aux, nullptr, nullptr, nullptr, nullptr}, rows, cols,
+        ws_rows = launch_op_cast<OP_DGELU>(tiles, sms, st, out_dtype, x, OpArgs{aux, nullptr, nullptr, nullptr, nullptr}, rows, cols,
                                  scale, out, out_t, amax, ws, pre, pdl);
     FP8DL_TRY(check_launch(name));
     if (dbias) {
-        const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        launch_colsum_reduce(ws, n_tiles, cols, dbias, st, pdl);
+        launch_colsum_reduce(ws, ws_rows, cols, dbias, st, pdl);
         FP8DL_TRY(check_launch(name));
     }
     return FP8DL_OK;
@@ -719,21 +798,21 @@ extern "C" fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x
     static std::mutex scratch_order;
     std::unique_lock<std::mutex> order(scratch_order, std::defer_lock);
     if (dbias) order.lock();
+    int64_t ws_rows = 0;  // ws rows the column-sum reduction adds
     if (x_dtype == FP8DL_BF16) {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_BF16, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_BF16, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     } else {
         if (out_dtype == FP8DL_E4M3)
-            launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_F32, FP8DL_E4M3>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
         else
-            launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
+            ws_rows = launch_cast<FP8DL_F32, FP8DL_E5M2>(tiles, sms, st, x, rows, cols, scale, out, out_t, amax, ws, pdl);
     }
     FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc"));
     if (dbias) {
-        const int64_t n_tiles = (rows + CT_ROWS - 1) / CT_ROWS;
-        launch_colsum_reduce(ws, n_tiles, cols, dbias, st, pdl);
+        launch_colsum_reduce(ws, ws_rows, cols, dbias, st, pdl);
         FP8DL_TRY(check_launch("fp8_cast_amax_transpose_noalloc(dbias reduce)"));
     }
     return FP8DL_OK;
