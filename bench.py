@@ -47,13 +47,13 @@ FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 # once those sources differ, the line reports null instead.
 _COMMON_SRC = ("fp8_delayed_scaling_gb300/csrc/tc.cuh", "fp8_delayed_scaling_gb300/csrc/common.cuh")
 GEMM_TRAFFIC = {
-    "ln_mlp": {"bytes": 1.228e9, "sources": ("fp8_delayed_scaling_gb300/csrc/gemm.cu",) + _COMMON_SRC,
-               "src_sha256": "6b558ec13f73c57c126b20f38d15f5b5964df1151f4c1511b9a2c60514912dbc",
-               "capture": "fp8_gemm_pair_kernel<0,0>/<1,0>/<2,1> of commit 1bd2690, mean of the 6 launches of a "
+    "ln_mlp": {"bytes": 1.205e9, "sources": ("fp8_delayed_scaling_gb300/csrc/gemm.cu",) + _COMMON_SRC,
+               "src_sha256": "df56eadbbc1060d2e4772f18863fdc9b735c45480d164b9f5304ff8711e70703",
+               "capture": "fp8_gemm_pair_kernel<0,0>/<1,0>/<2,1> of commit e2e84de, mean of the 6 launches of a "
                           "step over 17 steps"},
-    "mx_mlp": {"bytes": 3.710e9, "sources": ("fp8_delayed_scaling_gb300/csrc/mxfp8.cu",) + _COMMON_SRC,
-               "src_sha256": "fad80103f5cb02b10b8573d6ee5aaca7ad5417b17cbaadfba1678e1993a60853",
-               "capture": "mxfp8_gemm_kernel of commit 0e29eba, mean of the 6 launches of a step over 17 steps"},
+    "mx_mlp": {"bytes": 3.678e9, "sources": ("fp8_delayed_scaling_gb300/csrc/mxfp8.cu",) + _COMMON_SRC,
+               "src_sha256": "e8f2c3d65b0829a9de22a8d1edc8c3f72195f5070ceea2b70098cb1438cf42b6",
+               "capture": "mxfp8_gemm_kernel of commit e2e84de, mean of the 6 launches of a step over 17 steps"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
