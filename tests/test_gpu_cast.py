@@ -57,6 +57,26 @@ def test_cast_parity(shape, kind, fmt):
     assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= bound)
 
 
+# Column sums for dbias: the running-sum variant with its grid cut to a multiple of the
+# column-tile count (2048 x 6144: 48 column tiles, 768 tiles over 608 resident CTAs), and the
+# per-tile variant, which only a row wider than the resident grid (640 column tiles) takes.
+@pytest.mark.parametrize("shape", [(2048, 6144), (16, 81920)])
+def test_cast_dbias_paths(shape):
+    dev = gpu()
+    g = wl.generator(33, "cast-dbias/%s" % (shape,))
+    x = wl.with_outliers(wl.normal(shape, 1e-3, g, torch.bfloat16), 0.001, 1000.0, g)
+    xs = host(x)
+    scale = np.float32(oracle.fp8_max(1)) / oracle.amax(xs) / np.float32(2.0)
+    out, out_t, amax, db = _run_cast(x.to(dev), 1, float(scale), dbias=True)
+    q = oracle.quantize(1, xs, float(scale))
+    assert np.array_equal(out.cpu().numpy(), q)
+    assert np.array_equal(out_t.cpu().numpy(), q.T)
+    assert amax.item() == oracle.amax(xs)
+    s, sabs = oracle.colsum(xs)
+    bound = shape[0] * 2.0 ** -24 * sabs + 1e-30
+    assert np.all(np.abs(db.cpu().numpy().astype(np.float64) - s) <= bound)
+
+
 @pytest.mark.parametrize("kind,fmt", [(torch.bfloat16, 0), (torch.float32, 1)])
 def test_grouped_cast_parity(kind, fmt):
     """fp8_cast_amax_transpose_multi: several tensors of different (ragged) shapes and scales in
