@@ -102,8 +102,8 @@ fp8dl_status launch_layernorm_tile_cast(const void *x, const float *mu, const fl
 //     and block j is normalised and written.
 // The forward reduces block j+1 and then gathers block j, spreading the merge
 // over all threads (one barrier publishes both); the backward, with shorter
-// blocks, pushes block j+1 first so that block j's pushes have longer to
-// arrive, and warp 0 merges.
+// blocks, pushes block j+1 (warp 0) before block j is gathered (warp 1), so
+// that block j's pushes have longer to arrive.
 // The exchange's latency is thus hidden behind a whole block's work, and no
 // cluster-wide barrier or release fence (which would also wait for the
 // previous block's global stores) sits in the loop.  Slots rotate over four
@@ -752,19 +752,20 @@ __global__ void __launch_bounds__(LC_THREADS, LB_CTAS) ln_bwd_cluster_kernel(
             __syncthreads();
             push(nslot);
         }
-        if (t < BLK) {
+        if (t >= 32 && t < 32 + BLK) {  // warp 1 gathers while warp 0 pushes
+            const int r = t - 32;
             // every CTA's partials of block j have arrived (a wait that runs out leaves NaN)
             const bool arrived = mbar_wait_bounded(smem_u32(&xbar[slot]), (uint32_t)((j / LC_SLOTS) & 1));
             const float nan = __int_as_float(0x7fc00000);
             float2 tot = arrived ? make_float2(0.0f, 0.0f) : make_float2(nan, nan);
             for (uint32_t k = 0; k < ncta; k++) {  // rank order
-                const float2 p = gath[(slot * ncta + k) * BLK + t];
+                const float2 p = gath[(slot * ncta + k) * BLK + r];
                 tot.x += p.x;
                 tot.y += p.y;
             }
-            cst[t] = make_float2(tot.x * inv_cols, tot.y * inv_cols);
+            cst[r] = make_float2(tot.x * inv_cols, tot.y * inv_cols);
             // the slot's next block: its barrier counts the pushes of block j + LC_SLOTS
-            if (t == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
+            if (r == 0 && j + LC_SLOTS < nb) mbar_expect_tx(smem_u32(&xbar[slot]), push_bytes);
         }
         __syncthreads();
         if (r0 + RPT * g < rows) {  // rows are a multiple of 16: always
