@@ -43,27 +43,37 @@ METRIC = "FP8 linear fwd+bwd TFLOP/s & cast/amax GB/s, % of GB300 FP8/HBM peak"
 FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 # DRAM bytes (read + write) per GEMM launch, the mean over one step's GEMM launches, from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of every GEMM launch of the
-# workload's steps).  Each figure carries the SHA-256 of the kernel sources it was taken with;
-# once those sources differ, the line reports null instead.
+# workload's steps).  Each figure carries the SHA-256 of the code of the kernel sources it was
+# taken with (comments left out); once that code differs, the line reports null instead.
 _COMMON_SRC = ("fp8_delayed_scaling_gb300/csrc/tc.cuh", "fp8_delayed_scaling_gb300/csrc/common.cuh")
 GEMM_TRAFFIC = {
     "ln_mlp": {"bytes": 1.205e9, "sources": ("fp8_delayed_scaling_gb300/csrc/gemm.cu",) + _COMMON_SRC,
-               "src_sha256": "df56eadbbc1060d2e4772f18863fdc9b735c45480d164b9f5304ff8711e70703",
+               "src_sha256": "70cc0cd69d2b8960bfcfffa2cb9ad72a1bb6ce0c90d0e7dfb23f08c21e8425c4",
                "capture": "fp8_gemm_pair_kernel<0,0>/<1,0>/<2,1> of commit e2e84de, mean of the 6 launches of a "
                           "step over 17 steps"},
     "mx_mlp": {"bytes": 3.678e9, "sources": ("fp8_delayed_scaling_gb300/csrc/mxfp8.cu",) + _COMMON_SRC,
-               "src_sha256": "e8f2c3d65b0829a9de22a8d1edc8c3f72195f5070ceea2b70098cb1438cf42b6",
+               "src_sha256": "7a324d5472d4af9d0fd416758f392649800eda844bdaf2278ec4e5e704e651a6",
                "capture": "mxfp8_gemm_kernel of commit e2e84de, mean of the 6 launches of a step over 17 steps"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def source_code(src):
+    """C/C++ source without its comments and blank lines (what the compiler sees of it, near enough
+    that a comment-only edit leaves it unchanged)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def source_sha(paths):
+    """SHA-256 of the code of the given sources, comments left out."""
     import hashlib
     h = hashlib.sha256()
     for rel in paths:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel)) as f:
+            h.update(source_code(f.read()).encode())
     return h.hexdigest()
 
 

@@ -58,9 +58,10 @@ inline bool dim_ok(int64_t d, int64_t mult) { return d > 0 && d % mult == 0 && d
     } while (0)
 
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch.  The library launches its kernels with the
-// programmatic stream serialization attribute (unless FP8DL_PDL=0), so a kernel
-// may start while the previous kernel of its stream is still running: its
+// Programmatic dependent launch.  The library launches the kernels of short
+// calls (short_call_bytes / short_call_flops below) with the programmatic
+// stream serialization attribute (unless FP8DL_PDL=0), so such a kernel may
+// start while the previous kernel of its stream is still running: its
 // launch and set-up (barrier initialisation, tensor-memory allocation,
 // descriptor prefetch) overlap that kernel's tail.  pdl_wait() blocks until the
 // previous kernel has completed and its memory operations are visible; every

@@ -413,12 +413,13 @@ uint64_t fp8dl_kernel_launches(void);
  *                               its stream has finished (read once per process)
  * All but FP8DL_DEBUG and FP8DL_PDL are read at each call.
  *
- * Launch order.  Every compute kernel is launched with the programmatic stream
- * serialization attribute: it may be scheduled while the previous kernel of the
- * stream is still running, does only its own set-up (shared-memory barriers,
- * tensor-memory allocation, descriptor prefetch), and waits for that kernel to
- * complete before its first access to global memory.  Stream order and results
- * are those of ordinary launches. */
+ * Launch order.  The kernels of a short call (under 64 MB moved or 64 GFLOP)
+ * are launched with the programmatic stream serialization attribute: such a
+ * kernel may be scheduled while the previous kernel of the stream is still
+ * running, does only its own set-up (shared-memory barriers, tensor-memory
+ * allocation, descriptor prefetch), and waits for that kernel to complete
+ * before its first access to global memory.  Every kernel makes that wait, so
+ * stream order and results are those of ordinary launches. */
 
 #ifdef __cplusplus
 }
