@@ -72,6 +72,38 @@ struct OpArgs {
     const uint16_t *gamma, *beta;
 };
 
+// Column sums (csum: this thread's 16 columns as pairs, in the tile's phase-1 layout) added
+// over the CTA's threads in a fixed order (lanes l, l+8, l+16, l+24 of a warp, then the eight
+// warps) and written to ws_row[0 .. 128) (columns c0 .. c0 + 127; none beyond cols).  Every
+// thread calls it; it holds two CTA barriers.
+__device__ __forceinline__ void colsum_flush(float2 (&csum)[8], float (*red)[CT_COLS], float *ws_row, int64_t c0,
+                                             int64_t cols) {
+    const int t = threadIdx.x, lane = t & 31, wi = t >> 5, cb = t & 7;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+#pragma unroll
+        for (int o = 8; o <= 16; o <<= 1) {
+            const float2 p = make_float2(__shfl_xor_sync(0xffffffffu, csum[k].x, o),
+                                         __shfl_xor_sync(0xffffffffu, csum[k].y, o));
+            csum[k] = __fadd2_rn(csum[k], p);
+        }
+    }
+    if (lane < 8) {
+        float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
+#pragma unroll
+        for (int j = 0; j < 4; j++)
+            dst[j] = make_float4(csum[2 * j].x, csum[2 * j].y, csum[2 * j + 1].x, csum[2 * j + 1].y);
+    }
+    __syncthreads();
+    if (t < CT_COLS && c0 + t < cols) {
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
+        ws_row[t] = s;
+    }
+    __syncthreads();
+}
+
 // One 128 x 128 tile of the cast; every thread of the CTA calls it with the same tile.
 // amax: the calling thread's running max of |x|.
 template <int XKIND, int FMT, int OP, bool ACC>
@@ -197,27 +229,8 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
                 accsm[k * CT_THREADS + t] = __fadd2_rn(accsm[k * CT_THREADS + t], csum[k]);
         }
     }
-    const bool wsf = !ACC && ws;
-    if (wsf) {
-        // lanes l, l+8, l+16, l+24 share a column block: reduce over them, then lanes 0-7
-        // hold the warp's 16-row partial of columns 16*cb .. 16*cb+15
-#pragma unroll
-        for (int k = 0; k < 8; k++) {
-#pragma unroll
-            for (int o = 8; o <= 16; o <<= 1) {
-                const float2 p = make_float2(__shfl_xor_sync(0xffffffffu, csum[k].x, o),
-                                             __shfl_xor_sync(0xffffffffu, csum[k].y, o));
-                csum[k] = __fadd2_rn(csum[k], p);
-            }
-        }
-        if (lane < 8) {
-            float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
-#pragma unroll
-            for (int j = 0; j < 4; j++)
-                dst[j] = make_float4(csum[2 * j].x, csum[2 * j].y, csum[2 * j + 1].x, csum[2 * j + 1].y);
-        }
-    }
-    if (out_t || wsf) __syncthreads();
+    const bool wsf = !ACC && ws;  // this tile's column sums go to its own ws row (after phase 2)
+    if (out_t) __syncthreads();
     if (out_t) {
         const int rl = 32 * p2_rg + 16 * p2_h;  // first of this thread's 16 rows within the tile
         if (r0 + rl < rows && c0 + 4 * p2_w < cols) {
@@ -243,47 +256,8 @@ __device__ __forceinline__ void cast_tile(const void *__restrict__ x, const OpAr
                     make_uint4(col[j][0], col[j][1], col[j][2], col[j][3]);
         }
     }
-    if (wsf) {
-        const int64_t tr = r0 / CT_ROWS;
-        if (t < CT_COLS && c0 + t < cols) {
-            float s = 0.0f;
-#pragma unroll
-            for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
-            ws[tr * cols + c0 + t] = s;
-        }
-    }
-    if (out_t || wsf) __syncthreads();
-}
-
-// The CTA's column sums (csum: this thread's 16 columns as pairs, phase-1 layout) added over
-// its threads in the fixed order of the per-tile flush above and written to ws_row[0 .. 128)
-// (columns c0 .. c0 + 127; none beyond cols).  Every thread calls it.
-__device__ __forceinline__ void colsum_flush(float2 (&csum)[8], float (*red)[CT_COLS], float *ws_row, int64_t c0,
-                                             int64_t cols) {
-    const int t = threadIdx.x, lane = t & 31, wi = t >> 5, cb = t & 7;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-#pragma unroll
-        for (int o = 8; o <= 16; o <<= 1) {
-            const float2 p = make_float2(__shfl_xor_sync(0xffffffffu, csum[k].x, o),
-                                         __shfl_xor_sync(0xffffffffu, csum[k].y, o));
-            csum[k] = __fadd2_rn(csum[k], p);
-        }
-    }
-    if (lane < 8) {
-        float4 *dst = reinterpret_cast<float4 *>(&red[wi][16 * cb]);
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-            dst[j] = make_float4(csum[2 * j].x, csum[2 * j].y, csum[2 * j + 1].x, csum[2 * j + 1].y);
-    }
-    __syncthreads();
-    if (t < CT_COLS && c0 + t < cols) {
-        float s = 0.0f;
-#pragma unroll
-        for (int k = 0; k < CT_THREADS / 32; k++) s += red[k][t];
-        ws_row[t] = s;
-    }
-    __syncthreads();
+    if (out_t) __syncthreads();
+    if (wsf) colsum_flush(csum, red, ws + (r0 / CT_ROWS) * cols + c0, c0, cols);
 }
 
 // The CTA's largest |x| max-ed into *amax_p; every thread calls it (wmax: CT_THREADS / 32 floats).

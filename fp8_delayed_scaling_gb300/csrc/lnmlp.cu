@@ -178,9 +178,10 @@ __device__ __forceinline__ float2 chan_equal(float2 a, float2 b, float half_n) {
 // ch of row r sits at chunk ch ^ ((r >> 2) & 7) of its row, so the two chunk
 // loads of a lane's row hit every bank group four times per warp.
 // Statistics: each lane takes the mean and M2 of its 16 values of a row (two
-// passes over registers); the four lanes of a row group, the eight warps and
-// the cluster's slabs (in rank order, general equal-count form
-// M2 = sum_k M2_k + n sum_k (m_k - mean)^2) are merged; var = M2 / cols,
+// passes over registers); the four lanes of a row group and then the eight
+// warps merge them (Chan's equal-count update), and the cluster's slabs are
+// combined as mean = sum_k m_k / n_slabs, M2 = sum_k (M2_k + 512 (m_k - mean)^2)
+// (each sum a fixed butterfly over the slabs); var = M2 / cols,
 // rs = 1/sqrt(var + eps).  Every CTA then normalises its slab:
 // y = bf16((x - mu) * rs * gamma + beta), codes = cvt(y * scale), written
 // row-major (out: 16 bytes per lane and row) and transposed (out_t: the four
