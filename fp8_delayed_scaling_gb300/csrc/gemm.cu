@@ -314,7 +314,9 @@ constexpr int QT_BYTES = BN * BM;  // transposed FP8 codes of one CTA's 128 x 25
 // The fused epilogues stage their transposed codes in one tile beside the full operand ring.
 __host__ __device__ constexpr int stages(int) { return STAGES; }
 __host__ __device__ constexpr int qt_bufs(int epi) { return epi ? 1 : 0; }
-constexpr int smem_bytes(int epi) { return stages(epi) * STAGE_BYTES + 1024 + qt_bufs(epi) * QT_BYTES + 1024; }
+constexpr int smem_bytes(int epi, int tn = BN) {
+    return stages(epi) * (A_BYTES + tn / 2 * BK) + 1024 + qt_bufs(epi) * QT_BYTES + 1024;
+}
 }  // namespace g2
 
 // EPI = 0: D = round(acc * s + bias).  EPI = 1 (fc1 of the LayerNormMLP): also
@@ -359,16 +361,21 @@ __device__ __forceinline__ void reduce_scatter_step(float (&y)[L], int lane) {
     }
 }
 
-template <int EPI, int QF>  // QF: FP8 format of the fused epilogue's codes
+// TN: the tile's columns, 256, or 128 for the plain GEMM of a small problem (more tiles to
+// spread over the CTA pairs).
+template <int EPI, int QF, int TN>  // QF: FP8 format of the fused epilogue's codes
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_qt, const GemmArgs args) {
     using namespace g2;
+    static_assert(TN == BN || (TN == BN / 2 && EPI == 0), "128-column tiles for the plain GEMM only");
+    constexpr int TNH = TN / 2;                    // B rows per CTA
+    constexpr int SB = A_BYTES + TNH * BK;         // one operand stage of one CTA
     constexpr int NST = stages(EPI);  // operand stages
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-    uint8_t *bar_area = smem + NST * STAGE_BYTES;
+    uint8_t *bar_area = smem + NST * SB;
     uint64_t *full = reinterpret_cast<uint64_t *>(bar_area);
     uint64_t *empty = full + NST;
     uint64_t *tfull = empty + NST;
@@ -381,7 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int64_t tiles_m = (args.M + 2 * BM - 1) / (2 * BM), tiles_n = (args.N + BN - 1) / BN;
+    const int64_t tiles_m = (args.M + 2 * BM - 1) / (2 * BM), tiles_n = (args.N + TN - 1) / TN;
     const int64_t tiles = tiles_m * tiles_n;
     const int num_kb = (int)((args.K + BK - 1) / BK);
 
@@ -427,11 +434,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     }
                     const uint32_t fb_local = smem_u32(&full[s]);
                     const uint32_t fb = mapa_shared(fb_local, 0);
-                    if (leader) mbar_expect_tx(fb_local, 2 * STAGE_BYTES);
-                    uint8_t *sa = smem + s * STAGE_BYTES;
+                    if (leader) mbar_expect_tx(fb_local, 2 * SB);
+                    uint8_t *sa = smem + s * SB;
                     tma_load_2d_pair(smem_u32(sa), &tmap_a, fb, kb * BK, (int32_t)(tm * 2 * BM + rank * BM));
                     tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmap_b, fb, kb * BK,
-                                     (int32_t)(tn * BN + rank * BNH));
+                                     (int32_t)(tn * TN + rank * TNH));
                     issued++;
                     if (++s == NST) {
                         s = 0;
@@ -459,14 +466,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * TN);
                 for (int kb = 0; kb < num_kb; kb++) {
                     if (!mbar_wait(smem_u32(&full[s]), ph, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t lo_a = desc0.lo + (uint32_t)s * (STAGE_BYTES >> 4);
+                    const uint32_t lo_a = desc0.lo + (uint32_t)s * (SB >> 4);
                     const uint32_t lo_b = lo_a + (A_BYTES >> 4);
 #pragma unroll
                     for (int kk = 0; kk < BK / 32; kk++)  // K = 32 bytes per MMA: 2 descriptor units
@@ -493,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
     } else {  // ------------------------------------------------------------ epilogue (both CTAs)
         const int q = warp & 3;                              // TMEM lane quarter
         const int part = (warp - 2) >> 2;                    // column part of the quarter
-        constexpr int CHUNKS = BN / 32 / (epi_warps(EPI) / 4);  // 32-column chunks per warp
+        constexpr int CHUNKS = TN / 32 / (epi_warps(EPI) / 4);  // 32-column chunks per warp
         constexpr int NEPI = 32 * epi_warps(EPI);            // epilogue threads
         const float sc = __fmul_rn(__ldg(args.a_scale_inv), __ldg(args.b_scale_inv));
         const float qscale = EPI ? __ldg(args.q_scale) : 0.0f;
@@ -519,8 +526,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
             const bool row_ok = row < args.M;
             const __nv_bfloat16 *hrow =
                 EPI == 2 ? static_cast<const __nv_bfloat16 *>(args.h_in) + row * args.N : nullptr;
-            if (EPI == 2 && row_ok && tn * BN + part * CHUNKS * 32 < args.N)  // this thread's h: one 128-byte line
-                prefetch_l2(hrow + tn * BN + part * CHUNKS * 32);
+            if (EPI == 2 && row_ok && tn * TN + part * CHUNKS * 32 < args.N)  // this thread's h: one 128-byte line
+                prefetch_l2(hrow + tn * TN + part * CHUNKS * 32);
             if (!mbar_wait(smem_u32(&tfull[acc]), aph, abort_flag, args.status)) break;
             tc_fence_after();
             uint8_t *qt_buf = qt_stage;
@@ -534,9 +541,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
 #pragma unroll 1
             for (int cc = 0; cc < CHUNKS; cc++) {
                 const int c = part * CHUNKS + cc;  // chunk of 32 columns within the tile
-                const int64_t n0 = tn * BN + c * 32;
+                const int64_t n0 = tn * TN + c * 32;
                 uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * BN + c * 32) + ((uint32_t)(32 * q) << 16), r);
+                tmem_ld_32x32b_x32(tmem_base + (uint32_t)(acc * TN + c * 32) + ((uint32_t)(32 * q) << 16), r);
                 float v[32];
                 if (args.bias_dtype >= 0) {
                     float b[32];
@@ -699,7 +706,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                 fence_proxy_async_smem();
                 named_barrier(1, NEPI);
                 if (threadIdx.x == 64 && tm * 2 * BM + rank * BM < args.M) {  // no store when all rows lie beyond M
-                    tma_store_2d(&tmap_qt, smem_u32(qt_buf), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * BN));
+                    tma_store_2d(&tmap_qt, smem_u32(qt_buf), (int32_t)(tm * 2 * BM + rank * BM), (int32_t)(tn * TN));
                     bulk_commit();
                 }
             }
@@ -841,15 +848,16 @@ static fp8dl_status gemm_device_setup(int dev, int sms) {
     std::lock_guard<std::mutex> lock(init_mutex());
     if (g_attr_set[dev].load(std::memory_order_relaxed)) return FP8DL_OK;
     cudaError_t e = cudaFuncSetAttribute(fp8_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g1::SMEM_BYTES);
-    const void *pair_kernels[] = {(const void *)fp8_gemm_pair_kernel<0, 0>,
-                                  (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3>,
-                                  (const void *)fp8_gemm_pair_kernel<1, FP8DL_E5M2>,
-                                  (const void *)fp8_gemm_pair_kernel<2, FP8DL_E4M3>,
-                                  (const void *)fp8_gemm_pair_kernel<2, FP8DL_E5M2>};
-    const int pair_epi[] = {0, 1, 1, 2, 2};
-    for (int k = 0; k < 5 && e == cudaSuccess; k++)
+    const void *pair_kernels[] = {(const void *)fp8_gemm_pair_kernel<0, 0, g2::BN>,
+                                  (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3, g2::BN>,
+                                  (const void *)fp8_gemm_pair_kernel<1, FP8DL_E5M2, g2::BN>,
+                                  (const void *)fp8_gemm_pair_kernel<2, FP8DL_E4M3, g2::BN>,
+                                  (const void *)fp8_gemm_pair_kernel<2, FP8DL_E5M2, g2::BN>,
+                                  (const void *)fp8_gemm_pair_kernel<0, 0, g2::BN / 2>};
+    const int pair_epi[] = {0, 1, 1, 2, 2, 0}, pair_tn[] = {g2::BN, g2::BN, g2::BN, g2::BN, g2::BN, g2::BN / 2};
+    for (int k = 0; k < 6 && e == cudaSuccess; k++)
         e = cudaFuncSetAttribute(pair_kernels[k], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 g2::smem_bytes(pair_epi[k]));
+                                 g2::smem_bytes(pair_epi[k], pair_tn[k]));
     if (e != cudaSuccess) return fail(FP8DL_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
     // how many CTA pairs can be resident at once (both pair kernels hold one CTA per SM)
     cudaLaunchConfig_t cfg = {};
@@ -857,7 +865,7 @@ static fp8dl_status gemm_device_setup(int dev, int sms) {
     cfg.blockDim = dim3(g2::threads(1), 1, 1);
     cfg.dynamicSmemBytes = g2::smem_bytes(1);
     int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&clusters, (const void *)fp8_gemm_pair_kernel<1, FP8DL_E4M3, g2::BN>, &cfg);
     if (e != cudaSuccess || clusters < 1) {
         cudaGetLastError();
         clusters = 0;  // the pair kernels are not used on this device
@@ -884,14 +892,24 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
     const bool pdl = short_call_flops(2.0 * (double)M * (double)N * (double)K);
     // Instruction descriptor, kind::f8f6f4: D fp32 (bit 4), A type bits 7-9, B type bits 10-12
     // (0 = E4M3, 1 = E5M2), both K-major, N>>3 at bits 17-22, M>>4 at bits 24-28
-    // (M = 128 for one CTA, 256 for a CTA pair; N = 256 either way).
-    const uint32_t idesc_base = (1u << 4) | ((uint32_t)a_dtype << 7) | ((uint32_t)b_dtype << 10) |
-                                ((uint32_t)(g1::BN >> 3) << 17);
+    // (M = 128 for one CTA, 256 for a CTA pair; N = the tile's columns).
+    const uint32_t idesc_ab = (1u << 4) | ((uint32_t)a_dtype << 7) | ((uint32_t)b_dtype << 10);
+    const uint32_t idesc_base = idesc_ab | ((uint32_t)(g1::BN >> 3) << 17);
     FP8DL_TRY(encode_tmap_2d_u8(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)K, g1::BK, g1::BM,
                                 CU_TENSOR_MAP_SWIZZLE_128B));
     if (use_pair) {
-        // both operands in 128-row boxes: each CTA of a pair loads its own halves
-        FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g2::BK, g2::BNH,
+        // Tile columns: 256, or 128 for a short plain GEMM (under 64 GFLOP) whose 256-column
+        // tiles would not fill two waves of the resident pairs: twice the tiles to spread.  For
+        // a long GEMM with few tiles the narrow tiles lose more than they gain (twice the MMA
+        // issues and A loads per FLOP: a 2048-token Llama micro-batch step ran 21 % slower).
+        // FP8DL_GEMM_TILE_N=256|128 overrides (testing).
+        const int64_t tiles256 = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
+        int tn = (epi == 0 && pdl && tiles256 < 2 * (int64_t)g_pair_clusters[dev]) ? g2::BN / 2 : g2::BN;
+        const char *tv = getenv("FP8DL_GEMM_TILE_N");
+        if (epi == 0 && tv && atoi(tv) == 128) tn = g2::BN / 2;
+        if (tv && atoi(tv) == 256) tn = g2::BN;
+        // A in 128-row boxes and B in tn/2-row boxes: each CTA of a pair loads its own halves
+        FP8DL_TRY(encode_tmap_2d_u8(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K, g2::BK, (uint32_t)(tn / 2),
                                     CU_TENSOR_MAP_SWIZZLE_128B));
         if (epi) {
             // q^T [N x M] codes, stored in boxes of 128 rows of the output (inner) x 256 columns
@@ -900,22 +918,25 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
         } else {
             tq = ta;  // unused
         }
-        args.idesc = idesc_base | ((uint32_t)(2 * g2::BM >> 4) << 24);
-        pick_raster(M, N, K, 2 * g2::BM, g2::BN, args.raster_n, args.group);
-        const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + g2::BN - 1) / g2::BN);
+        args.idesc = idesc_ab | ((uint32_t)(tn >> 3) << 17) | ((uint32_t)(2 * g2::BM >> 4) << 24);
+        pick_raster(M, N, K, 2 * g2::BM, tn, args.raster_n, args.group);
+        const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + tn - 1) / tn);
         const int64_t pairs = tiles < g_pair_clusters[dev] ? tiles : g_pair_clusters[dev];
         const unsigned grid = (unsigned)(2 * pairs);
         const bool e4 = args.q_fmt == FP8DL_E4M3;
         if (epi == 2 && e4)
-            (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E4M3>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E4M3, g2::BN>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
         else if (epi == 2)
-            (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E5M2>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E5M2, g2::BN>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
         else if (epi == 1 && e4)
-            (void)launch_kernel(fp8_gemm_pair_kernel<1, FP8DL_E4M3>, grid, g2::threads(1), g2::smem_bytes(1), stream, 0, pdl, ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<1, FP8DL_E4M3, g2::BN>, grid, g2::threads(1), g2::smem_bytes(1), stream, 0, pdl, ta, tb, tq, args);
         else if (epi == 1)
-            (void)launch_kernel(fp8_gemm_pair_kernel<1, FP8DL_E5M2>, grid, g2::threads(1), g2::smem_bytes(1), stream, 0, pdl, ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<1, FP8DL_E5M2, g2::BN>, grid, g2::threads(1), g2::smem_bytes(1), stream, 0, pdl, ta, tb, tq, args);
+        else if (tn == g2::BN)
+            (void)launch_kernel(fp8_gemm_pair_kernel<0, 0, g2::BN>, grid, g2::threads(0), g2::smem_bytes(0), stream, 0, pdl, ta, tb, tq, args);
         else
-            (void)launch_kernel(fp8_gemm_pair_kernel<0, 0>, grid, g2::threads(0), g2::smem_bytes(0), stream, 0, pdl, ta, tb, tq, args);
+            (void)launch_kernel(fp8_gemm_pair_kernel<0, 0, g2::BN / 2>, grid, g2::threads(0),
+                                g2::smem_bytes(0, g2::BN / 2), stream, 0, pdl, ta, tb, tq, args);
         note_launch();
         return check_launch(epi == 2 ? "fp8_gemm_dgelu_cast(pair)"
                                      : epi == 1 ? "fp8_gemm_gelu_cast(pair)" : "fp8_gemm(pair)");

@@ -122,3 +122,25 @@ def test_pair_tile_order_leaves_results_unchanged(M, N, K, monkeypatch):
         out.append(_gemm(A, 0, B, 0, 0.01, 0.02, None, torch.bfloat16, dev))
     assert not torch.isnan(out[0].float()).any()
     assert torch.equal(out[0], out[1]) and torch.equal(out[0], out[2])
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 3072, 768), (1040, 528, 2048), (2048, 784, 400)])
+def test_pair_tile_width_leaves_results_unchanged(M, N, K, monkeypatch):
+    """A plain GEMM too small to fill two waves of 256-column pair tiles runs 128-column tiles;
+    both widths give the same bits (each output element's sum runs over K in the same order),
+    and the 128-column result meets the oracle's bound on sampled elements."""
+    monkeypatch.setenv("FP8DL_GEMM_VARIANT", "2sm")
+    dev = gpu()
+    rng = np.random.default_rng(7 * M + N + K)
+    A = _codes(rng, 0, (M, K))
+    B = _codes(rng, 1, (N, K))
+    bias = torch.from_numpy(rng.standard_normal(N).astype(np.float32)).to(dev)
+    out = []
+    for width in ("128", "256"):
+        monkeypatch.setenv("FP8DL_GEMM_TILE_N", width)
+        out.append(_gemm(A, 0, B, 1, 0.01, 0.02, bias, torch.bfloat16, dev))
+    assert not torch.isnan(out[0].float()).any()
+    assert torch.equal(out[0], out[1])
+    ms, ns = sample_elems(M, N, np.random.default_rng(5), n=2048, tile_n=128)
+    ref, absr = oracle.gemm_elems(A, 0, B, 1, 0.01, 0.02, bias.cpu().numpy(), ms, ns)
+    check_gemm(out[0], ref, absr, ms, ns)
