@@ -11,6 +11,11 @@ axis with its own E8M0 scale, so there is no amax history and no delay:
             dX[M,K] = mx_gemm(dY_row, W_col)     (reduction over N)
             dW[N,K] = mx_gemm(dY_col, X_col)     (reduction over M)
             db      = column sums of dY, in the same pass as dY's quantisation
+
+Micro-batching (te modules' is_first_microbatch): forward(..., is_first_microbatch=True)
+quantises the weight and keeps both copies; later micro-batches (False) reuse them and launch
+no weight quantisation.  MXFP8 has no scaling state, so the cached codes and E8M0 scales stand
+alone.  None (the default) quantises the weight at every forward.
 """
 from __future__ import annotations
 
@@ -50,10 +55,16 @@ class MxLinear:
         self.dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
         self.db = torch.empty(N, dtype=torch.float32, device=dev) if bias is not None else None
         self.ws = torch.empty(fp8_cast_workspace_size(M, N), dtype=torch.uint8, device=dev) if bias is not None else None
+        self.w_cached = False  # mx_w holds the current weight's copies, kept for reuse
 
-    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, stream=None, is_first_microbatch=None) -> torch.Tensor:
+        if is_first_microbatch is False and not self.w_cached:
+            raise RuntimeError("is_first_microbatch=False, but no MXFP8 copy of the weight is cached: "
+                               "quantise it first with is_first_microbatch=True")
         self.mx_x.quantize(x, stream=stream)
-        self.mx_w.quantize(self.w, stream=stream)
+        if is_first_microbatch is not False:
+            self.mx_w.quantize(self.w, stream=stream)
+            self.w_cached = bool(is_first_microbatch)
         mxfp8_gemm(self.mx_x.row_q, self.mx_x.row_s, self.mx_w.row_q, self.mx_w.row_s, self.y, bias=self.b,
                    stream=stream)
         return self.y

@@ -198,3 +198,39 @@ def test_mx_linear_step_sampled():
         ref, absr = oracle.mx_gemm_elems(Ah, tiled_to_plain(As.cpu().numpy(), m, k // 32), Bh,
                                          tiled_to_plain(Bs.cpu().numpy(), n, k // 32), None, ms, ns)
         check_gemm(D, ref, absr, ms, ns, what="mx " + name)
+
+
+def test_mx_linear_weight_cache():
+    """MxLinear over micro-batches: is_first_microbatch=True quantises the weight and keeps it,
+    False reuses it with no weight quantisation (its launches are saved) and gives the same bits
+    as quantising again; False with nothing cached raises before any launch."""
+    import fp8_delayed_scaling_gb300 as fd
+    from fp8_delayed_scaling_gb300.mxlinear import MxLinear
+    dev = gpu()
+    M, K, N = 512, 1024, 768
+    seed = wl.SEEDS["mx_mlp"]
+    w = wl.normal((N, K), 0.02, wl.generator(seed, "W-cache"), torch.bfloat16).to(dev)
+    x1 = wl.channel_scaled_normal(M, K, wl.generator(seed, "X1-cache")).to(dev)
+    x2 = wl.channel_scaled_normal(M, K, wl.generator(seed, "X2-cache")).to(dev)
+    lin = MxLinear(w, None, M)
+    with pytest.raises(RuntimeError):
+        lin.forward(x1, is_first_microbatch=False)
+    fresh = MxLinear(w, None, M)
+    lin.forward(x1, is_first_microbatch=True)
+    torch.cuda.synchronize()
+    n0 = fd.fp8dl_kernel_launches()
+    y2 = lin.forward(x2, is_first_microbatch=False).clone()
+    n1 = fd.fp8dl_kernel_launches()
+    y2_ref = fresh.forward(x2).clone()
+    n2 = fd.fp8dl_kernel_launches()
+    torch.cuda.synchronize()
+    n3 = fd.fp8dl_kernel_launches()
+    fresh.mx_w.quantize(w)  # what one quantisation of the weight launches
+    n4 = fd.fp8dl_kernel_launches()
+    torch.cuda.synchronize()
+    assert torch.equal(y2, y2_ref)
+    assert n4 - n3 >= 1 and (n2 - n1) - (n1 - n0) == n4 - n3
+    dx, dw, _ = lin.backward(torch.ones((M, N), dtype=torch.bfloat16, device=dev))
+    dx_ref, dw_ref, _ = fresh.backward(torch.ones((M, N), dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dx_ref) and torch.equal(dw, dw_ref)
