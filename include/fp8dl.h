@@ -406,6 +406,9 @@ uint64_t fp8dl_kernel_launches(void);
  *   FP8DL_GEMM_VARIANT=1sm|2sm  force the one-CTA or the CTA-pair FP8 GEMM
  *   FP8DL_GEMM_RASTER=m|n       group the GEMM tiles along rows (m) or columns (n)
  *   FP8DL_GEMM_GROUP=g          tiles per group (g > 0)
+ *   FP8DL_GEMM_TILE_N=256|128   tile width of the plain pair GEMM (by default 128
+ *                               only for a short GEMM with under two waves of
+ *                               256-column tiles)
  *   FP8DL_LN_VARIANT=tiles      LayerNorm by the two-pass tile kernels
  *   FP8DL_LN_CLUSTERS=n         cap on the clusters of the LayerNorm cluster kernels
  *   FP8DL_PDL=0                 launch without programmatic dependent launch: every
