@@ -45,6 +45,7 @@ struct GemmArgs {
     int64_t M, N, K;
     int raster_n;    // 1: groups of `group` column tiles, rows outer (B panels stay in L2)
     int64_t group;   // tiles per group along the grouped dimension
+    int snake;       // 1: every other tile of a CTA pair reads its k-blocks last to first
     uint32_t idesc;
     const float *a_scale_inv, *b_scale_inv;
     const void *bias;
@@ -424,7 +425,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t tile = pair; tile < tiles && ok; tile += npairs) {
+            bool rev = false;  // this tile's k-blocks last to first (alternates per tile when snake)
+            for (int64_t tile = pair; tile < tiles && ok; tile += npairs, rev = args.snake && !rev) {
                 int64_t tm, tn;
                 tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
                 for (int kb = 0; kb < num_kb; kb++) {
@@ -436,9 +438,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(g2::threads(EPI), 1)
                     const uint32_t fb = mapa_shared(fb_local, 0);
                     if (leader) mbar_expect_tx(fb_local, 2 * SB);
                     uint8_t *sa = smem + s * SB;
-                    tma_load_2d_pair(smem_u32(sa), &tmap_a, fb, kb * BK, (int32_t)(tm * 2 * BM + rank * BM));
-                    tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmap_b, fb, kb * BK,
-                                     (int32_t)(tn * TN + rank * TNH));
+                    const int32_t kx = (rev ? num_kb - 1 - kb : kb) * BK;
+                    tma_load_2d_pair(smem_u32(sa), &tmap_a, fb, kx, (int32_t)(tm * 2 * BM + rank * BM));
+                    tma_load_2d_pair(smem_u32(sa + A_BYTES), &tmap_b, fb, kx, (int32_t)(tn * TN + rank * TNH));
                     issued++;
                     if (++s == NST) {
                         s = 0;
@@ -804,6 +806,23 @@ void pick_raster(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n
     if (g && atoll(g) > 0) group = atoll(g);
 }
 
+// K order: a CTA (pair) that runs several tiles reads the k-blocks of every other tile
+// last to first.  The tiles in flight step through K together and share panels with the
+// next wave's tiles (the grouped dimension's panels); when the next tile starts where the
+// last one ended, its first k-blocks are the ones most recently read, still in L2, instead
+// of the oldest ones, which a wave's panels have pushed out.  Each tile's sum then runs
+// over K in one of two orders, fixed by the tile's position in the CTA's sequence: the
+// result is the same on every call with the same grid and tiling.  Used only when the
+// launch has at least two waves (so short GEMMs keep one order whatever their tile width)
+// and K > 8192.  Measured DRAM reads per launch: 16384 x 4096 x 16384 1001 -> 928 MB,
+// MXFP8 16384 x 8192 x 28672 4085 -> 3509 MB; with K = 4096 or 8192, whose panels already
+// stay in L2 across waves, they rose by 1-8 %.  FP8DL_GEMM_SNAKE=0 turns it off (testing).
+int pick_snake(int64_t tiles, int64_t ctas, int64_t K) {
+    const char *v = getenv("FP8DL_GEMM_SNAKE");
+    if (v && v[0] == '0') return 0;
+    return tiles >= 2 * ctas && K > 8192 ? 1 : 0;
+}
+
 static fp8dl_status check_gemm_common(int64_t M, int64_t N, int64_t K, int64_t mult, const void *A, const void *B,
                                       const void *bias, int32_t bias_dtype, const void *D, int32_t d_dtype,
                                       bool d_required = true) {
@@ -923,6 +942,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
         const int64_t tiles = ((M + 2 * g2::BM - 1) / (2 * g2::BM)) * ((N + tn - 1) / tn);
         const int64_t pairs = tiles < g_pair_clusters[dev] ? tiles : g_pair_clusters[dev];
         const unsigned grid = (unsigned)(2 * pairs);
+        args.snake = tn == g2::BN ? pick_snake(tiles, pairs, K) : 0;
         const bool e4 = args.q_fmt == FP8DL_E4M3;
         if (epi == 2 && e4)
             (void)launch_kernel(fp8_gemm_pair_kernel<2, FP8DL_E4M3, g2::BN>, grid, g2::threads(2), g2::smem_bytes(2), stream, 0, pdl, ta, tb, tq, args);
@@ -945,6 +965,7 @@ static fp8dl_status launch_gemm(const uint8_t *A, int32_t a_dtype, const uint8_t
                                 CU_TENSOR_MAP_SWIZZLE_128B));
     args.idesc = idesc_base | ((uint32_t)(g1::BM >> 4) << 24);
     pick_raster(M, N, K, g1::BM, g1::BN, args.raster_n, args.group);
+    args.snake = 0;  // the one-CTA kernel reads K first to last
     const int64_t tiles = ((M + g1::BM - 1) / g1::BM) * ((N + g1::BN - 1) / g1::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
     (void)launch_kernel(fp8_gemm_kernel, grid, g1::THREADS, g1::SMEM_BYTES, stream, 0, pdl, ta, tb, args);

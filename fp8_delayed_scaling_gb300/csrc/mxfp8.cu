@@ -14,6 +14,7 @@
 namespace fp8dl {
 
 void pick_raster(int64_t M, int64_t N, int64_t K, int64_t tile_m, int64_t tile_n, int &raster_n, int64_t &group);
+int pick_snake(int64_t tiles, int64_t ctas, int64_t K);
 
 // ---------------------------------------------------------------------------
 // quantisation
@@ -366,6 +367,7 @@ struct MxArgs {
     int64_t M, N, K;
     int raster_n;
     int64_t group;
+    int snake;        // 1: every other tile of a CTA reads its k-blocks last to first
     const uint8_t *sfa, *sfb;
     int64_t kg;       // 4-block groups per row of the scale layout = ceil(K / 128)
     int64_t sfb_rows; // 128-row scale tiles of B = ceil(N / 128)
@@ -446,11 +448,13 @@ __global__ void __launch_bounds__(mx::THREADS, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            bool rev = false;  // this tile's k-blocks last to first (alternates per tile when snake)
+            for (int64_t tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, rev = args.snake && !rev) {
                 int64_t tm, tn;
                 mx_tile_coords(tile, tiles_m, tiles_n, args.raster_n, args.group, tm, tn);
                 const bool sfb1 = 2 * tn + 1 < args.sfb_rows;
-                for (int kb = 0; kb < num_kb; kb++) {
+                for (int kq = 0; kq < num_kb; kq++) {
+                    const int kb = rev ? num_kb - 1 - kq : kq;
                     if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1, abort_flag, args.status)) {
                         ok = false;
                         break;
@@ -743,6 +747,7 @@ fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, 
     }
     const int64_t tiles = ((M + mx::BM - 1) / mx::BM) * ((N + mx::BN - 1) / mx::BN);
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
+    args.snake = pick_snake(tiles, grid, K);
     const bool pdl = short_call_flops(2.0 * (double)M * (double)N * (double)K);
     (void)launch_kernel(mxfp8_gemm_kernel, grid, mx::THREADS, mx::SMEM_BYTES, (cudaStream_t)stream, 0, pdl, ta, tb, args);
     note_launch();

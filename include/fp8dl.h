@@ -221,6 +221,10 @@ fp8dl_status fp8_cast_amax_transpose_noalloc(const void *x, int32_t x_dtype, int
  *   D[m,n] = round_d( acc[m,n] * fl32(a_scale_inv * b_scale_inv) + bias[n] )
  *   (the product and the bias add are one fp32 fused multiply-add)
  *   acc[m,n] = sum_k A[m,k] * B[n,k] on the tcgen05 tensor cores, fp32 accumulate.
+ *     A GEMM with K > 8192 and at least two waves of tiles sums the k-blocks of
+ *     every other tile of a CTA (pair) last to first (less DRAM traffic); the
+ *     order is fixed by the shape and the GPU's SM count, so repeated calls give
+ *     the same bits.
  *   A [M x K] codes of a_dtype, B [N x K] codes of b_dtype (E4M3/E5M2 mixed ok)
  *   a_scale_inv, b_scale_inv   device floats (the operands' slots' scale_inv)
  *   bias       [N] of bias_dtype, or NULL
@@ -312,7 +316,7 @@ fp8dl_status mxfp8_quantize(const void *x, int32_t x_dtype, int64_t rows, int64_
  * B [N x K] E4M3 with scales B_s (tiled layout, R = N, NB = K/32), as produced
  * by mxfp8_quantize (row_q/row_s of X and W for the forward GEMM; col_q/col_s
  * for the operands of the gradient GEMMs).  M, N, K multiples of 32.
- * bias, D, dev_status as for fp8_gemm. */
+ * bias, D, dev_status and the order of the k-blocks as for fp8_gemm. */
 fp8dl_status mxfp8_gemm(const uint8_t *A, const uint8_t *A_s, const uint8_t *B, const uint8_t *B_s,
                         int64_t M, int64_t N, int64_t K, const void *bias, int32_t bias_dtype,
                         void *D, int32_t d_dtype, int32_t *dev_status, fp8dl_stream_t stream);
@@ -398,9 +402,11 @@ uint64_t fp8dl_kernel_launches(void);
 
 /* ----------------------------------------------------------------------------
  * Environment switches (testing and diagnosis).  They choose which kernel, tile
- * order or grid runs.  The GEMM switches leave every output bit unchanged; the
- * LayerNorm ones can change the rounding of the row statistics and of dgamma /
- * dbeta, within the tolerances the tests state.
+ * order or grid runs.  The GEMM switches leave every output bit unchanged in a
+ * GEMM of under two waves of tiles; in larger ones they change which tiles sum
+ * K last to first, within the GEMM's error bound.  The LayerNorm ones can
+ * change the rounding of the row statistics and of dgamma / dbeta, within the
+ * tolerances the tests state.
  *   FP8DL_DEBUG=1               print every launch and error message to stderr
  *                               (read once per process)
  *   FP8DL_GEMM_VARIANT=1sm|2sm  force the one-CTA or the CTA-pair FP8 GEMM
@@ -409,6 +415,7 @@ uint64_t fp8dl_kernel_launches(void);
  *   FP8DL_GEMM_TILE_N=256|128   tile width of the plain pair GEMM (by default 128
  *                               only for a short GEMM with under two waves of
  *                               256-column tiles)
+ *   FP8DL_GEMM_SNAKE=0          every GEMM tile sums K first to last
  *   FP8DL_LN_VARIANT=tiles      LayerNorm by the two-pass tile kernels
  *   FP8DL_LN_CLUSTERS=n         cap on the clusters of the LayerNorm cluster kernels
  *   FP8DL_PDL=0                 launch without programmatic dependent launch: every

@@ -20,7 +20,7 @@ def _codes(rng, shape):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 128), (512, 1024, 256), (384, 768, 1040), (2048, 4096, 1024),
-                                   (128, 256, 64), (272, 528, 256)])
+                                   (128, 256, 64), (272, 528, 256), (4096, 2576, 8208)])
 def test_fused_gelu_epilogue_matches_unfused_and_oracle(M, N, K):
     import fp8_delayed_scaling_gb300 as fd
     dev = gpu()
@@ -71,7 +71,7 @@ def _codes_fmt(rng, fmt, shape, lim=8.0):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 128), (384, 768, 1040), (2048, 4096, 1024), (128, 256, 64),
-                                   (272, 528, 256), (48, 80, 32)])
+                                   (272, 528, 256), (48, 80, 32), (4096, 2576, 8208)])
 def test_fused_dgelu_epilogue_matches_unfused_and_oracle(M, N, K, monkeypatch):
     """fp8_gemm_dgelu_cast (fc2 dgrad with dGELU + E5M2 cast + amax + db1 in its epilogue)
     against fp8_gemm + fp8_dgelu_cast on the same pair kernel, and against the oracle."""

@@ -144,3 +144,27 @@ def test_pair_tile_width_leaves_results_unchanged(M, N, K, monkeypatch):
     ms, ns = sample_elems(M, N, np.random.default_rng(5), n=2048, tile_n=128)
     ref, absr = oracle.gemm_elems(A, 0, B, 1, 0.01, 0.02, bias.cpu().numpy(), ms, ns)
     check_gemm(out[0], ref, absr, ms, ns)
+
+
+def test_alternating_k_order(monkeypatch):
+    """A GEMM with K > 8192 and at least two waves of pair tiles sums the k-blocks of every
+    other tile of a CTA pair last to first (the ragged last k-block included).  That order stays within the
+    oracle's bound on sampled elements, gives the same bits on a repeated call, and differs
+    in rounding from the first-to-last order (FP8DL_GEMM_SNAKE=0), which meets the bound too."""
+    monkeypatch.setenv("FP8DL_GEMM_VARIANT", "2sm")
+    dev = gpu()
+    M, N, K = 4096, 2576, 8208  # 16 x 11 = 176 pair tiles (over two waves of 76 CTA pairs), K > 8192
+    rng = np.random.default_rng(17)
+    A = _codes(rng, 0, (M, K))
+    B = _codes(rng, 1, (N, K))
+    bias = torch.from_numpy(rng.standard_normal(N).astype(np.float32)).to(dev)
+    D1 = _gemm(A, 0, B, 1, 0.01, 0.02, bias, torch.bfloat16, dev)
+    D2 = _gemm(A, 0, B, 1, 0.01, 0.02, bias, torch.bfloat16, dev)
+    monkeypatch.setenv("FP8DL_GEMM_SNAKE", "0")
+    D0 = _gemm(A, 0, B, 1, 0.01, 0.02, bias, torch.bfloat16, dev)
+    assert torch.equal(D1, D2)
+    assert not torch.equal(D1, D0)
+    ms, ns = sample_elems(M, N, np.random.default_rng(6), n=4096, tile_m=256)
+    ref, absr = oracle.gemm_elems(A, 0, B, 1, 0.01, 0.02, bias.cpu().numpy(), ms, ns)
+    check_gemm(D1, ref, absr, ms, ns, what="alternating K order")
+    check_gemm(D0, ref, absr, ms, ns, what="first-to-last K order")

@@ -155,6 +155,29 @@ def test_mx_gemm_parity(M, N, K):
     check_gemm(D, ref, absr, ms.ravel(), ns.ravel(), what="mx gemm")
 
 
+def test_mx_gemm_alternating_k_order(monkeypatch):
+    """With K > 8192 and at least two waves of tiles every other tile of a CTA sums its k-blocks (and their
+    block scales) last to first: within the oracle's bound on sampled elements, the same bits
+    on a repeated call, and different rounding from the first-to-last order
+    (FP8DL_GEMM_SNAKE=0), which meets the bound too."""
+    dev = gpu()
+    M, N, K = 4096, 2560, 8224  # 32 x 10 = 320 tiles of 128 x 256 (over two waves of 152 CTAs), K > 8192
+    rng = np.random.default_rng(23)
+    A, B = _codes(rng, (M, K)), _codes(rng, (N, K))
+    As = rng.integers(118, 136, (M, K // 32)).astype(np.uint8)
+    Bs = rng.integers(118, 136, (N, K // 32)).astype(np.uint8)
+    D1 = _mx_gemm(A, As, B, Bs, dev)
+    D2 = _mx_gemm(A, As, B, Bs, dev)
+    monkeypatch.setenv("FP8DL_GEMM_SNAKE", "0")
+    D0 = _mx_gemm(A, As, B, Bs, dev)
+    assert torch.equal(D1, D2)
+    assert not torch.equal(D1, D0)
+    ms, ns = sample_elems(M, N, np.random.default_rng(8), n=4096)
+    ref, absr = oracle.mx_gemm_elems(A, As, B, Bs, None, ms, ns)
+    check_gemm(D1, ref, absr, ms, ns, what="mx alternating K order")
+    check_gemm(D0, ref, absr, ms, ns, what="mx first-to-last K order")
+
+
 @pytest.mark.parametrize("d_dtype", [torch.bfloat16, torch.float32])
 def test_mx_gemm_bias_and_fp32_out(d_dtype):
     dev = gpu()
