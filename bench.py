@@ -47,13 +47,15 @@ FP8_PER_BF16 = 2.0  # nominal dense FP8 : BF16 tensor rate (4.5 : 2.25 PFLOP/s)
 # taken with (comments left out); once that code differs, the line reports null instead.
 _COMMON_SRC = ("fp8_delayed_scaling_gb300/csrc/tc.cuh", "fp8_delayed_scaling_gb300/csrc/common.cuh")
 GEMM_TRAFFIC = {
-    "ln_mlp": {"bytes": 1.229e9, "sources": ("fp8_delayed_scaling_gb300/csrc/gemm.cu",) + _COMMON_SRC,
-               "src_sha256": "100556f15fae87ade58856dde3721f1f3c69e8f6da2521b77f4878ec54cace21",
-               "capture": "fp8_gemm_pair_kernel<0,0,256>/<1,0,256>/<2,1,256> of commit 6b3a1f9, mean of the 6 "
+    "ln_mlp": {"bytes": 1.185e9, "sources": ("fp8_delayed_scaling_gb300/csrc/gemm.cu",) + _COMMON_SRC,
+               "src_sha256": "268867d7440e6b7698e6b92d11d45119dcd9845a3303220d8b49a29031b5d2c9",
+               "capture": "fp8_gemm_pair_kernel<0,0,256>/<1,0,256>/<2,1,256> of commit b64b0d7, mean of the 6 "
                           "launches of a step over 17 steps"},
-    "mx_mlp": {"bytes": 3.678e9, "sources": ("fp8_delayed_scaling_gb300/csrc/mxfp8.cu",) + _COMMON_SRC,
-               "src_sha256": "7a324d5472d4af9d0fd416758f392649800eda844bdaf2278ec4e5e704e651a6",
-               "capture": "mxfp8_gemm_kernel of commit e2e84de, mean of the 6 launches of a step over 17 steps"},
+    # gemm.cu holds the tile order and K order the MXFP8 GEMM's host code picks
+    "mx_mlp": {"bytes": 3.405e9, "sources": ("fp8_delayed_scaling_gb300/csrc/mxfp8.cu",
+                                             "fp8_delayed_scaling_gb300/csrc/gemm.cu") + _COMMON_SRC,
+               "src_sha256": "57296a13eb8d09eebf5e08a1917b0dd222ade21650717dfbf20ae24d43cfc7b3",
+               "capture": "mxfp8_gemm_kernel of commit b64b0d7, mean of the 6 launches of a step over 17 steps"},
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
