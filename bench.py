@@ -813,7 +813,8 @@ def run_oracle_sample(cfg, seed, rows=64, gemm_rows=8, gemm_cols=None):
 # ---------------------------------------------------------------------------
 def run_only(args, dev):
     """Time one kernel alone at one shape: `--only gemm --shape M,N,K` (E4M3 x E4M3 -> bf16),
-    `--only cast --shape R,C` (bf16 -> E4M3 + transposed copy + amax),
+    `--only cast --shape R,C` (bf16 -> E4M3 + transposed copy + amax; `castdb`: E5M2 and the
+    bias gradient, as for grad_output),
     `--only mxq --shape R,C` (bf16 -> row- and column-wise MXFP8),
     `--only mxgemm --shape M,N,K`.  Inputs are seeded; L2 is flushed between launches."""
     import fp8_delayed_scaling_gb300 as fd
@@ -888,13 +889,20 @@ def run_only(args, dev):
     else:
         R, C = shape
         x = wl.normal((R, C), 1.0, g, torch.bfloat16).to(dev)
-        if args.only == "cast":
+        if args.only in ("cast", "castdb"):
             q = torch.empty((R, C), dtype=torch.uint8, device=dev)
             qt = torch.empty((C, R), dtype=torch.uint8, device=dev)
             sc = torch.ones(1, dtype=torch.float32, device=dev)
             am = torch.zeros(1, dtype=torch.float32, device=dev)
-            fn = lambda: fd.fp8_cast_amax_transpose(x, fd.E4M3, sc, out=q, out_t=qt, amax=am)  # noqa: E731
-            work = R * C * (2 + 1 + 1)
+            if args.only == "cast":
+                fn = lambda: fd.fp8_cast_amax_transpose(x, fd.E4M3, sc, out=q, out_t=qt, amax=am)  # noqa: E731
+                work = R * C * (2 + 1 + 1)
+            else:  # the grad_output cast of a layer with a bias: E5M2 codes and the column sums
+                db = torch.empty(C, dtype=torch.float32, device=dev)
+                ws = torch.empty(fd.fp8_cast_workspace_size(R, C), dtype=torch.uint8, device=dev)
+                fn = lambda: fd.fp8_cast_amax_transpose(x, fd.E5M2, sc, out=q, out_t=qt, amax=am,  # noqa: E731
+                                                        dbias=db, workspace=ws)
+                work = R * C * (2 + 1 + 1) + 4 * C
         else:
             rq = torch.empty((R, C), dtype=torch.uint8, device=dev)
             rs = torch.empty((R, C // 32), dtype=torch.uint8, device=dev)
@@ -932,7 +940,7 @@ def main():
     ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
                     help="one workload alone; without it: ln_mlp, then te.Linear and the MXFP8 MLP beside it")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--only", default=None, choices=["gemm", "gemm_gelu", "gemm_dgelu", "cast", "mxq", "mxgemm", "gelu", "dgelu",
+    ap.add_argument("--only", default=None, choices=["gemm", "gemm_gelu", "gemm_dgelu", "cast", "castdb", "mxq", "mxgemm", "gelu", "dgelu",
                                                           "ln", "lnbwd"])
     ap.add_argument("--shape", default="8192,12288,4096")
     ap.add_argument("--no-graph", action="store_true", help="issue the timed steps one launch at a time")
