@@ -35,3 +35,27 @@ def test_ln_mlp_hbm_bytes_match_hand_counts():
     # codes written, bias gradient) are HBM passes of their own
     u = bench.hbm_bytes(bench.WORKLOADS["ln_mlp_separate"], fused=False)
     assert u["norm_act"] - b["norm_act"] == M * F * 4 + M * F * 6 + 4 * F
+
+
+def test_gemm_traffic_is_keyed_to_the_kernel_code(tmp_path, monkeypatch):
+    """The DRAM traffic the bench line prints for a workload's GEMMs comes from an ncu capture
+    of specific kernel code: the key ignores comments, follows any code change (the line then
+    prints null), and matches the sources as committed (a GEMM change needs a new capture)."""
+    src = "int f(int x) {  // doubles\n    return 2 * x; /* a comment */\n}\n"
+    same = "int f(int x) {  // twice x\n\n    return 2 * x; /* another */\n}\n"
+    other = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench.source_code(src) == bench.source_code(same)
+    assert bench.source_code(src) != bench.source_code(other)
+    for name in ("ln_mlp", "mx_mlp"):
+        traffic, note = bench.gemm_traffic(name)
+        assert traffic is not None, "%s: %s (capture the GEMM traffic again)" % (name, note)
+        assert note.startswith("ncu capture: ")
+    (tmp_path / "k.cu").write_text(src)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    entry = dict(bench.GEMM_TRAFFIC["ln_mlp"], sources=("k.cu",), src_sha256=bench.source_sha(("k.cu",)))
+    monkeypatch.setitem(bench.GEMM_TRAFFIC, "ln_mlp", entry)
+    assert bench.gemm_traffic("ln_mlp")[0] == entry["bytes"]
+    (tmp_path / "k.cu").write_text(same)
+    assert bench.gemm_traffic("ln_mlp")[0] == entry["bytes"]
+    (tmp_path / "k.cu").write_text(other)
+    assert bench.gemm_traffic("ln_mlp") == (None, "the GEMM kernels changed since the capture")
