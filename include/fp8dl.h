@@ -402,9 +402,10 @@ uint64_t fp8dl_kernel_launches(void);
 
 /* ----------------------------------------------------------------------------
  * Environment switches (testing and diagnosis).  They choose which kernel, tile
- * order or grid runs.  The GEMM switches leave every output bit unchanged in a
- * GEMM of under two waves of tiles; in larger ones they change which tiles sum
- * K last to first, within the GEMM's error bound.  The LayerNorm ones can
+ * order or grid runs.  The GEMM switches leave every output bit unchanged,
+ * except in a GEMM with K > 8192 and two or more waves of tiles, where they
+ * can change which tiles sum K last to first (within the GEMM's error bound;
+ * the one-CTA kernel always sums first to last).  The LayerNorm ones can
  * change the rounding of the row statistics and of dgamma / dbeta, within the
  * tolerances the tests state.
  *   FP8DL_DEBUG=1               print every launch and error message to stderr
