@@ -102,6 +102,67 @@ def test_host_validation_without_gpu(lib):
     assert lib.fp8dl_last_error() != ""
 
 
+def test_layernorm_mlp_entry_validation_without_gpu(lib):
+    """The LayerNormMLP entry points (LayerNorm forward/backward, GELU/dGELU casts, the fused
+    GELU/dGELU GEMMs) reject bad arguments on the host, with the status the header names."""
+    L = _raw(lib)
+    a = 1 << 20  # a fake, 16-byte aligned address: validation fails before any use
+    E4, E5, BF = lib.E4M3, lib.E5M2, lib.BF16
+    ln = lambda x=a, rows=32, cols=64, g=a, b=a, eps=1e-5, fmt=E4, sc=a, out=a, mu=a: L.fp8_layernorm_cast(  # noqa: E731
+        x, rows, cols, g, b, eps, fmt, sc, out, None, None, mu, a, None, None)
+    assert ln(x=None) == lib.ERR_INVALID_ARG
+    assert ln(mu=None) == lib.ERR_INVALID_ARG
+    assert ln(fmt=2) == lib.ERR_INVALID_ARG
+    assert ln(sc=None) == lib.ERR_INVALID_ARG  # an FP8 output needs its scale
+    assert ln(eps=-1.0) == lib.ERR_INVALID_ARG
+    assert ln(rows=0) == lib.ERR_SHAPE
+    assert ln(cols=24) == lib.ERR_SHAPE
+    assert ln(cols=8192 + 16) == lib.ERR_SHAPE  # widest row: 8192
+    assert ln(g=a + 8) == lib.ERR_ALIGN
+    assert ln(out=a + 4) == lib.ERR_ALIGN
+    ws_ln = lib.fp8_layernorm_bwd_workspace_size(32, 64)
+    assert ws_ln > 0 and lib.fp8_layernorm_bwd_workspace_size(0, 64) == 0
+    lnb = lambda dx=a, rows=32, ws=a, wsb=ws_ln: L.fp8_layernorm_bwd(a, a, a, a, a, rows, 64, dx, a, a, ws, wsb,  # noqa: E731
+                                                                     None)
+    assert lnb(dx=None) == lib.ERR_INVALID_ARG
+    assert lnb(rows=33) == lib.ERR_SHAPE
+    assert lnb(dx=a + 2) == lib.ERR_ALIGN
+    assert lnb(ws=a + 8) == lib.ERR_ALIGN
+    assert lnb(ws=None) == lib.ERR_WORKSPACE
+    assert lnb(wsb=ws_ln - 1) == lib.ERR_WORKSPACE
+    # GELU / dGELU casts
+    assert L.fp8_gelu_cast(a, 32, 64, E4, a, None, None, None, None, None) == lib.ERR_INVALID_ARG  # nothing to do
+    assert L.fp8_gelu_cast(a, 32, 64, E4, None, a, None, None, None, None) == lib.ERR_INVALID_ARG  # no scale
+    assert L.fp8_gelu_cast(a, 32, 40, E4, a, a, None, None, None, None) == lib.ERR_SHAPE
+    assert L.fp8_gelu_cast(a, 32, 64, E4, a, a + 8, None, None, None, None) == lib.ERR_ALIGN
+    assert L.fp8_dgelu_cast(a, None, 32, 64, E5, a, a, None, None, None, None, 0, None, None) == lib.ERR_INVALID_ARG
+    ws_c = lib.fp8_cast_workspace_size(32, 64)
+    assert L.fp8_dgelu_cast(a, a, 32, 64, E5, a, a, None, None, a, None, 0, None, None) == lib.ERR_WORKSPACE
+    assert L.fp8_dgelu_cast(a, a, 32, 64, E5, a, a, None, None, a, a, ws_c - 1, None, None) == lib.ERR_WORKSPACE
+    assert L.fp8_dgelu_cast(a, a, 32, 64, E5, a, a, None, None, a, a + 8, ws_c, None, None) == lib.ERR_ALIGN
+    # fused GELU GEMM: the GEMM's own checks, then the cast's
+    gg = lambda N=64, q=a, qt=a, qfmt=E4, qs=a, H=a: L.fp8_gemm_gelu_cast(  # noqa: E731
+        a, E4, a, E4, 32, N, 64, a, a, None, BF, H, qfmt, qs, q, qt, None, None, None, None)
+    assert gg(N=24) == lib.ERR_SHAPE
+    assert gg(H=None) == lib.ERR_INVALID_ARG
+    assert gg(qfmt=3) == lib.ERR_INVALID_ARG
+    assert gg(q=None) == lib.ERR_INVALID_ARG
+    assert gg(qs=None) == lib.ERR_INVALID_ARG
+    assert gg(qt=a + 8) == lib.ERR_ALIGN
+    # fused dGELU GEMM (its dg output is optional); the bias gradient needs its workspace
+    ws_d = lib.fp8_gemm_dgelu_workspace_size(32, 64)
+    assert ws_d == 1 * 64 * 4 and lib.fp8_gemm_dgelu_workspace_size(33, 64) == 2 * 64 * 4
+    dgg = lambda h=a, db=None, ws=None, wsb=0, q=a, dh=None: L.fp8_gemm_dgelu_cast(  # noqa: E731
+        a, E5, a, E4, 32, 64, 64, a, a, h, None, E5, a, q, a, None, db, ws, wsb, dh, None, None)
+    assert dgg(h=None) == lib.ERR_INVALID_ARG
+    assert dgg(q=None) == lib.ERR_INVALID_ARG
+    assert dgg(dh=a + 8) == lib.ERR_ALIGN
+    assert dgg(db=a) == lib.ERR_WORKSPACE
+    assert dgg(db=a, ws=a, wsb=ws_d - 1) == lib.ERR_WORKSPACE
+    assert dgg(db=a, ws=a + 8, wsb=ws_d) == lib.ERR_ALIGN
+    assert lib.fp8dl_last_error() != ""
+
+
 def test_valid_call_without_gpu_fails_loudly(lib):
     """No GPU: a well-formed call must fail (no CPU fallback), never compute."""
     import torch
